@@ -1,0 +1,541 @@
+// C ABI of the MoE decode library: argument checks, workspace layout, kernel
+// choice by batch size and the stream schedule of the MoE layer.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <utility>
+
+#include "internal.h"
+
+using namespace dec;
+
+namespace {
+
+constexpr int kMaxM = 64;
+constexpr int kMaxTopK = 16;
+constexpr int kMaxE = 1024;
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
+
+#define DEC_CUDA(expr)                         \
+  do {                                         \
+    if ((expr) != cudaSuccess) return DEC_ERR_CUDA; \
+  } while (0)
+
+// Split a workspace into 256-byte-aligned pieces.
+struct Carver {
+  char* base;
+  size_t used = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t count) {
+    T* p = base ? reinterpret_cast<T*>(base + used) : nullptr;
+    used += al256(count * sizeof(T));
+    return p;
+  }
+};
+
+struct EngineRegion {
+  float* partials = nullptr;
+  int* counters = nullptr;
+};
+
+EngineRegion carve_engine(Carver& c, int grid, int nacc, long long max_tiles) {
+  EngineRegion r;
+  r.partials = c.take<float>((size_t)2 * grid * nacc * kTileN * kMaxCols);
+  r.counters = c.take<int>((size_t)std::max<long long>(max_tiles, 1));
+  return r;
+}
+
+bool linear_shape_ok(int M, int N, int K, int ldx) {
+  return M >= 1 && M <= kMaxM && N >= 1 && K >= 8 && K % 8 == 0 && ldx >= K && ldx % 8 == 0;
+}
+
+int choose_variant(const dec_handle* h, int M, int K) {
+  if (h->force_variant == DEC_VARIANT_SMALL_M || h->force_variant == DEC_VARIANT_SPLIT_K) return h->force_variant;
+  return (M <= 2 && gemv_supported(M, K)) ? DEC_VARIANT_SMALL_M : DEC_VARIANT_SPLIT_K;
+}
+
+dec_status linear_impl(dec_handle* h, const uint16_t* x, int ldx, const uint16_t* W, const uint16_t* r, uint16_t* y,
+                       int M, int N, int K, EngineRegion eng, cudaStream_t s) {
+  const int v = choose_variant(h, M, K);
+  cudaError_t e;
+  if (v == DEC_VARIANT_SMALL_M) {
+    if (!gemv_supported(M, K)) return DEC_ERR_UNSUPPORTED;
+    e = launch_gemv(h, x, ldx, W, r, N, y, N, M, N, K, s);
+  } else {
+    EngineLaunch L;
+    L.epi = EPI_LINEAR;
+    L.A = W;
+    L.a_rows = N;
+    L.B = x;
+    L.b_rows = M;
+    L.ldb = ldx;
+    L.K = K;
+    L.N = N;
+    L.count = M;
+    L.out = y;
+    L.ldo = N;
+    L.res = r;
+    L.ldr = N;
+    L.partials = eng.partials;
+    L.counters = eng.counters;
+    e = launch_engine(h, L, s);
+  }
+  h->last_variant = v;
+  return e == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- MoE workspace
+struct MoeWs {
+  int* table = nullptr;
+  uint16_t* xs = nullptr;
+  uint16_t* hbuf = nullptr;
+  float* y = nullptr;
+  uint16_t* hs = nullptr;
+  float* ys = nullptr;
+  EngineRegion r0, r1;
+};
+
+long long moe_tiles(int E, int H, int I) { return (long long)E * (std::max(H, I) / kTileN); }
+
+void carve_moe(Carver& c, const dec_handle* h, int M, int k, int E, int H, int I, long long extra_tiles,
+               MoeWs* w) {
+  const int n = M * k;
+  w->table = c.take<int>(TableLayout(E, n).words());
+  w->xs = c.take<uint16_t>((size_t)n * H);
+  w->hbuf = c.take<uint16_t>((size_t)n * I);
+  w->y = c.take<float>((size_t)n * H);
+  w->hs = c.take<uint16_t>((size_t)M * I);
+  w->ys = c.take<float>((size_t)M * H);
+  w->r0 = carve_engine(c, engine_grid(h), 2, std::max(moe_tiles(E, H, I), extra_tiles));
+  w->r1 = carve_engine(c, engine_grid(h), 2, std::max(H, I) / kTileN);
+}
+
+bool moe_shape_ok(int M, int k, int E, int H, int I) {
+  return M >= 1 && M <= kMaxM && k >= 1 && k <= kMaxTopK && E >= k && E <= kMaxE && H >= kTileN &&
+         H % kTileN == 0 && I >= kTileN && I % kTileN == 0;
+}
+
+// CTAs given to the shared expert while the routed experts run beside it: the
+// shared expert's share of the expected weight bytes (at least one SM, at
+// most half). Expected distinct experts for uniform routing: E (1 - (1 - k/E)^M).
+int shared_grid(const dec_handle* h, int M, int k, int E) {
+  if (h->shared_ctas > 0) return std::min(h->shared_ctas, h->sms - 1);
+  const double eu = E * (1.0 - std::pow(1.0 - (double)k / E, (double)M));
+  int g = (int)std::lround(h->sms * 1.0 / (1.0 + eu));
+  return std::max(1, std::min(g, h->sms / 2));
+}
+
+dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const float* w, int M, int k,
+                    const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I,
+                    const uint16_t* Wg_s, const uint16_t* Wu_s, const uint16_t* Wd_s, const uint16_t* residual,
+                    uint16_t* out, const MoeWs& ws, cudaStream_t s) {
+  const bool has_shared = Wg_s != nullptr;
+  const int n = M * k;
+  const int g1 = has_shared ? shared_grid(h, M, k, E) : 0;
+  const int g0 = h->sms - g1;
+  if (has_shared) {
+    DEC_CUDA(cudaEventRecord(h->ev_fork, s));
+    DEC_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+    EngineLaunch L;
+    L.epi = EPI_SWIGLU;
+    L.A = Wg_s;
+    L.A2 = Wu_s;
+    L.a_rows = I;
+    L.B = x;
+    L.b_rows = M;
+    L.ldb = H;
+    L.K = H;
+    L.N = I;
+    L.count = M;
+    L.out = ws.hs;
+    L.ldo = I;
+    L.partials = ws.r1.partials;
+    L.counters = ws.r1.counters;
+    L.grid = g1;
+    DEC_CUDA(launch_engine(h, L, h->side));
+    EngineLaunch D;
+    D.epi = EPI_F32;
+    D.A = Wd_s;
+    D.a_rows = H;
+    D.B = ws.hs;
+    D.b_rows = M;
+    D.ldb = I;
+    D.K = I;
+    D.N = H;
+    D.count = M;
+    D.out = ws.ys;
+    D.ldo = H;
+    D.partials = ws.r1.partials;
+    D.counters = ws.r1.counters;
+    D.grid = g1;
+    DEC_CUDA(launch_engine(h, D, h->side));
+    DEC_CUDA(cudaEventRecord(h->ev_join, h->side));
+  }
+  DEC_CUDA(launch_route_table(h, idx, M, k, E, x, H, ws.table, ws.xs, s));
+  EngineLaunch L;
+  L.epi = EPI_SWIGLU;
+  L.A = Wg;
+  L.A2 = Wu;
+  L.a_rows = (long long)E * I;
+  L.a_rows_per_prob = I;
+  L.B = ws.xs;
+  L.b_rows = n;
+  L.ldb = H;
+  L.K = H;
+  L.N = I;
+  L.table = ws.table;
+  L.E = E;
+  L.n_entries = n;
+  L.out = ws.hbuf;
+  L.ldo = I;
+  L.partials = ws.r0.partials;
+  L.counters = ws.r0.counters;
+  L.grid = g0;
+  DEC_CUDA(launch_engine(h, L, s));
+  EngineLaunch D;
+  D.epi = EPI_F32;
+  D.A = Wd;
+  D.a_rows = (long long)E * H;
+  D.a_rows_per_prob = H;
+  D.B = ws.hbuf;
+  D.b_rows = n;
+  D.ldb = I;
+  D.K = I;
+  D.N = H;
+  D.table = ws.table;
+  D.E = E;
+  D.n_entries = n;
+  D.out = ws.y;
+  D.ldo = H;
+  D.partials = ws.r0.partials;
+  D.counters = ws.r0.counters;
+  D.grid = g0;
+  DEC_CUDA(launch_engine(h, D, s));
+  if (has_shared) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
+  DEC_CUDA(launch_combine(h, ws.y, ws.table, w, M, k, E, has_shared ? ws.ys : nullptr, residual, out, H, s));
+  return DEC_OK;
+}
+
+// ---------------------------------------------------------------- decode layer workspace
+struct LayerWs {
+  uint16_t* a = nullptr;
+  uint16_t* yin = nullptr;
+  uint16_t* h1 = nullptr;
+  uint16_t* b = nullptr;
+  float* parts = nullptr;
+  int32_t* idx = nullptr;
+  float* w = nullptr;
+  MoeWs moe;
+};
+
+bool layer_ok(const dec_layer_weights* L, int M) {
+  if (!L || M < 1 || M > kMaxM) return false;
+  if (L->H < kTileN || L->H % kTileN != 0 || L->N_in < 8 || L->N_in % 8 != 0 || L->K_out < 8 ||
+      L->K_out % 8 != 0 || L->K_out > L->N_in)
+    return false;
+  return moe_shape_ok(M, L->k, L->E, L->H, L->I);
+}
+
+void carve_layer(Carver& c, const dec_handle* h, const dec_layer_weights* L, int M, LayerWs* w) {
+  const int H = L->H;
+  w->a = c.take<uint16_t>((size_t)M * H);
+  w->yin = c.take<uint16_t>((size_t)M * L->N_in);
+  w->h1 = c.take<uint16_t>((size_t)M * H);
+  w->b = c.take<uint16_t>((size_t)M * H);
+  w->parts = c.take<float>((size_t)router_ksplit(H) * M * L->E);
+  w->idx = c.take<int32_t>((size_t)M * L->k);
+  w->w = c.take<float>((size_t)M * L->k);
+  const long long dense_tiles = std::max<long long>((L->N_in + kTileN - 1) / kTileN, H / kTileN);
+  carve_moe(c, h, M, L->k, L->E, H, L->I, dense_tiles, &w->moe);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dec_status_string(dec_status s) {
+  switch (s) {
+    case DEC_OK: return "ok";
+    case DEC_ERR_INVALID_ARG: return "invalid argument";
+    case DEC_ERR_UNSUPPORTED: return "unsupported shape or configuration";
+    case DEC_ERR_CUDA: return "CUDA error";
+    case DEC_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+dec_status dec_create(dec_handle** out, int device) {
+  if (out == nullptr) return DEC_ERR_INVALID_ARG;
+  *out = nullptr;
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || device < 0 || device >= n) return DEC_ERR_CUDA;
+  int prev = 0;
+  DEC_CUDA(cudaGetDevice(&prev));
+  DEC_CUDA(cudaSetDevice(device));
+  dec_handle* h = new dec_handle();
+  h->device = device;
+  bool ok = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&h->pf, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->ev_pf_fork, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h->ev_pf_join, cudaEventDisableTiming) == cudaSuccess &&
+            cudaMalloc(&h->d_err, sizeof(int)) == cudaSuccess && cudaMemset(h->d_err, 0, sizeof(int)) == cudaSuccess;
+  if (ok) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    ok = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+             cudaSuccess &&
+         q == cudaDriverEntryPointSuccess && fn != nullptr;
+    h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  cudaSetDevice(prev);
+  if (!ok) {
+    dec_destroy(h);
+    return DEC_ERR_CUDA;
+  }
+  *out = h;
+  return DEC_OK;
+}
+
+dec_status dec_destroy(dec_handle* h) {
+  if (h == nullptr) return DEC_OK;
+  if (h->side) cudaStreamSynchronize(h->side);
+  if (h->pf) cudaStreamSynchronize(h->pf);
+  if (h->side) cudaStreamDestroy(h->side);
+  if (h->pf) cudaStreamDestroy(h->pf);
+  for (cudaEvent_t e : {h->ev_fork, h->ev_join, h->ev_pf_fork, h->ev_pf_join})
+    if (e) cudaEventDestroy(e);
+  if (h->d_err) cudaFree(h->d_err);
+  delete h;
+  return DEC_OK;
+}
+
+dec_status dec_workspace_init(dec_handle* h, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (h == nullptr || (ws == nullptr && ws_bytes != 0)) return DEC_ERR_INVALID_ARG;
+  if (ws_bytes == 0) return DEC_OK;
+  return cudaMemsetAsync(ws, 0, ws_bytes, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
+}
+
+dec_status dec_set_wait_limit_ns(dec_handle* h, uint64_t ns) {
+  if (h == nullptr || ns == 0) return DEC_ERR_INVALID_ARG;
+  h->wait_ns = ns;
+  return DEC_OK;
+}
+
+dec_status dec_set_pdl(dec_handle* h, int enable) {
+  if (h == nullptr) return DEC_ERR_INVALID_ARG;
+  h->pdl = enable ? 1 : 0;
+  return DEC_OK;
+}
+
+dec_status dec_set_force_variant(dec_handle* h, int variant) {
+  if (h == nullptr || variant < DEC_VARIANT_AUTO || variant > DEC_VARIANT_SPLIT_K) return DEC_ERR_INVALID_ARG;
+  h->force_variant = variant;
+  return DEC_OK;
+}
+
+int dec_last_variant(const dec_handle* h) { return h ? h->last_variant : 0; }
+
+dec_status dec_check_device_error(dec_handle* h) {
+  if (h == nullptr) return DEC_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return DEC_ERR_CUDA;
+  int v = 0;
+  DEC_CUDA(cudaMemcpy(&v, h->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (v == 0) return DEC_OK;
+  DEC_CUDA(cudaMemset(h->d_err, 0, sizeof(int)));
+  return DEC_ERR_TIMEOUT;
+}
+
+// ---------------------------------------------------------------- projections
+dec_status dec_linear_workspace_size(const dec_handle* h, int M, int N, int K, size_t* bytes) {
+  if (h == nullptr || bytes == nullptr || !linear_shape_ok(M, N, K, K)) return DEC_ERR_INVALID_ARG;
+  Carver c(nullptr);
+  carve_engine(c, engine_grid(h), 1, (N + kTileN - 1) / kTileN);
+  *bytes = c.used;
+  return DEC_OK;
+}
+
+static dec_status linear_entry(dec_handle* h, const dec_bf16* x, int ldx, const dec_bf16* W, const dec_bf16* r,
+                               dec_bf16* out, int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (h == nullptr || x == nullptr || W == nullptr || out == nullptr) return DEC_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(W) || !al16(out) || (r != nullptr && !al16(r))) return DEC_ERR_INVALID_ARG;
+  if (!linear_shape_ok(M, N, K, ldx)) return DEC_ERR_INVALID_ARG;
+  EngineRegion eng;
+  if (choose_variant(h, M, K) == DEC_VARIANT_SPLIT_K) {
+    size_t need = 0;
+    dec_linear_workspace_size(h, M, N, K, &need);
+    if (ws == nullptr || !al16(ws) || ws_bytes < need) return DEC_ERR_INVALID_ARG;
+    Carver c(ws);
+    eng = carve_engine(c, engine_grid(h), 1, (N + kTileN - 1) / kTileN);
+  }
+  return linear_impl(h, x, ldx, W, r, out, M, N, K, eng, s);
+}
+
+dec_status dec_linear(dec_handle* h, const dec_bf16* x, int ldx, const dec_bf16* W, dec_bf16* y, int M, int N,
+                      int K, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return linear_entry(h, x, ldx, W, nullptr, y, M, N, K, ws, ws_bytes, stream);
+}
+
+dec_status dec_linear_residual(dec_handle* h, const dec_bf16* x, int ldx, const dec_bf16* W, const dec_bf16* r,
+                               dec_bf16* out, int M, int N, int K, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+  if (r == nullptr) return DEC_ERR_INVALID_ARG;
+  return linear_entry(h, x, ldx, W, r, out, M, N, K, ws, ws_bytes, stream);
+}
+
+dec_status dec_rmsnorm(dec_handle* h, const dec_bf16* x, const dec_bf16* gamma, dec_bf16* y, int M, int H, float eps,
+                       cudaStream_t stream) {
+  if (h == nullptr || x == nullptr || gamma == nullptr || y == nullptr) return DEC_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(gamma) || !al16(y) || M < 1 || M > kMaxM || H < 8 || H % 8 != 0 || H > 65536 ||
+      !(eps >= 0.f))
+    return DEC_ERR_INVALID_ARG;
+  return launch_rmsnorm(h, x, gamma, y, M, H, eps, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- router
+dec_status moe_route_topk_workspace_size(const dec_handle* h, int M, int H, int E, size_t* bytes) {
+  if (h == nullptr || bytes == nullptr || M < 1 || M > kMaxM || H < 8 || H % 8 != 0 || E < 1 || E > kMaxE)
+    return DEC_ERR_INVALID_ARG;
+  *bytes = al256((size_t)router_ksplit(H) * M * E * sizeof(float));
+  return DEC_OK;
+}
+
+dec_status moe_route_topk(dec_handle* h, const dec_bf16* x, const float* Wr, int M, int H, int E, int k,
+                          int32_t* idx, float* w, float* scores, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (h == nullptr || x == nullptr || Wr == nullptr || idx == nullptr || w == nullptr) return DEC_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(Wr) || !al16(ws)) return DEC_ERR_INVALID_ARG;
+  if (M < 1 || M > kMaxM || H < 8 || H % 8 != 0 || E < 1 || E > kMaxE || k < 1 || k > kMaxTopK || k > E)
+    return DEC_ERR_INVALID_ARG;
+  size_t need = 0;
+  moe_route_topk_workspace_size(h, M, H, E, &need);
+  if (ws == nullptr || ws_bytes < need) return DEC_ERR_INVALID_ARG;
+  float* parts = static_cast<float*>(ws);
+  if (launch_router(h, x, Wr, M, H, E, parts, stream) != cudaSuccess) return DEC_ERR_CUDA;
+  if (launch_topk(h, parts, router_ksplit(H), M, E, k, idx, w, scores, stream) != cudaSuccess) return DEC_ERR_CUDA;
+  return DEC_OK;
+}
+
+// ---------------------------------------------------------------- experts
+dec_status moe_experts_workspace_size(const dec_handle* h, int M, int k, int E, int H, int I, size_t* bytes) {
+  if (h == nullptr || bytes == nullptr || !moe_shape_ok(M, k, E, H, I)) return DEC_ERR_INVALID_ARG;
+  Carver c(nullptr);
+  MoeWs w;
+  carve_moe(c, h, M, k, E, H, I, 0, &w);
+  *bytes = c.used;
+  return DEC_OK;
+}
+
+dec_status moe_experts(dec_handle* h, const dec_bf16* x, const int32_t* idx, const float* w, int M, int k,
+                       const dec_bf16* Wg, const dec_bf16* Wu, const dec_bf16* Wd, int E, int H, int I,
+                       const dec_bf16* Wg_s, const dec_bf16* Wu_s, const dec_bf16* Wd_s, const dec_bf16* residual,
+                       dec_bf16* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (h == nullptr || x == nullptr || idx == nullptr || w == nullptr || Wg == nullptr || Wu == nullptr ||
+      Wd == nullptr || out == nullptr)
+    return DEC_ERR_INVALID_ARG;
+  const bool any_s = Wg_s || Wu_s || Wd_s, all_s = Wg_s && Wu_s && Wd_s;
+  if (any_s && !all_s) return DEC_ERR_INVALID_ARG;
+  for (const void* p : {(const void*)x, (const void*)idx, (const void*)w, (const void*)Wg, (const void*)Wu,
+                        (const void*)Wd, (const void*)Wg_s, (const void*)Wu_s, (const void*)Wd_s,
+                        (const void*)residual, (const void*)out, (const void*)ws})
+    if (p != nullptr && !al16(p)) return DEC_ERR_INVALID_ARG;
+  if (!moe_shape_ok(M, k, E, H, I)) return DEC_ERR_INVALID_ARG;
+  if (out == x) return DEC_ERR_INVALID_ARG;
+  size_t need = 0;
+  moe_experts_workspace_size(h, M, k, E, H, I, &need);
+  if (ws == nullptr || ws_bytes < need) return DEC_ERR_INVALID_ARG;
+  Carver c(ws);
+  MoeWs mw;
+  carve_moe(c, h, M, k, E, H, I, 0, &mw);
+  return moe_impl(h, x, idx, w, M, k, Wg, Wu, Wd, E, H, I, Wg_s, Wu_s, Wd_s, residual, out, mw, stream);
+}
+
+// ---------------------------------------------------------------- decode layer
+dec_status decode_layer_workspace_size(const dec_handle* h, const dec_layer_weights* Wt, int M, size_t* bytes) {
+  if (h == nullptr || bytes == nullptr || !layer_ok(Wt, M)) return DEC_ERR_INVALID_ARG;
+  Carver c(nullptr);
+  LayerWs w;
+  carve_layer(c, h, Wt, M, &w);
+  *bytes = c.used;
+  return DEC_OK;
+}
+
+dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hidden, int M,
+                        const dec_layer_trace* trace, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (h == nullptr || Wt == nullptr || hidden == nullptr || !layer_ok(Wt, M)) return DEC_ERR_INVALID_ARG;
+  const dec_layer_weights& L = *Wt;
+  if (!L.gamma1 || !L.W_in || !L.W_o || !L.gamma2 || !L.W_r || !L.Wg || !L.Wu || !L.Wd) return DEC_ERR_INVALID_ARG;
+  const bool any_s = L.Wg_s || L.Wu_s || L.Wd_s, all_s = L.Wg_s && L.Wu_s && L.Wd_s;
+  if (any_s && !all_s) return DEC_ERR_INVALID_ARG;
+  for (const void* p : {(const void*)hidden, (const void*)L.gamma1, (const void*)L.W_in, (const void*)L.W_o,
+                        (const void*)L.gamma2, (const void*)L.W_r, (const void*)L.Wg, (const void*)L.Wu,
+                        (const void*)L.Wd, (const void*)L.Wg_s, (const void*)L.Wu_s, (const void*)L.Wd_s,
+                        (const void*)L.prefetch_next, (const void*)ws})
+    if (p != nullptr && !al16(p)) return DEC_ERR_INVALID_ARG;
+  if (L.prefetch_bytes % 16 != 0 || (L.prefetch_bytes && !L.prefetch_next) || !(L.eps >= 0.f))
+    return DEC_ERR_INVALID_ARG;
+  if (trace) {
+    for (const void* p : {(const void*)trace->h1, (const void*)trace->idx, (const void*)trace->w,
+                          (const void*)trace->scores})
+      if (p != nullptr && !al16(p)) return DEC_ERR_INVALID_ARG;
+  }
+  size_t need = 0;
+  decode_layer_workspace_size(h, Wt, M, &need);
+  if (ws == nullptr || ws_bytes < need) return DEC_ERR_INVALID_ARG;
+  Carver c(ws);
+  LayerWs w;
+  carve_layer(c, h, Wt, M, &w);
+  uint16_t* h1 = (trace && trace->h1) ? trace->h1 : w.h1;
+  int32_t* idx = (trace && trace->idx) ? trace->idx : w.idx;
+  float* wt = (trace && trace->w) ? trace->w : w.w;
+  float* scores = trace ? trace->scores : nullptr;
+  const int H = L.H;
+
+  if (launch_rmsnorm(h, hidden, L.gamma1, w.a, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
+  dec_status st = linear_impl(h, w.a, H, L.W_in, nullptr, w.yin, M, L.N_in, H, w.moe.r0, s);
+  if (st != DEC_OK) return st;
+  st = linear_impl(h, w.yin, L.N_in, L.W_o, hidden, h1, M, H, L.K_out, w.moe.r0, s);
+  if (st != DEC_OK) return st;
+  if (launch_rmsnorm(h, h1, L.gamma2, w.b, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
+  const bool pf = L.prefetch_next != nullptr && L.prefetch_bytes > 0;
+  if (pf) {
+    DEC_CUDA(cudaEventRecord(h->ev_pf_fork, s));
+    DEC_CUDA(cudaStreamWaitEvent(h->pf, h->ev_pf_fork, 0));
+    DEC_CUDA(launch_prefetch(h, L.prefetch_next, L.prefetch_bytes, 16, h->pf));
+    DEC_CUDA(cudaEventRecord(h->ev_pf_join, h->pf));
+  }
+  // The router / top-k phase is latency-bound; the shared expert (forked in
+  // moe_impl) and the prefetch stream use the idle bandwidth meanwhile.
+  if (launch_router(h, w.b, L.W_r, M, H, L.E, w.parts, s) != cudaSuccess) return DEC_ERR_CUDA;
+  if (launch_topk(h, w.parts, router_ksplit(H), M, L.E, L.k, idx, wt, scores, s) != cudaSuccess)
+    return DEC_ERR_CUDA;
+  st = moe_impl(h, w.b, idx, wt, M, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, h1, hidden, w.moe, s);
+  if (st != DEC_OK) return st;
+  if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
+  return DEC_OK;
+}
+
+dec_status dec_prefetch_l2(dec_handle* h, const void* ptr, size_t bytes, cudaStream_t stream) {
+  if (h == nullptr || (ptr == nullptr && bytes) || !al16(ptr) || bytes % 16 != 0) return DEC_ERR_INVALID_ARG;
+  return launch_prefetch(h, ptr, bytes, 16, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- test hooks
+dec_status dec_test_wait_timeout(dec_handle* h, cudaStream_t stream) {
+  if (h == nullptr) return DEC_ERR_INVALID_ARG;
+  return launch_wait_timeout_probe(h, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
+}
+
+dec_status dec_test_delayed_copy(dec_handle* h, void* dst, const void* src, size_t bytes, uint64_t delay_ns,
+                                 cudaStream_t stream) {
+  if (h == nullptr || dst == nullptr || src == nullptr || !al16(dst) || !al16(src) || bytes % 16 != 0 ||
+      delay_ns > 1000000000ull)
+    return DEC_ERR_INVALID_ARG;
+  return launch_delayed_copy(h, dst, src, bytes, delay_ns, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,145 @@
+// Small-matrix projection kernel for batch 1..2 (up to 4 when forced).
+//
+// Kimi K3 article, Part 1 §1 "Ajustar las formas" (and the aihirek.info
+// summary): at batch 1-2 the attention projections use specialised
+// small-matrix kernels. With one or two tokens every weight byte feeds one or
+// two FMAs, so the kernel is a pure weight stream and CUDA cores suffice.
+//
+// Layout of the work: the N weight rows are divided into one contiguous,
+// equal range per CTA (two 256-thread CTAs per SM), so every SM streams the
+// same bytes. Inside a CTA all 256 threads share each row: thread t owns the
+// 16-byte column vectors t, t+256, ... of every row, holds the matching
+// activation vectors in registers for the whole kernel, and streams weight
+// vectors with 128-bit, L1-bypassing, evict-first loads. RB rows are loaded
+// per step and the next step's loads are issued before the current step's
+// FMAs (8-16 loads in flight per thread). Per-row partial sums are reduced
+// with warp shuffles, then across the eight warps through shared memory, in a
+// fixed order.
+//
+// The first rows' weight loads are issued before griddepcontrol.wait, so they
+// overlap the previous kernel's tail; activations and the residual are read
+// only after it.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dec {
+
+constexpr int kGemvThreads = 256;
+
+template <int M, int VPT>
+__global__ void __launch_bounds__(kGemvThreads, 2)
+    gemv_kernel(const uint16_t* __restrict__ x, long long ldx, const uint16_t* __restrict__ W,
+                const uint16_t* __restrict__ res, long long ldr, uint16_t* __restrict__ y, long long ldy, int N,
+                int K) {
+  constexpr int RB = (8 / VPT) > 0 ? (8 / VPT) : 1;  // rows per step
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int K8 = K >> 3;
+  const long long G = gridDim.x;
+  const int r0 = (int)((long long)blockIdx.x * N / G);
+  const int r1 = (int)((long long)(blockIdx.x + 1) * N / G);
+  __shared__ float red[2][kGemvThreads / 32][RB * M];
+  const uint64_t pol = policy_evict_first();
+  pdl_trigger();
+
+  uint4 wa[RB][VPT];
+  auto load_rows = [&](uint4(&w)[RB][VPT], int rb) {
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = t + kGemvThreads * i;
+        const int rr = rb + r;
+        if (rr < r1 && v < K8)
+          w[r][i] = ld_stream(W + (size_t)rr * K + (size_t)v * 8, pol);
+        else
+          w[r][i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  if (r0 < r1) load_rows(wa, r0);
+
+  pdl_wait();
+  uint4 xr[M][VPT];
+#pragma unroll
+  for (int m = 0; m < M; ++m)
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = t + kGemvThreads * i;
+      xr[m][i] = (v < K8) ? *reinterpret_cast<const uint4*>(x + (size_t)m * ldx + (size_t)v * 8)
+                          : make_uint4(0, 0, 0, 0);
+    }
+
+  int buf = 0;
+  for (int rb = r0; rb < r1; rb += RB) {
+    uint4 wb[RB][VPT];
+    const bool more = rb + RB < r1;
+    if (more) load_rows(wb, rb + RB);
+    float acc[RB][M];
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) a = dot8(wa[r][i], xr[m][i], a);
+        acc[r][m] = a;
+      }
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], o);
+    if (lane == 0) {
+#pragma unroll
+      for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int m = 0; m < M; ++m) red[buf][warp][r * M + m] = acc[r][m];
+    }
+    __syncthreads();
+    if (t < RB * M) {
+      const int r = t / M, m = t % M, row = rb + r;
+      if (row < r1) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kGemvThreads / 32; ++w) s += red[buf][w][t];
+        if (res != nullptr) s += bf2f(res[(size_t)m * ldr + row]);
+        y[(size_t)m * ldy + row] = f2bf(s);
+      }
+    }
+    buf ^= 1;
+    if (more) {
+#pragma unroll
+      for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) wa[r][i] = wb[r][i];
+    }
+  }
+}
+
+bool gemv_supported(int M, int K) { return M >= 1 && M <= 4 && K >= 8 && K % 8 == 0 && K <= 8 * 8 * kGemvThreads; }
+
+template <int M>
+static cudaError_t gemv_m(dec_handle* h, const uint16_t* x, long long ldx, const uint16_t* W, const uint16_t* res,
+                          long long ldr, uint16_t* y, long long ldy, int N, int K, cudaStream_t s) {
+  const int K8 = K / 8;
+  const int grid = (int)std::min<long long>((long long)N, 2LL * h->sms);
+  const dim3 g(grid > 0 ? grid : 1), b(kGemvThreads);
+  if (K8 <= kGemvThreads) return launch_k(h, gemv_kernel<M, 1>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K);
+  if (K8 <= 2 * kGemvThreads) return launch_k(h, gemv_kernel<M, 2>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K);
+  if (K8 <= 4 * kGemvThreads) return launch_k(h, gemv_kernel<M, 4>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K);
+  return launch_k(h, gemv_kernel<M, 8>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K);
+}
+
+cudaError_t launch_gemv(dec_handle* h, const uint16_t* x, long long ldx, const uint16_t* W, const uint16_t* res,
+                        long long ldr, uint16_t* y, long long ldy, int M, int N, int K, cudaStream_t s) {
+  switch (M) {
+    case 1: return gemv_m<1>(h, x, ldx, W, res, ldr, y, ldy, N, K, s);
+    case 2: return gemv_m<2>(h, x, ldx, W, res, ldr, y, ldy, N, K, s);
+    case 3: return gemv_m<3>(h, x, ldx, W, res, ldr, y, ldy, N, K, s);
+    case 4: return gemv_m<4>(h, x, ldx, W, res, ldr, y, ldy, N, K, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dec

@@ -1,0 +1,116 @@
+// Internal interfaces between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/moe_decode.h"
+
+struct dec_handle {
+  int device = 0;
+  int sms = 0;
+  cudaStream_t side = nullptr;      // shared expert
+  cudaStream_t pf = nullptr;        // L2 prefetch
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_pf_fork = nullptr, ev_pf_join = nullptr;
+  int* d_err = nullptr;             // device error word
+  uint64_t wait_ns = 500ull * 1000 * 1000;
+  int pdl = 1;
+  int force_variant = 0;
+  int last_variant = 0;
+  int shared_ctas = 0;              // CTAs for the shared expert's kernels (0 = default)
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+};
+
+namespace dec {
+
+enum EpiKind { EPI_LINEAR = 0, EPI_SWIGLU = 1, EPI_F32 = 2 };
+
+constexpr int kTileN = 128;   // weight rows per tile (UMMA M)
+constexpr int kBlockK = 64;   // reduction elements per k-block (one 128-byte swizzle row)
+constexpr int kMaxCols = 64;  // tokens per problem (UMMA N up to 64)
+constexpr int kEngineThreads = 192;
+
+// Bytes of one engine workspace region (split-K partials + per-tile counters).
+size_t engine_ws_bytes(int grid, int nacc, long long max_tiles);
+int engine_grid(const dec_handle* h);
+
+// Layout of the routing table written by the route-table kernel (int32 words).
+struct TableLayout {
+  int E, n;  // experts, entries (M * k)
+  __host__ __device__ TableLayout(int E_, int n_) : E(E_), n(n_) {}
+  __host__ __device__ int U() const { return 0; }
+  __host__ __device__ int expert() const { return 1; }
+  __host__ __device__ int offset() const { return 1 + E; }
+  __host__ __device__ int count() const { return 1 + 2 * E; }
+  __host__ __device__ int slot_token() const { return 1 + 3 * E; }
+  __host__ __device__ int entry_slot() const { return 1 + 3 * E + n; }
+  __host__ __device__ int words() const { return 1 + 3 * E + 2 * n; }
+};
+
+struct EngineLaunch {
+  int epi = EPI_LINEAR;
+  const uint16_t* A = nullptr;   // weights [a_rows][K]
+  long long a_rows = 0;
+  const uint16_t* A2 = nullptr;  // second weight bank for EPI_SWIGLU (up), same shape
+  const uint16_t* B = nullptr;   // activations [b_rows][K], row stride ldb elements
+  long long b_rows = 0, ldb = 0;
+  int K = 0;
+  int N = 0;                     // weight rows per problem
+  long long a_rows_per_prob = 0; // row distance between problems in A (0 for one problem)
+  int count = 0;                 // tokens (dense mode)
+  const int* table = nullptr;    // routing table (grouped mode) or null (dense mode, one problem)
+  int E = 0;                     // table layout
+  int n_entries = 0;
+  void* out = nullptr;
+  long long ldo = 0;
+  const uint16_t* res = nullptr;
+  long long ldr = 0;
+  float* partials = nullptr;
+  int* counters = nullptr;
+  int grid = 0;                  // CTAs; 0 = all SMs
+};
+
+cudaError_t launch_engine(dec_handle* h, const EngineLaunch& L, cudaStream_t s);
+
+cudaError_t launch_gemv(dec_handle* h, const uint16_t* x, long long ldx, const uint16_t* W, const uint16_t* res,
+                        long long ldr, uint16_t* y, long long ldy, int M, int N, int K, cudaStream_t s);
+bool gemv_supported(int M, int K);
+
+cudaError_t launch_rmsnorm(dec_handle* h, const uint16_t* x, const uint16_t* gamma, uint16_t* y, int M, int H,
+                           float eps, cudaStream_t s);
+
+int router_ksplit(int H);
+cudaError_t launch_router(dec_handle* h, const uint16_t* x, const float* Wr, int M, int H, int E, float* parts,
+                          cudaStream_t s);
+cudaError_t launch_topk(dec_handle* h, const float* parts, int ks, int M, int E, int k, int32_t* idx, float* w,
+                        float* scores, cudaStream_t s);
+cudaError_t launch_route_table(dec_handle* h, const int32_t* idx, int M, int k, int E, const uint16_t* x, int H,
+                               int* table, uint16_t* xs, cudaStream_t s);
+cudaError_t launch_combine(dec_handle* h, const float* y, const int* table, const float* w, int M, int k, int E,
+                           const float* ys, const uint16_t* res, uint16_t* out, int H, cudaStream_t s);
+cudaError_t launch_prefetch(dec_handle* h, const void* p, size_t bytes, int ctas, cudaStream_t s);
+cudaError_t launch_wait_timeout_probe(dec_handle* h, cudaStream_t s);
+cudaError_t launch_delayed_copy(dec_handle* h, void* dst, const void* src, size_t bytes, uint64_t delay_ns,
+                                cudaStream_t s);
+
+// Launch with the handle's programmatic-dependent-launch setting.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(const dec_handle* h, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = h->pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+}  // namespace dec

@@ -1,0 +1,323 @@
+// MoE routing: router scores, top-k, the per-expert routing table (with the
+// gather of each expert's tokens into contiguous rows), and the final
+// weighted combine.
+//
+// Kimi K3 article, Part 1 §3 "Mejorar la programación de MoE": router scores
+// are computed before the experts run, and the expert schedule decides which
+// weights are read. The rule (sigmoid scores of fp32 router weights, top-k by
+// score with ties to the lower id, weights renormalised over the selected k)
+// is the workload's; the pages give no formula.
+#include <algorithm>
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dec {
+
+constexpr int kRouterChunk = 1024;  // reduction elements per split (one CTA column)
+constexpr int kRouterRows = 8;      // router rows per CTA, one per warp
+constexpr int kRouterTok = 16;      // tokens staged in shared memory per pass
+
+int router_ksplit(int H) { return (H + kRouterChunk - 1) / kRouterChunk; }
+
+// parts[ks][t][e] = sum over the ks-th chunk of H of x[t][h] * Wr[e][h] (fp32).
+// Grid: (ceil(E / 8), ksplit). Each warp owns one router row and keeps its
+// chunk of fp32 weights in registers (loaded before the dependency wait); the
+// tokens' bf16 activations pass through shared memory sixteen at a time.
+__global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict__ x, const float* __restrict__ Wr,
+                                                     int M, int H, int E, float* __restrict__ parts) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kRouterRows + warp;
+  const int ks = blockIdx.y;
+  const int k0 = ks * kRouterChunk;
+  const int kn = min(kRouterChunk, H - k0);
+  __shared__ __align__(16) uint16_t xs[kRouterTok][kRouterChunk];
+  pdl_trigger();
+  float4 wv[kRouterChunk / 128];
+#pragma unroll
+  for (int i = 0; i < kRouterChunk / 128; ++i) {
+    const int kk = 4 * (lane + 32 * i);
+    wv[i] = (e < E && kk < kn) ? __ldg(reinterpret_cast<const float4*>(Wr + (size_t)e * H + k0 + kk))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  pdl_wait();
+  const int kv = kn >> 3;
+  for (int t0 = 0; t0 < M; t0 += kRouterTok) {
+    const int nt = min(kRouterTok, M - t0);
+    __syncthreads();
+    for (int q = threadIdx.x; q < nt * kv; q += blockDim.x) {
+      const int tt = q / kv, v = q - tt * kv;
+      *reinterpret_cast<uint4*>(&xs[tt][v * 8]) =
+          *reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + k0 + v * 8);
+    }
+    __syncthreads();
+    float acc[kRouterTok];
+#pragma unroll
+    for (int tt = 0; tt < kRouterTok; ++tt) acc[tt] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRouterChunk / 128; ++i) {
+      const int kk = 4 * (lane + 32 * i);
+      if (kk < kn) {
+#pragma unroll
+        for (int tt = 0; tt < kRouterTok; ++tt) {
+          if (tt < nt) {
+            const uint2 xv = *reinterpret_cast<const uint2*>(&xs[tt][kk]);
+            float a = acc[tt];
+            a = fmaf(wv[i].x, bf_lo(xv.x), a);
+            a = fmaf(wv[i].y, bf_hi(xv.x), a);
+            a = fmaf(wv[i].z, bf_lo(xv.y), a);
+            a = fmaf(wv[i].w, bf_hi(xv.y), a);
+            acc[tt] = a;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < kRouterTok; ++tt)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[tt] += __shfl_xor_sync(0xffffffffu, acc[tt], o);
+    if (lane == 0 && e < E) {
+#pragma unroll
+      for (int tt = 0; tt < kRouterTok; ++tt)
+        if (tt < nt) parts[((size_t)ks * M + t0 + tt) * E + e] = acc[tt];
+    }
+  }
+}
+
+// One CTA per token: logits = sum of the split partials in split order,
+// s = 1 / (1 + exp(-logit)), then k rounds of a block-wide arg-max
+// (score descending, expert id ascending) and renormalisation.
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ parts, int ks, int M, int E, int k,
+                                                   int32_t* __restrict__ idx, float* __restrict__ w,
+                                                   float* __restrict__ scores) {
+  const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ float sv[1024];
+  __shared__ float red_v[8];
+  __shared__ int red_i[8];
+  __shared__ float wsel[16];
+  __shared__ int isel[16];
+  pdl_trigger();
+  pdl_wait();
+  for (int e = tid; e < E; e += blockDim.x) {
+    float z = 0.f;
+    for (int s = 0; s < ks; ++s) z += parts[((size_t)s * M + t) * E + e];
+    const float sc = 1.0f / (1.0f + expf(-z));
+    sv[e] = sc;
+    if (scores != nullptr) scores[(size_t)t * E + e] = sc;
+  }
+  __syncthreads();
+  for (int r = 0; r < k; ++r) {
+    float bv = -FLT_MAX;
+    int bi = INT_MAX;
+    for (int e = tid; e < E; e += blockDim.x) {
+      const float v = sv[e];
+      if (v > bv || (v == bv && e < bi)) {
+        bv = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      red_v[warp] = bv;
+      red_i[warp] = bi;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float v = red_v[0];
+      int i = red_i[0];
+      for (int q = 1; q < (int)(blockDim.x >> 5); ++q)
+        if (red_v[q] > v || (red_v[q] == v && red_i[q] < i)) {
+          v = red_v[q];
+          i = red_i[q];
+        }
+      wsel[r] = v;
+      isel[r] = i;
+      sv[i] = -FLT_MAX;  // taken
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    float sum = 0.f;
+    for (int r = 0; r < k; ++r) sum += wsel[r];
+    for (int r = 0; r < k; ++r) {
+      idx[(size_t)t * k + r] = isel[r];
+      w[(size_t)t * k + r] = wsel[r] / sum;
+    }
+  }
+}
+
+// Routing table from idx[M][k]: per active expert (ascending id) its first
+// slot and token count; slots are ordered by (expert, token, j). Every CTA
+// rebuilds the table in shared memory (n = M*k <= 1024 entries), CTA 0 writes
+// it out, and all CTAs gather x rows into the slot-ordered buffer xs so that
+// each expert's tokens are contiguous rows for the TMA loads of the experts.
+__global__ void __launch_bounds__(256) route_table_kernel(const int32_t* __restrict__ idx, int M, int k, int E,
+                                                          const uint16_t* __restrict__ x, int H, int* __restrict__ table,
+                                                          uint16_t* __restrict__ xs) {
+  extern __shared__ int sm[];
+  const int n = M * k;
+  int* cnt = sm;
+  int* off = cnt + E;
+  int* run = off + E;
+  int* eidx = run + E;
+  int* stok = eidx + n;
+  int* eslot = stok + n;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const TableLayout L(E, n);
+  pdl_trigger();
+  pdl_wait();
+  for (int e = tid; e < E; e += blockDim.x) {
+    cnt[e] = 0;
+    run[e] = 0;
+  }
+  for (int i = tid; i < n; i += blockDim.x) eidx[i] = idx[i];
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) atomicAdd(&cnt[eidx[i]], 1);
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int s_sum = 0, a_sum = 0;
+    for (int e = e0; e < e1; ++e) {
+      s_sum += cnt[e];
+      a_sum += cnt[e] > 0 ? 1 : 0;
+    }
+    int s_inc = s_sum, a_inc = a_sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int vs = __shfl_up_sync(0xffffffffu, s_inc, o);
+      const int va = __shfl_up_sync(0xffffffffu, a_inc, o);
+      if (lane >= o) {
+        s_inc += vs;
+        a_inc += va;
+      }
+    }
+    int s_run = s_inc - s_sum, a_run = a_inc - a_sum;
+    for (int e = e0; e < e1; ++e) {
+      off[e] = s_run;
+      if (cnt[e] > 0) {
+        if (blockIdx.x == 0) {
+          table[L.expert() + a_run] = e;
+          table[L.offset() + a_run] = s_run;
+          table[L.count() + a_run] = cnt[e];
+        }
+        ++a_run;
+      }
+      s_run += cnt[e];
+    }
+    if (lane == 31 && blockIdx.x == 0) table[L.U()] = a_inc;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      const bool valid = i < n;
+      const int e = valid ? eidx[i] : -1 - lane;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      if (valid) {
+        const int slot = off[e] + run[e] + rank;
+        eslot[i] = slot;
+        stok[slot] = i / k;
+      }
+      __syncwarp();
+      if (valid && rank == 0) run[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < n; i += blockDim.x) {
+      table[L.slot_token() + i] = stok[i];
+      table[L.entry_slot() + i] = eslot[i];
+    }
+  }
+  const int H8 = H >> 3;
+  const long long total = (long long)n * H8;
+  for (long long q = (long long)blockIdx.x * blockDim.x + tid; q < total; q += (long long)gridDim.x * blockDim.x) {
+    const int s = (int)(q / H8), v = (int)(q - (long long)s * H8);
+    *reinterpret_cast<uint4*>(xs + (size_t)s * H + (size_t)v * 8) =
+        *reinterpret_cast<const uint4*>(x + (size_t)stok[s] * H + (size_t)v * 8);
+  }
+}
+
+// out[t][:] = bf16( sum_j w[t][j] * y[slot(t, j)][:]  (+ ys[t][:])  (+ res[t][:]) ), fp32 sums in that order.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const int* __restrict__ table,
+                                                      const float* __restrict__ w, int M, int k, int E,
+                                                      const float* __restrict__ ys, const uint16_t* __restrict__ res,
+                                                      uint16_t* __restrict__ out, int H) {
+  const int t = blockIdx.y;
+  const int n0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  pdl_trigger();
+  pdl_wait();
+  if (n0 >= H) return;
+  const TableLayout L(E, M * k);
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int slot = table[L.entry_slot() + t * k + j];
+    const float wj = w[(size_t)t * k + j];
+    const float4 v = *reinterpret_cast<const float4*>(y + (size_t)slot * H + n0);
+    a0 = fmaf(wj, v.x, a0);
+    a1 = fmaf(wj, v.y, a1);
+    a2 = fmaf(wj, v.z, a2);
+    a3 = fmaf(wj, v.w, a3);
+  }
+  if (ys != nullptr) {
+    const float4 v = *reinterpret_cast<const float4*>(ys + (size_t)t * H + n0);
+    a0 += v.x;
+    a1 += v.y;
+    a2 += v.z;
+    a3 += v.w;
+  }
+  if (res != nullptr) {
+    const uint2 r = *reinterpret_cast<const uint2*>(res + (size_t)t * H + n0);
+    a0 += bf_lo(r.x);
+    a1 += bf_hi(r.x);
+    a2 += bf_lo(r.y);
+    a3 += bf_hi(r.y);
+  }
+  uint2 o;
+  o.x = (uint32_t)f2bf(a0) | ((uint32_t)f2bf(a1) << 16);
+  o.y = (uint32_t)f2bf(a2) | ((uint32_t)f2bf(a3) << 16);
+  *reinterpret_cast<uint2*>(out + (size_t)t * H + n0) = o;
+}
+
+// ---------------------------------------------------------------------------- launchers
+cudaError_t launch_router(dec_handle* h, const uint16_t* x, const float* Wr, int M, int H, int E, float* parts,
+                          cudaStream_t s) {
+  const dim3 grid((E + kRouterRows - 1) / kRouterRows, router_ksplit(H));
+  return launch_k(h, router_kernel, grid, dim3(256), 0, s, x, Wr, M, H, E, parts);
+}
+
+cudaError_t launch_topk(dec_handle* h, const float* parts, int ks, int M, int E, int k, int32_t* idx, float* w,
+                        float* scores, cudaStream_t s) {
+  return launch_k(h, topk_kernel, dim3(M), dim3(256), 0, s, parts, ks, M, E, k, idx, w, scores);
+}
+
+cudaError_t launch_route_table(dec_handle* h, const int32_t* idx, int M, int k, int E, const uint16_t* x, int H,
+                               int* table, uint16_t* xs, cudaStream_t s) {
+  const int n = M * k;
+  const long long vec = (long long)n * (H / 8);
+  int grid = (int)std::min<long long>((vec + 255) / 256, (long long)h->sms);
+  if (grid < 1) grid = 1;
+  const size_t smem = (size_t)(3 * E + 3 * n) * sizeof(int);
+  return launch_k(h, route_table_kernel, dim3(grid), dim3(256), smem, s, idx, M, k, E, x, H, table, xs);
+}
+
+cudaError_t launch_combine(dec_handle* h, const float* y, const int* table, const float* w, int M, int k, int E,
+                           const float* ys, const uint16_t* res, uint16_t* out, int H, cudaStream_t s) {
+  const dim3 grid((H / 4 + 255) / 256, M);
+  return launch_k(h, combine_kernel, grid, dim3(256), 0, s, y, table, w, M, k, E, ys, res, out, H);
+}
+
+}  // namespace dec

@@ -1,0 +1,445 @@
+// Split-K tcgen05 engine for weight-streaming skinny GEMMs (batch 3..64 and
+// the experts).
+//
+// Kimi K3 article, Part 1 §1 "Ajustar las formas": at batch sizes above two
+// the projection is a split-K kernel that shares the matrix product among
+// more GPU workers. Here a "worker" is an SM: the weight matrix is cut into
+// tiles of 128 rows, each tile into k-blocks of 64 columns, and the sequence
+// of all (tile, k-block) pairs is divided into one contiguous, equal-length
+// range per CTA (one persistent CTA per SM). Every SM therefore streams the
+// same number of weight bytes; a tile that straddles two ranges is finished by
+// whichever of its CTAs arrives last, which adds the fp32 partials of all
+// pieces in k order (deterministic, no float atomics).
+//
+// Per CTA: warp 0 issues TMA loads of weight tiles (128 x 64 bf16, 128-byte
+// swizzle, evict-first) and activation tiles (16-row boxes) into an smem ring;
+// warp 1 issues tcgen05.mma (M = 128 weight rows, N = 16..64 tokens, K = 16)
+// into a double-buffered TMEM accumulator; warps 2-5 read the accumulator
+// with tcgen05.ld and run the epilogue (bf16 out + residual, SwiGLU, or fp32).
+// The weights are the MMA's M operand ("swap AB"), so a batch of one to
+// sixty-four tokens fills the N dimension and no weight byte is wasted.
+//
+// Problems: one dense matrix, or a group of experts read from a device-side
+// routing table (expert id, first slot, token count); expert e's rows start at
+// e * a_rows_per_prob in a bank tensor that covers all experts.
+#include <algorithm>
+#include <cstdio>
+#include <utility>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dec {
+
+struct EngineParams {
+  int K, KB, N, tiles;
+  long long a_rows_per_prob;
+  int count;           // dense mode: tokens
+  const int* table;    // grouped mode: routing table
+  int E, n_entries;
+  void* out;
+  long long ldo;
+  const uint16_t* res;
+  long long ldr;
+  float* partials;
+  int slot_floats;     // floats per partial slot (nacc * 128 * cols)
+  int cols;            // columns per accumulator in a slot
+  int* counters;
+  int* err;
+  unsigned long long wait_ns;
+};
+
+template <int NA>
+struct EngineSmem {
+  static constexpr int kABytes = kTileN * kBlockK * 2;     // 16 KB weight tile
+  static constexpr int kBBytes = kMaxCols * kBlockK * 2;    // 8 KB activation tile (up to 64 rows)
+  static constexpr int kStageBytes = NA * kABytes + kBBytes;
+  static constexpr int kStages = (NA == 1) ? 8 : 5;
+  static constexpr int kBarOff = kStages * kStageBytes;
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kTotal = kMiscOff + 64 + 1024;       // + alignment slack
+  static constexpr uint32_t kTmemCols = NA * kMaxCols * 2;  // two accumulator buffers
+};
+
+__device__ __forceinline__ long long range_start(long long c, long long W, long long G) { return c * W / G; }
+// CTA whose range holds k-block index j.
+__device__ __forceinline__ long long cta_of(long long j, long long W, long long G) { return ((j + 1) * G - 1) / W; }
+
+struct Prob {
+  int e, off, cnt;
+};
+
+__device__ __forceinline__ Prob prob_info(const EngineParams& P, int p) {
+  if (P.table == nullptr) return Prob{0, 0, P.count};
+  const TableLayout L(P.E, P.n_entries);
+  return Prob{P.table[L.expert() + p], P.table[L.offset() + p], P.table[L.count() + p]};
+}
+
+__device__ __forceinline__ long long total_kblocks(const EngineParams& P) {
+  const long long nprob = (P.table == nullptr) ? 1 : P.table[0];
+  return nprob * P.tiles * P.KB;
+}
+
+// Bounded wait that ignores the abort flag (used when draining in-flight work).
+static __device__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err, uint64_t limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) == 0 && globaltimer() - t0 > limit) {
+      atomicOr(err, DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kEngineThreads, 1)
+    engine_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                  const __grid_constant__ CUtensorMap tmB, const EngineParams P) {
+  constexpr int NA = (EPI == EPI_SWIGLU) ? 2 : 1;
+  using S = EngineSmem<NA>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  uint64_t* empty = full + S::kStages;
+  uint64_t* tfull = empty + S::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kMiscOff + 4);
+  volatile int* s_last = reinterpret_cast<volatile int*>(smem + S::kMiscOff + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long G = gridDim.x, c = blockIdx.x;
+  const int KB = P.KB, tiles = P.tiles;
+
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    *s_last = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tmap_prefetch(&tmA);
+    if (NA == 2) tmap_prefetch(&tmA2);
+    tmap_prefetch(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, S::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{abort_flag, P.err, P.wait_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();  // weights: read once
+      const uint64_t pol_x = policy_evict_last();   // activations: read by every CTA
+      long long issued = 0;
+      auto load_A = [&](int s, int tau, int kb, long long a_row) {
+        uint8_t* st = smem + s * S::kStageBytes;
+        tma_load_2d(st, &tmA, &full[s], kb * kBlockK, (int)a_row, pol_w);
+        if (NA == 2) tma_load_2d(st + S::kABytes, &tmA2, &full[s], kb * kBlockK, (int)a_row, pol_w);
+      };
+      auto load_B = [&](int s, int kb, int row0, int nb) {
+        uint8_t* st = smem + s * S::kStageBytes + NA * S::kABytes;
+        for (int b = 0; b < nb; ++b) tma_load_2d(st + b * 2048, &tmB, &full[s], kb * kBlockK, row0 + 16 * b, pol_x);
+      };
+      if (P.table == nullptr) {
+        // Dense: the k-block range is known before the dependency wait, so the
+        // first ring's worth of static weights streams in while the previous
+        // kernel drains. Activations are loaded only after pdl_wait().
+        const long long W = (long long)tiles * KB;
+        const long long j0 = range_start(c, W, G), j1 = range_start(c + 1, W, G);
+        const int nb = (P.count + 15) >> 4;
+        const uint32_t bytes = NA * S::kABytes + nb * 2048;
+        const long long npre = min(j1 - j0, (long long)S::kStages);
+        for (long long i = 0; i < npre; ++i) {
+          const long long j = j0 + i;
+          mbar_arrive_expect_tx(&full[i], bytes);
+          load_A((int)i, (int)(j / KB), (int)(j % KB), (j / KB) * kTileN);
+        }
+        pdl_wait();
+        for (long long i = 0; i < j1 - j0; ++i) {
+          const long long j = j0 + i;
+          const int s = (int)(i % S::kStages);
+          const uint32_t ph = (uint32_t)((i / S::kStages) & 1);
+          const int kb = (int)(j % KB);
+          if (i >= npre) {
+            if (!mbar_wait(&empty[s], ph ^ 1u, wc)) break;
+            mbar_arrive_expect_tx(&full[s], bytes);
+            load_A(s, (int)(j / KB), kb, (j / KB) * kTileN);
+          }
+          load_B(s, kb, 0, nb);
+          issued = i + 1;
+        }
+      } else {
+        pdl_wait();
+        const long long W = total_kblocks(P);
+        const long long j0 = range_start(c, W, G), j1 = range_start(c + 1, W, G);
+        for (long long i = 0; i < j1 - j0; ++i) {
+          const long long j = j0 + i;
+          const int s = (int)(i % S::kStages);
+          const uint32_t ph = (uint32_t)((i / S::kStages) & 1);
+          const int tau = (int)(j / KB), kb = (int)(j % KB);
+          const Prob pr = prob_info(P, tau / tiles);
+          const int nb = (pr.cnt + 15) >> 4;
+          if (!mbar_wait(&empty[s], ph ^ 1u, wc)) break;
+          mbar_arrive_expect_tx(&full[s], NA * S::kABytes + nb * 2048);
+          load_A(s, tau, kb, (long long)pr.e * P.a_rows_per_prob + (long long)(tau % tiles) * kTileN);
+          load_B(s, kb, pr.off, nb);
+          issued = i + 1;
+        }
+      }
+      // No copy may still be in flight when the CTA exits: wait for the last
+      // ring's worth of loads (all of them have landed on the normal path).
+      for (long long i = max(0LL, issued - S::kStages); i < issued; ++i)
+        mbar_wait_drain(&full[i % S::kStages], (uint32_t)((i / S::kStages) & 1), P.err, P.wait_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      pdl_wait();
+      const long long W = total_kblocks(P);
+      const long long j0 = range_start(c, W, G), j1 = range_start(c + 1, W, G);
+      uint32_t tphase[2] = {0, 0};
+      int buf = 0;
+      long long i = 0;
+      bool ok = true;
+      for (long long j = j0; ok && j < j1;) {
+        const int tau = (int)(j / KB), kb0 = (int)(j % KB);
+        const int kb1 = (int)min((long long)KB, kb0 + (j1 - j));
+        const Prob pr = prob_info(P, tau / tiles);
+        const uint32_t idesc = umma_idesc_bf16(kTileN, ((pr.cnt + 15) >> 4) * 16);
+        if (!mbar_wait(&tempty[buf], tphase[buf] ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + (uint32_t)(buf * NA * kMaxCols);
+        for (int kb = kb0; kb < kb1; ++kb, ++i) {
+          const int s = (int)(i % S::kStages);
+          if (!mbar_wait(&full[s], (uint32_t)((i / S::kStages) & 1), wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * S::kStageBytes);
+          const uint32_t b_addr = a_addr + NA * S::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 16; ++kk) {
+            const uint64_t bd = sw128_desc(b_addr + kk * 32);
+            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+            umma_bf16(d0, sw128_desc(a_addr + kk * 32), bd, idesc, acc);
+            if (NA == 2) umma_bf16(d0 + kMaxCols, sw128_desc(a_addr + S::kABytes + kk * 32), bd, idesc, acc);
+          }
+          umma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        umma_commit(&tfull[buf]);
+        tphase[buf] ^= 1u;
+        buf ^= 1;
+        j += kb1 - kb0;
+      }
+      // Every MMA issued above must complete before TMEM is released.
+      umma_commit(done);
+      mbar_wait_drain(done, 0, P.err, P.wait_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;              // TMEM lanes 32q..32q+31 are visible to this warp
+    const int row = q * 32 + lane;       // row within the 128-row tile
+    const int et = threadIdx.x - 64;     // 0..127
+    pdl_wait();
+    const long long W = total_kblocks(P);
+    const long long j0 = range_start(c, W, G), j1 = range_start(c + 1, W, G);
+    uint32_t tphase[2] = {0, 0};
+    int buf = 0;
+    uint16_t* out16 = reinterpret_cast<uint16_t*>(P.out);
+    float* out32 = reinterpret_cast<float*>(P.out);
+
+    auto emit = [&](const Prob& pr, int n, int jcol, float v0, float v1) {
+      const long long orow = (long long)pr.off + jcol;
+      if (EPI == EPI_LINEAR) {
+        float s = v0;
+        if (P.res != nullptr) s += bf2f(P.res[orow * P.ldr + n]);
+        out16[orow * P.ldo + n] = f2bf(s);
+      } else if (EPI == EPI_SWIGLU) {
+        const float g = v0;
+        out16[orow * P.ldo + n] = f2bf(g / (1.0f + expf(-g)) * v1);
+      } else {
+        out32[orow * P.ldo + n] = v0;
+      }
+    };
+
+    for (long long j = j0; j < j1;) {
+      const int tau = (int)(j / KB), kb0 = (int)(j % KB);
+      const int kb1 = (int)min((long long)KB, kb0 + (j1 - j));
+      const bool first_seg = (j == j0);
+      j += kb1 - kb0;
+      const bool got = mbar_wait(&tfull[buf], tphase[buf], wc);
+      if (!named_bar_and(1, 128, got)) break;  // leave together if any thread gave up
+      tc_fence_after();
+      const Prob pr = prob_info(P, tau / tiles);
+      const int n = (tau % tiles) * kTileN + row;
+      const bool valid_row = n < P.N;
+      const int nch = (pr.cnt + 15) >> 4;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NA * kMaxCols);
+      const bool whole = (kb0 == 0 && kb1 == KB);
+      float* slot = nullptr;
+      if (!whole) slot = P.partials + (size_t)(c * 2 + (first_seg ? 0 : 1)) * P.slot_floats;
+      for (int ch = 0; ch < nch; ++ch) {
+        float v0[16], v1[16];
+        tmem_ld16(taddr + ch * 16, v0);
+        if (NA == 2) tmem_ld16(taddr + kMaxCols + ch * 16, v1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int jc = ch * 16 + i;
+          if (jc < pr.cnt) {
+            if (whole) {
+              if (valid_row) emit(pr, n, jc, v0[i], NA == 2 ? v1[i] : 0.f);
+            } else {
+              slot[(size_t)jc * kTileN + row] = v0[i];
+              if (NA == 2) slot[(size_t)P.cols * kTileN + (size_t)jc * kTileN + row] = v1[i];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
+      tphase[buf] ^= 1u;
+      buf ^= 1;
+      if (whole) continue;
+
+      // Split tile: the last of its CTAs to finish adds all pieces in k order.
+      __threadfence();
+      named_bar_sync(1, 128);
+      const long long kfirst = (long long)tau * KB;
+      const long long c_first = cta_of(kfirst, W, G), c_last = cta_of(kfirst + KB - 1, W, G);
+      if (et == 0) {
+        int np = 0;
+        for (long long cc = c_first; cc <= c_last; ++cc)
+          np += (range_start(cc + 1, W, G) > range_start(cc, W, G)) ? 1 : 0;
+        const int old = atomicAdd(&P.counters[tau], 1);
+        *s_last = (old == np - 1) ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      if (*s_last) {
+        __threadfence();
+        for (int jc = 0; jc < pr.cnt; ++jc) {
+          float a0 = 0.f, a1 = 0.f;
+          for (long long cc = c_first; cc <= c_last; ++cc) {
+            const long long st = range_start(cc, W, G);
+            if (range_start(cc + 1, W, G) <= st) continue;  // empty range: no piece
+            const int which = (st >= kfirst) ? 0 : 1;
+            const float* ps = P.partials + (size_t)(cc * 2 + which) * P.slot_floats;
+            a0 += __ldcg(ps + (size_t)jc * kTileN + row);
+            if (NA == 2) a1 += __ldcg(ps + (size_t)P.cols * kTileN + (size_t)jc * kTileN + row);
+          }
+          if (valid_row) emit(pr, n, jc, a0, a1);
+        }
+        if (et == 0) P.counters[tau] = 0;  // leave the workspace reusable
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------- host side
+static bool encode_2d(const dec_handle* h, CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                      uint64_t row_stride_bytes, uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)kBlockK, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = h->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int engine_grid(const dec_handle* h) { return h->sms; }
+
+size_t engine_ws_bytes(int grid, int nacc, long long max_tiles) {
+  auto al = [](size_t b) { return (b + 255) & ~size_t(255); };
+  return al((size_t)2 * grid * nacc * kTileN * kMaxCols * sizeof(float)) + al((size_t)max_tiles * sizeof(int));
+}
+
+template <int EPI>
+static cudaError_t launch_epi(dec_handle* h, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
+                              const EngineParams& P, int grid, cudaStream_t s) {
+  constexpr int NA = (EPI == EPI_SWIGLU) ? 2 : 1;
+  static bool attr_set = false;  // per process; every device gets the same attribute
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(engine_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         EngineSmem<NA>::kTotal);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_k(h, engine_kernel<EPI>, dim3(grid), dim3(kEngineThreads), (size_t)EngineSmem<NA>::kTotal, s, ta,
+                  ta2, tb, P);
+}
+
+cudaError_t launch_engine(dec_handle* h, const EngineLaunch& L, cudaStream_t s) {
+  CUtensorMap ta, ta2, tb;
+  if (!encode_2d(h, &ta, L.A, (uint64_t)L.K, (uint64_t)L.a_rows, (uint64_t)L.K * 2, kTileN))
+    return cudaErrorInvalidValue;
+  if (L.epi == EPI_SWIGLU) {
+    if (!encode_2d(h, &ta2, L.A2, (uint64_t)L.K, (uint64_t)L.a_rows, (uint64_t)L.K * 2, kTileN))
+      return cudaErrorInvalidValue;
+  } else {
+    ta2 = ta;
+  }
+  if (!encode_2d(h, &tb, L.B, (uint64_t)L.K, (uint64_t)L.b_rows, (uint64_t)L.ldb * 2, 16))
+    return cudaErrorInvalidValue;
+  const int nacc = (L.epi == EPI_SWIGLU) ? 2 : 1;
+  EngineParams P;
+  P.K = L.K;
+  P.KB = (L.K + kBlockK - 1) / kBlockK;
+  P.N = L.N;
+  P.tiles = (L.N + kTileN - 1) / kTileN;
+  P.a_rows_per_prob = L.a_rows_per_prob;
+  P.count = L.count;
+  P.table = L.table;
+  P.E = L.E;
+  P.n_entries = L.n_entries;
+  P.out = L.out;
+  P.ldo = L.ldo;
+  P.res = L.res;
+  P.ldr = L.ldr;
+  P.partials = L.partials;
+  P.cols = kMaxCols;
+  P.slot_floats = nacc * kTileN * kMaxCols;
+  P.counters = L.counters;
+  P.err = h->d_err;
+  P.wait_ns = h->wait_ns;
+  int grid = L.grid > 0 ? L.grid : engine_grid(h);
+  if (L.table == nullptr) grid = (int)std::min<long long>(grid, (long long)P.tiles * P.KB);
+  if (grid < 1) grid = 1;
+  switch (L.epi) {
+    case EPI_LINEAR: return launch_epi<EPI_LINEAR>(h, ta, ta2, tb, P, grid, s);
+    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(h, ta, ta2, tb, P, grid, s);
+    default: return launch_epi<EPI_F32>(h, ta, ta2, tb, P, grid, s);
+  }
+}
+
+}  // namespace dec

@@ -59,6 +59,20 @@ def as_f64(a) -> np.ndarray:
     return a.astype(np.float64)
 
 
+def round_bf16(a) -> np.ndarray:
+    """Nearest-even rounding of float64 values to bfloat16, returned as float64.
+
+    v = q * 2^(e-8) with q an integer of at most 8 significant bits, chosen by
+    round-half-to-even (numpy rint) on the exactly scaled significand. Used
+    only where the workload stores an activation as bf16 between operations.
+    """
+    v = np.asarray(a, dtype=np.float64)
+    _, e = np.frexp(v)                      # v = m 2^e, 0.5 <= |m| < 1
+    e = np.maximum(e, -125)                 # below 2^-126: bf16 subnormal spacing
+    q = np.rint(np.ldexp(v, 8 - e))         # exact scaling, then round half to even
+    return np.ldexp(q, e - 8)
+
+
 # ----------------------------------------------------------------------------- dense steps
 def linear(x, W) -> np.ndarray:
     """y = x W^T: the decode projection, nn.Linear layout W[N, K].
@@ -187,7 +201,8 @@ def moe(x, idx, w, expert: ExpertFn, shared: Optional[Sequence] = None, residual
 
 # ----------------------------------------------------------------------------- decode layer
 def decode_layer(h, gamma1, W_in, W_o, gamma2, Wr, k: int, expert: ExpertFn, shared: Optional[Sequence],
-                 k_out: Optional[int] = None, eps: float = RMS_EPS, tokens: Optional[Sequence[int]] = None):
+                 k_out: Optional[int] = None, eps: float = RMS_EPS, tokens: Optional[Sequence[int]] = None,
+                 storage: str = "bf16"):
     """One decode layer: RMSNorm -> input projection -> out-projection + residual
     -> RMSNorm -> MoE (+ residual).
 
@@ -197,18 +212,28 @@ def decode_layer(h, gamma1, W_in, W_o, gamma2, Wr, k: int, expert: ExpertFn, sha
     out-projection) straight to the out-projection. The MoE block is pre-norm
     with its own residual: out = h1 + MoE(RMSNorm(h1)).
 
+    ``storage``: the layer's activations are bf16 tensors, so with "bf16"
+    (default) the output of each operation (a, y_in, h1, b) is rounded to bf16
+    before the next operation reads it; each operation itself is exact fp64.
+    This keeps the routing decision (an arg-max over scores) in the precision
+    the layer defines. "f64" rounds nothing.
+
     Returns a dict with the intermediates (a, y_in, h1, b, logits, scores,
-    idx, w) and the output ``out``; ``tokens`` limits all of it to some rows.
+    idx, w) and the output ``out`` (unrounded); ``tokens`` limits all of it to
+    some rows.
     """
+    if storage not in ("bf16", "f64"):
+        raise ValueError("storage must be 'bf16' or 'f64'")
+    st = round_bf16 if storage == "bf16" else (lambda v: v)
     h = as_f64(h)
     rows = list(range(h.shape[0])) if tokens is None else [int(t) for t in tokens]
     h = h[rows]
     W_o64 = as_f64(W_o)
     k_out = W_o64.shape[1] if k_out is None else k_out
-    a = rmsnorm(h, gamma1, eps)
-    y_in = linear(a, W_in)
-    h1 = linear_residual(y_in[:, :k_out], W_o64, h)
-    b = rmsnorm(h1, gamma2, eps)
+    a = st(rmsnorm(h, gamma1, eps))
+    y_in = st(linear(a, W_in))
+    h1 = st(linear_residual(y_in[:, :k_out], W_o64, h))
+    b = st(rmsnorm(h1, gamma2, eps))
     logits, scores = router_scores(b, Wr)
     idx, w = topk(scores, k)
     out = h1 + moe(b, idx, w, expert, shared)

@@ -1,0 +1,94 @@
+"""GPU parity of the MoE expert layer (moe_experts): routed SwiGLU experts
+over the selected ids, the shared expert on the side stream, weighted combine
+and optional residual, against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _util import SEED, HostBank, assert_bf16_close, dev_bf16, dev_f32, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def h():
+    import torch
+    import moe_layers_gb300 as M
+    assert torch.cuda.is_available()
+    M.build()
+    with M.Handle(0) as hd:
+        yield hd
+
+
+def _routing(M, E, k, rng, skew=False):
+    if skew:  # every token picks the same experts: one expert sees all M tokens
+        ids = np.tile(rng.permutation(E)[:k], (M, 1))
+    else:
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(M)])
+    w = rng.random((M, k)) + 0.1
+    w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    return ids.astype(np.int32), w
+
+
+def _small_bank(E, H, I, base):
+    n = E * I * H
+    g = synth.bf16(n, SEED, base, 0, 0.05)
+    u = synth.bf16(n, SEED, base + 1, 0, 0.05)
+    d = synth.bf16(n, SEED, base + 2, 0, 0.05)
+    return g.reshape(E, I, H), u.reshape(E, I, H), d.reshape(E, H, I)
+
+
+@pytest.mark.parametrize("M,E,H,I,k,shared,resid,skew", [
+    (1, 16, 256, 128, 4, True, False, False),
+    (3, 16, 256, 256, 4, False, True, False),
+    (17, 32, 384, 128, 8, True, True, False),
+    (64, 24, 256, 128, 8, True, False, False),
+    (64, 40, 128, 256, 16, True, True, True),
+    (20, 8, 512, 384, 2, False, False, True),
+])
+def test_experts_small(h, M, E, H, I, k, shared, resid, skew):
+    import moe_layers_gb300 as ML
+    rng = np.random.default_rng(M * 131 + E)
+    g, u, d = _small_bank(E, H, I, 4000 + E + H)
+    x = synth.bf16(M * H, SEED, 4100 + M, 0, 1.0).reshape(M, H)
+    idx, w = _routing(M, E, k, rng, skew)
+    sh = None
+    if shared:
+        sg = synth.bf16(I * H, SEED, 4200, 0, 0.05).reshape(I, H)
+        su = synth.bf16(I * H, SEED, 4201, 0, 0.05).reshape(I, H)
+        sd = synth.bf16(H * I, SEED, 4202, 0, 0.05).reshape(H, I)
+        sh = (sg, su, sd)
+    r = synth.bf16(M * H, SEED, 4300 + M, 0, 1.0).reshape(M, H) if resid else None
+    import torch
+    out = ML.moe_experts(h, dev_bf16(x, (M, H)), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
+                         dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
+                         shared=None if sh is None else tuple(dev_bf16(a, a.shape) for a in sh),
+                         residual=None if r is None else dev_bf16(r, (M, H)))
+    ref = oracle.moe(x, idx, w, lambda e: (g[e], u[e], d[e]), sh, r)
+    assert_bf16_close(host_bits(out), ref, f"moe M={M} E={E}")
+    assert h.check_device_error() == ML.DEC_OK
+
+
+# ---------------------------------------------------------------------------- workload size
+from conftest import E_FULL, H_FULL, I_FULL, K_FULL
+
+
+@pytest.mark.parametrize("M", [1, 8, 64])
+def test_experts_full_size(h, full_bank, M):
+    import torch
+    import moe_layers_gb300 as ML
+    Wg, Wu, Wd, sh = full_bank
+    rng = np.random.default_rng(5000 + M)
+    idx, w = _routing(M, E_FULL, K_FULL, rng)
+    x = synth.bf16_rows(synth.X_BASE + 20, range(M), H_FULL, SEED)
+    out = ML.moe_experts(h, dev_bf16(x, (M, H_FULL)), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
+                         Wg, Wu, Wd, shared=sh)
+    bank = HostBank(E_FULL, H_FULL, I_FULL)
+    shared = tuple(oracle.bf16_to_f64(synth.bf16(I_FULL * H_FULL, SEED, tid, 0, 0.02)).reshape(shape)
+                   for tid, shape in ((synth.W_G_S, (I_FULL, H_FULL)), (synth.W_U_S, (I_FULL, H_FULL)),
+                                      (synth.W_D_S, (H_FULL, I_FULL))))
+    tokens = sorted(set([0, M - 1, M // 2]))  # sampled tokens; each is a full output row
+    ref = oracle.moe(x, idx, w, bank, shared, tokens=tokens)
+    got = host_bits(out)[tokens]
+    assert_bf16_close(got, ref, f"moe full M={M}")

@@ -1,0 +1,121 @@
+"""GPU parity of the whole decode layer (decode_layer) against the oracle:
+indices bit-exact (router inputs drawn with a 1e-3 top-(k+1) gap), h1 and the
+layer output within the bf16 tolerance."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _util import SEED, HostBank, assert_bf16_close, dev_bf16, dev_f32, gap_rows, host_bits
+from conftest import E_FULL, H_FULL, I_FULL, K_FULL, K_OUT_FULL, N_IN_FULL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def h():
+    import torch
+    import moe_layers_gb300 as M
+    assert torch.cuda.is_available()
+    M.build()
+    with M.Handle(0) as hd:
+        yield hd
+
+
+def _bits(a):
+    return (np.asarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+class Layer:
+    """Host (bits) and device copies of one decode layer's dense weights."""
+
+    def __init__(self, H, N_in, K_out, E, I, k, base, gamma_noise=True, sigma=0.02, sr=0.01):
+        self.H, self.N_in, self.K_out, self.E, self.I, self.k = H, N_in, K_out, E, I, k
+        if gamma_noise:
+            g1 = oracle.round_bf16(1.0 + oracle.bf16_to_f64(synth.bf16(H, SEED, base, 0, 0.1)))
+            g2 = oracle.round_bf16(1.0 + oracle.bf16_to_f64(synth.bf16(H, SEED, base + 1, 0, 0.1)))
+        else:
+            g1 = g2 = np.ones(H)
+        self.g1, self.g2 = _bits(g1), _bits(g2)
+        self.W_in = synth.bf16(N_in * H, SEED, base + 2, 0, sigma).reshape(N_in, H)
+        self.W_o = synth.bf16(H * K_out, SEED, base + 3, 0, sigma).reshape(H, K_out)
+        self.Wr = synth.f32(E * H, SEED, base + 4, 0, sr).reshape(E, H)
+        self.W_in64 = oracle.bf16_to_f64(self.W_in)
+        self.W_o64 = oracle.bf16_to_f64(self.W_o)
+
+    def scores(self, rows):
+        a = oracle.round_bf16(oracle.rmsnorm(rows, self.g1))
+        y = oracle.round_bf16(oracle.linear(a, self.W_in64))
+        h1 = oracle.round_bf16(oracle.linear_residual(y[:, :self.K_out], self.W_o64, rows))
+        b = oracle.round_bf16(oracle.rmsnorm(h1, self.g2))
+        return oracle.router_scores(b, self.Wr)[1]
+
+    def oracle(self, hbits, expert, shared, tokens=None):
+        return oracle.decode_layer(hbits, self.g1, self.W_in64, self.W_o64, self.g2, self.Wr, self.k, expert,
+                                   shared, k_out=self.K_out, tokens=tokens)
+
+    def device(self, Wg, Wu, Wd, shared):
+        import moe_layers_gb300 as ML
+        return ML.LayerWeights(gamma1=dev_bf16(self.g1, (self.H,)), W_in=dev_bf16(self.W_in, self.W_in.shape),
+                               W_o=dev_bf16(self.W_o, self.W_o.shape), gamma2=dev_bf16(self.g2, (self.H,)),
+                               W_r=dev_f32(self.Wr), Wg=Wg, Wu=Wu, Wd=Wd,
+                               Wg_s=None if shared is None else shared[0],
+                               Wu_s=None if shared is None else shared[1],
+                               Wd_s=None if shared is None else shared[2], k=self.k, k_out=self.K_out)
+
+
+def _run(h, L, dev_w, hbits):
+    import moe_layers_gb300 as ML
+    M = hbits.shape[0]
+    hid = dev_bf16(hbits, hbits.shape)
+    tr = ML.decode_layer(h, dev_w, hid, trace=True)
+    return hid, tr
+
+
+@pytest.mark.parametrize("M,shared", [(1, True), (2, False), (3, True), (16, True), (64, True)])
+def test_layer_small(h, M, shared):
+    H, N_in, K_out, E, I, k = 256, 520, 384, 32, 128, 4
+    L = Layer(H, N_in, K_out, E, I, k, base=6000 + M)
+    n = E * I * H
+    g = synth.bf16(n, SEED, 6100, 0, 0.05).reshape(E, I, H)
+    u = synth.bf16(n, SEED, 6101, 0, 0.05).reshape(E, I, H)
+    d = synth.bf16(n, SEED, 6102, 0, 0.05).reshape(E, H, I)
+    sh = None
+    if shared:
+        sh = (synth.bf16(I * H, SEED, 6103, 0, 0.05).reshape(I, H), synth.bf16(I * H, SEED, 6104, 0, 0.05).reshape(I, H),
+              synth.bf16(H * I, SEED, 6105, 0, 0.05).reshape(H, I))
+    hbits, _ = gap_rows(L.scores, M, H, k, base=6200 + M)
+    dev_w = L.device(dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
+                     None if sh is None else tuple(dev_bf16(a, a.shape) for a in sh))
+    hid, tr = _run(h, L, dev_w, hbits)
+    ref = L.oracle(hbits, lambda e: (g[e], u[e], d[e]), sh)
+    assert np.array_equal(tr["idx"].cpu().numpy(), ref["idx"])
+    assert_bf16_close(host_bits(tr["h1"]), ref["h1"], "h1")
+    assert_bf16_close(host_bits(hid), ref["out"], f"layer M={M}")
+
+
+@pytest.fixture(scope="module")
+def full_layer():
+    return Layer(H_FULL, N_IN_FULL, K_OUT_FULL, E_FULL, I_FULL, K_FULL, base=synth.W_IN * 0 + 7000,
+                 gamma_noise=False)
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
+def test_layer_full_size(h, full_bank, full_layer, M):
+    Wg, Wu, Wd, sh = full_bank
+    L = full_layer
+    hbits, _ = gap_rows(L.scores, M, H_FULL, K_FULL, base=synth.X_BASE + 30)
+    hid, tr = _run(h, L, L.device(Wg, Wu, Wd, sh), hbits)
+    bank = HostBank(E_FULL, H_FULL, I_FULL)
+    shared = tuple(oracle.bf16_to_f64(synth.bf16(I_FULL * H_FULL, SEED, tid, 0, 0.02)).reshape(shape)
+                   for tid, shape in ((synth.W_G_S, (I_FULL, H_FULL)), (synth.W_U_S, (I_FULL, H_FULL)),
+                                      (synth.W_D_S, (H_FULL, I_FULL))))
+    tokens = sorted(set([0, M // 2, M - 1]))
+    ref = L.oracle(hbits, bank, shared, tokens=tokens)
+    assert np.array_equal(tr["idx"].cpu().numpy()[tokens], ref["idx"])
+    assert_bf16_close(host_bits(tr["h1"])[tokens], ref["h1"], "h1 full")
+    assert_bf16_close(host_bits(hid)[tokens], ref["out"], f"layer full M={M}")
+    # indices of all tokens: bit-exact against the oracle's router on every row
+    s_all = L.scores(hbits)
+    i_all, _ = oracle.topk(s_all, K_FULL)
+    assert np.array_equal(tr["idx"].cpu().numpy(), i_all)

@@ -267,6 +267,38 @@ def pin_moe_properties(o):
     assert np.allclose(sub, base[[4, 1]], rtol=1e-13, atol=1e-13)
 
 
+# ============================================================================ bf16 storage
+def _exact_bf16(v: float) -> float:
+    """Nearest-even bf16 value of v by exact rational arithmetic (independent of the oracle)."""
+    if v == 0.0:
+        return 0.0
+    a = Fraction(abs(v))
+    e = 0
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, -126)
+    q = a / Fraction(2) ** (e - 7)
+    fl = math.floor(q)
+    r = q - fl
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    out = float(fl * Fraction(2) ** (e - 7))
+    return -out if v < 0 else out
+
+
+def pin_round_bf16(o):
+    rng = np.random.default_rng(10)
+    vals = np.concatenate([rng.standard_normal(2000), rng.standard_normal(300) * 1e-3, rng.standard_normal(300) * 1e4,
+                           np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -(1.0 + 2 ** -8), 2 ** -130, 0.0, 255.5])])
+    got = o.round_bf16(vals)
+    for v, g in zip(vals, got):
+        assert g == _exact_bf16(float(v)), (v, g)
+    # idempotent, and exact for representable values
+    assert np.array_equal(o.round_bf16(got), got)
+
+
 # ============================================================================ decode layer
 def _tiny_layer(rng, H=16, N_in=24, K_out=12, E=12, k=3, I=8):
     W_in = rng.standard_normal((N_in, H)) * 0.4
@@ -284,7 +316,17 @@ def pin_decode_layer(o):
     rng = np.random.default_rng(9)
     L = _tiny_layer(rng)
     h = rng.standard_normal((4, 16))
-    full = o.decode_layer(h, **L)
+    # bf16 storage rounds each operation's output, and only that
+    fb = o.decode_layer(h, **L)
+    a = o.round_bf16(o.rmsnorm(h, L["gamma1"]))
+    y = o.round_bf16(o.linear(a, L["W_in"]))
+    h1 = o.round_bf16(h + o.linear(y[:, :12], L["W_o"]))
+    b = o.round_bf16(o.rmsnorm(h1, L["gamma2"]))
+    _, s = o.router_scores(b, L["Wr"])
+    idx, w = o.topk(s, L["k"])
+    assert np.array_equal(fb["idx"], idx)
+    assert np.allclose(fb["out"], h1 + o.moe(b, idx, w, L["expert"], L["shared"]), rtol=1e-13, atol=1e-13)
+    full = o.decode_layer(h, storage="f64", **L)
     # composition of the separately pinned stages
     a = o.rmsnorm(h, L["gamma1"])
     y = o.linear(a, L["W_in"])
@@ -297,16 +339,16 @@ def pin_decode_layer(o):
     assert np.allclose(full["out"], out, rtol=1e-13, atol=1e-13)
     # M-invariance: each row of a batch equals the batch-of-one result on that row
     for t in range(4):
-        one = o.decode_layer(h[t:t + 1], **L)
+        one = o.decode_layer(h[t:t + 1], storage="f64", **L)
         assert np.array_equal(one["idx"][0], full["idx"][t])
         assert np.allclose(one["out"][0], full["out"][t], rtol=1e-12, atol=1e-12)
-    sub = o.decode_layer(h, tokens=[3, 0], **L)
+    sub = o.decode_layer(h, tokens=[3, 0], storage="f64", **L)
     assert np.allclose(sub["out"], full["out"][[3, 0]], rtol=1e-12, atol=1e-12)
 
 
 PINS = [pin_linear_bruteforce, pin_linear_integer_exact, pin_linear_orientation, pin_linear_linearity,
         pin_linear_residual, pin_rmsnorm, pin_router_golden, pin_router_properties, pin_swiglu_golden,
-        pin_swiglu_odd_part, pin_moe_properties, pin_decode_layer]
+        pin_swiglu_odd_part, pin_moe_properties, pin_round_bf16, pin_decode_layer]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -395,7 +437,12 @@ def _mut_layer_no_moe_residual(mp):
     mp.setattr(oracle, "decode_layer", dl)
 
 
-MUTATIONS = [_mut_linear_transposed, _mut_linear_dropped_term, _mut_residual_sign, _mut_rms_sum,
+def _mut_round_half_up(mp):
+    mp.setattr(oracle, "round_bf16", lambda a: (lambda v, e: np.ldexp(np.floor(np.ldexp(v, 8 - e) + 0.5), e - 8))(
+        np.asarray(a, dtype=np.float64), np.maximum(np.frexp(np.asarray(a, dtype=np.float64))[1], -125)))
+
+
+MUTATIONS = [_mut_round_half_up, _mut_linear_transposed, _mut_linear_dropped_term, _mut_residual_sign, _mut_rms_sum,
              _mut_rms_eps_outside, _mut_sigmoid_sign, _mut_softmax_scores, _mut_tie_high_id, _mut_no_renorm,
              _mut_silu_as_sigmoid, _mut_gate_up_swapped, _mut_moe_unweighted, _mut_moe_no_shared,
              _mut_layer_no_moe_residual]
