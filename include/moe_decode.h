@@ -226,6 +226,28 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
  * [K3 P1§4]. ptr and bytes multiples of 16. */
 dec_status dec_prefetch_l2(dec_handle* h, const void* ptr, size_t bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------ measurement */
+
+/* Per-kernel timing record returned by dec_profile_read. */
+typedef struct dec_kernel_time {
+  char name[32];   /* kernel tag, e.g. "in_proj", "gate_up", "shared_down" */
+  int launches;    /* launches since the last read */
+  double total_ms; /* summed device time of those launches */
+} dec_kernel_time;
+
+/* Enable (1) or disable (0) per-kernel timing: every kernel launch is then
+ * bracketed by CUDA events on the stream it is launched on. The events
+ * separate kernels, so programmatic dependent launch overlap is lost while
+ * profiling is on; use it for per-kernel durations, not for step times. */
+dec_status dec_set_profiling(dec_handle* h, int enable);
+
+/* Synchronise, then aggregate the timing records by kernel tag into
+ * out[0 .. capacity) (*count receives the number of tags) and clear them. */
+dec_status dec_profile_read(dec_handle* h, dec_kernel_time* out, int capacity, int* count);
+
+/* Number of kernels this handle has launched since it was created. */
+uint64_t dec_launch_count(const dec_handle* h);
+
 /* ------------------------------------------------------------------ test hooks */
 
 /* Launch a kernel whose mbarrier wait can never complete; it must give up

@@ -42,6 +42,10 @@ class _LayerWeights(ctypes.Structure):
                [("prefetch_bytes", ctypes.c_size_t)]
 
 
+class _KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
+
+
 class _LayerTrace(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("h1", "idx", "w", "scores")]
 
@@ -76,6 +80,8 @@ def _load():
         "dec_prefetch_l2": [P, P, Z, P],
         "dec_test_wait_timeout": [P, P],
         "dec_test_delayed_copy": [P, P, P, Z, U64, P],
+        "dec_set_profiling": [P, I],
+        "dec_profile_read": [P, ctypes.POINTER(_KernelTime), I, ctypes.POINTER(I)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -85,6 +91,8 @@ def _load():
     lib.dec_status_string.restype = ctypes.c_char_p
     lib.dec_last_variant.argtypes = [P]
     lib.dec_last_variant.restype = ctypes.c_int
+    lib.dec_launch_count.argtypes = [P]
+    lib.dec_launch_count.restype = ctypes.c_uint64
     _lib = lib
     return lib
 
@@ -181,6 +189,20 @@ class Handle:
 
     def check_device_error(self) -> int:
         return _load().dec_check_device_error(self._h)
+
+    def set_profiling(self, enable: bool) -> None:
+        _check(_load().dec_set_profiling(self._h, 1 if enable else 0), "dec_set_profiling")
+
+    def profile_read(self) -> dict:
+        """{kernel tag: (launches, total_ms)} since the last read (synchronises)."""
+        buf = (_KernelTime * 64)()
+        n = ctypes.c_int()
+        _check(_load().dec_profile_read(self._h, buf, 64, ctypes.byref(n)), "dec_profile_read")
+        return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(n.value)}
+
+    @property
+    def launch_count(self) -> int:
+        return int(_load().dec_launch_count(self._h))
 
 
 # ---------------------------------------------------------------------------- projections

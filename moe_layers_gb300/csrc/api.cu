@@ -23,6 +23,37 @@ inline size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
     if ((expr) != cudaSuccess) return DEC_ERR_CUDA; \
   } while (0)
 
+cudaEvent_t pool_event(dec_handle* h) {
+  if (!h->event_pool.empty()) {
+    cudaEvent_t e = h->event_pool.back();
+    h->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Counts every kernel launch; when profiling, brackets it with events on its stream.
+struct LaunchScope {
+  dec_handle* h;
+  cudaStream_t s;
+  int rec = -1;
+  LaunchScope(dec_handle* h_, const char* tag, cudaStream_t s_) : h(h_), s(s_) {
+    h->launches++;
+    if (h->profiling) {
+      dec_handle::ProfRec r{tag, pool_event(h), pool_event(h)};
+      if (r.a && r.b && cudaEventRecord(r.a, s) == cudaSuccess) {
+        h->prof.push_back(r);
+        rec = (int)h->prof.size() - 1;
+      }
+    }
+  }
+  ~LaunchScope() {
+    if (rec >= 0) cudaEventRecord(h->prof[rec].b, s);
+  }
+};
+
 // Split a workspace into 256-byte-aligned pieces.
 struct Carver {
   char* base;
@@ -58,9 +89,10 @@ int choose_variant(const dec_handle* h, int M, int K) {
 }
 
 dec_status linear_impl(dec_handle* h, const uint16_t* x, int ldx, const uint16_t* W, const uint16_t* r, uint16_t* y,
-                       int M, int N, int K, EngineRegion eng, cudaStream_t s) {
+                       int M, int N, int K, EngineRegion eng, cudaStream_t s, const char* tag = "linear") {
   const int v = choose_variant(h, M, K);
   cudaError_t e;
+  LaunchScope scope(h, tag, s);
   if (v == DEC_VARIANT_SMALL_M) {
     if (!gemv_supported(M, K)) return DEC_ERR_UNSUPPORTED;
     e = launch_gemv(h, x, ldx, W, r, N, y, N, M, N, K, s);
@@ -155,7 +187,10 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
     L.partials = ws.r1.partials;
     L.counters = ws.r1.counters;
     L.grid = g1;
-    DEC_CUDA(launch_engine(h, L, h->side));
+    {
+      LaunchScope scope(h, "shared_gate_up", h->side);
+      DEC_CUDA(launch_engine(h, L, h->side));
+    }
     EngineLaunch D;
     D.epi = EPI_F32;
     D.A = Wd_s;
@@ -171,10 +206,16 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
     D.partials = ws.r1.partials;
     D.counters = ws.r1.counters;
     D.grid = g1;
-    DEC_CUDA(launch_engine(h, D, h->side));
+    {
+      LaunchScope scope(h, "shared_down", h->side);
+      DEC_CUDA(launch_engine(h, D, h->side));
+    }
     DEC_CUDA(cudaEventRecord(h->ev_join, h->side));
   }
-  DEC_CUDA(launch_route_table(h, idx, M, k, E, x, H, ws.table, ws.xs, s));
+  {
+    LaunchScope scope(h, "route_table", s);
+    DEC_CUDA(launch_route_table(h, idx, M, k, E, x, H, ws.table, ws.xs, s));
+  }
   EngineLaunch L;
   L.epi = EPI_SWIGLU;
   L.A = Wg;
@@ -194,7 +235,10 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
   L.partials = ws.r0.partials;
   L.counters = ws.r0.counters;
   L.grid = g0;
-  DEC_CUDA(launch_engine(h, L, s));
+  {
+    LaunchScope scope(h, "gate_up", s);
+    DEC_CUDA(launch_engine(h, L, s));
+  }
   EngineLaunch D;
   D.epi = EPI_F32;
   D.A = Wd;
@@ -213,9 +257,15 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
   D.partials = ws.r0.partials;
   D.counters = ws.r0.counters;
   D.grid = g0;
-  DEC_CUDA(launch_engine(h, D, s));
+  {
+    LaunchScope scope(h, "down", s);
+    DEC_CUDA(launch_engine(h, D, s));
+  }
   if (has_shared) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
-  DEC_CUDA(launch_combine(h, ws.y, ws.table, w, M, k, E, has_shared ? ws.ys : nullptr, residual, out, H, s));
+  {
+    LaunchScope scope(h, "combine", s);
+    DEC_CUDA(launch_combine(h, ws.y, ws.table, w, M, k, E, has_shared ? ws.ys : nullptr, residual, out, H, s));
+  }
   return DEC_OK;
 }
 
@@ -310,6 +360,11 @@ dec_status dec_destroy(dec_handle* h) {
   if (h->pf) cudaStreamDestroy(h->pf);
   for (cudaEvent_t e : {h->ev_fork, h->ev_join, h->ev_pf_fork, h->ev_pf_join})
     if (e) cudaEventDestroy(e);
+  for (const auto& r : h->prof) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (cudaEvent_t e : h->event_pool) cudaEventDestroy(e);
   if (h->d_err) cudaFree(h->d_err);
   delete h;
   return DEC_OK;
@@ -373,7 +428,7 @@ static dec_status linear_entry(dec_handle* h, const dec_bf16* x, int ldx, const 
     Carver c(ws);
     eng = carve_engine(c, engine_grid(h), 1, (N + kTileN - 1) / kTileN);
   }
-  return linear_impl(h, x, ldx, W, r, out, M, N, K, eng, s);
+  return linear_impl(h, x, ldx, W, r, out, M, N, K, eng, s, r ? "linear_residual" : "linear");
 }
 
 dec_status dec_linear(dec_handle* h, const dec_bf16* x, int ldx, const dec_bf16* W, dec_bf16* y, int M, int N,
@@ -394,6 +449,7 @@ dec_status dec_rmsnorm(dec_handle* h, const dec_bf16* x, const dec_bf16* gamma, 
   if (!al16(x) || !al16(gamma) || !al16(y) || M < 1 || M > kMaxM || H < 8 || H % 8 != 0 || H > 65536 ||
       !(eps >= 0.f))
     return DEC_ERR_INVALID_ARG;
+  LaunchScope scope(h, "rmsnorm", stream);
   return launch_rmsnorm(h, x, gamma, y, M, H, eps, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
 }
 
@@ -415,8 +471,14 @@ dec_status moe_route_topk(dec_handle* h, const dec_bf16* x, const float* Wr, int
   moe_route_topk_workspace_size(h, M, H, E, &need);
   if (ws == nullptr || ws_bytes < need) return DEC_ERR_INVALID_ARG;
   float* parts = static_cast<float*>(ws);
-  if (launch_router(h, x, Wr, M, H, E, parts, stream) != cudaSuccess) return DEC_ERR_CUDA;
-  if (launch_topk(h, parts, router_ksplit(H), M, E, k, idx, w, scores, stream) != cudaSuccess) return DEC_ERR_CUDA;
+  {
+    LaunchScope scope(h, "router", stream);
+    if (launch_router(h, x, Wr, M, H, E, parts, stream) != cudaSuccess) return DEC_ERR_CUDA;
+  }
+  {
+    LaunchScope scope(h, "topk", stream);
+    if (launch_topk(h, parts, router_ksplit(H), M, E, k, idx, w, scores, stream) != cudaSuccess) return DEC_ERR_CUDA;
+  }
   return DEC_OK;
 }
 
@@ -495,24 +557,39 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   float* scores = trace ? trace->scores : nullptr;
   const int H = L.H;
 
-  if (launch_rmsnorm(h, hidden, L.gamma1, w.a, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
-  dec_status st = linear_impl(h, w.a, H, L.W_in, nullptr, w.yin, M, L.N_in, H, w.moe.r0, s);
+  {
+    LaunchScope scope(h, "rmsnorm1", s);
+    if (launch_rmsnorm(h, hidden, L.gamma1, w.a, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
+  }
+  dec_status st = linear_impl(h, w.a, H, L.W_in, nullptr, w.yin, M, L.N_in, H, w.moe.r0, s, "in_proj");
   if (st != DEC_OK) return st;
-  st = linear_impl(h, w.yin, L.N_in, L.W_o, hidden, h1, M, H, L.K_out, w.moe.r0, s);
+  st = linear_impl(h, w.yin, L.N_in, L.W_o, hidden, h1, M, H, L.K_out, w.moe.r0, s, "out_proj");
   if (st != DEC_OK) return st;
-  if (launch_rmsnorm(h, h1, L.gamma2, w.b, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
+  {
+    LaunchScope scope(h, "rmsnorm2", s);
+    if (launch_rmsnorm(h, h1, L.gamma2, w.b, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
+  }
   const bool pf = L.prefetch_next != nullptr && L.prefetch_bytes > 0;
   if (pf) {
     DEC_CUDA(cudaEventRecord(h->ev_pf_fork, s));
     DEC_CUDA(cudaStreamWaitEvent(h->pf, h->ev_pf_fork, 0));
-    DEC_CUDA(launch_prefetch(h, L.prefetch_next, L.prefetch_bytes, 16, h->pf));
+    {
+      LaunchScope scope(h, "prefetch", h->pf);
+      DEC_CUDA(launch_prefetch(h, L.prefetch_next, L.prefetch_bytes, 16, h->pf));
+    }
     DEC_CUDA(cudaEventRecord(h->ev_pf_join, h->pf));
   }
   // The router / top-k phase is latency-bound; the shared expert (forked in
   // moe_impl) and the prefetch stream use the idle bandwidth meanwhile.
-  if (launch_router(h, w.b, L.W_r, M, H, L.E, w.parts, s) != cudaSuccess) return DEC_ERR_CUDA;
-  if (launch_topk(h, w.parts, router_ksplit(H), M, L.E, L.k, idx, wt, scores, s) != cudaSuccess)
-    return DEC_ERR_CUDA;
+  {
+    LaunchScope scope(h, "router", s);
+    if (launch_router(h, w.b, L.W_r, M, H, L.E, w.parts, s) != cudaSuccess) return DEC_ERR_CUDA;
+  }
+  {
+    LaunchScope scope(h, "topk", s);
+    if (launch_topk(h, w.parts, router_ksplit(H), M, L.E, L.k, idx, wt, scores, s) != cudaSuccess)
+      return DEC_ERR_CUDA;
+  }
   st = moe_impl(h, w.b, idx, wt, M, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, h1, hidden, w.moe, s);
   if (st != DEC_OK) return st;
   if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
@@ -521,12 +598,49 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
 
 dec_status dec_prefetch_l2(dec_handle* h, const void* ptr, size_t bytes, cudaStream_t stream) {
   if (h == nullptr || (ptr == nullptr && bytes) || !al16(ptr) || bytes % 16 != 0) return DEC_ERR_INVALID_ARG;
+  LaunchScope scope(h, "prefetch", stream);
   return launch_prefetch(h, ptr, bytes, 16, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
 }
+
+dec_status dec_set_profiling(dec_handle* h, int enable) {
+  if (h == nullptr) return DEC_ERR_INVALID_ARG;
+  h->profiling = enable ? 1 : 0;
+  return DEC_OK;
+}
+
+dec_status dec_profile_read(dec_handle* h, dec_kernel_time* out, int capacity, int* count) {
+  if (h == nullptr || count == nullptr || capacity < 0 || (capacity > 0 && out == nullptr)) return DEC_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return DEC_ERR_CUDA;
+  int n = 0;
+  for (const auto& r : h->prof) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) ms = 0.f;
+    int i = 0;
+    while (i < n && std::strncmp(out[i].name, r.tag, sizeof(out[i].name)) != 0) ++i;
+    if (i == n) {
+      if (n >= capacity) continue;
+      std::memset(&out[n], 0, sizeof(out[n]));
+      std::strncpy(out[n].name, r.tag, sizeof(out[n].name) - 1);
+      ++n;
+    }
+    out[i].launches += 1;
+    out[i].total_ms += ms;
+  }
+  for (const auto& r : h->prof) {
+    h->event_pool.push_back(r.a);
+    h->event_pool.push_back(r.b);
+  }
+  h->prof.clear();
+  *count = n;
+  return DEC_OK;
+}
+
+uint64_t dec_launch_count(const dec_handle* h) { return h ? h->launches : 0; }
 
 // ---------------------------------------------------------------- test hooks
 dec_status dec_test_wait_timeout(dec_handle* h, cudaStream_t stream) {
   if (h == nullptr) return DEC_ERR_INVALID_ARG;
+  LaunchScope scope(h, "test_wait_probe", stream);
   return launch_wait_timeout_probe(h, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
 }
 
@@ -535,6 +649,7 @@ dec_status dec_test_delayed_copy(dec_handle* h, void* dst, const void* src, size
   if (h == nullptr || dst == nullptr || src == nullptr || !al16(dst) || !al16(src) || bytes % 16 != 0 ||
       delay_ns > 1000000000ull)
     return DEC_ERR_INVALID_ARG;
+  LaunchScope scope(h, "test_delayed_copy", stream);
   return launch_delayed_copy(h, dst, src, bytes, delay_ns, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
 }
 

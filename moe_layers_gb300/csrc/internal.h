@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <utility>
+#include <vector>
 
 #include "../../include/moe_decode.h"
 
@@ -22,6 +24,15 @@ struct dec_handle {
   int last_variant = 0;
   int shared_ctas = 0;              // CTAs for the shared expert's kernels (0 = default)
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  // measurement
+  uint64_t launches = 0;
+  int profiling = 0;
+  struct ProfRec {
+    const char* tag;
+    cudaEvent_t a, b;
+  };
+  std::vector<ProfRec> prof;
+  std::vector<cudaEvent_t> event_pool;
 };
 
 namespace dec {
