@@ -63,6 +63,41 @@ __device__ __forceinline__ uint4 ld_stream(const void* p, uint64_t pol) {
   return v;
 }
 
+// Loads of activations: data written by an earlier kernel. They are volatile
+// asm so that the compiler can never move them above pdl_wait() (a const
+// __restrict__ pointer would let it hoist them, reading stale data while the
+// producer still runs). Only static weights use plain or restrict loads.
+__device__ __forceinline__ uint4 ld_act16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 ld_act8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_act_f4(const void* p) {
+  float4 v;
+  asm volatile("ld.global.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_act_f32(const void* p) {
+  float v;
+  asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_act_s32(const void* p) {
+  int v;
+  asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint16_t ld_act_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------- PDL
 // Programmatic dependent launch: a kernel may start while its predecessor on
 // the stream drains. Everything before pdl_wait() may touch only memory that

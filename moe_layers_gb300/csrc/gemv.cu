@@ -28,9 +28,8 @@ constexpr int kGemvThreads = 256;
 
 template <int M, int VPT>
 __global__ void __launch_bounds__(kGemvThreads, 2)
-    gemv_kernel(const uint16_t* __restrict__ x, long long ldx, const uint16_t* __restrict__ W,
-                const uint16_t* __restrict__ res, long long ldr, uint16_t* __restrict__ y, long long ldy, int N,
-                int K) {
+    gemv_kernel(const uint16_t* x, long long ldx, const uint16_t* __restrict__ W, const uint16_t* res, long long ldr,
+                uint16_t* y, long long ldy, int N, int K) {
   constexpr int RB = (8 / VPT) > 0 ? (8 / VPT) : 1;  // rows per step
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int K8 = K >> 3;
@@ -65,8 +64,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int v = t + kGemvThreads * i;
-      xr[m][i] = (v < K8) ? *reinterpret_cast<const uint4*>(x + (size_t)m * ldx + (size_t)v * 8)
-                          : make_uint4(0, 0, 0, 0);
+      xr[m][i] = (v < K8) ? ld_act16(x + (size_t)m * ldx + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
     }
 
   int buf = 0;
@@ -103,7 +101,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
         float s = 0.f;
 #pragma unroll
         for (int w = 0; w < kGemvThreads / 32; ++w) s += red[buf][w][t];
-        if (res != nullptr) s += bf2f(res[(size_t)m * ldr + row]);
+        if (res != nullptr) s += bf2f(ld_act_u16(res + (size_t)m * ldr + row));
         y[(size_t)m * ldy + row] = f2bf(s);
       }
     }

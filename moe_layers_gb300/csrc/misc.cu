@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const u
   const int H8 = H >> 3;
   float ss = 0.f;
   for (int v = tid; v < H8; v += blockDim.x) {
-    const uint4 a = *reinterpret_cast<const uint4*>(xr + (size_t)v * 8);
+    const uint4 a = ld_act16(xr + (size_t)v * 8);
     const uint32_t ws[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const u
   for (int q = 0; q < (int)(blockDim.x >> 5); ++q) tot += red[q];
   const float r = rsqrtf(tot / (float)H + eps);
   for (int v = tid; v < H8; v += blockDim.x) {
-    const uint4 a = *reinterpret_cast<const uint4*>(xr + (size_t)v * 8);
+    const uint4 a = ld_act16(xr + (size_t)v * 8);
     const uint4 g = *reinterpret_cast<const uint4*>(gamma + (size_t)v * 8);
     const uint32_t ws[4] = {a.x, a.y, a.z, a.w}, gs[4] = {g.x, g.y, g.z, g.w};
     uint32_t o[4];

@@ -26,8 +26,8 @@ int router_ksplit(int H) { return (H + kRouterChunk - 1) / kRouterChunk; }
 // Grid: (ceil(E / 8), ksplit). Each warp owns one router row and keeps its
 // chunk of fp32 weights in registers (loaded before the dependency wait); the
 // tokens' bf16 activations pass through shared memory sixteen at a time.
-__global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict__ x, const float* __restrict__ Wr,
-                                                     int M, int H, int E, float* __restrict__ parts) {
+__global__ void __launch_bounds__(256) router_kernel(const uint16_t* x, const float* __restrict__ Wr, int M, int H,
+                                                     int E, float* parts) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRouterRows + warp;
   const int ks = blockIdx.y;
@@ -49,8 +49,7 @@ __global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict_
     __syncthreads();
     for (int q = threadIdx.x; q < nt * kv; q += blockDim.x) {
       const int tt = q / kv, v = q - tt * kv;
-      *reinterpret_cast<uint4*>(&xs[tt][v * 8]) =
-          *reinterpret_cast<const uint4*>(x + (size_t)(t0 + tt) * H + k0 + v * 8);
+      *reinterpret_cast<uint4*>(&xs[tt][v * 8]) = ld_act16(x + (size_t)(t0 + tt) * H + k0 + v * 8);
     }
     __syncthreads();
     float acc[kRouterTok];
@@ -89,9 +88,8 @@ __global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict_
 // One CTA per token: logits = sum of the split partials in split order,
 // s = 1 / (1 + exp(-logit)), then k rounds of a block-wide arg-max
 // (score descending, expert id ascending) and renormalisation.
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ parts, int ks, int M, int E, int k,
-                                                   int32_t* __restrict__ idx, float* __restrict__ w,
-                                                   float* __restrict__ scores) {
+__global__ void __launch_bounds__(256) topk_kernel(const float* parts, int ks, int M, int E, int k, int32_t* idx,
+                                                   float* w, float* scores) {
   const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __shared__ float sv[1024];
   __shared__ float red_v[8];
@@ -102,7 +100,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
   pdl_wait();
   for (int e = tid; e < E; e += blockDim.x) {
     float z = 0.f;
-    for (int s = 0; s < ks; ++s) z += parts[((size_t)s * M + t) * E + e];
+    for (int s = 0; s < ks; ++s) z += ld_act_f32(parts + ((size_t)s * M + t) * E + e);
     const float sc = 1.0f / (1.0f + expf(-z));
     sv[e] = sc;
     if (scores != nullptr) scores[(size_t)t * E + e] = sc;
@@ -161,9 +159,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
 // rebuilds the table in shared memory (n = M*k <= 1024 entries), CTA 0 writes
 // it out, and all CTAs gather x rows into the slot-ordered buffer xs so that
 // each expert's tokens are contiguous rows for the TMA loads of the experts.
-__global__ void __launch_bounds__(256) route_table_kernel(const int32_t* __restrict__ idx, int M, int k, int E,
-                                                          const uint16_t* __restrict__ x, int H, int* __restrict__ table,
-                                                          uint16_t* __restrict__ xs) {
+__global__ void __launch_bounds__(256) route_table_kernel(const int32_t* idx, int M, int k, int E, const uint16_t* x,
+                                                          int H, int* table, uint16_t* xs) {
   extern __shared__ int sm[];
   const int n = M * k;
   int* cnt = sm;
@@ -180,7 +177,7 @@ __global__ void __launch_bounds__(256) route_table_kernel(const int32_t* __restr
     cnt[e] = 0;
     run[e] = 0;
   }
-  for (int i = tid; i < n; i += blockDim.x) eidx[i] = idx[i];
+  for (int i = tid; i < n; i += blockDim.x) eidx[i] = ld_act_s32(idx + i);
   __syncthreads();
   for (int i = tid; i < n; i += blockDim.x) atomicAdd(&cnt[eidx[i]], 1);
   __syncthreads();
@@ -246,16 +243,14 @@ __global__ void __launch_bounds__(256) route_table_kernel(const int32_t* __restr
   const long long total = (long long)n * H8;
   for (long long q = (long long)blockIdx.x * blockDim.x + tid; q < total; q += (long long)gridDim.x * blockDim.x) {
     const int s = (int)(q / H8), v = (int)(q - (long long)s * H8);
-    *reinterpret_cast<uint4*>(xs + (size_t)s * H + (size_t)v * 8) =
-        *reinterpret_cast<const uint4*>(x + (size_t)stok[s] * H + (size_t)v * 8);
+    *reinterpret_cast<uint4*>(xs + (size_t)s * H + (size_t)v * 8) = ld_act16(x + (size_t)stok[s] * H + (size_t)v * 8);
   }
 }
 
 // out[t][:] = bf16( sum_j w[t][j] * y[slot(t, j)][:]  (+ ys[t][:])  (+ res[t][:]) ), fp32 sums in that order.
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const int* __restrict__ table,
-                                                      const float* __restrict__ w, int M, int k, int E,
-                                                      const float* __restrict__ ys, const uint16_t* __restrict__ res,
-                                                      uint16_t* __restrict__ out, int H) {
+__global__ void __launch_bounds__(256) combine_kernel(const float* y, const int* table, const float* w, int M, int k,
+                                                      int E, const float* ys, const uint16_t* res, uint16_t* out,
+                                                      int H) {
   const int t = blockIdx.y;
   const int n0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   pdl_trigger();
@@ -264,23 +259,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const TableLayout L(E, M * k);
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   for (int j = 0; j < k; ++j) {
-    const int slot = table[L.entry_slot() + t * k + j];
-    const float wj = w[(size_t)t * k + j];
-    const float4 v = *reinterpret_cast<const float4*>(y + (size_t)slot * H + n0);
+    const int slot = ld_act_s32(table + L.entry_slot() + t * k + j);
+    const float wj = ld_act_f32(w + (size_t)t * k + j);
+    const float4 v = ld_act_f4(y + (size_t)slot * H + n0);
     a0 = fmaf(wj, v.x, a0);
     a1 = fmaf(wj, v.y, a1);
     a2 = fmaf(wj, v.z, a2);
     a3 = fmaf(wj, v.w, a3);
   }
   if (ys != nullptr) {
-    const float4 v = *reinterpret_cast<const float4*>(ys + (size_t)t * H + n0);
+    const float4 v = ld_act_f4(ys + (size_t)t * H + n0);
     a0 += v.x;
     a1 += v.y;
     a2 += v.z;
     a3 += v.w;
   }
   if (res != nullptr) {
-    const uint2 r = *reinterpret_cast<const uint2*>(res + (size_t)t * H + n0);
+    const uint2 r = ld_act8(res + (size_t)t * H + n0);
     a0 += bf_lo(r.x);
     a1 += bf_hi(r.x);
     a2 += bf_lo(r.y);

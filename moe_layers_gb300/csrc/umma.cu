@@ -73,11 +73,12 @@ struct Prob {
 __device__ __forceinline__ Prob prob_info(const EngineParams& P, int p) {
   if (P.table == nullptr) return Prob{0, 0, P.count};
   const TableLayout L(P.E, P.n_entries);
-  return Prob{P.table[L.expert() + p], P.table[L.offset() + p], P.table[L.count() + p]};
+  return Prob{ld_act_s32(P.table + L.expert() + p), ld_act_s32(P.table + L.offset() + p),
+              ld_act_s32(P.table + L.count() + p)};
 }
 
 __device__ __forceinline__ long long total_kblocks(const EngineParams& P) {
-  const long long nprob = (P.table == nullptr) ? 1 : P.table[0];
+  const long long nprob = (P.table == nullptr) ? 1 : ld_act_s32(P.table);
   return nprob * P.tiles * P.KB;
 }
 
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
       const long long orow = (long long)pr.off + jcol;
       if (EPI == EPI_LINEAR) {
         float s = v0;
-        if (P.res != nullptr) s += bf2f(P.res[orow * P.ldr + n]);
+        if (P.res != nullptr) s += bf2f(ld_act_u16(P.res + orow * P.ldr + n));
         out16[orow * P.ldo + n] = f2bf(s);
       } else if (EPI == EPI_SWIGLU) {
         const float g = v0;

@@ -60,8 +60,23 @@ def bf16_report(gpu_bits: np.ndarray, ref: np.ndarray) -> dict:
                 nonfinite=int(np.count_nonzero(~np.isfinite(g))))
 
 
-def assert_bf16_close(gpu_bits: np.ndarray, ref: np.ndarray, what: str = "", tol: float = TOL) -> dict:
+def ulp_bf16(ref: np.ndarray) -> np.ndarray:
+    return 2.0 * half_ulp_bf16(ref)
+
+
+def assert_bf16_close(gpu_bits: np.ndarray, ref: np.ndarray, what: str = "", tol: float = TOL,
+                      passthrough=None) -> dict:
+    """Pass iff max(|gpu - ref| - half_ulp(ref) - passthrough) <= tol * rms(ref).
+
+    passthrough (optional, elementwise) is a difference that enters the output
+    unchanged through a residual add: for a layer output h1 + MoE, the
+    measured |h1_gpu - h1_oracle| of the stored bf16 residual, which two
+    correct roundings of h1 (fp32 vs fp64 sums) may leave one ulp apart."""
     r = bf16_report(gpu_bits, ref)
+    if passthrough is not None:
+        g = oracle.bf16_to_f64(gpu_bits).reshape(ref.shape)
+        adj = np.abs(g - ref) - half_ulp_bf16(ref) - np.asarray(passthrough).reshape(ref.shape)
+        r["adjusted"] = float(adj.max() / r["rms"])
     assert r["nonfinite"] == 0, f"{what}: non-finite outputs"
     assert r["adjusted"] <= tol, f"{what}: {r}"
     return r

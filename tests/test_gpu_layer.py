@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synth
-from _util import SEED, HostBank, assert_bf16_close, dev_bf16, dev_f32, gap_rows, host_bits
+from _util import SEED, HostBank, assert_bf16_close, dev_bf16, dev_f32, gap_rows, host_bits, ulp_bf16
 from conftest import E_FULL, H_FULL, I_FULL, K_FULL, K_OUT_FULL, N_IN_FULL
 
 pytestmark = pytest.mark.gpu
@@ -89,9 +89,18 @@ def test_layer_small(h, M, shared):
                      None if sh is None else tuple(dev_bf16(a, a.shape) for a in sh))
     hid, tr = _run(h, L, dev_w, hbits)
     ref = L.oracle(hbits, lambda e: (g[e], u[e], d[e]), sh)
-    assert np.array_equal(tr["idx"].cpu().numpy(), ref["idx"])
-    assert_bf16_close(host_bits(tr["h1"]), ref["h1"], "h1")
-    assert_bf16_close(host_bits(hid), ref["out"], f"layer M={M}")
+    _check_layer(tr, hid, ref, slice(None), f"layer M={M}")
+
+
+def _check_layer(tr, hid, ref, rows, what):
+    assert np.array_equal(tr["idx"].cpu().numpy()[rows], ref["idx"]), what + ": top-k indices"
+    h1g = oracle.bf16_to_f64(host_bits(tr["h1"])[rows])
+    dh1 = np.abs(h1g - ref["h1"])
+    # h1 is a stored bf16 activation: the kernels' fp32 sum and the oracle's fp64 sum,
+    # each rounded once, agree to within one bf16 ulp
+    assert np.all(dh1 <= ulp_bf16(ref["h1"])), what + ": h1 beyond one ulp"
+    assert_bf16_close(host_bits(tr["h1"])[rows], ref["h1"], what + " h1")
+    assert_bf16_close(host_bits(hid)[rows], ref["out"], what + " out", passthrough=dh1)
 
 
 @pytest.fixture(scope="module")
@@ -112,9 +121,7 @@ def test_layer_full_size(h, full_bank, full_layer, M):
                                       (synth.W_D_S, (H_FULL, I_FULL))))
     tokens = sorted(set([0, M // 2, M - 1]))
     ref = L.oracle(hbits, bank, shared, tokens=tokens)
-    assert np.array_equal(tr["idx"].cpu().numpy()[tokens], ref["idx"])
-    assert_bf16_close(host_bits(tr["h1"])[tokens], ref["h1"], "h1 full")
-    assert_bf16_close(host_bits(hid)[tokens], ref["out"], f"layer full M={M}")
+    _check_layer(tr, hid, ref, tokens, f"layer full M={M}")
     # indices of all tokens: bit-exact against the oracle's router on every row
     s_all = L.scores(hbits)
     i_all, _ = oracle.topk(s_all, K_FULL)

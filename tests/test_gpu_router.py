@@ -36,7 +36,7 @@ def _check(h, xbits, Wr, k):
 @pytest.mark.parametrize("M,H,E,k", [(1, 256, 64, 4), (5, 512, 128, 8), (17, 2056, 384, 8), (64, 1024, 40, 16),
                                      (3, 64, 16, 1)])
 def test_router_small(h, M, H, E, k):
-    Wr = synth.f32(E * H, SEED, 3000 + E, 0, 0.05).reshape(E, H)
+    Wr = synth.f32(E * H, SEED, 3000 + E, 0, 0.8 / np.sqrt(H)).reshape(E, H)  # logits ~ N(0, 0.8^2)
     score = lambda rows: oracle.router_scores(rows, Wr)[1]
     xbits, _ = gap_rows(score, M, H, k, base=3100 + H, gap=GAP)
     _check(h, xbits, Wr, k)
