@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Decode-layer benchmark of the GB300 MoE decode library.
+
+One step = one full decode layer (RMSNorm -> input projection 7168->12288 ->
+out-projection 8192->7168 + residual -> RMSNorm -> router/top-8 over 384
+experts -> routed + shared SwiGLU experts 7168->2048->7168 -> combine +
+residual) on a batch of M tokens, through the library's decode_layer entry
+point. Weights are seeded random tensors of the workload's shapes (about
+34.5 GB in HBM); activations are seeded N(0,1) rows. The layer is applied
+repeatedly to its own output, so routing (and the experts read) changes
+every step; the dense weights alternate between two copies. Every step reads
+1.1-25 GB, far more than the 129 MB L2.
+
+Reported (one JSON line, rank 0):
+  value        device-timed microseconds per step at --batch (CUDA events, inputs resident)
+  e2e          same through the C ABI with the step's input copied from pinned
+               host memory and its output copied back inside the timed region
+  sweep        the same for every M in --sweep, with weight-stream GB/s (the
+               unique bytes the step must read, incl. the actual distinct experts U)
+  roofline     dominant kernel of the --batch step: algorithmic bytes / its
+               event-timed duration, against the measured HBM copy bandwidth
+  cpu_baseline the fp64 oracle on the host cores, on one token of the step
+With --impl reference the fp64 oracle is the timed arm.
+
+Multi-GPU (torchrun, --gpus N): the decode layer does not shard across GPUs
+here (replicas only); each rank runs the same workload on its own GPU and the
+time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode layer µs/step and weight-stream HBM GB/s (% of GB300 peak), batch 1–64"
+H, N_IN, K_OUT, E, TOPK, I = 7168, 12288, 8192, 384, 8, 2048
+WORKLOAD = ("full decode layer step: RMSNorm -> input projection (K=7168, N=12288) -> out-projection "
+            "(K=8192, N=7168) + residual -> RMSNorm -> MoE (router W_r[384,7168] fp32, sigmoid, top-8 "
+            "renormalised; 384 routed + 1 shared SwiGLU experts 7168->2048->7168), bf16")
+EXPERT_BYTES = 3 * I * H * 2
+DENSE_BYTES = N_IN * H * 2 + H * K_OUT * 2 + E * H * 4 + 2 * H * 2
+
+
+def step_bytes(M: int, U: float) -> float:
+    """Unique bytes one step must move: weights read once + activations in/out."""
+    act = M * H * 2 * 2 + M * N_IN * 2 * 2
+    return DENSE_BYTES + (U + 1) * EXPERT_BYTES + act
+
+
+def kernel_bytes(tag: str, M: int, U: float) -> float:
+    """Algorithmic bytes of one launch of a kernel of the step."""
+    return {
+        "in_proj": N_IN * H * 2 + M * H * 2 + M * N_IN * 2,
+        "out_proj": H * K_OUT * 2 + M * K_OUT * 2 + 2 * M * H * 2,
+        "router": E * H * 4 + M * H * 2,
+        "gate_up": U * 2 * I * H * 2 + M * TOPK * (H + I) * 2,
+        "down": U * H * I * 2 + M * TOPK * (I * 2 + H * 4),
+        "shared_gate_up": 2 * I * H * 2 + M * (H + I) * 2,
+        "shared_down": H * I * 2 + M * (I * 2 + H * 4),
+    }.get(tag, 0.0)
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------- distributed helpers
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and str(device).startswith("cuda"):
+            dist.barrier(device_ids=[int(str(device).split(":")[1])])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.lines, self.proc, self.th = gpu, [], None, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.th:
+            self.th.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- our arm
+def build_weights(dev: str, copies: int = 2):
+    import torch
+    import moe_layers_gb300 as ML
+    import synth
+
+    def fill_bf16(shape, tid, sigma):
+        t = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        synth.fill_bf16_dev(t.data_ptr(), t.numel(), 0, tid, 0, sigma)
+        return t
+
+    Wg = fill_bf16((E, I, H), synth.W_G, 0.02)
+    Wu = fill_bf16((E, I, H), synth.W_U, 0.02)
+    Wd = fill_bf16((E, H, I), synth.W_D, 0.02)
+    Ws = (fill_bf16((I, H), synth.W_G_S, 0.02), fill_bf16((I, H), synth.W_U_S, 0.02),
+          fill_bf16((H, I), synth.W_D_S, 0.02))
+    Wr = torch.empty((E, H), dtype=torch.float32, device=dev)
+    synth.fill_f32_dev(Wr.data_ptr(), Wr.numel(), 0, synth.W_R, 0, 0.01)
+    ones = torch.ones(H, dtype=torch.bfloat16, device=dev)
+    layers = []
+    for c in range(copies):
+        W_in = fill_bf16((N_IN, H), synth.W_IN, 0.02)
+        W_o = fill_bf16((H, K_OUT), synth.W_O, 0.02)
+        layers.append(ML.LayerWeights(gamma1=ones, W_in=W_in, W_o=W_o, gamma2=ones, W_r=Wr, Wg=Wg, Wu=Wu, Wd=Wd,
+                                      Wg_s=Ws[0], Wu_s=Ws[1], Wd_s=Ws[2], k=TOPK, k_out=K_OUT))
+    torch.cuda.synchronize()
+    return layers
+
+
+def run_ours(args, rank, local, world):
+    import numpy as np
+    import torch
+    import moe_layers_gb300 as ML
+    import synth
+
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    ML.build()
+    h = ML.Handle(local)
+    layers = build_weights(dev)
+    cws = [L.c_struct() for L in layers]
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+    sweep = sorted(set([int(m) for m in args.sweep.split(",") if m] + [args.batch]))
+    results = {}
+    clocks = ClockSampler(local)
+    clock_started = False
+
+    for M in sweep:
+        ws = h.workspace(("bench", M), ML.decode_layer_workspace_size(h, layers[0], M),
+                         ("layer", M))
+        x0 = synth.bf16_rows(synth.X_BASE + 100, range(M), H, 0)
+        host_in = torch.from_numpy(x0.view(np.int16)).view(torch.bfloat16).reshape(M, H).pin_memory()
+        host_out = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
+        hidden = host_in.to(dev)
+        K = args.steps
+        idx_all = torch.empty((K, M, TOPK), dtype=torch.int32, device=dev)
+
+        def step(i, trace=None):
+            ML.decode_layer(h, layers[i % 2], hidden, trace=trace, ws=ws, _cw=cws[i % 2])
+
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        # ---- timed: inputs resident, K steps
+        if not clock_started:
+            clocks.start()
+            clock_started = True
+            time.sleep(0.3)
+        barrier(dev)
+        torch.cuda.synchronize()
+        launches0 = h.launch_count
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(K):
+            step(i, trace={"idx": idx_all[i]})
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dev)
+        us = ev0.elapsed_time(ev1) * 1000.0 / K
+        launches = h.launch_count - launches0
+        us_max = reduce_max(us, dev)
+        idx_host = idx_all.cpu().numpy()
+        U = float(np.mean([len(np.unique(idx_host[i])) for i in range(K)]))
+        # ---- profiled pass: per-kernel event times (separate; events break PDL overlap)
+        h.set_profiling(True)
+        for i in range(K):
+            step(i, trace={"idx": idx_all[i]})
+        prof = h.profile_read()
+        h.set_profiling(False)
+        idx_host = idx_all.cpu().numpy()
+        U_prof = float(np.mean([len(np.unique(idx_host[i])) for i in range(K)]))
+        # ---- end to end: H2D of the step's input, the layer, D2H of its output
+        torch.cuda.synchronize()
+        barrier(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            hidden.copy_(host_in, non_blocking=True)
+            step(i)
+            host_out.copy_(hidden, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us_e2e = reduce_max(e0.elapsed_time(e1) * 1000.0 / K, dev)
+        b = step_bytes(M, U)
+        kern = {}
+        for tag, (n, ms) in prof.items():
+            avg_us = ms * 1000.0 / max(n, 1)
+            kb = kernel_bytes(tag, M, U_prof)
+            kern[tag] = {"launches_per_step": n / K, "avg_us": round(avg_us, 2),
+                         "GBps": round(kb / (avg_us * 1e3), 1) if kb and avg_us > 0 else None}
+        results[M] = dict(M=M, us_per_step=round(us_max, 2), e2e_us=round(us_e2e, 2), U=round(U, 2),
+                          step_bytes=int(b), weight_stream_GBps=round(b / (us_max * 1e3), 1),
+                          hbm_frac=round(b / (us_max * 1e3) / peaks["hbm_gbs"], 4),
+                          kernels_per_step=launches / K, gpu_launches=launches, kernels=kern)
+    clk = clocks.stop()
+    if h.check_device_error() != ML.DEC_OK:
+        raise RuntimeError("device error word set during the benchmark")
+
+    hl = results[args.batch]
+    dom = max((t for t in hl["kernels"] if kernel_bytes(t, args.batch, 1.0) > 0),
+              key=lambda t: hl["kernels"][t]["avg_us"] * hl["kernels"][t]["launches_per_step"])
+    dk = hl["kernels"][dom]
+    achieved = dk["GBps"]
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None, "traffic": None,
+                "peak_source": peaks["source"], "avg_us": dk["avg_us"]}
+    out = {"metric": METRIC, "value": hl["us_per_step"], "unit": "us/step", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(hl["us_per_step"] / 1000.0, 5), "higher_is_better": False,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic: seeded random-init weights of the workload's shapes, seeded N(0,1) activations",
+           "config": {"workload": WORKLOAD, "batch": args.batch, "parallelism": "replicas" if world > 1 else "1 GPU",
+                      "l2": "inputs larger than L2: each step reads >= 1.1 GB (L2 129 MB); dense weights alternate "
+                            "between 2 copies; routing changes every step",
+                      "weight_stream_GBps": hl["weight_stream_GBps"], "hbm_frac": hl["hbm_frac"],
+                      "distinct_experts_U": hl["U"],
+                      "sweep": [{k: v for k, v in results[m].items() if k != "kernels"} for m in sweep],
+                      "kernels_at_batch": hl["kernels"]},
+           "weight_stream_GBps": hl["weight_stream_GBps"], "hbm_frac": hl["hbm_frac"],
+           "roofline": roofline,
+           "e2e": {"value": hl["e2e_us"], "unit": "us/step", "h2d_bytes_per_step": args.batch * H * 2,
+                   "d2h_bytes_per_step": args.batch * H * 2},
+           "gpu_launches": hl["gpu_launches"], "clocks": clk}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.batch, steps=1)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    h.close()
+
+
+# ---------------------------------------------------------------------------- oracle arm
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    env = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    return int(env) if env else (os.cpu_count() or 1)
+
+
+class _OracleSample:
+    """One token of the decode-layer step, as the fp64 oracle computes it.
+    Input bytes (weights, the token) are generated before any timing."""
+
+    def __init__(self, M: int):
+        import numpy as np
+        import synth
+        self.M = M
+        self.W_in = synth.bf16(N_IN * H, 0, synth.W_IN, 0, 0.02).reshape(N_IN, H)
+        self.W_o = synth.bf16(H * K_OUT, 0, synth.W_O, 0, 0.02).reshape(H, K_OUT)
+        self.Wr = synth.f32(E * H, 0, synth.W_R, 0, 0.01).reshape(E, H)
+        self.g = np.full(H, 0x3F80, dtype=np.uint16)
+        self.x = synth.bf16_rows(synth.X_BASE + 100, [0], H, 0)
+        self.shared = (synth.bf16(I * H, 0, synth.W_G_S, 0, 0.02).reshape(I, H),
+                       synth.bf16(I * H, 0, synth.W_U_S, 0, 0.02).reshape(I, H),
+                       synth.bf16(H * I, 0, synth.W_D_S, 0, 0.02).reshape(H, I))
+        self.cache = {}
+
+    def expert(self, e: int):
+        import synth
+        if e not in self.cache:
+            n = I * H
+            self.cache[e] = (synth.bf16(n, 0, synth.W_G, e * n, 0.02).reshape(I, H),
+                             synth.bf16(n, 0, synth.W_U, e * n, 0.02).reshape(I, H),
+                             synth.bf16(n, 0, synth.W_D, e * n, 0.02).reshape(H, I))
+        return self.cache[e]
+
+    def prepare(self):
+        """Route the token once so that its experts' bytes exist before timing."""
+        import oracle
+        r = oracle.decode_layer(self.x, self.g, self.W_in, self.W_o, self.g, self.Wr, TOPK, self.expert, self.shared,
+                                k_out=K_OUT)
+        for e in r["idx"][0]:
+            self.expert(int(e))
+
+    def run(self) -> float:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.decode_layer(self.x, self.g, self.W_in, self.W_o, self.g, self.Wr, TOPK, self.expert, self.shared,
+                            k_out=K_OUT)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(M: int, steps: int = 1) -> dict:
+    s = _OracleSample(M)
+    s.prepare()
+    secs = [s.run() for _ in range(max(1, steps))]
+    per_token_us = statistics.median(secs) * 1e6
+    return {"value": round(per_token_us * M, 1), "unit": "us/step", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"1 token of the M={M} decode-layer step (fp64 numpy oracle, weights widened inside), "
+                      f"scaled by M; median of {len(secs)} run(s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    s = _OracleSample(args.batch)
+    s.prepare()
+    for _ in range(args.warmup):
+        s.run()
+    secs = [s.run() for _ in range(args.steps)]
+    us = sum(secs) / len(secs) * 1e6 * args.batch
+    cb = {"value": round(us, 1), "unit": "us/step", "cores": blas_threads(), "kind": "oracle",
+          "sample": f"1 token of the M={args.batch} decode-layer step per timed step, scaled by M"}
+    print(json.dumps({"metric": METRIC, "value": round(us, 1), "unit": "us/step", "impl": "reference",
+                      "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False, "scaling": "weak",
+                      "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs as the GPU arm)",
+                      "config": {"workload": WORKLOAD, "batch": args.batch, "parallelism": "host cores"},
+                      "cpu_baseline": cb,
+                      "e2e": {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=1, help="headline batch M (1..64)")
+    ap.add_argument("--sweep", default="1,2,4,8,16,32,64")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps < 2:
+        ap.error("--steps must be at least 2")
+    rank, local, world = dist_env()
+    if args.impl == "reference":
+        if world > 1 and args.steps > 3:
+            args.steps = min(args.steps, 20)
+        if args.steps > 20:
+            args.steps = 20
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl", device_id=torch.device(f"cuda:{local}"))
+    try:
+        run_ours(args, rank, local, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -25,10 +25,11 @@
  *    16-byte aligned and every K (inner extent) a multiple of 8.
  *  - Calls are asynchronous on the given stream and never allocate device
  *    memory. Scratch space is the caller's workspace `ws` of `ws_bytes`
- *    bytes, sized by the matching *_workspace_size() query. Before its first
- *    use a workspace must be zeroed (dec_workspace_init); every call leaves
- *    it in that reusable state. One workspace must not be used by two calls
- *    that can run at the same time.
+ *    bytes, sized by the matching *_workspace_size() query. A workspace must
+ *    be zeroed (dec_workspace_init) before its first use and before it is
+ *    reused by a call of another entry point or another shape; calls of the
+ *    same entry point and shape leave it ready for the next one. One
+ *    workspace must not be used by two calls that can run at the same time.
  *  - Arguments are checked on the host before anything is launched; a bad
  *    argument returns DEC_ERR_INVALID_ARG or DEC_ERR_UNSUPPORTED and launches
  *    nothing. A failed launch returns DEC_ERR_CUDA. No call aborts, exits or

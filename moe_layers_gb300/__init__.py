@@ -165,13 +165,17 @@ class Handle:
         except Exception:
             pass
 
-    def workspace(self, key, nbytes: int, stream=None):
-        """A zero-initialised workspace of at least nbytes, reused per key."""
+    def workspace(self, key, nbytes: int, layout=None):
+        """A workspace of at least nbytes, reused per key. It is zeroed when it
+        is created and whenever the layout (entry point and shape) that uses it
+        changes, as the C ABI requires; calls with the same layout leave it ready."""
         import torch
-        t = self._ws.get(key)
+        t, last = self._ws.get(key, (None, None))
         if t is None or t.numel() < nbytes:
             t = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=f"cuda:{self.device}")
-            self._ws[key] = t
+        elif layout != last:
+            t.zero_()
+        self._ws[key] = (t, layout)
         return t
 
     def set_force_variant(self, v: int) -> None:
@@ -220,7 +224,7 @@ def dec_linear(h: Handle, x, W, y=None, stream=None, ws=None):
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     nb = ctypes.c_size_t()
     _check(lib.dec_linear_workspace_size(h.ptr, M, N, K, ctypes.byref(nb)), "dec_linear_workspace_size")
-    ws = h.workspace(("linear", id(stream)), nb.value) if ws is None else ws
+    ws = h.workspace(("linear", id(stream)), nb.value, ("linear", M, N, K)) if ws is None else ws
     _check(lib.dec_linear(h.ptr, _ptr(x), _rows(x, "x"), _ptr(W), _ptr(y), M, N, K, _ptr(ws), ws.numel(),
                           _stream(stream)), "dec_linear")
     return y
@@ -239,7 +243,7 @@ def dec_linear_residual(h: Handle, x, W, r, out=None, stream=None, ws=None):
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     nb = ctypes.c_size_t()
     _check(lib.dec_linear_workspace_size(h.ptr, M, N, K, ctypes.byref(nb)), "dec_linear_workspace_size")
-    ws = h.workspace(("linear", id(stream)), nb.value) if ws is None else ws
+    ws = h.workspace(("linear", id(stream)), nb.value, ("linear", M, N, K)) if ws is None else ws
     _check(lib.dec_linear_residual(h.ptr, _ptr(x), _rows(x, "x"), _ptr(W), _ptr(r), _ptr(out), M, N, K, _ptr(ws),
                                    ws.numel(), _stream(stream)), "dec_linear_residual")
     return out
@@ -271,7 +275,7 @@ def moe_route_topk(h: Handle, x, Wr, k: int, want_scores: bool = True, stream=No
     scores = torch.empty((M, E), dtype=torch.float32, device=x.device) if want_scores else None
     nb = ctypes.c_size_t()
     _check(lib.moe_route_topk_workspace_size(h.ptr, M, H, E, ctypes.byref(nb)), "moe_route_topk_workspace_size")
-    ws = h.workspace(("router", id(stream)), nb.value)
+    ws = h.workspace(("router", id(stream)), nb.value, ("router", M, H, E))
     _check(lib.moe_route_topk(h.ptr, _ptr(x), _ptr(Wr), M, H, E, int(k), _ptr(idx), _ptr(w), _ptr(scores),
                               _ptr(ws), ws.numel(), _stream(stream)), "moe_route_topk")
     return idx, w, scores
@@ -295,7 +299,7 @@ def moe_experts(h: Handle, x, idx, w, Wg, Wu, Wd, shared: Optional[Sequence] = N
         out = torch.empty_like(x)
     nb = ctypes.c_size_t()
     _check(lib.moe_experts_workspace_size(h.ptr, M, k, E, H, I, ctypes.byref(nb)), "moe_experts_workspace_size")
-    ws = h.workspace(("experts", id(stream)), nb.value)
+    ws = h.workspace(("experts", id(stream)), nb.value, ("experts", M, k, E, H, I))
     _check(lib.moe_experts(h.ptr, _ptr(x), _ptr(idx), _ptr(w), M, k, _ptr(Wg), _ptr(Wu), _ptr(Wd), E, H, I,
                            _ptr(sg), _ptr(su), _ptr(sd), _ptr(residual), _ptr(out), _ptr(ws), ws.numel(),
                            _stream(stream)), "moe_experts")
@@ -343,27 +347,32 @@ def decode_layer_workspace_size(h: Handle, weights: LayerWeights, M: int) -> int
     return nb.value
 
 
-def decode_layer(h: Handle, weights: LayerWeights, hidden, trace: bool = False, stream=None, ws=None,
-                 _cw=None):
-    """One decode layer in place on hidden bf16 [M,H]. With trace=True returns
-    a dict of intermediates (h1, idx, w, scores) as device tensors."""
+def decode_layer(h: Handle, weights: LayerWeights, hidden, trace=False, stream=None, ws=None, _cw=None):
+    """One decode layer in place on hidden bf16 [M,H].
+
+    trace=True returns a dict of new device tensors with the intermediates
+    (h1, idx, w, scores); trace may also be a dict of preallocated tensors
+    (any of those keys, others omitted) that receive them."""
     import torch
     lib = _load()
     _require(hidden, torch.bfloat16, "hidden", 2)
     M = hidden.shape[0]
     cw = weights.c_struct() if _cw is None else _cw
     if ws is None:
-        ws = h.workspace(("layer", id(stream)), decode_layer_workspace_size(h, weights, M))
+        ws = h.workspace(("layer", id(stream)), decode_layer_workspace_size(h, weights, M),
+                         ("layer", M, cw.H, cw.N_in, cw.K_out, cw.E, cw.k, cw.I))
     tr = None
     out = None
-    if trace:
-        E = cw.E
+    if trace is True:
         out = dict(h1=torch.empty_like(hidden),
                    idx=torch.empty((M, cw.k), dtype=torch.int32, device=hidden.device),
                    w=torch.empty((M, cw.k), dtype=torch.float32, device=hidden.device),
-                   scores=torch.empty((M, E), dtype=torch.float32, device=hidden.device))
+                   scores=torch.empty((M, cw.E), dtype=torch.float32, device=hidden.device))
+    elif isinstance(trace, dict):
+        out = trace
+    if out is not None:
         tr = _LayerTrace()
-        tr.h1, tr.idx, tr.w, tr.scores = (_ptr(out[n]) for n in ("h1", "idx", "w", "scores"))
+        tr.h1, tr.idx, tr.w, tr.scores = (_ptr(out.get(n)) for n in ("h1", "idx", "w", "scores"))
     _check(lib.decode_layer(h.ptr, ctypes.byref(cw), _ptr(hidden), M, ctypes.byref(tr) if tr is not None else None,
                             _ptr(ws), ws.numel(), _stream(stream)), "decode_layer")
     return out

@@ -72,10 +72,19 @@ struct EngineRegion {
   int* counters = nullptr;
 };
 
+// Split-K tile counters must be zero when a call starts (each call leaves them
+// zero). They are carved first in every layout, so that a workspace reused by
+// a call of another shape finds its counters in bytes that were counters before.
+void carve_counters(Carver& c, EngineRegion& r, long long max_tiles) {
+  r.counters = c.take<int>((size_t)std::max<long long>(max_tiles, 1));
+}
+void carve_partials(Carver& c, EngineRegion& r, int grid, int nacc) {
+  r.partials = c.take<float>((size_t)2 * grid * nacc * kTileN * kMaxCols);
+}
 EngineRegion carve_engine(Carver& c, int grid, int nacc, long long max_tiles) {
   EngineRegion r;
-  r.partials = c.take<float>((size_t)2 * grid * nacc * kTileN * kMaxCols);
-  r.counters = c.take<int>((size_t)std::max<long long>(max_tiles, 1));
+  carve_counters(c, r, max_tiles);
+  carve_partials(c, r, grid, nacc);
   return r;
 }
 
@@ -132,8 +141,12 @@ struct MoeWs {
 
 long long moe_tiles(int E, int H, int I) { return (long long)E * (std::max(H, I) / kTileN); }
 
-void carve_moe(Carver& c, const dec_handle* h, int M, int k, int E, int H, int I, long long extra_tiles,
-               MoeWs* w) {
+void carve_moe_counters(Carver& c, int E, int H, int I, long long extra_tiles, MoeWs* w) {
+  carve_counters(c, w->r0, std::max(moe_tiles(E, H, I), extra_tiles));
+  carve_counters(c, w->r1, std::max(H, I) / kTileN);
+}
+
+void carve_moe_data(Carver& c, const dec_handle* h, int M, int k, int E, int H, int I, MoeWs* w) {
   const int n = M * k;
   w->table = c.take<int>(TableLayout(E, n).words());
   w->xs = c.take<uint16_t>((size_t)n * H);
@@ -141,8 +154,14 @@ void carve_moe(Carver& c, const dec_handle* h, int M, int k, int E, int H, int I
   w->y = c.take<float>((size_t)n * H);
   w->hs = c.take<uint16_t>((size_t)M * I);
   w->ys = c.take<float>((size_t)M * H);
-  w->r0 = carve_engine(c, engine_grid(h), 2, std::max(moe_tiles(E, H, I), extra_tiles));
-  w->r1 = carve_engine(c, engine_grid(h), 2, std::max(H, I) / kTileN);
+  carve_partials(c, w->r0, engine_grid(h), 2);
+  carve_partials(c, w->r1, engine_grid(h), 2);
+}
+
+void carve_moe(Carver& c, const dec_handle* h, int M, int k, int E, int H, int I, long long extra_tiles,
+               MoeWs* w) {
+  carve_moe_counters(c, E, H, I, extra_tiles, w);
+  carve_moe_data(c, h, M, k, E, H, I, w);
 }
 
 bool moe_shape_ok(int M, int k, int E, int H, int I) {
@@ -291,6 +310,8 @@ bool layer_ok(const dec_layer_weights* L, int M) {
 
 void carve_layer(Carver& c, const dec_handle* h, const dec_layer_weights* L, int M, LayerWs* w) {
   const int H = L->H;
+  const long long dense_tiles = std::max<long long>((L->N_in + kTileN - 1) / kTileN, H / kTileN);
+  carve_moe_counters(c, L->E, H, L->I, dense_tiles, &w->moe);
   w->a = c.take<uint16_t>((size_t)M * H);
   w->yin = c.take<uint16_t>((size_t)M * L->N_in);
   w->h1 = c.take<uint16_t>((size_t)M * H);
@@ -298,8 +319,7 @@ void carve_layer(Carver& c, const dec_handle* h, const dec_layer_weights* L, int
   w->parts = c.take<float>((size_t)router_ksplit(H) * M * L->E);
   w->idx = c.take<int32_t>((size_t)M * L->k);
   w->w = c.take<float>((size_t)M * L->k);
-  const long long dense_tiles = std::max<long long>((L->N_in + kTileN - 1) / kTileN, H / kTileN);
-  carve_moe(c, h, M, L->k, L->E, H, L->I, dense_tiles, &w->moe);
+  carve_moe_data(c, h, M, L->k, L->E, H, L->I, &w->moe);
 }
 
 }  // namespace
