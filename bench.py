@@ -50,6 +50,13 @@ EXPERT_BYTES = 3 * I * H * 2
 DENSE_BYTES = N_IN * H * 2 + H * K_OUT * 2 + E * H * 4 + 2 * H * 2
 
 
+def set_experts(n: int) -> None:
+    """Routed experts in the bank (384 for the workload; fewer only for small profiling captures)."""
+    global E, DENSE_BYTES
+    E = int(n)
+    DENSE_BYTES = N_IN * H * 2 + H * K_OUT * 2 + E * H * 4 + 2 * H * 2
+
+
 def step_bytes(M: int, U: float) -> float:
     """Unique bytes one step must move: weights read once + activations in/out."""
     act = M * H * 2 * 2 + M * N_IN * 2 * 2
@@ -286,7 +293,8 @@ def run_ours(args, rank, local, world):
            "warmup": args.warmup, "ms_per_step": round(hl["us_per_step"] / 1000.0, 5), "higher_is_better": False,
            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
            "data": "synthetic: seeded random-init weights of the workload's shapes, seeded N(0,1) activations",
-           "config": {"workload": WORKLOAD, "batch": args.batch, "parallelism": "replicas" if world > 1 else "1 GPU",
+           "config": {"workload": WORKLOAD if E == 384 else WORKLOAD + f" (profiling variant: {E} routed experts)",
+                      "batch": args.batch, "parallelism": "replicas" if world > 1 else "1 GPU",
                       "l2": "inputs larger than L2: each step reads >= 1.1 GB (L2 129 MB); dense weights alternate "
                             "between 2 copies; routing changes every step",
                       "weight_stream_GBps": hl["weight_stream_GBps"], "hbm_frac": hl["hbm_frac"],
@@ -401,7 +409,10 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=1, help="headline batch M (1..64)")
     ap.add_argument("--sweep", default="1,2,4,8,16,32,64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=E,
+                    help="routed experts in the bank (default 384, the workload; smaller only for ncu captures)")
     args = ap.parse_args(argv)
+    set_experts(args.experts)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.steps < 2:
