@@ -130,6 +130,27 @@ dec_status dec_linear_residual(dec_handle* h, const dec_bf16* x, int ldx, const 
                                dec_bf16* out, int M, int N, int K, void* ws, size_t ws_bytes,
                                cudaStream_t stream);
 
+/* out[M][N] = [r[M][N] +] x[M][K] W[N][K]^T with no workspace argument and
+ * no device allocation, for callers that cannot provide scratch memory: for
+ * example a plugin running inside a serving runtime whose memory pool owns
+ * all device memory and gives plugins no allocator, or a latency-critical
+ * caller that must not call cudaMalloc (which can block and synchronise the
+ * device). The paper has no counterpart; this is an interface convenience.
+ * It runs the split-K tcgen05 kernel of dec_linear with its scratch (10 MiB
+ * of split-K partial sums and 4 KiB of tile counters) in one static device
+ * array that every GPU loading the library holds until the process exits.
+ * - The first call on a device looks up that array's address
+ *   (cudaGetSymbolAddress, with the handle's device made current); make that
+ *   first call before any stream capture.
+ * - Every call shares the array and it keeps the last call's contents: each
+ *   call clears the counters it uses, and calls that overlap on the GPU (for
+ *   instance on two streams at once) race on it.
+ * - Limits: 1 <= M <= 64 and N <= 131072 (DEC_ERR_UNSUPPORTED beyond), plus
+ *   the shape rules of dec_linear. r may be NULL; out may alias r exactly.
+ * - Calls no cudaMalloc, cudaFree or other allocating routine. */
+dec_status dec_linear_noalloc(dec_handle* h, const dec_bf16* x, int ldx, const dec_bf16* W, const dec_bf16* r,
+                              dec_bf16* out, int M, int N, int K, cudaStream_t stream);
+
 /* y[M][H] = x / sqrt(mean(x^2) + eps) * gamma per row (fp32 math, bf16 out).
  * The RMSNorm of the pre-norm decode layer; not named on the pages. y may
  * alias x. 1 <= M <= 64, 8 <= H <= 65536, H % 8 == 0. */

@@ -70,6 +70,7 @@ def _load():
         "dec_linear_workspace_size": [P, I, I, I, ctypes.POINTER(Z)],
         "dec_linear": [P, P, I, P, P, I, I, I, P, Z, P],
         "dec_linear_residual": [P, P, I, P, P, P, I, I, I, P, Z, P],
+        "dec_linear_noalloc": [P, P, I, P, P, P, I, I, I, P],
         "dec_rmsnorm": [P, P, P, P, I, I, F, P],
         "moe_route_topk_workspace_size": [P, I, I, I, ctypes.POINTER(Z)],
         "moe_route_topk": [P, P, P, I, I, I, I, P, P, P, P, Z, P],
@@ -246,6 +247,21 @@ def dec_linear_residual(h: Handle, x, W, r, out=None, stream=None, ws=None):
     ws = h.workspace(("linear", id(stream)), nb.value, ("linear", M, N, K)) if ws is None else ws
     _check(lib.dec_linear_residual(h.ptr, _ptr(x), _rows(x, "x"), _ptr(W), _ptr(r), _ptr(out), M, N, K, _ptr(ws),
                                    ws.numel(), _stream(stream)), "dec_linear_residual")
+    return out
+
+
+def dec_linear_noalloc(h: Handle, x, W, r=None, out=None, stream=None):
+    """out = [r +] x W^T through the entry point that takes no workspace and
+    allocates nothing (its scratch is a static device array in the library)."""
+    import torch
+    _require(x, torch.bfloat16, "x", 2)
+    _require(W, torch.bfloat16, "W", 2)
+    M, K = x.shape
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(_load().dec_linear_noalloc(h.ptr, _ptr(x), _rows(x, "x"), _ptr(W), _ptr(r), _ptr(out), M, N, K,
+                                      _stream(stream)), "dec_linear_noalloc")
     return out
 
 
