@@ -249,6 +249,7 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
   L.table = ws.table;
   L.E = E;
   L.n_entries = n;
+  L.count = M;  // bound on the tokens of any one expert
   L.out = ws.hbuf;
   L.ldo = I;
   L.partials = ws.r0.partials;
@@ -271,6 +272,7 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
   D.table = ws.table;
   D.E = E;
   D.n_entries = n;
+  D.count = M;
   D.out = ws.y;
   D.ldo = H;
   D.partials = ws.r0.partials;

@@ -71,7 +71,7 @@ struct EngineLaunch {
   int K = 0;
   int N = 0;                     // weight rows per problem
   long long a_rows_per_prob = 0; // row distance between problems in A (0 for one problem)
-  int count = 0;                 // tokens (dense mode)
+  int count = 0;                 // tokens (dense mode); the batch, bounding any expert's tokens (grouped)
   const int* table = nullptr;    // routing table (grouped mode) or null (dense mode, one problem)
   int E = 0;                     // table layout
   int n_entries = 0;

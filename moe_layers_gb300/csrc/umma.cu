@@ -49,17 +49,33 @@ struct EngineParams {
   unsigned long long wait_ns;
 };
 
-template <int NA>
+// Shared-memory plan of one engine instantiation. A stage holds KSUB 64-wide
+// k sub-blocks of NA weight tiles (128 rows x 64 bf16 = 16 KB each, 128-byte
+// swizzle) and of the activation tile (BROWS rows). Single-matrix kernels
+// take two sub-blocks per stage; the SwiGLU kernel already loads two weight
+// tiles (gate and up). The activation slice is sized to the batch, and the
+// ring takes as many stages as the 227 KB of shared memory allow: the weight
+// bytes in flight per SM are what sets the streaming rate.
+template <int NA, int BROWS>
 struct EngineSmem {
-  static constexpr int kABytes = kTileN * kBlockK * 2;     // 16 KB weight tile
-  static constexpr int kBBytes = kMaxCols * kBlockK * 2;    // 8 KB activation tile (up to 64 rows)
-  static constexpr int kStageBytes = NA * kABytes + kBBytes;
-  static constexpr int kStages = (NA == 1) ? 8 : 5;
+  static constexpr int kKSub = (NA == 1) ? 2 : 1;
+  static constexpr int kBK = kBlockK * kKSub;              // reduction elements per k-block (stage)
+  static constexpr int kABox = kTileN * kBlockK * 2;       // 16 KB weight box
+  static constexpr int kBBox = BROWS * kBlockK * 2;        // activation box of one sub-block
+  static constexpr int kABytes = NA * kKSub * kABox;
+  static constexpr int kStageBytes = kABytes + kKSub * kBBox;
+  static constexpr int kBudget = 232448 - 1024 - 512;      // opt-in maximum minus alignment and barriers
+  static constexpr int kStages = (kBudget / kStageBytes) < 12 ? (kBudget / kStageBytes) : 12;
   static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kNumBars = 2 * kStages + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kTotal = kMiscOff + 64 + 1024;       // + alignment slack
-  static constexpr uint32_t kTmemCols = NA * kMaxCols * 2;  // two accumulator buffers
+  static constexpr int kTotal = kMiscOff + 64 + 1024;      // + alignment slack
+  static constexpr uint32_t kTmemCols = NA * kMaxCols * 2; // two accumulator buffers
+  static_assert(kStages >= 3, "engine ring too shallow");
+  static_assert(kTotal <= 232448, "engine shared memory above the opt-in maximum");
+  // Offsets inside a stage.
+  __device__ static constexpr int a_off(int u, int a) { return (u * NA + a) * kABox; }
+  __device__ static constexpr int b_off(int u) { return kABytes + u * kBBox; }
 };
 
 __device__ __forceinline__ long long range_start(long long c, long long W, long long G) { return c * W / G; }
@@ -95,12 +111,12 @@ static __device__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err,
   }
 }
 
-template <int EPI>
+template <int EPI, int BROWS>
 __global__ void __launch_bounds__(kEngineThreads, 1)
     engine_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                   const __grid_constant__ CUtensorMap tmB, const EngineParams P) {
   constexpr int NA = (EPI == EPI_SWIGLU) ? 2 : 1;
-  using S = EngineSmem<NA>;
+  using S = EngineSmem<NA, BROWS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
@@ -154,12 +170,20 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
       long long issued = 0;
       auto load_A = [&](int s, int tau, int kb, long long a_row) {
         uint8_t* st = smem + s * S::kStageBytes;
-        tma_load_2d(st, &tmA, &full[s], kb * kBlockK, (int)a_row, pol_w);
-        if (NA == 2) tma_load_2d(st + S::kABytes, &tmA2, &full[s], kb * kBlockK, (int)a_row, pol_w);
+#pragma unroll
+        for (int u = 0; u < S::kKSub; ++u) {
+          const int k0 = (kb * S::kKSub + u) * kBlockK;
+          tma_load_2d(st + S::a_off(u, 0), &tmA, &full[s], k0, (int)a_row, pol_w);
+          if (NA == 2) tma_load_2d(st + S::a_off(u, 1), &tmA2, &full[s], k0, (int)a_row, pol_w);
+        }
       };
       auto load_B = [&](int s, int kb, int row0, int nb) {
-        uint8_t* st = smem + s * S::kStageBytes + NA * S::kABytes;
-        for (int b = 0; b < nb; ++b) tma_load_2d(st + b * 2048, &tmB, &full[s], kb * kBlockK, row0 + 16 * b, pol_x);
+        uint8_t* st = smem + s * S::kStageBytes;
+#pragma unroll
+        for (int u = 0; u < S::kKSub; ++u) {
+          const int k0 = (kb * S::kKSub + u) * kBlockK;
+          for (int b = 0; b < nb; ++b) tma_load_2d(st + S::b_off(u) + b * 2048, &tmB, &full[s], k0, row0 + 16 * b, pol_x);
+        }
       };
       if (P.table == nullptr) {
         // Dense: the k-block range is known before the dependency wait, so the
@@ -168,7 +192,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
         const long long W = (long long)tiles * KB;
         const long long j0 = range_start(c, W, G), j1 = range_start(c + 1, W, G);
         const int nb = (P.count + 15) >> 4;
-        const uint32_t bytes = NA * S::kABytes + nb * 2048;
+        const uint32_t bytes = S::kABytes + S::kKSub * nb * 2048;
         const long long npre = min(j1 - j0, (long long)S::kStages);
         for (long long i = 0; i < npre; ++i) {
           const long long j = j0 + i;
@@ -201,7 +225,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
           const Prob pr = prob_info(P, tau / tiles);
           const int nb = (pr.cnt + 15) >> 4;
           if (!mbar_wait(&empty[s], ph ^ 1u, wc)) break;
-          mbar_arrive_expect_tx(&full[s], NA * S::kABytes + nb * 2048);
+          mbar_arrive_expect_tx(&full[s], S::kABytes + S::kKSub * nb * 2048);
           load_A(s, tau, kb, (long long)pr.e * P.a_rows_per_prob + (long long)(tau % tiles) * kTileN);
           load_B(s, kb, pr.off, nb);
           issued = i + 1;
@@ -237,14 +261,17 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + s * S::kStageBytes);
-          const uint32_t b_addr = a_addr + NA * S::kABytes;
+          const uint32_t st_addr = smem_u32(smem + s * S::kStageBytes);
 #pragma unroll
-          for (int kk = 0; kk < kBlockK / 16; ++kk) {
-            const uint64_t bd = sw128_desc(b_addr + kk * 32);
-            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-            umma_bf16(d0, sw128_desc(a_addr + kk * 32), bd, idesc, acc);
-            if (NA == 2) umma_bf16(d0 + kMaxCols, sw128_desc(a_addr + S::kABytes + kk * 32), bd, idesc, acc);
+          for (int u = 0; u < S::kKSub; ++u) {
+            const uint32_t a_addr = st_addr + S::a_off(u, 0), b_addr = st_addr + S::b_off(u);
+#pragma unroll
+            for (int kk = 0; kk < kBlockK / 16; ++kk) {
+              const uint64_t bd = sw128_desc(b_addr + kk * 32);
+              const uint32_t acc = (kb > kb0 || u > 0 || kk > 0) ? 1u : 0u;
+              umma_bf16(d0, sw128_desc(a_addr + kk * 32), bd, idesc, acc);
+              if (NA == 2) umma_bf16(d0 + kMaxCols, sw128_desc(st_addr + S::a_off(u, 1) + kk * 32), bd, idesc, acc);
+            }
           }
           umma_commit(&empty[s]);
         }
@@ -385,19 +412,41 @@ size_t engine_ws_bytes(int grid, int nacc, long long max_tiles) {
   return al((size_t)2 * grid * nacc * kTileN * kMaxCols * sizeof(float)) + al((size_t)max_tiles * sizeof(int));
 }
 
-template <int EPI>
+template <int EPI, int BROWS>
 static cudaError_t launch_epi(dec_handle* h, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
                               const EngineParams& P, int grid, cudaStream_t s) {
   constexpr int NA = (EPI == EPI_SWIGLU) ? 2 : 1;
+  using S = EngineSmem<NA, BROWS>;
   static bool attr_set = false;  // per process; every device gets the same attribute
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(engine_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         EngineSmem<NA>::kTotal);
+    cudaError_t e =
+        cudaFuncSetAttribute(engine_kernel<EPI, BROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_k(h, engine_kernel<EPI>, dim3(grid), dim3(kEngineThreads), (size_t)EngineSmem<NA>::kTotal, s, ta,
-                  ta2, tb, P);
+  return launch_k(h, engine_kernel<EPI, BROWS>, dim3(grid), dim3(kEngineThreads), (size_t)S::kTotal, s, ta, ta2, tb,
+                  P);
+}
+
+// The dense grid never exceeds the number of k-blocks (a CTA per k-block at most).
+template <int EPI, int BROWS>
+static cudaError_t launch_kb(dec_handle* h, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
+                             EngineParams& P, int grid, cudaStream_t s) {
+  constexpr int NA = (EPI == EPI_SWIGLU) ? 2 : 1;
+  constexpr int BK = EngineSmem<NA, BROWS>::kBK;
+  P.KB = (P.K + BK - 1) / BK;
+  if (P.table == nullptr) grid = (int)std::min<long long>(grid, (long long)P.tiles * P.KB);
+  return launch_epi<EPI, BROWS>(h, ta, ta2, tb, P, grid < 1 ? 1 : grid, s);
+}
+
+// Activation rows per stage: the smallest of 16 / 32 / 64 that holds the
+// largest token count of any problem in the launch.
+template <int EPI>
+static cudaError_t launch_rows(dec_handle* h, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
+                               EngineParams& P, int max_cols, int grid, cudaStream_t s) {
+  if (max_cols <= 16) return launch_kb<EPI, 16>(h, ta, ta2, tb, P, grid, s);
+  if (max_cols <= 32) return launch_kb<EPI, 32>(h, ta, ta2, tb, P, grid, s);
+  return launch_kb<EPI, 64>(h, ta, ta2, tb, P, grid, s);
 }
 
 cudaError_t launch_engine(dec_handle* h, const EngineLaunch& L, cudaStream_t s) {
@@ -415,7 +464,7 @@ cudaError_t launch_engine(dec_handle* h, const EngineLaunch& L, cudaStream_t s) 
   const int nacc = (L.epi == EPI_SWIGLU) ? 2 : 1;
   EngineParams P;
   P.K = L.K;
-  P.KB = (L.K + kBlockK - 1) / kBlockK;
+  P.KB = 0;  // set per instantiation (k-block width depends on the stage plan)
   P.N = L.N;
   P.tiles = (L.N + kTileN - 1) / kTileN;
   P.a_rows_per_prob = L.a_rows_per_prob;
@@ -433,13 +482,13 @@ cudaError_t launch_engine(dec_handle* h, const EngineLaunch& L, cudaStream_t s) 
   P.counters = L.counters;
   P.err = h->d_err;
   P.wait_ns = h->wait_ns;
-  int grid = L.grid > 0 ? L.grid : engine_grid(h);
-  if (L.table == nullptr) grid = (int)std::min<long long>(grid, (long long)P.tiles * P.KB);
-  if (grid < 1) grid = 1;
+  const int grid = L.grid > 0 ? L.grid : engine_grid(h);
+  const int max_cols = L.count;  // dense: the tokens; grouped: the batch, a bound on any expert's tokens
+  if (max_cols < 1 || max_cols > kMaxCols) return cudaErrorInvalidValue;
   switch (L.epi) {
-    case EPI_LINEAR: return launch_epi<EPI_LINEAR>(h, ta, ta2, tb, P, grid, s);
-    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(h, ta, ta2, tb, P, grid, s);
-    default: return launch_epi<EPI_F32>(h, ta, ta2, tb, P, grid, s);
+    case EPI_LINEAR: return launch_rows<EPI_LINEAR>(h, ta, ta2, tb, P, max_cols, grid, s);
+    case EPI_SWIGLU: return launch_rows<EPI_SWIGLU>(h, ta, ta2, tb, P, max_cols, grid, s);
+    default: return launch_rows<EPI_F32>(h, ta, ta2, tb, P, max_cols, grid, s);
   }
 }
 
