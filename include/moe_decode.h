@@ -63,7 +63,7 @@ typedef enum dec_status {
 
 /* Kernel families of the projections [K3 P1§1]. */
 typedef enum dec_variant {
-  DEC_VARIANT_AUTO = 0,    /* choose by batch: SMALL_M for M <= 2, SPLIT_K above */
+  DEC_VARIANT_AUTO = 0,    /* choose by batch: SMALL_M for M = 1, SPLIT_K above (measured faster at M = 2) */
   DEC_VARIANT_SMALL_M = 1, /* CUDA-core small-matrix kernel: each CTA streams whole weight rows */
   DEC_VARIANT_SPLIT_K = 2  /* tcgen05 kernel; the weight k-blocks are split evenly over all SMs */
 } dec_variant;
@@ -114,8 +114,9 @@ dec_status dec_check_device_error(dec_handle* h);
 dec_status dec_linear_workspace_size(const dec_handle* h, int M, int N, int K, size_t* bytes);
 
 /* y[M][N] = x[M][K] W[N][K]^T  (bf16 in, fp32 accumulate, bf16 out).
- * [K3 P1§1], [hu-sum]: the small-matrix kernel at M <= 2, the split-K tcgen05
- * kernel above (or as forced). x has row stride ldx >= K elements (ldx = K
+ * [K3 P1§1], [hu-sum]: the small-matrix kernel at M = 1, the split-K tcgen05
+ * kernel above (or as forced; the pages use the small-matrix kernel at batch
+ * 1-2, but on GB300 the split-K kernel measured faster at batch 2). x has row stride ldx >= K elements (ldx = K
  * for a dense matrix; a larger stride reads the leading K columns of a wider
  * activation). 1 <= M <= 64, N >= 1, 8 <= K, K % 8 == 0, ldx % 8 == 0.
  * y must not overlap x or W. */

@@ -31,8 +31,10 @@ def nvcc() -> str:
 
 
 def flags() -> list:
+    # MOE_DECODE_NVCC_EXTRA: extra nvcc flags (e.g. -DDEC_ENGINE_KSUB_SINGLE=4) for tuning builds.
+    extra = os.environ.get("MOE_DECODE_NVCC_EXTRA", "").split()
     return ["-O3", "-std=c++17", f"-gencode=arch=compute_{ARCH},code=sm_{ARCH}", "-lineinfo",
-            "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
+            "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")] + extra
 
 
 def _mtime(p: str) -> float:
@@ -41,6 +43,14 @@ def _mtime(p: str) -> float:
 
 def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
+    stamp = os.path.join(BUILD, "flags.txt")
+    want = " ".join(flags())
+    if not os.path.exists(stamp) or open(stamp).read() != want:
+        for f in os.listdir(BUILD):
+            if f.endswith(".o"):
+                os.remove(os.path.join(BUILD, f))
+        with open(stamp, "w") as fh:
+            fh.write(want)
     deps = [os.path.join(CSRC, h) for h in HEADERS] + [PUBLIC]
     dep_time = max(_mtime(d) for d in deps)
     jobs = []

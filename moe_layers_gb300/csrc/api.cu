@@ -94,7 +94,9 @@ bool linear_shape_ok(int M, int N, int K, int ldx) {
 
 int choose_variant(const dec_handle* h, int M, int K) {
   if (h->force_variant == DEC_VARIANT_SMALL_M || h->force_variant == DEC_VARIANT_SPLIT_K) return h->force_variant;
-  return (M <= 2 && gemv_supported(M, K)) ? DEC_VARIANT_SMALL_M : DEC_VARIANT_SPLIT_K;
+  // Measured on GB300 (CUDA-graph replay, 115-240 MB weights): the small-matrix kernel streams at
+  // 6.7-6.9 TB/s with one token but 3.9-4.9 TB/s with two, where the split-K kernel reaches 5.8-6.2.
+  return (M == 1 && gemv_supported(M, K)) ? DEC_VARIANT_SMALL_M : DEC_VARIANT_SPLIT_K;
 }
 
 dec_status linear_impl(dec_handle* h, const uint16_t* x, int ldx, const uint16_t* W, const uint16_t* r, uint16_t* y,
@@ -170,12 +172,13 @@ bool moe_shape_ok(int M, int k, int E, int H, int I) {
 }
 
 // CTAs given to the shared expert while the routed experts run beside it: the
-// shared expert's share of the expected weight bytes (at least one SM, at
-// most half). Expected distinct experts for uniform routing: E (1 - (1 - k/E)^M).
+// shared expert's share of the expected weight bytes, rounded up with a margin
+// (at least one SM, at most half). Expected distinct experts for uniform routing: E (1 - (1 - k/E)^M).
 int shared_grid(const dec_handle* h, int M, int k, int E) {
   if (h->shared_ctas > 0) return std::min(h->shared_ctas, h->sms - 1);
   const double eu = E * (1.0 - std::pow(1.0 - (double)k / E, (double)M));
-  int g = (int)std::lround(h->sms * 1.0 / (1.0 + eu));
+  // Rounded up with a 25% margin: the shared expert must not finish after the routed experts.
+  int g = (int)std::ceil(1.25 * h->sms / (1.0 + eu));
   return std::max(1, std::min(g, h->sms / 2));
 }
 

@@ -1,9 +1,11 @@
-// Small-matrix projection kernel for batch 1..2 (up to 4 when forced).
+// Small-matrix projection kernel: chosen at batch 1, available up to 4 when forced.
 //
 // Kimi K3 article, Part 1 §1 "Ajustar las formas" (and the aihirek.info
 // summary): at batch 1-2 the attention projections use specialised
-// small-matrix kernels. With one or two tokens every weight byte feeds one or
-// two FMAs, so the kernel is a pure weight stream and CUDA cores suffice.
+// small-matrix kernels. With one token every weight byte feeds one FMA, so the
+// kernel is a pure weight stream and CUDA cores suffice; it reaches the HBM
+// copy rate on GB300. At batch 2 the split-K tcgen05 kernel measured faster
+// here, so the automatic choice uses this kernel for one token only.
 //
 // Layout of the work: the N weight rows are divided into one contiguous,
 // equal range per CTA (two 256-thread CTAs per SM), so every SM streams the
@@ -19,6 +21,8 @@
 // The first rows' weight loads are issued before griddepcontrol.wait, so they
 // overlap the previous kernel's tail; activations and the residual are read
 // only after it.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,7 +34,8 @@ template <int M, int VPT>
 __global__ void __launch_bounds__(kGemvThreads, 2)
     gemv_kernel(const uint16_t* x, long long ldx, const uint16_t* __restrict__ W, const uint16_t* res, long long ldr,
                 uint16_t* y, long long ldy, int N, int K) {
-  constexpr int RB = (8 / VPT) > 0 ? (8 / VPT) : 1;  // rows per step
+  // Rows per step: 8 (M = 1) or 4 (M > 1) weight vectors per thread in flight, kept within 128 registers.
+  constexpr int RB = ((M == 1 ? 8 : 4) / VPT) > 0 ? ((M == 1 ? 8 : 4) / VPT) : 1;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int K8 = K >> 3;
   const long long G = gridDim.x;

@@ -56,22 +56,34 @@ struct EngineParams {
 // tiles (gate and up). The activation slice is sized to the batch, and the
 // ring takes as many stages as the 227 KB of shared memory allow: the weight
 // bytes in flight per SM are what sets the streaming rate.
+// Upper bound on the pieces one tile is split into: at most one per CTA, and
+// the grid never exceeds this (checked on the host).
+constexpr int kMaxPieces = 256;
+
+// 64-wide k sub-blocks per stage (build-time tunables; the defaults are the measured best).
+#ifndef DEC_ENGINE_KSUB_SINGLE
+#define DEC_ENGINE_KSUB_SINGLE 2
+#endif
+#ifndef DEC_ENGINE_KSUB_PAIR
+#define DEC_ENGINE_KSUB_PAIR 1
+#endif
+
 template <int NA, int BROWS>
 struct EngineSmem {
-  static constexpr int kKSub = (NA == 1) ? 2 : 1;
+  static constexpr int kKSub = (NA == 1) ? DEC_ENGINE_KSUB_SINGLE : DEC_ENGINE_KSUB_PAIR;
   static constexpr int kBK = kBlockK * kKSub;              // reduction elements per k-block (stage)
   static constexpr int kABox = kTileN * kBlockK * 2;       // 16 KB weight box
   static constexpr int kBBox = BROWS * kBlockK * 2;        // activation box of one sub-block
   static constexpr int kABytes = NA * kKSub * kABox;
   static constexpr int kStageBytes = kABytes + kKSub * kBBox;
-  static constexpr int kBudget = 232448 - 1024 - 512;      // opt-in maximum minus alignment and barriers
+  static constexpr int kBudget = 232448 - 1024 - 512 - 4 * kMaxPieces;  // opt-in maximum minus slack, barriers, pieces
   static constexpr int kStages = (kBudget / kStageBytes) < 12 ? (kBudget / kStageBytes) : 12;
   static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kNumBars = 2 * kStages + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kTotal = kMiscOff + 64 + 1024;      // + alignment slack
+  static constexpr int kTotal = kMiscOff + 16 + 4 * kMaxPieces + 1024;  // + piece list + alignment slack
   static constexpr uint32_t kTmemCols = NA * kMaxCols * 2; // two accumulator buffers
-  static_assert(kStages >= 3, "engine ring too shallow");
+  static_assert(kStages >= 2, "engine ring too shallow");
   static_assert(kTotal <= 232448, "engine shared memory above the opt-in maximum");
   // Offsets inside a stage.
   __device__ static constexpr int a_off(int u, int a) { return (u * NA + a) * kABox; }
@@ -127,6 +139,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kMiscOff + 4);
   volatile int* s_last = reinterpret_cast<volatile int*>(smem + S::kMiscOff + 8);
+  volatile int* s_np = reinterpret_cast<volatile int*>(smem + S::kMiscOff + 12);
+  int* s_piece = reinterpret_cast<int*>(smem + S::kMiscOff + 16);  // kMaxPieces ints
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long G = gridDim.x, c = blockIdx.x;
@@ -298,17 +312,34 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
     uint16_t* out16 = reinterpret_cast<uint16_t*>(P.out);
     float* out32 = reinterpret_cast<float*>(P.out);
 
-    auto emit = [&](const Prob& pr, int n, int jcol, float v0, float v1) {
-      const long long orow = (long long)pr.off + jcol;
+    // Writes columns [ch*16, ch*16 + 16) of this thread's output row n. Residual
+    // values are all loaded first (independent loads in flight together), then
+    // combined and stored.
+    auto emit_chunk = [&](const Prob& pr, int n, int ch, const float (&v0)[16], const float (&v1)[16]) {
+      const int jn = min(16, pr.cnt - ch * 16);
       if (EPI == EPI_LINEAR) {
-        float s = v0;
-        if (P.res != nullptr) s += bf2f(ld_act_u16(P.res + orow * P.ldr + n));
-        out16[orow * P.ldo + n] = f2bf(s);
+        float r[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = 0.f;
+        if (P.res != nullptr) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (i < jn) r[i] = bf2f(ld_act_u16(P.res + ((long long)pr.off + ch * 16 + i) * P.ldr + n));
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < jn) out16[((long long)pr.off + ch * 16 + i) * P.ldo + n] = f2bf(v0[i] + r[i]);
       } else if (EPI == EPI_SWIGLU) {
-        const float g = v0;
-        out16[orow * P.ldo + n] = f2bf(g / (1.0f + expf(-g)) * v1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < jn) {
+            const float g = v0[i];
+            out16[((long long)pr.off + ch * 16 + i) * P.ldo + n] = f2bf(g / (1.0f + expf(-g)) * v1[i]);
+          }
       } else {
-        out32[orow * P.ldo + n] = v0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < jn) out32[((long long)pr.off + ch * 16 + i) * P.ldo + n] = v0[i];
       }
     };
 
@@ -332,13 +363,13 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
         float v0[16], v1[16];
         tmem_ld16(taddr + ch * 16, v0);
         if (NA == 2) tmem_ld16(taddr + kMaxCols + ch * 16, v1);
+        if (whole) {
+          if (valid_row) emit_chunk(pr, n, ch, v0, v1);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int jc = ch * 16 + i;
-          if (jc < pr.cnt) {
-            if (whole) {
-              if (valid_row) emit(pr, n, jc, v0[i], NA == 2 ? v1[i] : 0.f);
-            } else {
+          for (int i = 0; i < 16; ++i) {
+            const int jc = ch * 16 + i;
+            if (jc < pr.cnt) {
               slot[(size_t)jc * kTileN + row] = v0[i];
               if (NA == 2) slot[(size_t)P.cols * kTileN + (size_t)jc * kTileN + row] = v1[i];
             }
@@ -357,26 +388,36 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
       const long long kfirst = (long long)tau * KB;
       const long long c_first = cta_of(kfirst, W, G), c_last = cta_of(kfirst + KB - 1, W, G);
       if (et == 0) {
+        // The non-empty CTAs that hold pieces of this tile, in k order, and their partial slots.
         int np = 0;
-        for (long long cc = c_first; cc <= c_last; ++cc)
-          np += (range_start(cc + 1, W, G) > range_start(cc, W, G)) ? 1 : 0;
+        for (long long cc = c_first; cc <= c_last; ++cc) {
+          const long long st = range_start(cc, W, G);
+          if (range_start(cc + 1, W, G) <= st) continue;
+          if (np < kMaxPieces) s_piece[np] = (int)(cc * 2 + ((st >= kfirst) ? 0 : 1));
+          ++np;
+        }
         const int old = atomicAdd(&P.counters[tau], 1);
         *s_last = (old == np - 1) ? 1 : 0;
+        *s_np = np;
       }
       named_bar_sync(1, 128);
       if (*s_last) {
         __threadfence();
-        for (int jc = 0; jc < pr.cnt; ++jc) {
-          float a0 = 0.f, a1 = 0.f;
-          for (long long cc = c_first; cc <= c_last; ++cc) {
-            const long long st = range_start(cc, W, G);
-            if (range_start(cc + 1, W, G) <= st) continue;  // empty range: no piece
-            const int which = (st >= kfirst) ? 0 : 1;
-            const float* ps = P.partials + (size_t)(cc * 2 + which) * P.slot_floats;
-            a0 += __ldcg(ps + (size_t)jc * kTileN + row);
-            if (NA == 2) a1 += __ldcg(ps + (size_t)P.cols * kTileN + (size_t)jc * kTileN + row);
+        const int np = min(*s_np, kMaxPieces);
+        for (int ch = 0; ch < nch; ++ch) {
+          float a0[16], a1[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) a0[i] = a1[i] = 0.f;
+          for (int p = 0; p < np; ++p) {
+            const float* ps = P.partials + (size_t)s_piece[p] * P.slot_floats + (size_t)ch * 16 * kTileN + row;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (ch * 16 + i < pr.cnt) {
+                a0[i] += __ldcg(ps + (size_t)i * kTileN);
+                if (NA == 2) a1[i] += __ldcg(ps + (size_t)P.cols * kTileN + (size_t)i * kTileN);
+              }
           }
-          if (valid_row) emit(pr, n, jc, a0, a1);
+          if (valid_row) emit_chunk(pr, n, ch, a0, a1);
         }
         if (et == 0) P.counters[tau] = 0;  // leave the workspace reusable
       }
@@ -483,6 +524,7 @@ cudaError_t launch_engine(dec_handle* h, const EngineLaunch& L, cudaStream_t s) 
   P.err = h->d_err;
   P.wait_ns = h->wait_ns;
   const int grid = L.grid > 0 ? L.grid : engine_grid(h);
+  if (grid > kMaxPieces) return cudaErrorInvalidConfiguration;
   const int max_cols = L.count;  // dense: the tokens; grouped: the batch, a bound on any expert's tokens
   if (max_cols < 1 || max_cols > kMaxCols) return cudaErrorInvalidValue;
   switch (L.epi) {

@@ -121,7 +121,7 @@ def test_input_projection_batch_sweep(h, w_in, M):
     x = synth.bf16_rows(synth.X_BASE, range(M), 7168, SEED)
     Wd = dev_bf16(w_in, (12288, 7168))
     y = ML.dec_linear(h, dev_bf16(x, (M, 7168)), Wd)
-    assert h.last_variant == (ML.VARIANT_SMALL_M if M <= 2 else ML.VARIANT_SPLIT_K)
+    assert h.last_variant == (ML.VARIANT_SMALL_M if M == 1 else ML.VARIANT_SPLIT_K)
     assert_bf16_close(host_bits(y), oracle.linear(x, w_in), f"in-proj M={M}")
 
 
