@@ -203,6 +203,7 @@ def run_ours(args, rank, local, world):
     torch.cuda.set_device(local)
     ML.build()
     h = ML.Handle(local)
+    h.set_shared_sms(args.shared_sms)
     layers = build_weights(dev)
     cws = [L.c_struct() for L in layers]
     stream = torch.cuda.current_stream()
@@ -326,7 +327,7 @@ def run_ours(args, rank, local, world):
                       "l2": "inputs larger than L2: each step reads >= 1.1 GB (L2 129 MB); dense weights alternate "
                             "between 2 copies; routing changes every step",
                       "weight_stream_GBps": hl["weight_stream_GBps"], "hbm_frac": hl["hbm_frac"],
-                      "distinct_experts_U": hl["U"],
+                      "distinct_experts_U": hl["U"], "shared_expert_sms": {0: "auto", -1: "overlap"}.get(args.shared_sms, args.shared_sms),
                       "sweep": [{k: v for k, v in results[m].items() if k != "kernels"} for m in sweep],
                       "kernels_at_batch": hl["kernels"]},
            "weight_stream_GBps": hl["weight_stream_GBps"], "hbm_frac": hl["hbm_frac"],
@@ -440,6 +441,8 @@ def main(argv=None):
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time the K steps as stream launches only (default: also capture them in a CUDA graph "
                          "and report the replay time as the value)")
+    ap.add_argument("--shared-sms", type=int, default=0,
+                    help="SMs for the shared expert: 0 automatic share (default), -1 every SM overlapped, n fixed")
     ap.add_argument("--experts", type=int, default=E,
                     help="routed experts in the bank (default 384, the workload; smaller only for ncu captures)")
     args = ap.parse_args(argv)

@@ -95,6 +95,14 @@ dec_status dec_set_wait_limit_ns(dec_handle* h, uint64_t ns);
  * behind the dependency wait, weight reads may go before it]. */
 dec_status dec_set_pdl(dec_handle* h, int enable);
 
+/* How the shared expert and the routed experts share the SMs [K3 P1§3: the
+ * schedule sets how many GPU resources each operation uses]. The shared
+ * expert is always launched first, beside the router / top-k phase.
+ *  0 (default): it keeps its share of the expected weight bytes (rounded up);
+ * -1: it starts on every SM and the routed experts take SMs as it finishes;
+ *  n > 0: it keeps n SMs. */
+dec_status dec_set_shared_sms(dec_handle* h, int sms);
+
 /* Force a projection kernel family (DEC_VARIANT_AUTO restores the choice by
  * batch) so that tests can run both families at the same batch. */
 dec_status dec_set_force_variant(dec_handle* h, int variant);

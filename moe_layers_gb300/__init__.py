@@ -66,6 +66,7 @@ def _load():
         "dec_set_wait_limit_ns": [P, U64],
         "dec_set_pdl": [P, I],
         "dec_set_force_variant": [P, I],
+        "dec_set_shared_sms": [P, I],
         "dec_check_device_error": [P],
         "dec_linear_workspace_size": [P, I, I, I, ctypes.POINTER(Z)],
         "dec_linear": [P, P, I, P, P, I, I, I, P, Z, P],
@@ -181,6 +182,10 @@ class Handle:
 
     def set_force_variant(self, v: int) -> None:
         _check(_load().dec_set_force_variant(self._h, int(v)), "dec_set_force_variant")
+
+    def set_shared_sms(self, n: int) -> None:
+        """0: automatic SM share by expected bytes; -1: every SM, overlapped; n > 0: a fixed n-SM partition."""
+        _check(_load().dec_set_shared_sms(self._h, int(n)), "dec_set_shared_sms")
 
     def set_pdl(self, enable: bool) -> None:
         _check(_load().dec_set_pdl(self._h, 1 if enable else 0), "dec_set_pdl")

@@ -171,25 +171,39 @@ bool moe_shape_ok(int M, int k, int E, int H, int I) {
          H % kTileN == 0 && I >= kTileN && I % kTileN == 0;
 }
 
-// CTAs given to the shared expert while the routed experts run beside it: the
-// shared expert's share of the expected weight bytes, rounded up with a margin
-// (at least one SM, at most half). Expected distinct experts for uniform routing: E (1 - (1 - k/E)^M).
+// SM shares of the shared and the routed experts ("the schedule controls how
+// many GPU resources each op uses", Kimi K3 article, Part 1 §3).
+//  - automatic (h->shared_ctas == 0, default): the shared expert keeps its
+//    share of the expected weight bytes, rounded up with a 25% margin so that
+//    it never finishes after the routed experts (at least one SM, at most
+//    half). Expected distinct experts for uniform routing: E (1 - (1 - k/E)^M).
+//  - overlap (h->shared_ctas < 0): both use every SM; the hardware hands SMs
+//    to the routed kernels as the shared expert's CTAs finish.
+//  - fixed (h->shared_ctas > 0): that many SMs for the shared expert.
+// Measured on GB300 (layer step, CUDA-graph replay): the automatic share is
+// best or within 3% at M = 1..64 except M = 16, where overlap is 6-8% faster.
 int shared_grid(const dec_handle* h, int M, int k, int E) {
   if (h->shared_ctas > 0) return std::min(h->shared_ctas, h->sms - 1);
+  if (h->shared_ctas < 0) return h->sms;
   const double eu = E * (1.0 - std::pow(1.0 - (double)k / E, (double)M));
-  // Rounded up with a 25% margin: the shared expert must not finish after the routed experts.
-  int g = (int)std::ceil(1.25 * h->sms / (1.0 + eu));
+  const int g = (int)std::ceil(1.25 * h->sms / (1.0 + eu));
   return std::max(1, std::min(g, h->sms / 2));
 }
 
-dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const float* w, int M, int k,
-                    const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I,
-                    const uint16_t* Wg_s, const uint16_t* Wu_s, const uint16_t* Wd_s, const uint16_t* residual,
-                    uint16_t* out, const MoeWs& ws, cudaStream_t s) {
+int routed_grid(const dec_handle* h, int M, int k, int E, bool has_shared) {
+  if (!has_shared || h->shared_ctas < 0) return h->sms;
+  return h->sms - shared_grid(h, M, k, E);
+}
+
+// The shared expert on the handle's side stream, forked from `s` now. It does
+// not depend on routing, so it is launched before the router: its weight
+// stream fills the bandwidth that the latency-bound router / top-k / routing
+// table phase leaves idle (Kimi K3 article, Part 1 §3). Joined by moe_routed.
+dec_status moe_shared_fork(dec_handle* h, const uint16_t* x, int M, int k, int E, int H, int I,
+                           const uint16_t* Wg_s, const uint16_t* Wu_s, const uint16_t* Wd_s, const MoeWs& ws,
+                           cudaStream_t s) {
   const bool has_shared = Wg_s != nullptr;
-  const int n = M * k;
   const int g1 = has_shared ? shared_grid(h, M, k, E) : 0;
-  const int g0 = h->sms - g1;
   if (has_shared) {
     DEC_CUDA(cudaEventRecord(h->ev_fork, s));
     DEC_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
@@ -234,6 +248,14 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
     }
     DEC_CUDA(cudaEventRecord(h->ev_join, h->side));
   }
+  return DEC_OK;
+}
+
+dec_status moe_routed(dec_handle* h, const uint16_t* x, const int32_t* idx, const float* w, int M, int k,
+                      const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I,
+                      bool has_shared, const uint16_t* residual, uint16_t* out, const MoeWs& ws, cudaStream_t s) {
+  const int n = M * k;
+  const int g0 = routed_grid(h, M, k, E, has_shared);
   {
     LaunchScope scope(h, "route_table", s);
     DEC_CUDA(launch_route_table(h, idx, M, k, E, x, H, ws.table, ws.xs, s));
@@ -291,6 +313,15 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
     DEC_CUDA(launch_combine(h, ws.y, ws.table, w, M, k, E, has_shared ? ws.ys : nullptr, residual, out, H, s));
   }
   return DEC_OK;
+}
+
+dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const float* w, int M, int k,
+                    const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I,
+                    const uint16_t* Wg_s, const uint16_t* Wu_s, const uint16_t* Wd_s, const uint16_t* residual,
+                    uint16_t* out, const MoeWs& ws, cudaStream_t s) {
+  dec_status st = moe_shared_fork(h, x, M, k, E, H, I, Wg_s, Wu_s, Wd_s, ws, s);
+  if (st != DEC_OK) return st;
+  return moe_routed(h, x, idx, w, M, k, Wg, Wu, Wd, E, H, I, Wg_s != nullptr, residual, out, ws, s);
 }
 
 // ---------------------------------------------------------------- decode layer workspace
@@ -410,6 +441,12 @@ dec_status dec_set_wait_limit_ns(dec_handle* h, uint64_t ns) {
 dec_status dec_set_pdl(dec_handle* h, int enable) {
   if (h == nullptr) return DEC_ERR_INVALID_ARG;
   h->pdl = enable ? 1 : 0;
+  return DEC_OK;
+}
+
+dec_status dec_set_shared_sms(dec_handle* h, int sms) {
+  if (h == nullptr || sms < -1 || sms >= h->sms) return DEC_ERR_INVALID_ARG;
+  h->shared_ctas = sms;
   return DEC_OK;
 }
 
@@ -604,8 +641,10 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
     }
     DEC_CUDA(cudaEventRecord(h->ev_pf_join, h->pf));
   }
-  // The router / top-k phase is latency-bound; the shared expert (forked in
-  // moe_impl) and the prefetch stream use the idle bandwidth meanwhile.
+  // The router / top-k phase is latency-bound; the shared expert and the
+  // prefetch stream use the idle bandwidth meanwhile.
+  st = moe_shared_fork(h, w.b, M, L.k, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, w.moe, s);
+  if (st != DEC_OK) return st;
   {
     LaunchScope scope(h, "router", s);
     if (launch_router(h, w.b, L.W_r, M, H, L.E, w.parts, s) != cudaSuccess) return DEC_ERR_CUDA;
@@ -615,7 +654,7 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
     if (launch_topk(h, w.parts, router_ksplit(H), M, L.E, L.k, idx, wt, scores, s) != cudaSuccess)
       return DEC_ERR_CUDA;
   }
-  st = moe_impl(h, w.b, idx, wt, M, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, h1, hidden, w.moe, s);
+  st = moe_routed(h, w.b, idx, wt, M, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s != nullptr, h1, hidden, w.moe, s);
   if (st != DEC_OK) return st;
   if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
   return DEC_OK;

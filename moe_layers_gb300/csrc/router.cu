@@ -18,14 +18,14 @@ namespace dec {
 
 constexpr int kRouterChunk = 1024;  // reduction elements per split (one CTA column)
 constexpr int kRouterRows = 8;      // router rows per CTA, one per warp
-constexpr int kRouterTok = 16;      // tokens staged in shared memory per pass
+constexpr int kRouterTok = 4;       // tokens staged in shared memory per pass (8 KB: co-resides with the engine)
 
 int router_ksplit(int H) { return (H + kRouterChunk - 1) / kRouterChunk; }
 
 // parts[ks][t][e] = sum over the ks-th chunk of H of x[t][h] * Wr[e][h] (fp32).
 // Grid: (ceil(E / 8), ksplit). Each warp owns one router row and keeps its
 // chunk of fp32 weights in registers (loaded before the dependency wait); the
-// tokens' bf16 activations pass through shared memory sixteen at a time.
+// tokens' bf16 activations pass through shared memory four at a time.
 __global__ void __launch_bounds__(256) router_kernel(const uint16_t* x, const float* __restrict__ Wr, int M, int H,
                                                      int E, float* parts) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
