@@ -204,6 +204,7 @@ def run_ours(args, rank, local, world):
     ML.build()
     h = ML.Handle(local)
     h.set_shared_sms(args.shared_sms)
+    h.set_prefetch_shared(args.prefetch_shared)
     layers = build_weights(dev)
     cws = [L.c_struct() for L in layers]
     stream = torch.cuda.current_stream()
@@ -296,9 +297,10 @@ def run_ours(args, rank, local, world):
         us_e2e = reduce_max(e0.elapsed_time(e1) * 1000.0 / K, dev)
         b = step_bytes(M, U)
         kern = {}
+        merged_shared = "shared_gate_up" not in prof  # batch 1: the shared expert runs inside gate_up / down
         for tag, (n, ms) in prof.items():
             avg_us = ms * 1000.0 / max(n, 1)
-            kb = kernel_bytes(tag, M, U_prof)
+            kb = kernel_bytes(tag, M, U_prof + (1 if merged_shared and tag in ("gate_up", "down") else 0))
             kern[tag] = {"launches_per_step": n / K, "avg_us": round(avg_us, 2),
                          "GBps": round(kb / (avg_us * 1e3), 1) if kb and avg_us > 0 else None}
         results[M] = dict(M=M, us_per_step=round(us_max, 2), us_per_step_stream=round(us_eager, 2),
@@ -443,6 +445,8 @@ def main(argv=None):
                          "and report the replay time as the value)")
     ap.add_argument("--shared-sms", type=int, default=0,
                     help="SMs for the shared expert: 0 automatic share (default), -1 every SM overlapped, n fixed")
+    ap.add_argument("--prefetch-shared", action="store_true",
+                    help="at batch 1, pull the shared expert into L2 during the router phase (off: measured slower)")
     ap.add_argument("--experts", type=int, default=E,
                     help="routed experts in the bank (default 384, the workload; smaller only for ncu captures)")
     args = ap.parse_args(argv)

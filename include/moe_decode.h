@@ -103,6 +103,13 @@ dec_status dec_set_pdl(dec_handle* h, int enable);
  *  n > 0: it keeps n SMs. */
 dec_status dec_set_shared_sms(dec_handle* h, int sms);
 
+/* At batch 1 decode_layer runs the shared expert inside the routed experts'
+ * launches and, while the router / top-k phase leaves the memory idle, pulls
+ * its weights into L2 on a side stream [K3 P1§4]. 1 enables that prefetch,
+ * 0 (default) disables it: measured on GB300 it slows the step, because 88 MB
+ * of evict-last lines crowd the weight stream out of the 129 MB L2. */
+dec_status dec_set_prefetch_shared(dec_handle* h, int enable);
+
 /* Force a projection kernel family (DEC_VARIANT_AUTO restores the choice by
  * batch) so that tests can run both families at the same batch. */
 dec_status dec_set_force_variant(dec_handle* h, int variant);
@@ -110,6 +117,12 @@ dec_status dec_set_force_variant(dec_handle* h, int variant);
 /* Variant used by the most recent dec_linear / dec_linear_residual call on
  * this handle (a dec_variant value; 0 before any call). */
 int dec_last_variant(const dec_handle* h);
+
+/* Kernel family of the most recent expert launches (moe_experts,
+ * decode_layer): DEC_VARIANT_SMALL_M (batch 1: one token per expert) or
+ * DEC_VARIANT_SPLIT_K; 0 before any call. dec_set_force_variant(SPLIT_K)
+ * also forces the split-K family for the experts. */
+int dec_last_expert_variant(const dec_handle* h);
 
 /* Synchronise the device and read the device error word: DEC_OK if clear,
  * DEC_ERR_TIMEOUT if a kernel gave up a wait since the last check (the word

@@ -67,6 +67,7 @@ def _load():
         "dec_set_pdl": [P, I],
         "dec_set_force_variant": [P, I],
         "dec_set_shared_sms": [P, I],
+        "dec_set_prefetch_shared": [P, I],
         "dec_check_device_error": [P],
         "dec_linear_workspace_size": [P, I, I, I, ctypes.POINTER(Z)],
         "dec_linear": [P, P, I, P, P, I, I, I, P, Z, P],
@@ -93,6 +94,8 @@ def _load():
     lib.dec_status_string.restype = ctypes.c_char_p
     lib.dec_last_variant.argtypes = [P]
     lib.dec_last_variant.restype = ctypes.c_int
+    lib.dec_last_expert_variant.argtypes = [P]
+    lib.dec_last_expert_variant.restype = ctypes.c_int
     lib.dec_launch_count.argtypes = [P]
     lib.dec_launch_count.restype = ctypes.c_uint64
     _lib = lib
@@ -187,6 +190,9 @@ class Handle:
         """0: automatic SM share by expected bytes; -1: every SM, overlapped; n > 0: a fixed n-SM partition."""
         _check(_load().dec_set_shared_sms(self._h, int(n)), "dec_set_shared_sms")
 
+    def set_prefetch_shared(self, enable: bool) -> None:
+        _check(_load().dec_set_prefetch_shared(self._h, 1 if enable else 0), "dec_set_prefetch_shared")
+
     def set_pdl(self, enable: bool) -> None:
         _check(_load().dec_set_pdl(self._h, 1 if enable else 0), "dec_set_pdl")
 
@@ -196,6 +202,10 @@ class Handle:
     @property
     def last_variant(self) -> int:
         return _load().dec_last_variant(self._h)
+
+    @property
+    def last_expert_variant(self) -> int:
+        return _load().dec_last_expert_variant(self._h)
 
     def check_device_error(self) -> int:
         return _load().dec_check_device_error(self._h)

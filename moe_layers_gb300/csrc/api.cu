@@ -171,6 +171,12 @@ bool moe_shape_ok(int M, int k, int E, int H, int I) {
          H % kTileN == 0 && I >= kTileN && I % kTileN == 0;
 }
 
+// Expert kernel family: the small-matrix kernels for one token (unless the
+// split-K family is forced), the split-K tcgen05 engine otherwise.
+bool experts_small(const dec_handle* h, int M, int H, int I) {
+  return M == 1 && h->force_variant != DEC_VARIANT_SPLIT_K && gemv_moe_supported(H) && gemv_moe_supported(I);
+}
+
 // SM shares of the shared and the routed experts ("the schedule controls how
 // many GPU resources each op uses", Kimi K3 article, Part 1 §3).
 //  - automatic (h->shared_ctas == 0, default): the shared expert keeps its
@@ -204,6 +210,8 @@ dec_status moe_shared_fork(dec_handle* h, const uint16_t* x, int M, int k, int E
                            cudaStream_t s) {
   const bool has_shared = Wg_s != nullptr;
   const int g1 = has_shared ? shared_grid(h, M, k, E) : 0;
+  // At one token the shared expert is problem 0 of the routed launches (see moe_routed).
+  if (experts_small(h, M, H, I)) return DEC_OK;
   if (has_shared) {
     DEC_CUDA(cudaEventRecord(h->ev_fork, s));
     DEC_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
@@ -253,13 +261,37 @@ dec_status moe_shared_fork(dec_handle* h, const uint16_t* x, int M, int k, int E
 
 dec_status moe_routed(dec_handle* h, const uint16_t* x, const int32_t* idx, const float* w, int M, int k,
                       const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I,
-                      bool has_shared, const uint16_t* residual, uint16_t* out, const MoeWs& ws, cudaStream_t s) {
+                      const uint16_t* Wg_s, const uint16_t* Wu_s, const uint16_t* Wd_s, const uint16_t* residual,
+                      uint16_t* out, const MoeWs& ws, cudaStream_t s) {
+  const bool has_shared = Wg_s != nullptr;
   const int n = M * k;
   const int g0 = routed_grid(h, M, k, E, has_shared);
   {
     LaunchScope scope(h, "route_table", s);
     DEC_CUDA(launch_route_table(h, idx, M, k, E, x, H, ws.table, ws.xs, s));
   }
+  if (experts_small(h, M, H, I)) {
+    // One token: routed and shared experts in one balanced launch per matrix
+    // over every SM (the shared expert is problem 0).
+    h->last_expert_variant = DEC_VARIANT_SMALL_M;
+    const GemvMoeShared sgu{Wg_s, Wu_s, x, ws.hs}, sdn{Wd_s, nullptr, ws.hs, ws.ys};
+    {
+      LaunchScope scope(h, "gate_up", s);
+      DEC_CUDA(launch_gemv_moe(h, true, Wg, Wu, I, I, H, ws.xs, H, ws.table, E, n, ws.hbuf, I, h->sms, s,
+                               has_shared ? &sgu : nullptr));
+    }
+    {
+      LaunchScope scope(h, "down", s);
+      DEC_CUDA(launch_gemv_moe(h, false, Wd, nullptr, H, H, I, ws.hbuf, I, ws.table, E, n, ws.y, H, h->sms, s,
+                               has_shared ? &sdn : nullptr));
+    }
+    {
+      LaunchScope scope(h, "combine", s);
+      DEC_CUDA(launch_combine(h, ws.y, ws.table, w, M, k, E, has_shared ? ws.ys : nullptr, residual, out, H, s));
+    }
+    return DEC_OK;
+  }
+  h->last_expert_variant = DEC_VARIANT_SPLIT_K;
   EngineLaunch L;
   L.epi = EPI_SWIGLU;
   L.A = Wg;
@@ -321,7 +353,7 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
                     uint16_t* out, const MoeWs& ws, cudaStream_t s) {
   dec_status st = moe_shared_fork(h, x, M, k, E, H, I, Wg_s, Wu_s, Wd_s, ws, s);
   if (st != DEC_OK) return st;
-  return moe_routed(h, x, idx, w, M, k, Wg, Wu, Wd, E, H, I, Wg_s != nullptr, residual, out, ws, s);
+  return moe_routed(h, x, idx, w, M, k, Wg, Wu, Wd, E, H, I, Wg_s, Wu_s, Wd_s, residual, out, ws, s);
 }
 
 // ---------------------------------------------------------------- decode layer workspace
@@ -444,6 +476,12 @@ dec_status dec_set_pdl(dec_handle* h, int enable) {
   return DEC_OK;
 }
 
+dec_status dec_set_prefetch_shared(dec_handle* h, int enable) {
+  if (h == nullptr) return DEC_ERR_INVALID_ARG;
+  h->prefetch_shared = enable ? 1 : 0;
+  return DEC_OK;
+}
+
 dec_status dec_set_shared_sms(dec_handle* h, int sms) {
   if (h == nullptr || sms < -1 || sms >= h->sms) return DEC_ERR_INVALID_ARG;
   h->shared_ctas = sms;
@@ -457,6 +495,8 @@ dec_status dec_set_force_variant(dec_handle* h, int variant) {
 }
 
 int dec_last_variant(const dec_handle* h) { return h ? h->last_variant : 0; }
+
+int dec_last_expert_variant(const dec_handle* h) { return h ? h->last_expert_variant : 0; }
 
 dec_status dec_check_device_error(dec_handle* h) {
   if (h == nullptr) return DEC_ERR_INVALID_ARG;
@@ -631,13 +671,25 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
     LaunchScope scope(h, "rmsnorm2", s);
     if (launch_rmsnorm(h, h1, L.gamma2, w.b, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
   }
-  const bool pf = L.prefetch_next != nullptr && L.prefetch_bytes > 0;
+  // Kimi K3 article, Part 1 §4: while the router / top-k phase leaves the
+  // memory idle, a side-stream kernel pulls weights that come next into L2:
+  // at one token the shared expert (it runs inside the routed launches), and
+  // the caller's next-operator region if given.
+  const bool pf_shared = L.Wg_s != nullptr && experts_small(h, M, H, L.I) && h->prefetch_shared;
+  const bool pf = (L.prefetch_next != nullptr && L.prefetch_bytes > 0) || pf_shared;
   if (pf) {
     DEC_CUDA(cudaEventRecord(h->ev_pf_fork, s));
     DEC_CUDA(cudaStreamWaitEvent(h->pf, h->ev_pf_fork, 0));
     {
       LaunchScope scope(h, "prefetch", h->pf);
-      DEC_CUDA(launch_prefetch(h, L.prefetch_next, L.prefetch_bytes, 16, h->pf));
+      if (pf_shared) {
+        const size_t mat = (size_t)L.I * H * sizeof(uint16_t);
+        DEC_CUDA(launch_prefetch(h, L.Wg_s, mat, 16, h->pf));
+        DEC_CUDA(launch_prefetch(h, L.Wu_s, mat, 16, h->pf));
+        DEC_CUDA(launch_prefetch(h, L.Wd_s, mat, 16, h->pf));
+      }
+      if (L.prefetch_next != nullptr && L.prefetch_bytes > 0)
+        DEC_CUDA(launch_prefetch(h, L.prefetch_next, L.prefetch_bytes, 16, h->pf));
     }
     DEC_CUDA(cudaEventRecord(h->ev_pf_join, h->pf));
   }
@@ -654,7 +706,7 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
     if (launch_topk(h, w.parts, router_ksplit(H), M, L.E, L.k, idx, wt, scores, s) != cudaSuccess)
       return DEC_ERR_CUDA;
   }
-  st = moe_routed(h, w.b, idx, wt, M, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s != nullptr, h1, hidden, w.moe, s);
+  st = moe_routed(h, w.b, idx, wt, M, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, h1, hidden, w.moe, s);
   if (st != DEC_OK) return st;
   if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
   return DEC_OK;

@@ -22,7 +22,9 @@ struct dec_handle {
   int pdl = 1;
   int force_variant = 0;
   int last_variant = 0;
+  int last_expert_variant = 0;      // kernel family of the most recent expert launches
   int shared_ctas = 0;              // CTAs for the shared expert's kernels (0 = default)
+  int prefetch_shared = 0;          // batch 1: pull the shared expert into L2 during the router phase
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   // measurement
   uint64_t launches = 0;
@@ -89,6 +91,23 @@ cudaError_t launch_engine(dec_handle* h, const EngineLaunch& L, cudaStream_t s);
 cudaError_t launch_gemv(dec_handle* h, const uint16_t* x, long long ldx, const uint16_t* W, const uint16_t* res,
                         long long ldr, uint16_t* y, long long ldy, int M, int N, int K, cudaStream_t s);
 bool gemv_supported(int M, int K);
+
+// Small-matrix expert kernels for one token (gemv_moe.cu): gate/up with the
+// SwiGLU epilogue (swiglu) or down with fp32 output; problems from the routing
+// table, or one dense expert when table is null.
+// A dense expert processed as problem 0 of the same launch (the shared
+// expert at batch 1): its weights, its activation row and its output row.
+struct GemvMoeShared {
+  const uint16_t* A;
+  const uint16_t* A2;
+  const uint16_t* x;
+  void* out;
+};
+cudaError_t launch_gemv_moe(dec_handle* h, bool swiglu, const uint16_t* A, const uint16_t* A2,
+                            long long rows_per_prob_bank, int R, int K, const uint16_t* x, long long ldx,
+                            const int* table, int E, int n_entries, void* out, long long ldo, int sms,
+                            cudaStream_t s, const GemvMoeShared* shared = nullptr);
+bool gemv_moe_supported(int K);
 
 cudaError_t launch_rmsnorm(dec_handle* h, const uint16_t* x, const uint16_t* gamma, uint16_t* y, int M, int H,
                            float eps, cudaStream_t s);

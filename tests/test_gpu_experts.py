@@ -39,7 +39,9 @@ def _small_bank(E, H, I, base):
     return g.reshape(E, I, H), u.reshape(E, I, H), d.reshape(E, H, I)
 
 
+@pytest.mark.parametrize("family", ["auto", "split_k"])
 @pytest.mark.parametrize("M,E,H,I,k,shared,resid,skew", [
+    (1, 24, 384, 256, 8, True, True, False),
     (1, 16, 256, 128, 4, True, False, False),
     (3, 16, 256, 256, 4, False, True, False),
     (17, 32, 384, 128, 8, True, True, False),
@@ -47,8 +49,11 @@ def _small_bank(E, H, I, base):
     (64, 40, 128, 256, 16, True, True, True),
     (20, 8, 512, 384, 2, False, False, True),
 ])
-def test_experts_small(h, M, E, H, I, k, shared, resid, skew):
+def test_experts_small(h, M, E, H, I, k, shared, resid, skew, family):
     import moe_layers_gb300 as ML
+    if family == "split_k" and M > 1:
+        pytest.skip("above one token the split-K family is the automatic choice")
+    h.set_force_variant(ML.VARIANT_SPLIT_K if family == "split_k" else ML.VARIANT_AUTO)
     rng = np.random.default_rng(M * 131 + E)
     g, u, d = _small_bank(E, H, I, 4000 + E + H)
     x = synth.bf16(M * H, SEED, 4100 + M, 0, 1.0).reshape(M, H)
@@ -65,8 +70,10 @@ def test_experts_small(h, M, E, H, I, k, shared, resid, skew):
                          dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
                          shared=None if sh is None else tuple(dev_bf16(a, a.shape) for a in sh),
                          residual=None if r is None else dev_bf16(r, (M, H)))
+    h.set_force_variant(ML.VARIANT_AUTO)
+    assert h.last_expert_variant == (ML.VARIANT_SMALL_M if (M == 1 and family == "auto") else ML.VARIANT_SPLIT_K)
     ref = oracle.moe(x, idx, w, lambda e: (g[e], u[e], d[e]), sh, r)
-    assert_bf16_close(host_bits(out), ref, f"moe M={M} E={E}")
+    assert_bf16_close(host_bits(out), ref, f"moe M={M} E={E} {family}")
     assert h.check_device_error() == ML.DEC_OK
 
 
@@ -74,16 +81,18 @@ def test_experts_small(h, M, E, H, I, k, shared, resid, skew):
 from conftest import E_FULL, H_FULL, I_FULL, K_FULL
 
 
-@pytest.mark.parametrize("M", [1, 8, 64])
-def test_experts_full_size(h, full_bank, M):
+@pytest.mark.parametrize("M,family", [(1, "auto"), (1, "split_k"), (8, "auto"), (64, "auto")])
+def test_experts_full_size(h, full_bank, M, family):
     import torch
     import moe_layers_gb300 as ML
+    h.set_force_variant(ML.VARIANT_SPLIT_K if family == "split_k" else ML.VARIANT_AUTO)
     Wg, Wu, Wd, sh = full_bank
     rng = np.random.default_rng(5000 + M)
     idx, w = _routing(M, E_FULL, K_FULL, rng)
     x = synth.bf16_rows(synth.X_BASE + 20, range(M), H_FULL, SEED)
     out = ML.moe_experts(h, dev_bf16(x, (M, H_FULL)), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
                          Wg, Wu, Wd, shared=sh)
+    h.set_force_variant(ML.VARIANT_AUTO)
     bank = HostBank(E_FULL, H_FULL, I_FULL)
     shared = tuple(oracle.bf16_to_f64(synth.bf16(I_FULL * H_FULL, SEED, tid, 0, 0.02)).reshape(shape)
                    for tid, shape in ((synth.W_G_S, (I_FULL, H_FULL)), (synth.W_U_S, (I_FULL, H_FULL)),
