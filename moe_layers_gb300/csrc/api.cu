@@ -99,14 +99,17 @@ int choose_variant(const dec_handle* h, int M, int K) {
   return (M == 1 && gemv_supported(M, K)) ? DEC_VARIANT_SMALL_M : DEC_VARIANT_SPLIT_K;
 }
 
+// gamma (small-matrix kernel, one token only): the input row is RMS-normalised
+// inside the projection kernel.
 dec_status linear_impl(dec_handle* h, const uint16_t* x, int ldx, const uint16_t* W, const uint16_t* r, uint16_t* y,
-                       int M, int N, int K, EngineRegion eng, cudaStream_t s, const char* tag = "linear") {
+                       int M, int N, int K, EngineRegion eng, cudaStream_t s, const char* tag = "linear",
+                       const uint16_t* gamma = nullptr, float eps = 0.f) {
   const int v = choose_variant(h, M, K);
   cudaError_t e;
   LaunchScope scope(h, tag, s);
   if (v == DEC_VARIANT_SMALL_M) {
     if (!gemv_supported(M, K)) return DEC_ERR_UNSUPPORTED;
-    e = launch_gemv(h, x, ldx, W, r, N, y, N, M, N, K, s);
+    e = launch_gemv(h, x, ldx, W, r, N, y, N, M, N, K, s, gamma, eps);
   } else {
     EngineLaunch L;
     L.epi = EPI_LINEAR;
@@ -279,6 +282,13 @@ dec_status moe_routed(dec_handle* h, const uint16_t* x, const int32_t* idx, cons
       LaunchScope scope(h, "gate_up", s);
       DEC_CUDA(launch_gemv_moe(h, true, Wg, Wu, I, I, H, ws.xs, H, ws.table, E, n, ws.hbuf, I, h->sms, s,
                                has_shared ? &sgu : nullptr));
+    }
+    if (gemv_down_combine_supported(k, I)) {
+      // down projection + weighted combine + residual in one kernel
+      LaunchScope scope(h, "down", s);
+      DEC_CUDA(launch_gemv_down_combine(h, Wd, H, has_shared ? Wd_s : nullptr, H, I, ws.hbuf, ws.hs, ws.table, E, k,
+                                        w, residual, out, h->sms, s));
+      return DEC_OK;
     }
     {
       LaunchScope scope(h, "down", s);
@@ -659,11 +669,16 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   float* scores = trace ? trace->scores : nullptr;
   const int H = L.H;
 
-  {
+  // One token with the small-matrix kernel: the first RMSNorm runs inside the
+  // input projection (same arithmetic, one launch fewer).
+  const bool fuse_norm1 = M == 1 && choose_variant(h, M, H) == DEC_VARIANT_SMALL_M;
+  if (!fuse_norm1) {
     LaunchScope scope(h, "rmsnorm1", s);
     if (launch_rmsnorm(h, hidden, L.gamma1, w.a, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
   }
-  dec_status st = linear_impl(h, w.a, H, L.W_in, nullptr, w.yin, M, L.N_in, H, w.moe.r0, s, "in_proj");
+  dec_status st = fuse_norm1 ? linear_impl(h, hidden, H, L.W_in, nullptr, w.yin, M, L.N_in, H, w.moe.r0, s, "in_proj",
+                                           L.gamma1, L.eps)
+                             : linear_impl(h, w.a, H, L.W_in, nullptr, w.yin, M, L.N_in, H, w.moe.r0, s, "in_proj");
   if (st != DEC_OK) return st;
   st = linear_impl(h, w.yin, L.N_in, L.W_o, hidden, h1, M, H, L.K_out, w.moe.r0, s, "out_proj");
   if (st != DEC_OK) return st;

@@ -33,7 +33,7 @@ constexpr int kGemvThreads = 256;
 template <int M, int VPT>
 __global__ void __launch_bounds__(kGemvThreads, 2)
     gemv_kernel(const uint16_t* x, long long ldx, const uint16_t* __restrict__ W, const uint16_t* res, long long ldr,
-                uint16_t* y, long long ldy, int N, int K) {
+                uint16_t* y, long long ldy, int N, int K, const uint16_t* __restrict__ gamma, float eps) {
   // Rows per step: 8 (M = 1) or 4 (M > 1) weight vectors per thread in flight, kept within 128 registers.
   constexpr int RB = ((M == 1 ? 8 : 4) / VPT) > 0 ? ((M == 1 ? 8 : 4) / VPT) : 1;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -61,6 +61,15 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
     }
   };
   if (r0 < r1) load_rows(wa, r0);
+  // Optional RMSNorm of the (single) input row, fused: gains are static weights.
+  uint4 gv[VPT];
+  if (M == 1 && gamma != nullptr) {
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = t + kGemvThreads * i;
+      gv[i] = (v < K8) ? *reinterpret_cast<const uint4*>(gamma + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+    }
+  }
 
   pdl_wait();
   uint4 xr[M][VPT];
@@ -71,6 +80,46 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
       const int v = t + kGemvThreads * i;
       xr[m][i] = (v < K8) ? ld_act16(x + (size_t)m * ldx + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
     }
+  if (M == 1 && gamma != nullptr) {
+    // a = bf16(x / sqrt(mean(x^2) + eps) * gamma), in the reduction order of
+    // the stand-alone RMSNorm kernel (so the result is the same bits).
+    __shared__ float rred[kGemvThreads / 32];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = t + kGemvThreads * i;
+      if (v < K8) {
+        const uint32_t ws[4] = {xr[0][i].x, xr[0][i].y, xr[0][i].z, xr[0][i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = bf_lo(ws[e]), hi = bf_hi(ws[e]);
+          ss = fmaf(lo, lo, ss);
+          ss = fmaf(hi, hi, ss);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) rred[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int q = 0; q < kGemvThreads / 32; ++q) tot += rred[q];
+    const float rs = rsqrtf(tot / (float)K + eps);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const uint32_t ws[4] = {xr[0][i].x, xr[0][i].y, xr[0][i].z, xr[0][i].w};
+      const uint32_t gs[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint16_t l = f2bf(bf_lo(ws[e]) * rs * bf_lo(gs[e]));
+        const uint16_t u = f2bf(bf_hi(ws[e]) * rs * bf_hi(gs[e]));
+        o[e] = (uint32_t)l | ((uint32_t)u << 16);
+      }
+      xr[0][i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
 
   int buf = 0;
   for (int rb = r0; rb < r1; rb += RB) {
@@ -124,23 +173,26 @@ bool gemv_supported(int M, int K) { return M >= 1 && M <= 4 && K >= 8 && K % 8 =
 
 template <int M>
 static cudaError_t gemv_m(dec_handle* h, const uint16_t* x, long long ldx, const uint16_t* W, const uint16_t* res,
-                          long long ldr, uint16_t* y, long long ldy, int N, int K, cudaStream_t s) {
+                          long long ldr, uint16_t* y, long long ldy, int N, int K, cudaStream_t s,
+                          const uint16_t* gamma, float eps) {
   const int K8 = K / 8;
   const int grid = (int)std::min<long long>((long long)N, 2LL * h->sms);
   const dim3 g(grid > 0 ? grid : 1), b(kGemvThreads);
-  if (K8 <= kGemvThreads) return launch_k(h, gemv_kernel<M, 1>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K);
-  if (K8 <= 2 * kGemvThreads) return launch_k(h, gemv_kernel<M, 2>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K);
-  if (K8 <= 4 * kGemvThreads) return launch_k(h, gemv_kernel<M, 4>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K);
-  return launch_k(h, gemv_kernel<M, 8>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K);
+  if (K8 <= kGemvThreads) return launch_k(h, gemv_kernel<M, 1>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps);
+  if (K8 <= 2 * kGemvThreads) return launch_k(h, gemv_kernel<M, 2>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps);
+  if (K8 <= 4 * kGemvThreads) return launch_k(h, gemv_kernel<M, 4>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps);
+  return launch_k(h, gemv_kernel<M, 8>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps);
 }
 
 cudaError_t launch_gemv(dec_handle* h, const uint16_t* x, long long ldx, const uint16_t* W, const uint16_t* res,
-                        long long ldr, uint16_t* y, long long ldy, int M, int N, int K, cudaStream_t s) {
+                        long long ldr, uint16_t* y, long long ldy, int M, int N, int K, cudaStream_t s,
+                        const uint16_t* gamma, float eps) {
+  if (gamma != nullptr && M != 1) return cudaErrorInvalidValue;
   switch (M) {
-    case 1: return gemv_m<1>(h, x, ldx, W, res, ldr, y, ldy, N, K, s);
-    case 2: return gemv_m<2>(h, x, ldx, W, res, ldr, y, ldy, N, K, s);
-    case 3: return gemv_m<3>(h, x, ldx, W, res, ldr, y, ldy, N, K, s);
-    case 4: return gemv_m<4>(h, x, ldx, W, res, ldr, y, ldy, N, K, s);
+    case 1: return gemv_m<1>(h, x, ldx, W, res, ldr, y, ldy, N, K, s, gamma, eps);
+    case 2: return gemv_m<2>(h, x, ldx, W, res, ldr, y, ldy, N, K, s, nullptr, 0.f);
+    case 3: return gemv_m<3>(h, x, ldx, W, res, ldr, y, ldy, N, K, s, nullptr, 0.f);
+    case 4: return gemv_m<4>(h, x, ldx, W, res, ldr, y, ldy, N, K, s, nullptr, 0.f);
     default: return cudaErrorInvalidValue;
   }
 }

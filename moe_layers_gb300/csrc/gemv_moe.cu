@@ -205,6 +205,136 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_kernel(const GemvMoePa
   }
 }
 
+// One token, down projection fused with the weighted combine and residual:
+//   out[n] = bf16( sum_j w_j (Wd_{e_j}[n] . h_j)  [+ Wd_s[n] . h_s]  [+ res[n]] )
+// with the fp32 sums in that order (the combine kernel's order). The unit is
+// one output row n; it reads row n of every selected expert's W_d (and of the
+// shared expert's), so no per-expert output is written and no combine kernel
+// runs. The k (+1) activation rows sit in shared memory and thread t streams
+// the weight vectors t, t+256, ... of each row. NP = k (+1 with a shared
+// expert) rows per unit.
+template <int NP, int VPT, bool SHARED>
+__global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_kernel(
+    const uint16_t* __restrict__ Wd, long long rows_bank, const uint16_t* __restrict__ Wd_s, int H, int K,
+    const uint16_t* hbuf, const uint16_t* hs, const int* table, int E, int k, const float* w, const uint16_t* res,
+    uint16_t* out) {
+  constexpr int NR = SHARED ? NP - 1 : NP;  // routed rows per unit
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int K8 = K >> 3;
+  __shared__ float red[2][kGmThreads / 32][NP];
+  const uint64_t pol = policy_evict_first();
+  pdl_trigger();
+  const long long G = gridDim.x, c = blockIdx.x;
+  const int n0 = (int)(c * H / G), n1 = (int)((c + 1) * H / G);
+  pdl_wait();
+  if (n0 >= n1) return;
+  const TableLayout L(E, k);
+  // Per selected row: the W_d row base, the combine weight, and the activation
+  // row (in shared memory; registers carry the weight stream).
+  __shared__ const uint16_t* s_rowbase[NP];
+  __shared__ float s_w[NP];
+  extern __shared__ uint4 s_x[];  // [NP][K8]
+  if (t < NP) {
+    if (SHARED && t == NP - 1) {
+      s_rowbase[t] = Wd_s;
+      s_w[t] = 1.f;
+    } else {
+      const int slot = ld_act_s32(table + L.entry_slot() + t);   // token 0, entry t
+      const long long e = ld_act_s32(table + L.expert() + slot); // one token: problem index == slot
+      s_rowbase[t] = Wd + e * rows_bank * K;
+      s_w[t] = ld_act_f32(w + t);
+    }
+  }
+  for (int q = t; q < NP * K8; q += kGmThreads) {
+    const int j = q / K8, v = q - j * K8;
+    const uint16_t* src;
+    if (SHARED && j == NP - 1) {
+      src = hs;
+    } else {
+      const int slot = ld_act_s32(table + L.entry_slot() + j);
+      src = hbuf + (size_t)slot * K;
+    }
+    s_x[q] = ld_act16(src + (size_t)v * 8);
+  }
+  // residual values of this CTA's rows, read once (kept off the per-row path)
+  __shared__ float s_res[64];
+  for (int q = t; q < n1 - n0 && q < 64; q += kGmThreads) s_res[q] = res ? bf2f(ld_act_u16(res + n0 + q)) : 0.f;
+  __syncthreads();
+  uint4 wa[NP][VPT];
+  auto load = [&](uint4(&wr)[NP][VPT], int n) {
+#pragma unroll
+    for (int j = 0; j < NP; ++j)
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = t + kGmThreads * i;
+        wr[j][i] = (v < K8) ? ld_stream(s_rowbase[j] + (size_t)n * K + (size_t)v * 8, pol) : make_uint4(0, 0, 0, 0);
+      }
+  };
+  load(wa, n0);
+  int buf = 0;
+  for (int n = n0; n < n1; ++n) {
+    uint4 wb[NP][VPT];
+    if (n + 1 < n1) load(wb, n + 1);
+    float acc[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = t + kGmThreads * i;
+        if (v < K8) sum = dot8(wa[j][i], s_x[j * K8 + v], sum);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      acc[j] = sum;
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < NP; ++j) red[buf][warp][j] = acc[j];
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane j sums expert j's partials over the warps; lane 0 then combines
+      // in entry order (the combine kernel's order)
+      float y = 0.f;
+      if (lane < NP) {
+#pragma unroll
+        for (int q = 0; q < kGmThreads / 32; ++q) y += red[buf][q][lane];
+      }
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < NR; ++j) a = fmaf(s_w[j], __shfl_sync(0xffffffffu, y, j), a);
+      if (SHARED) a += __shfl_sync(0xffffffffu, y, NP - 1);
+      if (lane == 0) {
+        if (res != nullptr) a += (n - n0 < 64) ? s_res[n - n0] : bf2f(ld_act_u16(res + n));
+        out[n] = f2bf(a);
+      }
+    }
+    buf ^= 1;
+#pragma unroll
+    for (int j = 0; j < NP; ++j)
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) wa[j][i] = wb[j][i];
+  }
+}
+
+// Rows of up to 2048 elements (one vector per thread); the activations take k+1 rows of shared memory.
+bool gemv_down_combine_supported(int k, int I) { return k == 8 && I >= 8 && I % 8 == 0 && I <= 8 * kGmThreads; }
+
+cudaError_t launch_gemv_down_combine(dec_handle* h, const uint16_t* Wd, long long rows_bank, const uint16_t* Wd_s,
+                                     int H, int I, const uint16_t* hbuf, const uint16_t* hs, const int* table, int E,
+                                     int k, const float* w, const uint16_t* res, uint16_t* out, int sms,
+                                     cudaStream_t s) {
+  if (!gemv_down_combine_supported(k, I)) return cudaErrorInvalidValue;
+  const dim3 g(std::max(1, 2 * sms)), b(kGmThreads);
+  const size_t smem = (size_t)(k + (Wd_s ? 1 : 0)) * (I / 8) * 16;
+  if (Wd_s != nullptr)
+    return launch_k(h, gemv_down_combine_kernel<9, 1, true>, g, b, smem, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs,
+                    table, E, k, w, res, out);
+  return launch_k(h, gemv_down_combine_kernel<8, 1, false>, g, b, smem, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs, table,
+                  E, k, w, res, out);
+}
+
 bool gemv_moe_supported(int K) { return K >= 8 && K % 8 == 0 && K <= 8 * 4 * kGmThreads; }
 
 template <bool SWIGLU>

@@ -88,8 +88,10 @@ struct EngineLaunch {
 
 cudaError_t launch_engine(dec_handle* h, const EngineLaunch& L, cudaStream_t s);
 
+// gamma (M = 1 only): normalise the input row first (RMSNorm with eps), fused.
 cudaError_t launch_gemv(dec_handle* h, const uint16_t* x, long long ldx, const uint16_t* W, const uint16_t* res,
-                        long long ldr, uint16_t* y, long long ldy, int M, int N, int K, cudaStream_t s);
+                        long long ldr, uint16_t* y, long long ldy, int M, int N, int K, cudaStream_t s,
+                        const uint16_t* gamma = nullptr, float eps = 0.f);
 bool gemv_supported(int M, int K);
 
 // Small-matrix expert kernels for one token (gemv_moe.cu): gate/up with the
@@ -108,6 +110,13 @@ cudaError_t launch_gemv_moe(dec_handle* h, bool swiglu, const uint16_t* A, const
                             const int* table, int E, int n_entries, void* out, long long ldo, int sms,
                             cudaStream_t s, const GemvMoeShared* shared = nullptr);
 bool gemv_moe_supported(int K);
+// One token: down projection of the k routed (+ shared) experts fused with the
+// weighted combine and the residual, written straight to out (bf16 [H]).
+bool gemv_down_combine_supported(int k, int I);
+cudaError_t launch_gemv_down_combine(dec_handle* h, const uint16_t* Wd, long long rows_bank, const uint16_t* Wd_s,
+                                     int H, int I, const uint16_t* hbuf, const uint16_t* hs, const int* table, int E,
+                                     int k, const float* w, const uint16_t* res, uint16_t* out, int sms,
+                                     cudaStream_t s);
 
 cudaError_t launch_rmsnorm(dec_handle* h, const uint16_t* x, const uint16_t* gamma, uint16_t* y, int M, int H,
                            float eps, cudaStream_t s);

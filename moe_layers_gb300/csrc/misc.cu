@@ -7,8 +7,14 @@
 namespace dec {
 
 // y = x / sqrt(mean(x^2) + eps) * gamma, one CTA per row, fp32 math. The
-// pre-norm of the decode layer (not named on the pages). y may alias x: every
-// element is re-read by the thread that writes it, after the block reduction.
+// pre-norm of the decode layer (not named on the pages). Rows of up to 8192
+// elements (VPT <= 4 vectors per thread) are read once into registers; longer
+// rows are read twice. The sum of squares is accumulated per thread over its
+// vectors in ascending order, reduced by warp shuffles, then over the warps in
+// order (the small-matrix projection repeats exactly this order when it
+// normalises its input itself). y may alias x: each element is written by the
+// thread that read it, after the block reduction.
+template <int VPT>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const uint16_t* __restrict__ gamma,
                                                       uint16_t* y, int H, float eps) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -18,9 +24,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const u
   pdl_trigger();
   pdl_wait();
   const int H8 = H >> 3;
-  float ss = 0.f;
-  for (int v = tid; v < H8; v += blockDim.x) {
-    const uint4 a = ld_act16(xr + (size_t)v * 8);
+  auto sq = [](const uint4& a, float ss) {
     const uint32_t ws[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -28,6 +32,21 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const u
       ss = fmaf(lo, lo, ss);
       ss = fmaf(hi, hi, ss);
     }
+    return ss;
+  };
+  uint4 xv[VPT > 0 ? VPT : 1];
+  float ss = 0.f;
+  if (VPT > 0) {
+#pragma unroll
+    for (int j = 0; j < (VPT > 0 ? VPT : 1); ++j) {
+      const int v = tid + 256 * j;
+      if (v < H8) {
+        xv[j] = ld_act16(xr + (size_t)v * 8);
+        ss = sq(xv[j], ss);
+      }
+    }
+  } else {
+    for (int v = tid; v < H8; v += blockDim.x) ss = sq(ld_act16(xr + (size_t)v * 8), ss);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -36,8 +55,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const u
   float tot = 0.f;
   for (int q = 0; q < (int)(blockDim.x >> 5); ++q) tot += red[q];
   const float r = rsqrtf(tot / (float)H + eps);
-  for (int v = tid; v < H8; v += blockDim.x) {
-    const uint4 a = ld_act16(xr + (size_t)v * 8);
+  auto put = [&](int v, const uint4& a) {
     const uint4 g = *reinterpret_cast<const uint4*>(gamma + (size_t)v * 8);
     const uint32_t ws[4] = {a.x, a.y, a.z, a.w}, gs[4] = {g.x, g.y, g.z, g.w};
     uint32_t o[4];
@@ -48,6 +66,15 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const u
       o[i] = (uint32_t)l | ((uint32_t)u << 16);
     }
     *reinterpret_cast<uint4*>(yr + (size_t)v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  if (VPT > 0) {
+#pragma unroll
+    for (int j = 0; j < (VPT > 0 ? VPT : 1); ++j) {
+      const int v = tid + 256 * j;
+      if (v < H8) put(v, xv[j]);
+    }
+  } else {
+    for (int v = tid; v < H8; v += blockDim.x) put(v, ld_act16(xr + (size_t)v * 8));
   }
 }
 
@@ -101,7 +128,11 @@ __global__ void delayed_copy_kernel(uint4* dst, const uint4* src, size_t n16, un
 
 cudaError_t launch_rmsnorm(dec_handle* h, const uint16_t* x, const uint16_t* gamma, uint16_t* y, int M, int H,
                            float eps, cudaStream_t s) {
-  return launch_k(h, rmsnorm_kernel, dim3(M), dim3(256), 0, s, x, gamma, y, H, eps);
+  const int H8 = H / 8;
+  if (H8 <= 256) return launch_k(h, rmsnorm_kernel<1>, dim3(M), dim3(256), 0, s, x, gamma, y, H, eps);
+  if (H8 <= 512) return launch_k(h, rmsnorm_kernel<2>, dim3(M), dim3(256), 0, s, x, gamma, y, H, eps);
+  if (H8 <= 1024) return launch_k(h, rmsnorm_kernel<4>, dim3(M), dim3(256), 0, s, x, gamma, y, H, eps);
+  return launch_k(h, rmsnorm_kernel<0>, dim3(M), dim3(256), 0, s, x, gamma, y, H, eps);
 }
 
 cudaError_t launch_prefetch(dec_handle* h, const void* p, size_t bytes, int ctas, cudaStream_t s) {

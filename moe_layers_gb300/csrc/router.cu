@@ -85,71 +85,103 @@ __global__ void __launch_bounds__(256) router_kernel(const uint16_t* x, const fl
   }
 }
 
-// One CTA per token: logits = sum of the split partials in split order,
-// s = 1 / (1 + exp(-logit)), then k rounds of a block-wide arg-max
-// (score descending, expert id ascending) and renormalisation.
+// One CTA per token. logits = sum of the split partials in split order,
+// s = 1 / (1 + exp(-logit)). Each of the 8 warps takes a contiguous eighth of
+// the experts (J per lane, in registers), keeps its local top-k by k rounds of
+// warp arg-max (score descending, expert id ascending), and warp 0 merges the
+// 8k candidates the same way; weights are the selected scores over their sum.
+// All partial-sum loads of a split are issued before any is used.
+template <int J>  // ceil(ceil(E / 8) / 32)
 __global__ void __launch_bounds__(256) topk_kernel(const float* parts, int ks, int M, int E, int k, int32_t* idx,
                                                    float* w, float* scores) {
-  const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  __shared__ float sv[1024];
-  __shared__ float red_v[8];
-  __shared__ int red_i[8];
-  __shared__ float wsel[16];
-  __shared__ int isel[16];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x;
+  const int Ew = (E + 7) / 8;
+  __shared__ float cv[8][16];
+  __shared__ int ci[8][16];
   pdl_trigger();
   pdl_wait();
-  for (int e = tid; e < E; e += blockDim.x) {
-    float z = 0.f;
-    for (int s = 0; s < ks; ++s) z += ld_act_f32(parts + ((size_t)s * M + t) * E + e);
-    const float sc = 1.0f / (1.0f + expf(-z));
-    sv[e] = sc;
-    if (scores != nullptr) scores[(size_t)t * E + e] = sc;
+  float sv[J];
+  int ev[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int off = lane + 32 * j;
+    ev[j] = warp * Ew + off;
+    sv[j] = 0.f;
+  }
+  for (int s = 0; s < ks; ++s) {
+    float tmp[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+      tmp[j] = (lane + 32 * j < Ew && ev[j] < E) ? ld_act_f32(parts + ((size_t)s * M + t) * E + ev[j]) : 0.f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) sv[j] += tmp[j];
+  }
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    if (lane + 32 * j < Ew && ev[j] < E) {
+      sv[j] = 1.0f / (1.0f + expf(-sv[j]));
+      if (scores != nullptr) scores[(size_t)t * E + ev[j]] = sv[j];
+    } else {
+      sv[j] = -FLT_MAX;
+      ev[j] = INT_MAX;
+    }
+  }
+  // k rounds of warp arg-max; returns the r-th selection in lane r.
+  auto select = [&](float* v, int* id, int n, float& out_v, int& out_i) {
+    for (int r = 0; r < k; ++r) {
+      float bv = -FLT_MAX;
+      int bi = INT_MAX;
+      for (int j = 0; j < n; ++j)
+        if (v[j] > bv || (v[j] == bv && id[j] < bi)) {
+          bv = v[j];
+          bi = id[j];
+        }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      for (int j = 0; j < n; ++j)
+        if (id[j] == bi) v[j] = -FLT_MAX;  // ids are unique: only the owner matches
+      if (lane == r) {
+        out_v = bv;
+        out_i = bi;
+      }
+    }
+  };
+  float mv = -FLT_MAX;
+  int mi = INT_MAX;
+  select(sv, ev, J, mv, mi);
+  if (lane < k) {
+    cv[warp][lane] = mv;
+    ci[warp][lane] = mi;
   }
   __syncthreads();
-  for (int r = 0; r < k; ++r) {
-    float bv = -FLT_MAX;
-    int bi = INT_MAX;
-    for (int e = tid; e < E; e += blockDim.x) {
-      const float v = sv[e];
-      if (v > bv || (v == bv && e < bi)) {
-        bv = v;
-        bi = e;
-      }
-    }
+  if (warp == 0) {
+    // 8 warps x k candidates: lane l holds candidates (l / k ... ) — two per lane when k <= 8
+    float v2[4];
+    int i2[4];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
+    for (int j = 0; j < 4; ++j) {
+      const int q = lane + 32 * j;  // candidate index in [0, 8k)
+      const int wq = q / k, rq = q - wq * k;
+      const bool ok = q < 8 * k;
+      v2[j] = ok ? cv[wq][rq] : -FLT_MAX;
+      i2[j] = ok ? ci[wq][rq] : INT_MAX;
     }
-    if (lane == 0) {
-      red_v[warp] = bv;
-      red_i[warp] = bi;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float v = red_v[0];
-      int i = red_i[0];
-      for (int q = 1; q < (int)(blockDim.x >> 5); ++q)
-        if (red_v[q] > v || (red_v[q] == v && red_i[q] < i)) {
-          v = red_v[q];
-          i = red_i[q];
-        }
-      wsel[r] = v;
-      isel[r] = i;
-      sv[i] = -FLT_MAX;  // taken
-    }
-    __syncthreads();
-  }
-  if (tid == 0) {
+    float fv = 0.f;
+    int fi = 0;
+    select(v2, i2, 4, fv, fi);
     float sum = 0.f;
-    for (int r = 0; r < k; ++r) sum += wsel[r];
-    for (int r = 0; r < k; ++r) {
-      idx[(size_t)t * k + r] = isel[r];
-      w[(size_t)t * k + r] = wsel[r] / sum;
+    for (int r = 0; r < k; ++r) sum += __shfl_sync(0xffffffffu, fv, r);
+    if (lane < k) {
+      idx[(size_t)t * k + lane] = fi;
+      w[(size_t)t * k + lane] = fv / sum;
     }
   }
 }
@@ -296,7 +328,11 @@ cudaError_t launch_router(dec_handle* h, const uint16_t* x, const float* Wr, int
 
 cudaError_t launch_topk(dec_handle* h, const float* parts, int ks, int M, int E, int k, int32_t* idx, float* w,
                         float* scores, cudaStream_t s) {
-  return launch_k(h, topk_kernel, dim3(M), dim3(256), 0, s, parts, ks, M, E, k, idx, w, scores);
+  const int Ew = (E + 7) / 8;
+  const dim3 g(M), b(256);
+  if (Ew <= 32) return launch_k(h, topk_kernel<1>, g, b, 0, s, parts, ks, M, E, k, idx, w, scores);
+  if (Ew <= 64) return launch_k(h, topk_kernel<2>, g, b, 0, s, parts, ks, M, E, k, idx, w, scores);
+  return launch_k(h, topk_kernel<4>, g, b, 0, s, parts, ks, M, E, k, idx, w, scores);
 }
 
 cudaError_t launch_route_table(dec_handle* h, const int32_t* idx, int M, int k, int E, const uint16_t* x, int H,

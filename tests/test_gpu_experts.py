@@ -42,6 +42,7 @@ def _small_bank(E, H, I, base):
 @pytest.mark.parametrize("family", ["auto", "split_k"])
 @pytest.mark.parametrize("M,E,H,I,k,shared,resid,skew", [
     (1, 24, 384, 256, 8, True, True, False),
+    (1, 24, 384, 256, 8, False, False, False),
     (1, 16, 256, 128, 4, True, False, False),
     (3, 16, 256, 256, 4, False, True, False),
     (17, 32, 384, 128, 8, True, True, False),
