@@ -262,6 +262,46 @@ dec_status moe_shared_fork(dec_handle* h, const uint16_t* x, int M, int k, int E
   return DEC_OK;
 }
 
+// One token, small-matrix kernels: routed and shared experts in one balanced
+// launch per matrix over every SM (the shared expert is problem 0), the down
+// projection fused with the combine and the residual where supported. The
+// routing table in ws.table is complete; slot j's activation row is at
+// x + j * ldx (ldx 0: one row for all slots).
+dec_status moe_small(dec_handle* h, const uint16_t* x, long long ldx, const float* w, int k, const uint16_t* Wg,
+                     const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I, const uint16_t* Wg_s,
+                     const uint16_t* Wu_s, const uint16_t* Wd_s, const uint16_t* residual, uint16_t* out,
+                     const MoeWs& ws, cudaStream_t s) {
+  const bool has_shared = Wg_s != nullptr;
+  h->last_expert_variant = DEC_VARIANT_SMALL_M;
+  // the shared expert's activation: slot 0's row (every slot holds the token's row)
+  const GemvMoeShared sgu{Wg_s, Wu_s, x, ws.hs}, sdn{Wd_s, nullptr, ws.hs, ws.ys};
+  const bool fused_down = gemv_down_combine_supported(k, I);
+  {
+    LaunchScope scope(h, "gate_up", s);
+    DEC_CUDA(launch_gemv_moe(h, true, Wg, Wu, I, I, H, x, ldx, ws.table, E, k, ws.hbuf, I, h->sms, s,
+                             has_shared ? &sgu : nullptr, k, fused_down));
+  }
+  if (fused_down) {
+    // down projection + weighted combine + residual in one kernel; the routing
+    // is read before its dependency wait (the gate/up launch triggers its
+    // dependents only after its own wait, when the routing is complete)
+    LaunchScope scope(h, "down", s);
+    DEC_CUDA(launch_gemv_down_combine(h, Wd, H, has_shared ? Wd_s : nullptr, H, I, ws.hbuf, ws.hs, ws.table, E, k, w,
+                                      residual, out, h->sms, s, true));
+    return DEC_OK;
+  }
+  {
+    LaunchScope scope(h, "down", s);
+    DEC_CUDA(launch_gemv_moe(h, false, Wd, nullptr, H, H, I, ws.hbuf, I, ws.table, E, k, ws.y, H, h->sms, s,
+                             has_shared ? &sdn : nullptr, k, false));
+  }
+  {
+    LaunchScope scope(h, "combine", s);
+    DEC_CUDA(launch_combine(h, ws.y, ws.table, w, 1, k, E, has_shared ? ws.ys : nullptr, residual, out, H, s));
+  }
+  return DEC_OK;
+}
+
 dec_status moe_routed(dec_handle* h, const uint16_t* x, const int32_t* idx, const float* w, int M, int k,
                       const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I,
                       const uint16_t* Wg_s, const uint16_t* Wu_s, const uint16_t* Wd_s, const uint16_t* residual,
@@ -269,37 +309,16 @@ dec_status moe_routed(dec_handle* h, const uint16_t* x, const int32_t* idx, cons
   const bool has_shared = Wg_s != nullptr;
   const int n = M * k;
   const int g0 = routed_grid(h, M, k, E, has_shared);
+  if (experts_small(h, M, H, I)) {
+    {
+      LaunchScope scope(h, "route_table", s);
+      DEC_CUDA(launch_one_token_table(h, idx, E, k, ws.table, s));
+    }
+    return moe_small(h, x, 0, w, k, Wg, Wu, Wd, E, H, I, Wg_s, Wu_s, Wd_s, residual, out, ws, s);
+  }
   {
     LaunchScope scope(h, "route_table", s);
     DEC_CUDA(launch_route_table(h, idx, M, k, E, x, H, ws.table, ws.xs, s));
-  }
-  if (experts_small(h, M, H, I)) {
-    // One token: routed and shared experts in one balanced launch per matrix
-    // over every SM (the shared expert is problem 0).
-    h->last_expert_variant = DEC_VARIANT_SMALL_M;
-    const GemvMoeShared sgu{Wg_s, Wu_s, x, ws.hs}, sdn{Wd_s, nullptr, ws.hs, ws.ys};
-    {
-      LaunchScope scope(h, "gate_up", s);
-      DEC_CUDA(launch_gemv_moe(h, true, Wg, Wu, I, I, H, ws.xs, H, ws.table, E, n, ws.hbuf, I, h->sms, s,
-                               has_shared ? &sgu : nullptr));
-    }
-    if (gemv_down_combine_supported(k, I)) {
-      // down projection + weighted combine + residual in one kernel
-      LaunchScope scope(h, "down", s);
-      DEC_CUDA(launch_gemv_down_combine(h, Wd, H, has_shared ? Wd_s : nullptr, H, I, ws.hbuf, ws.hs, ws.table, E, k,
-                                        w, residual, out, h->sms, s));
-      return DEC_OK;
-    }
-    {
-      LaunchScope scope(h, "down", s);
-      DEC_CUDA(launch_gemv_moe(h, false, Wd, nullptr, H, H, I, ws.hbuf, I, ws.table, E, n, ws.y, H, h->sms, s,
-                               has_shared ? &sdn : nullptr));
-    }
-    {
-      LaunchScope scope(h, "combine", s);
-      DEC_CUDA(launch_combine(h, ws.y, ws.table, w, M, k, E, has_shared ? ws.ys : nullptr, residual, out, H, s));
-    }
-    return DEC_OK;
   }
   h->last_expert_variant = DEC_VARIANT_SPLIT_K;
   EngineLaunch L;
@@ -368,6 +387,7 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
 
 // ---------------------------------------------------------------- decode layer workspace
 struct LayerWs {
+  int* sel_counter = nullptr;  // the one-token router's hand-off counter
   uint16_t* a = nullptr;
   uint16_t* yin = nullptr;
   uint16_t* h1 = nullptr;
@@ -389,6 +409,7 @@ bool layer_ok(const dec_layer_weights* L, int M) {
 void carve_layer(Carver& c, const dec_handle* h, const dec_layer_weights* L, int M, LayerWs* w) {
   const int H = L->H;
   const long long dense_tiles = std::max<long long>((L->N_in + kTileN - 1) / kTileN, H / kTileN);
+  w->sel_counter = c.take<int>(1);
   carve_moe_counters(c, L->E, H, L->I, dense_tiles, &w->moe);
   w->a = c.take<uint16_t>((size_t)M * H);
   w->yin = c.take<uint16_t>((size_t)M * L->N_in);
@@ -569,7 +590,7 @@ dec_status dec_rmsnorm(dec_handle* h, const dec_bf16* x, const dec_bf16* gamma, 
 dec_status moe_route_topk_workspace_size(const dec_handle* h, int M, int H, int E, size_t* bytes) {
   if (h == nullptr || bytes == nullptr || M < 1 || M > kMaxM || H < 8 || H % 8 != 0 || E < 1 || E > kMaxE)
     return DEC_ERR_INVALID_ARG;
-  *bytes = al256((size_t)router_ksplit(H) * M * E * sizeof(float));
+  *bytes = al256(sizeof(int)) + al256((size_t)router_ksplit(H) * M * E * sizeof(float));
   return DEC_OK;
 }
 
@@ -582,7 +603,17 @@ dec_status moe_route_topk(dec_handle* h, const dec_bf16* x, const float* Wr, int
   size_t need = 0;
   moe_route_topk_workspace_size(h, M, H, E, &need);
   if (ws == nullptr || ws_bytes < need) return DEC_ERR_INVALID_ARG;
-  float* parts = static_cast<float*>(ws);
+  Carver c(ws);
+  int* counter = c.take<int>(1);
+  float* parts = c.take<float>((size_t)router_ksplit(H) * M * E);
+  if (M == 1) {
+    // one launch: logits, then the top-k by the last CTA
+    LaunchScope scope(h, "router", stream);
+    return launch_router_select(h, x, nullptr, 0.f, Wr, H, E, k, nullptr, parts, counter, idx, w, scores, nullptr,
+                                stream) == cudaSuccess
+               ? DEC_OK
+               : DEC_ERR_CUDA;
+  }
   {
     LaunchScope scope(h, "router", stream);
     if (launch_router(h, x, Wr, M, H, E, parts, stream) != cudaSuccess) return DEC_ERR_CUDA;
@@ -682,7 +713,11 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   if (st != DEC_OK) return st;
   st = linear_impl(h, w.yin, L.N_in, L.W_o, hidden, h1, M, H, L.K_out, w.moe.r0, s, "out_proj");
   if (st != DEC_OK) return st;
-  {
+  // One token with the small-matrix experts: the second RMSNorm, the router,
+  // the top-k and the routing table are one launch (router_select), and the
+  // experts read the normalised row for every slot (no gather).
+  const bool one_token = experts_small(h, M, H, L.I);
+  if (!one_token) {
     LaunchScope scope(h, "rmsnorm2", s);
     if (launch_rmsnorm(h, h1, L.gamma2, w.b, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
   }
@@ -710,6 +745,17 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   }
   // The router / top-k phase is latency-bound; the shared expert and the
   // prefetch stream use the idle bandwidth meanwhile.
+  if (one_token) {
+    {
+      LaunchScope scope(h, "router", s);
+      DEC_CUDA(launch_router_select(h, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx, wt,
+                                    scores, w.moe.table, s));
+    }
+    st = moe_small(h, w.b, 0, wt, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, h1, hidden, w.moe, s);
+    if (st != DEC_OK) return st;
+    if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
+    return DEC_OK;
+  }
   st = moe_shared_fork(h, w.b, M, L.k, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, w.moe, s);
   if (st != DEC_OK) return st;
   {

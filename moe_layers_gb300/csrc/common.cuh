@@ -97,6 +97,46 @@ __device__ __forceinline__ uint16_t ld_act_u16(const void* p) {
   asm volatile("ld.global.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
   return v;
 }
+// L2-level loads (.cg, never served from L1) of values that other CTAs of the
+// running kernel wrote before a fence and an atomic hand-off, or that a kernel
+// two launches back wrote.
+__device__ __forceinline__ float ld_cg_f32(const void* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_cg_s32(const void* p) {
+  int v;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------- RMSNorm pieces
+// Every kernel that normalises a row uses these two, in the same order: the
+// sum of squares runs over each thread's 8-element vectors in ascending order,
+// element by element, so a row normalised in any of them has the same bits.
+__device__ __forceinline__ float sumsq8(const uint4& a, float ss) {
+  const uint32_t ws[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = bf_lo(ws[i]), hi = bf_hi(ws[i]);
+    ss = fmaf(lo, lo, ss);
+    ss = fmaf(hi, hi, ss);
+  }
+  return ss;
+}
+// bf16(x * r * gamma) for 8 elements.
+__device__ __forceinline__ uint4 norm8(const uint4& a, const uint4& g, float r) {
+  const uint32_t ws[4] = {a.x, a.y, a.z, a.w}, gs[4] = {g.x, g.y, g.z, g.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint16_t l = f2bf(bf_lo(ws[i]) * r * bf_lo(gs[i]));
+    const uint16_t u = f2bf(bf_hi(ws[i]) * r * bf_hi(gs[i]));
+    o[i] = (uint32_t)l | ((uint32_t)u << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 // ---------------------------------------------------------------- PDL
 // Programmatic dependent launch: a kernel may start while its predecessor on

@@ -88,15 +88,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int v = t + kGemvThreads * i;
-      if (v < K8) {
-        const uint32_t ws[4] = {xr[0][i].x, xr[0][i].y, xr[0][i].z, xr[0][i].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float lo = bf_lo(ws[e]), hi = bf_hi(ws[e]);
-          ss = fmaf(lo, lo, ss);
-          ss = fmaf(hi, hi, ss);
-        }
-      }
+      if (v < K8) ss = sumsq8(xr[0][i], ss);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -107,18 +99,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
     for (int q = 0; q < kGemvThreads / 32; ++q) tot += rred[q];
     const float rs = rsqrtf(tot / (float)K + eps);
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const uint32_t ws[4] = {xr[0][i].x, xr[0][i].y, xr[0][i].z, xr[0][i].w};
-      const uint32_t gs[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
-      uint32_t o[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint16_t l = f2bf(bf_lo(ws[e]) * rs * bf_lo(gs[e]));
-        const uint16_t u = f2bf(bf_hi(ws[e]) * rs * bf_hi(gs[e]));
-        o[e] = (uint32_t)l | ((uint32_t)u << 16);
-      }
-      xr[0][i] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
+    for (int i = 0; i < VPT; ++i) xr[0][i] = norm8(xr[0][i], gv[i], rs);
   }
 
   int buf = 0;

@@ -46,6 +46,8 @@ struct GemvMoeParams {
   int E, n_entries;
   void* out;           // SwiGLU: bf16 [slots][ldo]; down: fp32 [slots][ldo]
   long long ldo;
+  int nprob_known;     // routed problems if known at launch (one token: k), else 0
+  int late_trigger;    // trigger dependents after the dependency wait (they may then read the routing early)
 };
 
 template <bool SWIGLU, int VPT>
@@ -56,7 +58,7 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_kernel(const GemvMoePa
   const int K8 = P.K >> 3;
   __shared__ float red[2][kGmThreads / 32][RB * NR];
   const uint64_t pol = policy_evict_first();
-  pdl_trigger();
+  if (!P.late_trigger) pdl_trigger();
 
   // Problem bookkeeping (the routed table is read only after the dependency wait).
   const TableLayout L(P.E, P.n_entries);
@@ -95,16 +97,23 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_kernel(const GemvMoePa
   const long long G = gridDim.x, c = blockIdx.x;
   long long q0 = 0, q1 = 0;
   int pre_nu = 0;
-  if (P.table == nullptr) {  // dense: the range is known, start the weight stream now
-    const long long T = (long long)(1 + ns) * P.R;
+  // With the problem count known at launch the range is too; a range that
+  // starts in a dense problem starts its weight stream now.
+  const bool range_known = P.table == nullptr || P.nprob_known > 0;
+  if (range_known) {
+    const long long T = (long long)((P.table ? P.nprob_known : 1) + ns) * P.R;
     q0 = c * T / G;
     q1 = (c + 1) * T / G;
-    const long long e0 = (q0 / P.R < ns) ? -1 : 0;
-    pre_nu = (int)min((long long)RB, min(q1, (q0 / P.R + 1) * (long long)P.R) - q0);
-    if (pre_nu > 0) load_units(wa, mat0(e0), mat1(e0), (int)(q0 % P.R), pre_nu);
+    const long long p0 = q0 / P.R;
+    if (p0 < ns || P.table == nullptr) {
+      const long long e0 = p0 < ns ? -1 : 0;
+      pre_nu = (int)max(0LL, min((long long)RB, min(q1, (p0 + 1) * (long long)P.R) - q0));
+      if (pre_nu > 0) load_units(wa, mat0(e0), mat1(e0), (int)(q0 % P.R), pre_nu);
+    }
   }
   pdl_wait();
-  if (P.table != nullptr) {
+  if (P.late_trigger) pdl_trigger();
+  if (!range_known) {
     const long long T = nprob() * P.R;
     q0 = c * T / G;
     q1 = (c + 1) * T / G;
@@ -217,7 +226,7 @@ template <int NP, int VPT, bool SHARED>
 __global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_kernel(
     const uint16_t* __restrict__ Wd, long long rows_bank, const uint16_t* __restrict__ Wd_s, int H, int K,
     const uint16_t* hbuf, const uint16_t* hs, const int* table, int E, int k, const float* w, const uint16_t* res,
-    uint16_t* out) {
+    uint16_t* out, int routing_ready) {
   constexpr int NR = SHARED ? NP - 1 : NP;  // routed rows per unit
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int K8 = K >> 3;
@@ -226,24 +235,49 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_kernel(
   pdl_trigger();
   const long long G = gridDim.x, c = blockIdx.x;
   const int n0 = (int)(c * H / G), n1 = (int)((c + 1) * H / G);
-  pdl_wait();
-  if (n0 >= n1) return;
+  if (n0 >= n1) return;  // (before any barrier)
   const TableLayout L(E, k);
   // Per selected row: the W_d row base, the combine weight, and the activation
   // row (in shared memory; registers carry the weight stream).
   __shared__ const uint16_t* s_rowbase[NP];
   __shared__ float s_w[NP];
   extern __shared__ uint4 s_x[];  // [NP][K8]
-  if (t < NP) {
-    if (SHARED && t == NP - 1) {
-      s_rowbase[t] = Wd_s;
-      s_w[t] = 1.f;
-    } else {
-      const int slot = ld_act_s32(table + L.entry_slot() + t);   // token 0, entry t
-      const long long e = ld_act_s32(table + L.expert() + slot); // one token: problem index == slot
-      s_rowbase[t] = Wd + e * rows_bank * K;
-      s_w[t] = ld_act_f32(w + t);
+  auto routing = [&](bool cg) {
+    if (t < NP) {
+      if (SHARED && t == NP - 1) {
+        s_rowbase[t] = Wd_s;
+        s_w[t] = 1.f;
+      } else {
+        // token 0, entry t; one token: problem index == slot
+        const int slot = cg ? ld_cg_s32(table + L.entry_slot() + t) : ld_act_s32(table + L.entry_slot() + t);
+        const long long e = cg ? ld_cg_s32(table + L.expert() + slot) : ld_act_s32(table + L.expert() + slot);
+        s_rowbase[t] = Wd + e * rows_bank * K;
+        s_w[t] = cg ? ld_cg_f32(w + t) : ld_act_f32(w + t);
+      }
     }
+    __syncthreads();
+  };
+  uint4 wa[NP][VPT];
+  auto load = [&](uint4(&wr)[NP][VPT], int n) {
+#pragma unroll
+    for (int j = 0; j < NP; ++j)
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = t + kGmThreads * i;
+        wr[j][i] = (v < K8) ? ld_stream(s_rowbase[j] + (size_t)n * K + (size_t)v * 8, pol) : make_uint4(0, 0, 0, 0);
+      }
+  };
+  // routing_ready: the launch before this one triggered its dependents only
+  // after its own dependency wait, so the routing (written two launches back)
+  // is complete now; read it at L2 and start the weight stream before the wait.
+  if (routing_ready) {
+    routing(true);
+    load(wa, n0);
+  }
+  pdl_wait();
+  if (!routing_ready) {
+    routing(false);
+    load(wa, n0);
   }
   for (int q = t; q < NP * K8; q += kGmThreads) {
     const int j = q / K8, v = q - j * K8;
@@ -260,17 +294,6 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_kernel(
   __shared__ float s_res[64];
   for (int q = t; q < n1 - n0 && q < 64; q += kGmThreads) s_res[q] = res ? bf2f(ld_act_u16(res + n0 + q)) : 0.f;
   __syncthreads();
-  uint4 wa[NP][VPT];
-  auto load = [&](uint4(&wr)[NP][VPT], int n) {
-#pragma unroll
-    for (int j = 0; j < NP; ++j)
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int v = t + kGmThreads * i;
-        wr[j][i] = (v < K8) ? ld_stream(s_rowbase[j] + (size_t)n * K + (size_t)v * 8, pol) : make_uint4(0, 0, 0, 0);
-      }
-  };
-  load(wa, n0);
   int buf = 0;
   for (int n = n0; n < n1; ++n) {
     uint4 wb[NP][VPT];
@@ -324,15 +347,15 @@ bool gemv_down_combine_supported(int k, int I) { return k == 8 && I >= 8 && I % 
 cudaError_t launch_gemv_down_combine(dec_handle* h, const uint16_t* Wd, long long rows_bank, const uint16_t* Wd_s,
                                      int H, int I, const uint16_t* hbuf, const uint16_t* hs, const int* table, int E,
                                      int k, const float* w, const uint16_t* res, uint16_t* out, int sms,
-                                     cudaStream_t s) {
+                                     cudaStream_t s, bool routing_ready) {
   if (!gemv_down_combine_supported(k, I)) return cudaErrorInvalidValue;
   const dim3 g(std::max(1, 2 * sms)), b(kGmThreads);
   const size_t smem = (size_t)(k + (Wd_s ? 1 : 0)) * (I / 8) * 16;
   if (Wd_s != nullptr)
     return launch_k(h, gemv_down_combine_kernel<9, 1, true>, g, b, smem, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs,
-                    table, E, k, w, res, out);
+                    table, E, k, w, res, out, (int)routing_ready);
   return launch_k(h, gemv_down_combine_kernel<8, 1, false>, g, b, smem, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs, table,
-                  E, k, w, res, out);
+                  E, k, w, res, out, (int)routing_ready);
 }
 
 bool gemv_moe_supported(int K) { return K >= 8 && K % 8 == 0 && K <= 8 * 4 * kGmThreads; }
@@ -349,7 +372,7 @@ static cudaError_t launch_mode(dec_handle* h, const GemvMoeParams& P, int grid, 
 cudaError_t launch_gemv_moe(dec_handle* h, bool swiglu, const uint16_t* A, const uint16_t* A2,
                             long long rows_per_prob_bank, int R, int K, const uint16_t* x, long long ldx,
                             const int* table, int E, int n_entries, void* out, long long ldo, int sms,
-                            cudaStream_t s, const GemvMoeShared* shared) {
+                            cudaStream_t s, const GemvMoeShared* shared, int nprob_known, bool late_trigger) {
   if (!gemv_moe_supported(K)) return cudaErrorInvalidValue;
   GemvMoeParams P;
   P.sA = shared ? shared->A : nullptr;
@@ -368,6 +391,8 @@ cudaError_t launch_gemv_moe(dec_handle* h, bool swiglu, const uint16_t* A, const
   P.n_entries = n_entries;
   P.out = out;
   P.ldo = ldo;
+  P.nprob_known = table ? nprob_known : 0;
+  P.late_trigger = late_trigger ? 1 : 0;
   const int grid = std::max(1, 2 * sms);
   return swiglu ? launch_mode<true>(h, P, grid, s) : launch_mode<false>(h, P, grid, s);
 }

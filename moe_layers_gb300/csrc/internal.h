@@ -108,7 +108,8 @@ struct GemvMoeShared {
 cudaError_t launch_gemv_moe(dec_handle* h, bool swiglu, const uint16_t* A, const uint16_t* A2,
                             long long rows_per_prob_bank, int R, int K, const uint16_t* x, long long ldx,
                             const int* table, int E, int n_entries, void* out, long long ldo, int sms,
-                            cudaStream_t s, const GemvMoeShared* shared = nullptr);
+                            cudaStream_t s, const GemvMoeShared* shared = nullptr, int nprob_known = 0,
+                            bool late_trigger = false);
 bool gemv_moe_supported(int K);
 // One token: down projection of the k routed (+ shared) experts fused with the
 // weighted combine and the residual, written straight to out (bf16 [H]).
@@ -116,7 +117,7 @@ bool gemv_down_combine_supported(int k, int I);
 cudaError_t launch_gemv_down_combine(dec_handle* h, const uint16_t* Wd, long long rows_bank, const uint16_t* Wd_s,
                                      int H, int I, const uint16_t* hbuf, const uint16_t* hs, const int* table, int E,
                                      int k, const float* w, const uint16_t* res, uint16_t* out, int sms,
-                                     cudaStream_t s);
+                                     cudaStream_t s, bool routing_ready = false);
 
 cudaError_t launch_rmsnorm(dec_handle* h, const uint16_t* x, const uint16_t* gamma, uint16_t* y, int M, int H,
                            float eps, cudaStream_t s);
@@ -126,6 +127,12 @@ cudaError_t launch_router(dec_handle* h, const uint16_t* x, const float* Wr, int
                           cudaStream_t s);
 cudaError_t launch_topk(dec_handle* h, const float* parts, int ks, int M, int E, int k, int32_t* idx, float* w,
                         float* scores, cudaStream_t s);
+// One token: RMSNorm (if gamma) + router logits + top-k + routing table; counter zero on entry and on return.
+cudaError_t launch_router_select(dec_handle* h, const uint16_t* x, const uint16_t* gamma, float eps, const float* Wr,
+                                 int H, int E, int k, uint16_t* xn, float* parts, int* counter, int32_t* idx,
+                                 float* w, float* scores, int* table, cudaStream_t s);
+// One token: the routing table with entry j as problem j on slot j (expert idx[j]).
+cudaError_t launch_one_token_table(dec_handle* h, const int32_t* idx, int E, int k, int* table, cudaStream_t s);
 cudaError_t launch_route_table(dec_handle* h, const int32_t* idx, int M, int k, int E, const uint16_t* x, int H,
                                int* table, uint16_t* xs, cudaStream_t s);
 cudaError_t launch_combine(dec_handle* h, const float* y, const int* table, const float* w, int M, int k, int E,

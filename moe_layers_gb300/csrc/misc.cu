@@ -24,16 +24,6 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const u
   pdl_trigger();
   pdl_wait();
   const int H8 = H >> 3;
-  auto sq = [](const uint4& a, float ss) {
-    const uint32_t ws[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float lo = bf_lo(ws[i]), hi = bf_hi(ws[i]);
-      ss = fmaf(lo, lo, ss);
-      ss = fmaf(hi, hi, ss);
-    }
-    return ss;
-  };
   uint4 xv[VPT > 0 ? VPT : 1];
   float ss = 0.f;
   if (VPT > 0) {
@@ -42,11 +32,11 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const u
       const int v = tid + 256 * j;
       if (v < H8) {
         xv[j] = ld_act16(xr + (size_t)v * 8);
-        ss = sq(xv[j], ss);
+        ss = sumsq8(xv[j], ss);
       }
     }
   } else {
-    for (int v = tid; v < H8; v += blockDim.x) ss = sq(ld_act16(xr + (size_t)v * 8), ss);
+    for (int v = tid; v < H8; v += blockDim.x) ss = sumsq8(ld_act16(xr + (size_t)v * 8), ss);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -57,15 +47,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const u
   const float r = rsqrtf(tot / (float)H + eps);
   auto put = [&](int v, const uint4& a) {
     const uint4 g = *reinterpret_cast<const uint4*>(gamma + (size_t)v * 8);
-    const uint32_t ws[4] = {a.x, a.y, a.z, a.w}, gs[4] = {g.x, g.y, g.z, g.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint16_t l = f2bf(bf_lo(ws[i]) * r * bf_lo(gs[i]));
-      const uint16_t u = f2bf(bf_hi(ws[i]) * r * bf_hi(gs[i]));
-      o[i] = (uint32_t)l | ((uint32_t)u << 16);
-    }
-    *reinterpret_cast<uint4*>(yr + (size_t)v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(yr + (size_t)v * 8) = norm8(a, g, r);
   };
   if (VPT > 0) {
 #pragma unroll

@@ -85,41 +85,50 @@ __global__ void __launch_bounds__(256) router_kernel(const uint16_t* x, const fl
   }
 }
 
-// One CTA per token. logits = sum of the split partials in split order,
-// s = 1 / (1 + exp(-logit)). Each of the 8 warps takes a contiguous eighth of
-// the experts (J per lane, in registers), keeps its local top-k by k rounds of
-// warp arg-max (score descending, expert id ascending), and warp 0 merges the
-// 8k candidates the same way; weights are the selected scores over their sum.
-// All partial-sum loads of a split are issued before any is used.
-template <int J>  // ceil(ceil(E / 8) / 32)
-__global__ void __launch_bounds__(256) topk_kernel(const float* parts, int ks, int M, int E, int k, int32_t* idx,
-                                                   float* w, float* scores) {
+constexpr int kTopkSplitsInRegs = 16;  // split partials per expert loaded together (H <= 16384)
+
+// Top-k of token t, one 256-thread block. logits = sum of the split partials
+// in split order, s = 1 / (1 + exp(-logit)). Each of the 8 warps takes a
+// contiguous eighth of the experts (J per lane, in registers), keeps its local
+// top-k by k rounds of warp arg-max (score descending, expert id ascending),
+// and warp 0 merges the 8k candidates the same way; weights are the selected
+// scores over their sum. All partial-sum loads are issued before any is used.
+// CG: read the partials at L2 (written by other CTAs of the running kernel).
+// On return lane r < k of warp 0 holds the r-th selection in *sel_e, *sel_w.
+template <int J, bool CG>
+__device__ __forceinline__ void block_topk(const float* parts, int ks, int M, int t, int E, int k, int32_t* idx,
+                                           float* w, float* scores, int* sel_e, float* sel_w) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x;
   const int Ew = (E + 7) / 8;
   __shared__ float cv[8][16];
   __shared__ int ci[8][16];
-  pdl_trigger();
-  pdl_wait();
   float sv[J];
   int ev[J];
+  bool ok[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) {
     const int off = lane + 32 * j;
     ev[j] = warp * Ew + off;
+    ok[j] = off < Ew && ev[j] < E;
     sv[j] = 0.f;
   }
-  for (int s = 0; s < ks; ++s) {
-    float tmp[J];
+  auto ld = [&](const float* p) { return CG ? ld_cg_f32(p) : ld_act_f32(p); };
+  for (int s0 = 0; s0 < ks; s0 += kTopkSplitsInRegs) {
+    float tmp[kTopkSplitsInRegs][J];
 #pragma unroll
-    for (int j = 0; j < J; ++j)
-      tmp[j] = (lane + 32 * j < Ew && ev[j] < E) ? ld_act_f32(parts + ((size_t)s * M + t) * E + ev[j]) : 0.f;
+    for (int q = 0; q < kTopkSplitsInRegs; ++q)
 #pragma unroll
-    for (int j = 0; j < J; ++j) sv[j] += tmp[j];
+      for (int j = 0; j < J; ++j)
+        tmp[q][j] = (s0 + q < ks && ok[j]) ? ld(parts + ((size_t)(s0 + q) * M + t) * E + ev[j]) : 0.f;
+#pragma unroll
+    for (int q = 0; q < kTopkSplitsInRegs; ++q)
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        if (s0 + q < ks) sv[j] += tmp[q][j];
   }
 #pragma unroll
   for (int j = 0; j < J; ++j) {
-    if (lane + 32 * j < Ew && ev[j] < E) {
+    if (ok[j]) {
       sv[j] = 1.0f / (1.0f + expf(-sv[j]));
       if (scores != nullptr) scores[(size_t)t * E + ev[j]] = sv[j];
     } else {
@@ -163,16 +172,16 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* parts, int ks, i
   }
   __syncthreads();
   if (warp == 0) {
-    // 8 warps x k candidates: lane l holds candidates (l / k ... ) — two per lane when k <= 8
+    // the 8k candidates, up to four per lane
     float v2[4];
     int i2[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int q = lane + 32 * j;  // candidate index in [0, 8k)
       const int wq = q / k, rq = q - wq * k;
-      const bool ok = q < 8 * k;
-      v2[j] = ok ? cv[wq][rq] : -FLT_MAX;
-      i2[j] = ok ? ci[wq][rq] : INT_MAX;
+      const bool okq = q < 8 * k;
+      v2[j] = okq ? cv[wq][rq] : -FLT_MAX;
+      i2[j] = okq ? ci[wq][rq] : INT_MAX;
     }
     float fv = 0.f;
     int fi = 0;
@@ -182,8 +191,146 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* parts, int ks, i
     if (lane < k) {
       idx[(size_t)t * k + lane] = fi;
       w[(size_t)t * k + lane] = fv / sum;
+      *sel_e = fi;
+      *sel_w = fv / sum;
     }
   }
+}
+
+// One CTA per token (see block_topk).
+template <int J>
+__global__ void __launch_bounds__(256) topk_kernel(const float* parts, int ks, int M, int E, int k, int32_t* idx,
+                                                   float* w, float* scores) {
+  pdl_trigger();
+  pdl_wait();
+  int se;
+  float sw;
+  block_topk<J, false>(parts, ks, M, blockIdx.x, E, k, idx, w, scores, &se, &sw);
+}
+
+// One token: the RMSNorm of the layer's post-attention row, the router logits,
+// the top-k and the routing table in one launch (at one token the three
+// kernels in a row would each wait on the one before, with the memory idle).
+// Grid (ceil(E / 8), ksplit), as router_kernel. Every CTA normalises the row
+// itself in the RMSNorm kernel's order (so the normalised row has its bits),
+// keeps its chunk of it in shared memory (CTAs of column 0 also write their
+// chunk out for the experts) and stores its logit pieces. The last CTA to
+// finish (an atomic counter that it resets) runs the top-k and writes the
+// routing table of the single token: one problem per selected expert, in
+// selection order, problem j on slot j, so every problem reads the same
+// normalised row. Without gamma the input row is used as it is.
+template <int J>
+__global__ void __launch_bounds__(256) router_select_kernel(const uint16_t* xin, const uint16_t* __restrict__ gamma,
+                                                            float eps, const float* __restrict__ Wr, int H, int E,
+                                                            int k, uint16_t* xn, float* parts, int* counter,
+                                                            int32_t* idx, float* w, float* scores, int* table) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int e = blockIdx.x * kRouterRows + warp;
+  const int ks = blockIdx.y;
+  const int k0 = ks * kRouterChunk;
+  const int kn = min(kRouterChunk, H - k0);
+  const int kv = kn >> 3;
+  __shared__ __align__(16) uint16_t xs[kRouterChunk];
+  __shared__ float red[8];
+  __shared__ int s_last;
+  pdl_trigger();
+  float4 wv[kRouterChunk / 128];
+#pragma unroll
+  for (int i = 0; i < kRouterChunk / 128; ++i) {
+    const int kk = 4 * (lane + 32 * i);
+    wv[i] = (e < E && kk < kn) ? __ldg(reinterpret_cast<const float4*>(Wr + (size_t)e * H + k0 + kk))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  uint4 gv = make_uint4(0, 0, 0, 0);
+  if (gamma != nullptr && tid < kv) gv = *reinterpret_cast<const uint4*>(gamma + k0 + (size_t)tid * 8);
+  pdl_wait();
+  if (gamma != nullptr) {
+    // sum of squares over the whole row: up to four vectors per thread loaded
+    // together (rows up to 8192), then in ascending order
+    const int H8 = H >> 3;
+    float ss = 0.f;
+    uint4 hv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int v = tid + 256 * j;
+      hv[j] = v < H8 ? ld_act16(xin + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (tid + 256 * j < H8) ss = sumsq8(hv[j], ss);
+    for (int v = tid + 1024; v < H8; v += 256) ss = sumsq8(ld_act16(xin + (size_t)v * 8), ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int q = 0; q < (int)(blockDim.x >> 5); ++q) tot += red[q];
+    const float r = rsqrtf(tot / (float)H + eps);
+    if (tid < kv) {
+      const uint4 y = norm8(ld_act16(xin + k0 + (size_t)tid * 8), gv, r);
+      *reinterpret_cast<uint4*>(&xs[tid * 8]) = y;
+      if (blockIdx.x == 0 && xn != nullptr) *reinterpret_cast<uint4*>(xn + k0 + (size_t)tid * 8) = y;
+    }
+  } else if (tid < kv) {
+    *reinterpret_cast<uint4*>(&xs[tid * 8]) = ld_act16(xin + k0 + (size_t)tid * 8);
+  }
+  __syncthreads();
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRouterChunk / 128; ++i) {
+    const int kk = 4 * (lane + 32 * i);
+    if (kk < kn) {
+      const uint2 xv = *reinterpret_cast<const uint2*>(&xs[kk]);
+      acc = fmaf(wv[i].x, bf_lo(xv.x), acc);
+      acc = fmaf(wv[i].y, bf_hi(xv.x), acc);
+      acc = fmaf(wv[i].z, bf_lo(xv.y), acc);
+      acc = fmaf(wv[i].w, bf_hi(xv.y), acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0 && e < E) parts[(size_t)ks * E + e] = acc;
+
+  // hand-off to the last CTA
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(counter, 1) == (int)(gridDim.x * gridDim.y) - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  int se = 0;
+  float sw = 0.f;
+  block_topk<J, true>(parts, gridDim.y, 1, 0, E, k, idx, w, scores, &se, &sw);
+  if (table != nullptr && warp == 0) {
+    const TableLayout L(E, k);
+    if (lane < k) {
+      table[L.expert() + lane] = se;
+      table[L.offset() + lane] = lane;
+      table[L.count() + lane] = 1;
+      table[L.slot_token() + lane] = 0;
+      table[L.entry_slot() + lane] = lane;
+    }
+    if (lane == 0) table[L.U()] = k;
+  }
+  if (tid == 0) *counter = 0;  // leave the workspace reusable
+}
+
+// One token: its k entries are k problems, entry j on slot j with expert
+// idx[j] (a repeated expert is then simply two problems), U = k. This is the
+// table router_select_kernel writes.
+__global__ void one_token_table_kernel(const int32_t* idx, int E, int k, int* table) {
+  pdl_trigger();
+  pdl_wait();
+  const TableLayout L(E, k);
+  const int j = threadIdx.x;
+  if (j < k) {
+    table[L.expert() + j] = ld_act_s32(idx + j);
+    table[L.offset() + j] = j;
+    table[L.count() + j] = 1;
+    table[L.slot_token() + j] = 0;
+    table[L.entry_slot() + j] = j;
+  }
+  if (j == 0) table[L.U()] = k;
 }
 
 // Routing table from idx[M][k]: per active expert (ascending id) its first
@@ -333,6 +480,25 @@ cudaError_t launch_topk(dec_handle* h, const float* parts, int ks, int M, int E,
   if (Ew <= 32) return launch_k(h, topk_kernel<1>, g, b, 0, s, parts, ks, M, E, k, idx, w, scores);
   if (Ew <= 64) return launch_k(h, topk_kernel<2>, g, b, 0, s, parts, ks, M, E, k, idx, w, scores);
   return launch_k(h, topk_kernel<4>, g, b, 0, s, parts, ks, M, E, k, idx, w, scores);
+}
+
+cudaError_t launch_router_select(dec_handle* h, const uint16_t* x, const uint16_t* gamma, float eps, const float* Wr,
+                                 int H, int E, int k, uint16_t* xn, float* parts, int* counter, int32_t* idx,
+                                 float* w, float* scores, int* table, cudaStream_t s) {
+  const int Ew = (E + 7) / 8;
+  const dim3 g((E + kRouterRows - 1) / kRouterRows, router_ksplit(H)), b(256);
+  if (Ew <= 32)
+    return launch_k(h, router_select_kernel<1>, g, b, 0, s, x, gamma, eps, Wr, H, E, k, xn, parts, counter, idx, w,
+                    scores, table);
+  if (Ew <= 64)
+    return launch_k(h, router_select_kernel<2>, g, b, 0, s, x, gamma, eps, Wr, H, E, k, xn, parts, counter, idx, w,
+                    scores, table);
+  return launch_k(h, router_select_kernel<4>, g, b, 0, s, x, gamma, eps, Wr, H, E, k, xn, parts, counter, idx, w,
+                  scores, table);
+}
+
+cudaError_t launch_one_token_table(dec_handle* h, const int32_t* idx, int E, int k, int* table, cudaStream_t s) {
+  return launch_k(h, one_token_table_kernel, dim3(1), dim3(32), 0, s, idx, E, k, table);
 }
 
 cudaError_t launch_route_table(dec_handle* h, const int32_t* idx, int M, int k, int E, const uint16_t* x, int H,

@@ -82,6 +82,33 @@ def test_experts_small(h, M, E, H, I, k, shared, resid, skew, family):
 from conftest import E_FULL, H_FULL, I_FULL, K_FULL
 
 
+@pytest.mark.parametrize("family", ["auto", "split_k"])
+@pytest.mark.parametrize("k,ids", [(4, [3, 3, 7, 3]), (8, [5, 1, 5, 2, 5, 9, 1, 0])])
+def test_experts_one_token_repeated_ids(h, family, k, ids):
+    """A token may list an expert more than once (the top-k never does, a
+    caller of the expert layer may): the result is still the sum over its
+    entries. At one token each entry is its own problem."""
+    import moe_layers_gb300 as ML
+    import torch
+    E, H, I = 12, 256, 128
+    h.set_force_variant(ML.VARIANT_SPLIT_K if family == "split_k" else ML.VARIANT_AUTO)
+    g, u, d = _small_bank(E, H, I, 4500 + k)
+    x = synth.bf16(H, SEED, 4510 + k, 0, 1.0).reshape(1, H)
+    idx = np.array([ids], dtype=np.int32)
+    w = np.random.default_rng(k).random((1, k)).astype(np.float32) + 0.1
+    w /= w.sum()
+    sh = (synth.bf16(I * H, SEED, 4520, 0, 0.05).reshape(I, H), synth.bf16(I * H, SEED, 4521, 0, 0.05).reshape(I, H),
+          synth.bf16(H * I, SEED, 4522, 0, 0.05).reshape(H, I))
+    r = synth.bf16(H, SEED, 4530, 0, 1.0).reshape(1, H)
+    out = ML.moe_experts(h, dev_bf16(x, (1, H)), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
+                         dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
+                         shared=tuple(dev_bf16(a, a.shape) for a in sh), residual=dev_bf16(r, (1, H)))
+    h.set_force_variant(ML.VARIANT_AUTO)
+    ref = oracle.moe(x, idx, w, lambda e: (g[e], u[e], d[e]), sh, r)
+    assert_bf16_close(host_bits(out), ref, f"moe repeated ids k={k} {family}")
+    assert h.check_device_error() == ML.DEC_OK
+
+
 @pytest.mark.parametrize("M,family", [(1, "auto"), (1, "split_k"), (8, "auto"), (64, "auto")])
 def test_experts_full_size(h, full_bank, M, family):
     import torch

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synth
-from _util import SEED, HostBank, assert_bf16_close, dev_bf16, dev_f32, gap_rows, host_bits
+from _util import SCORE_TOL, SEED, WEIGHT_TOL, HostBank, assert_bf16_close, dev_bf16, dev_f32, gap_rows, host_bits
 from conftest import E_FULL, H_FULL, I_FULL, K_FULL, K_OUT_FULL, N_IN_FULL
 
 pytestmark = pytest.mark.gpu
@@ -89,10 +89,51 @@ def test_layer_small(h, M, shared):
                      None if sh is None else tuple(dev_bf16(a, a.shape) for a in sh))
     hid, tr = _run(h, L, dev_w, hbits)
     ref = L.oracle(hbits, lambda e: (g[e], u[e], d[e]), sh)
-    _check_layer(tr, hid, ref, slice(None), f"layer M={M}")
+    _check_layer(tr, hid, ref, slice(None), f"layer M={M}", L)
 
 
-def _check_layer(tr, hid, ref, rows, what):
+@pytest.mark.parametrize("H,E,k,shared", [(1152, 37, 5, True), (1152, 37, 5, False), (256, 9, 8, True)])
+def test_layer_one_token_shapes(h, H, E, k, shared):
+    """One token: the fused RMSNorm / router / top-k / routing-table launch on
+    a router row split into a full and a ragged chunk (H = 1152), with a
+    number of experts that leaves a partial row group, and k = 8 (the fused
+    down projection + combine) over only 9 experts."""
+    N_in, K_out, I = 264, 256, 128
+    L = Layer(H, N_in, K_out, E, I, k, base=6500 + E)
+    n = E * I * H
+    g = synth.bf16(n, SEED, 6510, 0, 0.05).reshape(E, I, H)
+    u = synth.bf16(n, SEED, 6511, 0, 0.05).reshape(E, I, H)
+    d = synth.bf16(n, SEED, 6512, 0, 0.05).reshape(E, H, I)
+    sh = None
+    if shared:
+        sh = (synth.bf16(I * H, SEED, 6513, 0, 0.05).reshape(I, H), synth.bf16(I * H, SEED, 6514, 0, 0.05).reshape(I, H),
+              synth.bf16(H * I, SEED, 6515, 0, 0.05).reshape(H, I))
+    dev_w = L.device(dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
+                     None if sh is None else tuple(dev_bf16(a, a.shape) for a in sh))
+    for rep in range(3):  # the hand-off counter must be left at zero by every call
+        hbits, _ = gap_rows(L.scores, 1, H, k, base=6600 + 10 * E + rep)
+        hid, tr = _run(h, L, dev_w, hbits)
+        ref = L.oracle(hbits, lambda e: (g[e], u[e], d[e]), sh)
+        _check_layer(tr, hid, ref, slice(None), f"layer one token H={H} E={E} rep={rep}", L)
+
+
+def _check_router_stage(L, tr, rows, what):
+    """Router scores and weights on the layer's own input: the oracle's RMSNorm
+    and router applied to the h1 the GPU produced. h1 is a bf16 activation
+    that may differ from the oracle's h1 in last bits (checked above), and a
+    last-bit change of the router input moves a logit by |W_r| * ulp, far
+    beyond the router's own tolerance over 7168 terms; on the same input the
+    router's fp32 error bound applies."""
+    h1g = host_bits(tr["h1"])[rows]
+    b = oracle.round_bf16(oracle.rmsnorm(h1g, L.g2))
+    _, s_ref = oracle.router_scores(b, L.Wr)
+    i_ref, w_ref = oracle.topk(s_ref, L.k)
+    assert np.array_equal(tr["idx"].cpu().numpy()[rows], i_ref), what + ": top-k on the layer's h1"
+    assert np.max(np.abs(tr["scores"].cpu().numpy()[rows] - s_ref)) <= SCORE_TOL, what + ": scores"
+    assert np.max(np.abs(tr["w"].cpu().numpy()[rows] - w_ref)) <= WEIGHT_TOL, what + ": weights"
+
+
+def _check_layer(tr, hid, ref, rows, what, L=None):
     assert np.array_equal(tr["idx"].cpu().numpy()[rows], ref["idx"]), what + ": top-k indices"
     h1g = oracle.bf16_to_f64(host_bits(tr["h1"])[rows])
     dh1 = np.abs(h1g - ref["h1"])
@@ -101,6 +142,8 @@ def _check_layer(tr, hid, ref, rows, what):
     # the residual add, and is allowed for there.
     assert_bf16_close(host_bits(tr["h1"])[rows], ref["h1"], what + " h1")
     assert_bf16_close(host_bits(hid)[rows], ref["out"], what + " out", passthrough=dh1)
+    if L is not None:
+        _check_router_stage(L, tr, rows, what)
 
 
 @pytest.fixture(scope="module")
@@ -121,7 +164,7 @@ def test_layer_full_size(h, full_bank, full_layer, M):
                                       (synth.W_D_S, (H_FULL, I_FULL))))
     tokens = sorted(set([0, M // 2, M - 1]))
     ref = L.oracle(hbits, bank, shared, tokens=tokens)
-    _check_layer(tr, hid, ref, tokens, f"layer full M={M}")
+    _check_layer(tr, hid, ref, tokens, f"layer full M={M}", L)
     # indices of all tokens: bit-exact against the oracle's router on every row
     s_all = L.scores(hbits)
     i_all, _ = oracle.topk(s_all, K_FULL)

@@ -34,7 +34,8 @@ def _check(h, xbits, Wr, k):
 
 
 @pytest.mark.parametrize("M,H,E,k", [(1, 256, 64, 4), (5, 512, 128, 8), (17, 2056, 384, 8), (64, 1024, 40, 16),
-                                     (3, 64, 16, 1)])
+                                     (3, 64, 16, 1), (1, 1032, 37, 5), (1, 2056, 1024, 4), (1, 1024, 40, 16), (1, 64, 16, 1),
+                                     (1, 3072, 9, 9)])
 def test_router_small(h, M, H, E, k):
     Wr = synth.f32(E * H, SEED, 3000 + E, 0, 0.8 / np.sqrt(H)).reshape(E, H)  # logits ~ N(0, 0.8^2)
     score = lambda rows: oracle.router_scores(rows, Wr)[1]
@@ -62,4 +63,26 @@ def test_router_ties_go_to_lower_ids(h):
     idx, w, sc = ML.moe_route_topk(h, dev_bf16(x, (M, H)), dev_f32(Wr), k)
     assert np.all(sc.cpu().numpy() == 0.5)
     assert np.array_equal(idx.cpu().numpy(), np.tile(np.arange(k, dtype=np.int32), (M, 1)))
+    assert np.all(w.cpu().numpy() == np.float32(1.0 / k))
+
+
+def test_router_one_token_repeated(h):
+    """One token runs as one launch whose last CTA takes the top-k; its
+    hand-off counter must be back at zero after every call."""
+    H, E, k = 1032, 100, 6
+    Wr = synth.f32(E * H, SEED, 3300, 0, 0.8 / np.sqrt(H)).reshape(E, H)
+    score = lambda rows: oracle.router_scores(rows, Wr)[1]
+    for rep in range(4):
+        xbits, _ = gap_rows(score, 1, H, k, base=3400 + rep, gap=GAP)
+        _check(h, xbits, Wr, k)
+
+
+def test_router_ties_one_token(h):
+    import moe_layers_gb300 as ML
+    H, E, k = 128, 40, 8
+    x = synth.bf16(H, SEED, 3201, 0, 1.0).reshape(1, H)
+    Wr = np.zeros((E, H), dtype=np.float32)
+    idx, w, sc = ML.moe_route_topk(h, dev_bf16(x, (1, H)), dev_f32(Wr), k)
+    assert np.all(sc.cpu().numpy() == 0.5)
+    assert np.array_equal(idx.cpu().numpy(), np.arange(k, dtype=np.int32)[None, :])
     assert np.all(w.cpu().numpy() == np.float32(1.0 / k))
