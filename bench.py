@@ -205,6 +205,8 @@ def run_ours(args, rank, local, world):
     h = ML.Handle(local)
     h.set_shared_sms(args.shared_sms)
     h.set_prefetch_shared(args.prefetch_shared)
+    if args.l2_ahead is not None:
+        h.set_l2_ahead(args.l2_ahead)
     layers = build_weights(dev)
     cws = [L.c_struct() for L in layers]
     stream = torch.cuda.current_stream()
@@ -445,6 +447,8 @@ def main(argv=None):
                          "and report the replay time as the value)")
     ap.add_argument("--shared-sms", type=int, default=0,
                     help="SMs for the shared expert: 0 automatic share (default), -1 every SM overlapped, n fixed")
+    ap.add_argument("--l2-ahead", type=int, default=None,
+                    help="bytes per CTA the small-matrix kernels keep requested into L2 ahead (default: library's)")
     ap.add_argument("--prefetch-shared", action="store_true",
                     help="at batch 1, pull the shared expert into L2 during the router phase (off: measured slower)")
     ap.add_argument("--experts", type=int, default=E,

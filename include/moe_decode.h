@@ -110,6 +110,16 @@ dec_status dec_set_shared_sms(dec_handle* h, int sms);
  * of evict-last lines crowd the weight stream out of the 129 MB L2. */
 dec_status dec_set_prefetch_shared(dec_handle* h, int enable);
 
+/* The small-matrix kernels (batch 1) keep about `bytes` of each CTA's
+ * upcoming weight rows requested into L2 (bulk L2 prefetches, issued from
+ * before the dependency wait on), beyond the rows their registers hold, so
+ * that far more of the weight stream is in flight than registers allow.
+ * 0 disables it; bytes in [0, 16 MiB]; default 49152 (measured on GB300:
+ * 32-64 KB per CTA take the batch-1 layer step from 193 to 172 us; above
+ * 128 KB the requested lines start to crowd L2). No counterpart on the pages:
+ * a GB300 tuning of the small-matrix kernels [K3 P1§1]. */
+dec_status dec_set_l2_ahead(dec_handle* h, int bytes);
+
 /* Force a projection kernel family (DEC_VARIANT_AUTO restores the choice by
  * batch) so that tests can run both families at the same batch. */
 dec_status dec_set_force_variant(dec_handle* h, int variant);

@@ -68,6 +68,7 @@ def _load():
         "dec_set_force_variant": [P, I],
         "dec_set_shared_sms": [P, I],
         "dec_set_prefetch_shared": [P, I],
+        "dec_set_l2_ahead": [P, I],
         "dec_check_device_error": [P],
         "dec_linear_workspace_size": [P, I, I, I, ctypes.POINTER(Z)],
         "dec_linear": [P, P, I, P, P, I, I, I, P, Z, P],
@@ -192,6 +193,9 @@ class Handle:
 
     def set_prefetch_shared(self, enable: bool) -> None:
         _check(_load().dec_set_prefetch_shared(self._h, 1 if enable else 0), "dec_set_prefetch_shared")
+
+    def set_l2_ahead(self, nbytes: int) -> None:
+        _check(_load().dec_set_l2_ahead(self._h, int(nbytes)), "dec_set_l2_ahead")
 
     def set_pdl(self, enable: bool) -> None:
         _check(_load().dec_set_pdl(self._h, 1 if enable else 0), "dec_set_pdl")

@@ -513,6 +513,12 @@ dec_status dec_set_prefetch_shared(dec_handle* h, int enable) {
   return DEC_OK;
 }
 
+dec_status dec_set_l2_ahead(dec_handle* h, int bytes) {
+  if (h == nullptr || bytes < 0 || bytes > (16 << 20)) return DEC_ERR_INVALID_ARG;
+  h->l2_ahead = bytes;
+  return DEC_OK;
+}
+
 dec_status dec_set_shared_sms(dec_handle* h, int sms) {
   if (h == nullptr || sms < -1 || sms >= h->sms) return DEC_ERR_INVALID_ARG;
   h->shared_ctas = sms;

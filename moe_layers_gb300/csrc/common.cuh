@@ -111,6 +111,13 @@ __device__ __forceinline__ int ld_cg_s32(const void* p) {
   return v;
 }
 
+// Device-scope acquire-release fetch-add (CTA hand-offs through a counter).
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- RMSNorm pieces
 // Every kernel that normalises a row uses these two, in the same order: the
 // sum of squares runs over each thread's 8-element vectors in ascending order,
@@ -240,6 +247,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
 // Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Request [p, p + bytes) into L2 in bulk pieces of at most 32 KB (p and bytes
+// multiples of 16). The small-matrix kernels keep their next rows requested
+// this way ahead of the register loads: it holds no registers, so far more
+// bytes stay in flight than the register double buffer allows.
+__device__ __forceinline__ void request_l2(const void* p, size_t bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (size_t off = 0; off < bytes; off += 32768) {
+    const size_t n = bytes - off < 32768 ? bytes - off : 32768;
+    bulk_prefetch_l2(c + off, (uint32_t)n);
+  }
 }
 
 // ---------------------------------------------------------------- tcgen05

@@ -20,7 +20,10 @@
 //
 // The first rows' weight loads are issued before griddepcontrol.wait, so they
 // overlap the previous kernel's tail; activations and the residual are read
-// only after it.
+// only after it. Beyond the register double buffer, thread 0 keeps about
+// `ahead` bytes of the CTA's next rows requested into L2 (bulk prefetches,
+// starting before the wait), so that the register loads mostly hit L2 and the
+// memory sees many more requests in flight than registers can hold.
 #include <algorithm>
 
 #include "common.cuh"
@@ -33,7 +36,8 @@ constexpr int kGemvThreads = 256;
 template <int M, int VPT>
 __global__ void __launch_bounds__(kGemvThreads, 2)
     gemv_kernel(const uint16_t* x, long long ldx, const uint16_t* __restrict__ W, const uint16_t* res, long long ldr,
-                uint16_t* y, long long ldy, int N, int K, const uint16_t* __restrict__ gamma, float eps) {
+                uint16_t* y, long long ldy, int N, int K, const uint16_t* __restrict__ gamma, float eps,
+                int ahead) {
   // Rows per step: 8 (M = 1) or 4 (M > 1) weight vectors per thread in flight, kept within 128 registers.
   constexpr int RB = ((M == 1 ? 8 : 4) / VPT) > 0 ? ((M == 1 ? 8 : 4) / VPT) : 1;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -61,6 +65,18 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
     }
   };
   if (r0 < r1) load_rows(wa, r0);
+  // L2 requests: rows [pf, ...) of this CTA's range are not yet requested.
+  const size_t rowb = (size_t)K * sizeof(uint16_t);
+  const int ahead_rows = ahead > 0 ? max(RB, (int)((size_t)ahead / rowb)) : 0;
+  int pf = r0 + RB;
+  auto request = [&](int upto) {
+    upto = min(upto, r1);
+    if (ahead_rows > 0 && upto > pf) {
+      if (t == 0) request_l2(W + (size_t)pf * K, (size_t)(upto - pf) * rowb);
+      pf = upto;
+    }
+  };
+  request(r0 + RB + ahead_rows);
   // Optional RMSNorm of the (single) input row, fused: gains are static weights.
   uint4 gv[VPT];
   if (M == 1 && gamma != nullptr) {
@@ -107,6 +123,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
     uint4 wb[RB][VPT];
     const bool more = rb + RB < r1;
     if (more) load_rows(wb, rb + RB);
+    request(rb + 2 * RB + ahead_rows);
     float acc[RB][M];
 #pragma unroll
     for (int r = 0; r < RB; ++r)
@@ -159,10 +176,14 @@ static cudaError_t gemv_m(dec_handle* h, const uint16_t* x, long long ldx, const
   const int K8 = K / 8;
   const int grid = (int)std::min<long long>((long long)N, 2LL * h->sms);
   const dim3 g(grid > 0 ? grid : 1), b(kGemvThreads);
-  if (K8 <= kGemvThreads) return launch_k(h, gemv_kernel<M, 1>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps);
-  if (K8 <= 2 * kGemvThreads) return launch_k(h, gemv_kernel<M, 2>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps);
-  if (K8 <= 4 * kGemvThreads) return launch_k(h, gemv_kernel<M, 4>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps);
-  return launch_k(h, gemv_kernel<M, 8>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps);
+  const int a = h->l2_ahead;
+  if (K8 <= kGemvThreads)
+    return launch_k(h, gemv_kernel<M, 1>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps, a);
+  if (K8 <= 2 * kGemvThreads)
+    return launch_k(h, gemv_kernel<M, 2>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps, a);
+  if (K8 <= 4 * kGemvThreads)
+    return launch_k(h, gemv_kernel<M, 4>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps, a);
+  return launch_k(h, gemv_kernel<M, 8>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps, a);
 }
 
 cudaError_t launch_gemv(dec_handle* h, const uint16_t* x, long long ldx, const uint16_t* W, const uint16_t* res,

@@ -47,6 +47,7 @@ struct GemvMoeParams {
   void* out;           // SwiGLU: bf16 [slots][ldo]; down: fp32 [slots][ldo]
   long long ldo;
   int nprob_known;     // routed problems if known at launch (one token: k), else 0
+  int ahead;           // weight bytes per CTA requested into L2 ahead of the register loads (0: none)
   int late_trigger;    // trigger dependents after the dependency wait (they may then read the routing early)
 };
 
@@ -97,6 +98,8 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_kernel(const GemvMoePa
   const long long G = gridDim.x, c = blockIdx.x;
   long long q0 = 0, q1 = 0;
   int pre_nu = 0;
+  const int rowb = P.K * (int)sizeof(uint16_t);
+  const int ahead_units = P.ahead > 0 ? max(1, P.ahead / (NR * rowb)) : 0;
   // With the problem count known at launch the range is too; a range that
   // starts in a dense problem starts its weight stream now.
   const bool range_known = P.table == nullptr || P.nprob_known > 0;
@@ -128,6 +131,14 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_kernel(const GemvMoePa
   const uint16_t* A1 = mat1(e);
   int nu = (int)min((long long)min(RB, P.R - r), left);
   if (pre_nu == 0) load_units(wa, A0, A1, r, nu);
+  // the first units past this one, up to `ahead_units`, in the same problem
+  if (t == 0 && ahead_units > 0) {
+    const long long n = min(min((long long)ahead_units, (long long)(P.R - r - nu)), left - nu);
+    if (n > 0) {
+      request_l2(A0 + (size_t)(r + nu) * P.K, (size_t)n * rowb);
+      if (NR == 2) request_l2(A1 + (size_t)(r + nu) * P.K, (size_t)n * rowb);
+    }
+  }
 
   uint4 xr[VPT];
   long long slot = slot_of(p);
@@ -159,6 +170,16 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_kernel(const GemvMoePa
     const int nun = (int)min((long long)min(RB, P.R - rn), leftn);
     uint4 wb[RB][NR][VPT];
     if (nun > 0) load_units(wb, N0, N1, rn, nun);  // issued before this step's FMAs
+    // L2 request for the units `ahead_units` past the next step, when they lie
+    // in the same problem and in this CTA's range (no lookup of later
+    // problems: the few units after a problem boundary go without).
+    if (t == 0 && ahead_units > 0 && nun > 0) {
+      const int ra = rn + ahead_units;
+      if (ra + nun <= P.R && (long long)ahead_units + nun <= leftn) {
+        request_l2(N0 + (size_t)ra * P.K, (size_t)nun * rowb);
+        if (NR == 2) request_l2(N1 + (size_t)ra * P.K, (size_t)nun * rowb);
+      }
+    }
 
     float acc[RB][NR];
 #pragma unroll
@@ -216,132 +237,137 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_kernel(const GemvMoePa
 
 // One token, down projection fused with the weighted combine and residual:
 //   out[n] = bf16( sum_j w_j (Wd_{e_j}[n] . h_j)  [+ Wd_s[n] . h_s]  [+ res[n]] )
-// with the fp32 sums in that order (the combine kernel's order). The unit is
-// one output row n; it reads row n of every selected expert's W_d (and of the
-// shared expert's), so no per-expert output is written and no combine kernel
-// runs. The k (+1) activation rows sit in shared memory and thread t streams
-// the weight vectors t, t+256, ... of each row. NP = k (+1 with a shared
-// expert) rows per unit.
+// The unit is one output row n; it reads row n of every selected expert's W_d
+// (and of the shared expert's), so no per-expert output is written and no
+// combine kernel runs. Thread t owns the 16-byte column vectors t, t+256, ...
+// of each row and holds the k (+1) activation rows' matching vectors in
+// registers. The combine is linear, so each thread applies the weights to its
+// own partial dot products first, a = sum_j w_j d_j (+ d_s), in entry order,
+// and the unit needs one warp reduction instead of one per expert; the eight
+// warp sums are added in order, then the residual. Weight vectors stream
+// through a ring of NP x VPT registers: consuming row n's vector of entry j
+// issues row n+1's, so NP x VPT loads stay in flight without a second buffer.
+// NP = k (+1 with a shared expert) rows per unit.
 template <int NP, int VPT, bool SHARED>
 __global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_kernel(
     const uint16_t* __restrict__ Wd, long long rows_bank, const uint16_t* __restrict__ Wd_s, int H, int K,
     const uint16_t* hbuf, const uint16_t* hs, const int* table, int E, int k, const float* w, const uint16_t* res,
-    uint16_t* out, int routing_ready) {
+    uint16_t* out, int routing_ready, int ahead) {
   constexpr int NR = SHARED ? NP - 1 : NP;  // routed rows per unit
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int K8 = K >> 3;
-  __shared__ float red[2][kGmThreads / 32][NP];
+  __shared__ __align__(16) float red[2][kGmThreads / 32];
   const uint64_t pol = policy_evict_first();
   pdl_trigger();
   const long long G = gridDim.x, c = blockIdx.x;
   const int n0 = (int)(c * H / G), n1 = (int)((c + 1) * H / G);
   if (n0 >= n1) return;  // (before any barrier)
   const TableLayout L(E, k);
-  // Per selected row: the W_d row base, the combine weight, and the activation
-  // row (in shared memory; registers carry the weight stream).
+  // Per selected row: the W_d row base, the activation row and the combine weight.
   __shared__ const uint16_t* s_rowbase[NP];
+  __shared__ const uint16_t* s_xrow[NP];
   __shared__ float s_w[NP];
-  extern __shared__ uint4 s_x[];  // [NP][K8]
   auto routing = [&](bool cg) {
     if (t < NP) {
       if (SHARED && t == NP - 1) {
         s_rowbase[t] = Wd_s;
+        s_xrow[t] = hs;
         s_w[t] = 1.f;
       } else {
         // token 0, entry t; one token: problem index == slot
         const int slot = cg ? ld_cg_s32(table + L.entry_slot() + t) : ld_act_s32(table + L.entry_slot() + t);
         const long long e = cg ? ld_cg_s32(table + L.expert() + slot) : ld_act_s32(table + L.expert() + slot);
         s_rowbase[t] = Wd + e * rows_bank * K;
+        s_xrow[t] = hbuf + (size_t)slot * K;
         s_w[t] = cg ? ld_cg_f32(w + t) : ld_act_f32(w + t);
       }
     }
     __syncthreads();
   };
-  uint4 wa[NP][VPT];
-  auto load = [&](uint4(&wr)[NP][VPT], int n) {
+  uint4 ring[NP][VPT];
+  auto load1 = [&](int j, int i, int n) {
+    const int v = t + kGmThreads * i;
+    return (v < K8) ? ld_stream(s_rowbase[j] + (size_t)n * K + (size_t)v * 8, pol) : make_uint4(0, 0, 0, 0);
+  };
+  auto load_row = [&](int n) {
 #pragma unroll
     for (int j = 0; j < NP; ++j)
 #pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int v = t + kGmThreads * i;
-        wr[j][i] = (v < K8) ? ld_stream(s_rowbase[j] + (size_t)n * K + (size_t)v * 8, pol) : make_uint4(0, 0, 0, 0);
-      }
+      for (int i = 0; i < VPT; ++i) ring[j][i] = load1(j, i, n);
+  };
+  // L2 requests: rows [pf, ...) of every selected matrix are not yet
+  // requested; thread j < NP requests matrix j's (contiguous) rows.
+  const int rowb = K * (int)sizeof(uint16_t);
+  const int ahead_rows = ahead > 0 ? max(1, ahead / (NP * rowb)) : 0;
+  int pf = n0 + 1;
+  auto request = [&](int upto) {
+    upto = min(upto, n1);
+    if (ahead_rows > 0 && upto > pf) {
+      if (t < NP) request_l2(s_rowbase[t] + (size_t)pf * K, (size_t)(upto - pf) * rowb);
+      pf = upto;
+    }
   };
   // routing_ready: the launch before this one triggered its dependents only
   // after its own dependency wait, so the routing (written two launches back)
   // is complete now; read it at L2 and start the weight stream before the wait.
   if (routing_ready) {
     routing(true);
-    load(wa, n0);
+    load_row(n0);
+    request(n0 + 1 + ahead_rows);
   }
   pdl_wait();
   if (!routing_ready) {
     routing(false);
-    load(wa, n0);
+    load_row(n0);
+    request(n0 + 1 + ahead_rows);
   }
-  for (int q = t; q < NP * K8; q += kGmThreads) {
-    const int j = q / K8, v = q - j * K8;
-    const uint16_t* src;
-    if (SHARED && j == NP - 1) {
-      src = hs;
-    } else {
-      const int slot = ld_act_s32(table + L.entry_slot() + j);
-      src = hbuf + (size_t)slot * K;
+  uint4 xr[NP][VPT];
+#pragma unroll
+  for (int j = 0; j < NP; ++j)
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = t + kGmThreads * i;
+      xr[j][i] = (v < K8) ? ld_act16(s_xrow[j] + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
     }
-    s_x[q] = ld_act16(src + (size_t)v * 8);
-  }
   // residual values of this CTA's rows, read once (kept off the per-row path)
   __shared__ float s_res[64];
   for (int q = t; q < n1 - n0 && q < 64; q += kGmThreads) s_res[q] = res ? bf2f(ld_act_u16(res + n0 + q)) : 0.f;
   __syncthreads();
   int buf = 0;
   for (int n = n0; n < n1; ++n) {
-    uint4 wb[NP][VPT];
-    if (n + 1 < n1) load(wb, n + 1);
-    float acc[NP];
+    const bool more = n + 1 < n1;
+    request(n + 2 + ahead_rows);
+    float a = 0.f;
 #pragma unroll
     for (int j = 0; j < NP; ++j) {
-      float sum = 0.f;
+      float d = 0.f;
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
-        const int v = t + kGmThreads * i;
-        if (v < K8) sum = dot8(wa[j][i], s_x[j * K8 + v], sum);
+        const uint4 wv = ring[j][i];
+        if (more) ring[j][i] = load1(j, i, n + 1);
+        d = dot8(wv, xr[j][i], d);
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      acc[j] = sum;
+      if (SHARED && j == NP - 1)
+        a += d;
+      else
+        a = fmaf(s_w[j], d, a);  // (a broadcast shared-memory read: registers hold the weight ring)
     }
-    if (lane == 0) {
 #pragma unroll
-      for (int j = 0; j < NP; ++j) red[buf][warp][j] = acc[j];
-    }
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    if (lane == 0) red[buf][warp] = a;
     __syncthreads();
-    if (warp == 0) {
-      // lane j sums expert j's partials over the warps; lane 0 then combines
-      // in entry order (the combine kernel's order)
-      float y = 0.f;
-      if (lane < NP) {
-#pragma unroll
-        for (int q = 0; q < kGmThreads / 32; ++q) y += red[buf][q][lane];
-      }
-      float a = 0.f;
-#pragma unroll
-      for (int j = 0; j < NR; ++j) a = fmaf(s_w[j], __shfl_sync(0xffffffffu, y, j), a);
-      if (SHARED) a += __shfl_sync(0xffffffffu, y, NP - 1);
-      if (lane == 0) {
-        if (res != nullptr) a += (n - n0 < 64) ? s_res[n - n0] : bf2f(ld_act_u16(res + n));
-        out[n] = f2bf(a);
-      }
+    if (t == 0) {
+      const float4 p0 = *reinterpret_cast<const float4*>(&red[buf][0]);
+      const float4 p1 = *reinterpret_cast<const float4*>(&red[buf][4]);
+      float y = ((((((p0.x + p0.y) + p0.z) + p0.w) + p1.x) + p1.y) + p1.z) + p1.w;
+      if (res != nullptr) y += (n - n0 < 64) ? s_res[n - n0] : bf2f(ld_act_u16(res + n));
+      out[n] = f2bf(y);
     }
     buf ^= 1;
-#pragma unroll
-    for (int j = 0; j < NP; ++j)
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) wa[j][i] = wb[j][i];
   }
 }
 
-// Rows of up to 2048 elements (one vector per thread); the activations take k+1 rows of shared memory.
+// Rows of up to 2048 elements (one vector per thread per row, activations in registers).
 bool gemv_down_combine_supported(int k, int I) { return k == 8 && I >= 8 && I % 8 == 0 && I <= 8 * kGmThreads; }
 
 cudaError_t launch_gemv_down_combine(dec_handle* h, const uint16_t* Wd, long long rows_bank, const uint16_t* Wd_s,
@@ -350,12 +376,12 @@ cudaError_t launch_gemv_down_combine(dec_handle* h, const uint16_t* Wd, long lon
                                      cudaStream_t s, bool routing_ready) {
   if (!gemv_down_combine_supported(k, I)) return cudaErrorInvalidValue;
   const dim3 g(std::max(1, 2 * sms)), b(kGmThreads);
-  const size_t smem = (size_t)(k + (Wd_s ? 1 : 0)) * (I / 8) * 16;
+  const size_t smem = 0;
   if (Wd_s != nullptr)
     return launch_k(h, gemv_down_combine_kernel<9, 1, true>, g, b, smem, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs,
-                    table, E, k, w, res, out, (int)routing_ready);
+                    table, E, k, w, res, out, (int)routing_ready, h->l2_ahead);
   return launch_k(h, gemv_down_combine_kernel<8, 1, false>, g, b, smem, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs, table,
-                  E, k, w, res, out, (int)routing_ready);
+                  E, k, w, res, out, (int)routing_ready, h->l2_ahead);
 }
 
 bool gemv_moe_supported(int K) { return K >= 8 && K % 8 == 0 && K <= 8 * 4 * kGmThreads; }
@@ -393,6 +419,7 @@ cudaError_t launch_gemv_moe(dec_handle* h, bool swiglu, const uint16_t* A, const
   P.ldo = ldo;
   P.nprob_known = table ? nprob_known : 0;
   P.late_trigger = late_trigger ? 1 : 0;
+  P.ahead = h->l2_ahead;
   const int grid = std::max(1, 2 * sms);
   return swiglu ? launch_mode<true>(h, P, grid, s) : launch_mode<false>(h, P, grid, s);
 }

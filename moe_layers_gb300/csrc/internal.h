@@ -24,6 +24,7 @@ struct dec_handle {
   int last_variant = 0;
   int last_expert_variant = 0;      // kernel family of the most recent expert launches
   int shared_ctas = 0;              // CTAs for the shared expert's kernels (0 = default)
+  int l2_ahead = 49152;             // small-matrix kernels: weight bytes per CTA requested into L2 ahead
   int prefetch_shared = 0;          // batch 1: pull the shared expert into L2 during the router phase
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   // measurement

@@ -241,8 +241,12 @@ __global__ void __launch_bounds__(256) router_select_kernel(const uint16_t* xin,
     wv[i] = (e < E && kk < kn) ? __ldg(reinterpret_cast<const float4*>(Wr + (size_t)e * H + k0 + kk))
                                : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  // Chunk vector i (of kv) is vector 128 ks + i of the row: in the sum-of-squares
+  // pass below thread 128 (ks & 1) + i loads it, as its vector j = ks / 2.
+  const int ci = tid & 127;
+  const bool owner = (tid >> 7) == (ks & 1) && ci < kv;
   uint4 gv = make_uint4(0, 0, 0, 0);
-  if (gamma != nullptr && tid < kv) gv = *reinterpret_cast<const uint4*>(gamma + k0 + (size_t)tid * 8);
+  if (gamma != nullptr && owner) gv = *reinterpret_cast<const uint4*>(gamma + k0 + (size_t)ci * 8);
   pdl_wait();
   if (gamma != nullptr) {
     // sum of squares over the whole row: up to four vectors per thread loaded
@@ -266,10 +270,13 @@ __global__ void __launch_bounds__(256) router_select_kernel(const uint16_t* xin,
     float tot = 0.f;
     for (int q = 0; q < (int)(blockDim.x >> 5); ++q) tot += red[q];
     const float r = rsqrtf(tot / (float)H + eps);
-    if (tid < kv) {
-      const uint4 y = norm8(ld_act16(xin + k0 + (size_t)tid * 8), gv, r);
-      *reinterpret_cast<uint4*>(&xs[tid * 8]) = y;
-      if (blockIdx.x == 0 && xn != nullptr) *reinterpret_cast<uint4*>(xn + k0 + (size_t)tid * 8) = y;
+    if (owner) {
+      const int jj = ks >> 1;
+      const uint4 xv = jj == 0 ? hv[0] : jj == 1 ? hv[1] : jj == 2 ? hv[2] : jj == 3 ? hv[3]
+                                                                            : ld_act16(xin + k0 + (size_t)ci * 8);
+      const uint4 y = norm8(xv, gv, r);
+      *reinterpret_cast<uint4*>(&xs[ci * 8]) = y;
+      if (blockIdx.x == 0 && xn != nullptr) *reinterpret_cast<uint4*>(xn + k0 + (size_t)ci * 8) = y;
     }
   } else if (tid < kv) {
     *reinterpret_cast<uint4*>(&xs[tid * 8]) = ld_act16(xin + k0 + (size_t)tid * 8);
@@ -291,13 +298,13 @@ __global__ void __launch_bounds__(256) router_select_kernel(const uint16_t* xin,
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0 && e < E) parts[(size_t)ks * E + e] = acc;
 
-  // hand-off to the last CTA
-  __threadfence();
+  // Hand-off to the last CTA: the barrier orders this CTA's stores before
+  // thread 0's acquire-release add; in the last CTA the barrier after it
+  // orders every thread's reads after the acquire.
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(counter, 1) == (int)(gridDim.x * gridDim.y) - 1;
+  if (tid == 0) s_last = atom_add_acq_rel_gpu(counter, 1) == (int)(gridDim.x * gridDim.y) - 1;
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   int se = 0;
   float sw = 0.f;
   block_topk<J, true>(parts, gridDim.y, 1, 0, E, k, idx, w, scores, &se, &sw);
