@@ -213,9 +213,12 @@ dec_status moe_experts_workspace_size(const dec_handle* h, int M, int k, int E, 
  * w fp32 [M][k]; expert banks Wg, Wu bf16 [E][I][H] and Wd bf16 [E][H][I];
  * shared expert Wg_s, Wu_s bf16 [I][H], Wd_s bf16 [H][I] (all three NULL for
  * none); residual bf16 [M][H] or NULL; out bf16 [M][H] (may alias residual,
- * not x). Each selected expert's weights are read once for all its tokens.
- * The shared expert runs on the handle's side stream, overlapped with the
- * routing table and the routed experts, and joins `stream` before return.
+ * not x). Each selected expert's weights are read once for all its tokens
+ * (at M = 1 each entry is its own problem, so an expert listed twice is read
+ * twice). For M >= 2 the shared expert runs on the handle's side stream,
+ * overlapped with the routing table and the routed experts, and joins
+ * `stream` before return; at M = 1 it is one more problem of the routed
+ * launches.
  * The SwiGLU output h is rounded to bf16; everything else stays fp32 until
  * the single bf16 rounding of out.
  * 1 <= M <= 64, 1 <= k <= 16, H and I multiples of 128. */
@@ -268,11 +271,16 @@ dec_status decode_layer_workspace_size(const dec_handle* h, const dec_layer_weig
  *   h1 = h + y[:, :K_out] W_o^T           (out-projection + residual)   [K3 P1§2]
  *   b  = RMSNorm(h1; gamma2)
  *   idx, w = top-k(sigmoid(b W_r^T))                                    [K3 P1§3]
- *   h  = h1 + sum_j w_j E_idx_j(b) + S(b)   (shared expert on a side stream)
+ *   h  = h1 + sum_j w_j E_idx_j(b) + S(b)
  * The attention core, which the pages do not define, is read as the identity
- * on the first K_out columns of y. While the router and top-k run, the
- * `prefetch_next` region (if any) is pulled into L2 on a second side stream
- * [K3 P1§4]. trace may be NULL. */
+ * on the first K_out columns of y. At M = 1 the layer is five launches on
+ * `stream`: in-projection with the first RMSNorm, out-projection with the
+ * residual, one routing launch (second RMSNorm, router, top-k, routing
+ * table), gate/up of the shared and selected experts, and the down
+ * projection fused with the combine and the residual. For M >= 2 the shared
+ * expert runs on the handle's side stream [K3 P1§3]. While the router and
+ * top-k run, the `prefetch_next` region (if any) is pulled into L2 on a
+ * second side stream [K3 P1§4]. trace may be NULL. */
 dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hidden, int M,
                         const dec_layer_trace* trace, void* ws, size_t ws_bytes, cudaStream_t stream);
 
