@@ -72,7 +72,8 @@ def step_bytes(M: int, U: float) -> float:
 # size, so a capture on a 32-expert bank gives the full workload's traffic.
 NCU_TRAFFIC = {
     ("gate_up", 1): {"bytes": 528544000 + 3325184,
-                     "sources": ("moe_layers_gb300/csrc/gemv_moe.cu", "moe_layers_gb300/csrc/common.cuh"),
+                     "sources": ("moe_layers_gb300/csrc/gemv_moe.cu", "moe_layers_gb300/csrc/common.cuh",
+                                 "moe_layers_gb300/csrc/api.cu", "moe_layers_gb300/csrc/route_shared.cu"),
                      "sha256": "68546ab4f887d3426b847a2f03130e17dba04527f5164666d252927d857a73d3"},
 }
 
@@ -90,9 +91,13 @@ def captured_traffic(tag: str, M: int):
     return rec["bytes"] if h.hexdigest() == rec["sha256"] else None
 
 
-def kernel_bytes(tag: str, M: int, U: float) -> float:
-    """Algorithmic bytes of one launch of a kernel of the step."""
-    return {
+def kernel_bytes(tag: str, M: int, U: float, shared_in: str | None = None) -> float:
+    """Algorithmic bytes of one launch of a kernel of the step. shared_in names
+    where the one-token schedule runs the shared expert's gate/up ("router":
+    inside the routing launch; "gate_up": problem 0 of the gate/up launch); its
+    down projection then is part of the down launch. None: the shared expert
+    has launches of its own (batch >= 2)."""
+    b = {
         "in_proj": N_IN * H * 2 + M * H * 2 + M * N_IN * 2,
         "out_proj": H * K_OUT * 2 + M * K_OUT * 2 + 2 * M * H * 2,
         "router": E * H * 4 + M * H * 2,
@@ -100,7 +105,11 @@ def kernel_bytes(tag: str, M: int, U: float) -> float:
         "down": U * H * I * 2 + M * TOPK * (I * 2 + H * 4),
         "shared_gate_up": 2 * I * H * 2 + M * (H + I) * 2,
         "shared_down": H * I * 2 + M * (I * 2 + H * 4),
-    }.get(tag, 0.0)
+    }
+    if shared_in is not None:
+        b[shared_in] += 2 * I * H * 2 + M * I * 2
+        b["down"] += H * I * 2
+    return b.get(tag, 0.0)
 
 
 def measured_peaks() -> dict:
@@ -232,6 +241,7 @@ def run_ours(args, rank, local, world):
     h.set_prefetch_shared(args.prefetch_shared)
     if args.l2_ahead is not None:
         h.set_l2_ahead(args.l2_ahead)
+    h.set_one_token_shared(args.shared_in_routing)
     layers = build_weights(dev)
     cws = [L.c_struct() for L in layers]
     stream = torch.cuda.current_stream()
@@ -324,10 +334,11 @@ def run_ours(args, rank, local, world):
         us_e2e = reduce_max(e0.elapsed_time(e1) * 1000.0 / K, dev)
         b = step_bytes(M, U)
         kern = {}
-        merged_shared = "shared_gate_up" not in prof  # batch 1: the shared expert runs inside gate_up / down
+        # batch 1: the shared expert runs inside the routing (or gate/up) and down launches
+        shared_in = None if "shared_gate_up" in prof else ("router" if args.shared_in_routing else "gate_up")
         for tag, (n, ms) in prof.items():
             avg_us = ms * 1000.0 / max(n, 1)
-            kb = kernel_bytes(tag, M, U_prof + (1 if merged_shared and tag in ("gate_up", "down") else 0))
+            kb = kernel_bytes(tag, M, U_prof, shared_in)
             kern[tag] = {"launches_per_step": n / K, "avg_us": round(avg_us, 2),
                          "GBps": round(kb / (avg_us * 1e3), 1) if kb and avg_us > 0 else None}
         results[M] = dict(M=M, us_per_step=round(us_max, 2), us_per_step_stream=round(us_eager, 2),
@@ -473,6 +484,8 @@ def main(argv=None):
                          "and report the replay time as the value)")
     ap.add_argument("--shared-sms", type=int, default=0,
                     help="SMs for the shared expert: 0 automatic share (default), -1 every SM overlapped, n fixed")
+    ap.add_argument("--shared-in-routing", type=int, choices=(0, 1), default=1,
+                    help="batch 1: shared expert gate/up inside the routing launch (1) or the gate/up launch (0)")
     ap.add_argument("--l2-ahead", type=int, default=None,
                     help="bytes per CTA the small-matrix kernels keep requested into L2 ahead (default: library's)")
     ap.add_argument("--prefetch-shared", action="store_true",

@@ -110,6 +110,13 @@ dec_status dec_set_shared_sms(dec_handle* h, int sms);
  * of evict-last lines crowd the weight stream out of the 129 MB L2. */
 dec_status dec_set_prefetch_shared(dec_handle* h, int enable);
 
+/* Where decode_layer runs the shared expert's gate/up at batch 1
+ * [K3 P1§3, §4]: 1 (default) inside the routing launch, whose CTAs stream it
+ * while the router / top-k chain runs; 0 as problem 0 of the routed gate/up
+ * launch. Both give the same result; the switch exists to measure and test
+ * both schedules. */
+dec_status dec_set_one_token_shared(dec_handle* h, int in_routing);
+
 /* The small-matrix kernels (batch 1) keep about `bytes` of each CTA's
  * upcoming weight rows requested into L2 (bulk L2 prefetches, issued from
  * before the dependency wait on), beyond the rows their registers hold, so
@@ -276,8 +283,9 @@ dec_status decode_layer_workspace_size(const dec_handle* h, const dec_layer_weig
  * on the first K_out columns of y. At M = 1 the layer is five launches on
  * `stream`: in-projection with the first RMSNorm, out-projection with the
  * residual, one routing launch (second RMSNorm, router, top-k, routing
- * table), gate/up of the shared and selected experts, and the down
- * projection fused with the combine and the residual. For M >= 2 the shared
+ * table, and the shared expert's gate/up streamed meanwhile), gate/up of the
+ * selected experts, and the down projection (selected and shared experts)
+ * fused with the combine and the residual. For M >= 2 the shared
  * expert runs on the handle's side stream [K3 P1§3]. While the router and
  * top-k run, the `prefetch_next` region (if any) is pulled into L2 on a
  * second side stream [K3 P1§4]. trace may be NULL. */

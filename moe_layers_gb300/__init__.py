@@ -69,6 +69,7 @@ def _load():
         "dec_set_shared_sms": [P, I],
         "dec_set_prefetch_shared": [P, I],
         "dec_set_l2_ahead": [P, I],
+        "dec_set_one_token_shared": [P, I],
         "dec_check_device_error": [P],
         "dec_linear_workspace_size": [P, I, I, I, ctypes.POINTER(Z)],
         "dec_linear": [P, P, I, P, P, I, I, I, P, Z, P],
@@ -193,6 +194,9 @@ class Handle:
 
     def set_prefetch_shared(self, enable: bool) -> None:
         _check(_load().dec_set_prefetch_shared(self._h, 1 if enable else 0), "dec_set_prefetch_shared")
+
+    def set_one_token_shared(self, in_routing: bool) -> None:
+        _check(_load().dec_set_one_token_shared(self._h, 1 if in_routing else 0), "dec_set_one_token_shared")
 
     def set_l2_ahead(self, nbytes: int) -> None:
         _check(_load().dec_set_l2_ahead(self._h, int(nbytes)), "dec_set_l2_ahead")

@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoedecode.so")
 ARCH = os.environ.get("MOE_DECODE_ARCH", "103a")
 
-SOURCES = ["api.cu", "gemv.cu", "umma.cu", "router.cu", "misc.cu", "noalloc.cu", "gemv_moe.cu"]
+SOURCES = ["api.cu", "gemv.cu", "umma.cu", "router.cu", "misc.cu", "noalloc.cu", "gemv_moe.cu", "route_shared.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 PUBLIC = os.path.join(ROOT, "include", "moe_decode.h")
 

@@ -266,11 +266,12 @@ dec_status moe_shared_fork(dec_handle* h, const uint16_t* x, int M, int k, int E
 // launch per matrix over every SM (the shared expert is problem 0), the down
 // projection fused with the combine and the residual where supported. The
 // routing table in ws.table is complete; slot j's activation row is at
-// x + j * ldx (ldx 0: one row for all slots).
+// x + j * ldx (ldx 0: one row for all slots). shared_gate_up_done: the
+// routing launch already wrote the shared expert's SwiGLU output to ws.hs.
 dec_status moe_small(dec_handle* h, const uint16_t* x, long long ldx, const float* w, int k, const uint16_t* Wg,
                      const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I, const uint16_t* Wg_s,
                      const uint16_t* Wu_s, const uint16_t* Wd_s, const uint16_t* residual, uint16_t* out,
-                     const MoeWs& ws, cudaStream_t s) {
+                     const MoeWs& ws, cudaStream_t s, bool shared_gate_up_done = false) {
   const bool has_shared = Wg_s != nullptr;
   h->last_expert_variant = DEC_VARIANT_SMALL_M;
   // the shared expert's activation: slot 0's row (every slot holds the token's row)
@@ -278,8 +279,13 @@ dec_status moe_small(dec_handle* h, const uint16_t* x, long long ldx, const floa
   const bool fused_down = gemv_down_combine_supported(k, I);
   {
     LaunchScope scope(h, "gate_up", s);
+    // Late trigger (dependents launch only after this launch's dependency
+    // wait): lets the fused down kernel read the routing early, and keeps the
+    // next routing launch from starting before this one's predecessor (the
+    // routing launch, whose row queue it reuses) has completed.
     DEC_CUDA(launch_gemv_moe(h, true, Wg, Wu, I, I, H, x, ldx, ws.table, E, k, ws.hbuf, I, h->sms, s,
-                             has_shared ? &sgu : nullptr, k, fused_down));
+                             (has_shared && !shared_gate_up_done) ? &sgu : nullptr, k,
+                             fused_down || shared_gate_up_done));
   }
   if (fused_down) {
     // down projection + weighted combine + residual in one kernel; the routing
@@ -387,7 +393,7 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
 
 // ---------------------------------------------------------------- decode layer workspace
 struct LayerWs {
-  int* sel_counter = nullptr;  // the one-token router's hand-off counter
+  int* sel_counter = nullptr;  // the one-token routing launch's counters (hand-off, row queue, done)
   uint16_t* a = nullptr;
   uint16_t* yin = nullptr;
   uint16_t* h1 = nullptr;
@@ -409,7 +415,7 @@ bool layer_ok(const dec_layer_weights* L, int M) {
 void carve_layer(Carver& c, const dec_handle* h, const dec_layer_weights* L, int M, LayerWs* w) {
   const int H = L->H;
   const long long dense_tiles = std::max<long long>((L->N_in + kTileN - 1) / kTileN, H / kTileN);
-  w->sel_counter = c.take<int>(1);
+  w->sel_counter = c.take<int>(4);
   carve_moe_counters(c, L->E, H, L->I, dense_tiles, &w->moe);
   w->a = c.take<uint16_t>((size_t)M * H);
   w->yin = c.take<uint16_t>((size_t)M * L->N_in);
@@ -510,6 +516,12 @@ dec_status dec_set_pdl(dec_handle* h, int enable) {
 dec_status dec_set_prefetch_shared(dec_handle* h, int enable) {
   if (h == nullptr) return DEC_ERR_INVALID_ARG;
   h->prefetch_shared = enable ? 1 : 0;
+  return DEC_OK;
+}
+
+dec_status dec_set_one_token_shared(dec_handle* h, int in_routing) {
+  if (h == nullptr || (in_routing != 0 && in_routing != 1)) return DEC_ERR_INVALID_ARG;
+  h->fuse_shared_routing = in_routing;
   return DEC_OK;
 }
 
@@ -752,12 +764,20 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   // The router / top-k phase is latency-bound; the shared expert and the
   // prefetch stream use the idle bandwidth meanwhile.
   if (one_token) {
+    // With a shared expert the routing launch also streams its gate/up.
+    const bool fuse_shared = L.Wg_s != nullptr && h->fuse_shared_routing &&
+                             route_shared_supported(h, H, L.E, L.k);
     {
       LaunchScope scope(h, "router", s);
-      DEC_CUDA(launch_router_select(h, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx, wt,
-                                    scores, w.moe.table, s));
+      if (fuse_shared)
+        DEC_CUDA(launch_route_shared(h, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx, wt,
+                                     scores, w.moe.table, L.Wg_s, L.Wu_s, L.I, w.moe.hs, s));
+      else
+        DEC_CUDA(launch_router_select(h, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx,
+                                      wt, scores, w.moe.table, s));
     }
-    st = moe_small(h, w.b, 0, wt, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, h1, hidden, w.moe, s);
+    st = moe_small(h, w.b, 0, wt, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, h1, hidden, w.moe, s,
+                   fuse_shared);
     if (st != DEC_OK) return st;
     if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
     return DEC_OK;

@@ -24,6 +24,7 @@ struct dec_handle {
   int last_variant = 0;
   int last_expert_variant = 0;      // kernel family of the most recent expert launches
   int shared_ctas = 0;              // CTAs for the shared expert's kernels (0 = default)
+  int fuse_shared_routing = 1;      // batch 1: the routing launch also streams the shared gate/up
   int l2_ahead = 49152;             // small-matrix kernels: weight bytes per CTA requested into L2 ahead
   int prefetch_shared = 0;          // batch 1: pull the shared expert into L2 during the router phase
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -133,6 +134,13 @@ cudaError_t launch_router_select(dec_handle* h, const uint16_t* x, const uint16_
                                  int H, int E, int k, uint16_t* xn, float* parts, int* counter, int32_t* idx,
                                  float* w, float* scores, int* table, cudaStream_t s);
 // One token: the routing table with entry j as problem j on slot j (expert idx[j]).
+// One token: launch_router_select's work plus the shared expert's gate/up
+// (h_s = bf16(silu(W_g,s b) * (W_u,s b))) streamed by the same CTAs; ctr: 3 ints, zero on entry and on return.
+bool route_shared_supported(const dec_handle* h, int H, int E, int k);
+cudaError_t launch_route_shared(dec_handle* h, const uint16_t* h1, const uint16_t* gamma, float eps, const float* Wr,
+                                int H, int E, int k, uint16_t* xn, float* parts, int* ctr, int32_t* idx, float* w,
+                                float* scores, int* table, const uint16_t* Wg_s, const uint16_t* Wu_s, int I,
+                                uint16_t* hs, cudaStream_t s);
 cudaError_t launch_one_token_table(dec_handle* h, const int32_t* idx, int E, int k, int* table, cudaStream_t s);
 cudaError_t launch_route_table(dec_handle* h, const int32_t* idx, int M, int k, int E, const uint16_t* x, int H,
                                int* table, uint16_t* xs, cudaStream_t s);

@@ -92,12 +92,15 @@ def test_layer_small(h, M, shared):
     _check_layer(tr, hid, ref, slice(None), f"layer M={M}", L)
 
 
-@pytest.mark.parametrize("H,E,k,shared", [(1152, 37, 5, True), (1152, 37, 5, False), (256, 9, 8, True)])
-def test_layer_one_token_shapes(h, H, E, k, shared):
+@pytest.mark.parametrize("in_routing", [True, False])
+@pytest.mark.parametrize("H,E,k,shared", [(1152, 37, 5, True), (1152, 37, 5, False), (256, 9, 8, True),
+                                          (2048, 300, 8, True)])
+def test_layer_one_token_shapes(h, H, E, k, shared, in_routing):
     """One token: the fused RMSNorm / router / top-k / routing-table launch on
     a router row split into a full and a ragged chunk (H = 1152), with a
-    number of experts that leaves a partial row group, and k = 8 (the fused
-    down projection + combine) over only 9 experts."""
+    number of experts that leaves a partial row group, k = 8 (the fused down
+    projection + combine) over only 9 experts, and 300 experts; the shared
+    expert's gate/up in the routing launch and in the routed gate/up launch."""
     N_in, K_out, I = 264, 256, 128
     L = Layer(H, N_in, K_out, E, I, k, base=6500 + E)
     n = E * I * H
@@ -110,9 +113,13 @@ def test_layer_one_token_shapes(h, H, E, k, shared):
               synth.bf16(H * I, SEED, 6515, 0, 0.05).reshape(H, I))
     dev_w = L.device(dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
                      None if sh is None else tuple(dev_bf16(a, a.shape) for a in sh))
-    for rep in range(3):  # the hand-off counter must be left at zero by every call
+    h.set_one_token_shared(in_routing)
+    for rep in range(3):  # the hand-off and queue counters must be left at zero by every call
         hbits, _ = gap_rows(L.scores, 1, H, k, base=6600 + 10 * E + rep)
-        hid, tr = _run(h, L, dev_w, hbits)
+        try:
+            hid, tr = _run(h, L, dev_w, hbits)
+        finally:
+            h.set_one_token_shared(True)
         ref = L.oracle(hbits, lambda e: (g[e], u[e], d[e]), sh)
         _check_layer(tr, hid, ref, slice(None), f"layer one token H={H} E={E} rep={rep}", L)
 
@@ -131,6 +138,34 @@ def _check_router_stage(L, tr, rows, what):
     assert np.array_equal(tr["idx"].cpu().numpy()[rows], i_ref), what + ": top-k on the layer's h1"
     assert np.max(np.abs(tr["scores"].cpu().numpy()[rows] - s_ref)) <= SCORE_TOL, what + ": scores"
     assert np.max(np.abs(tr["w"].cpu().numpy()[rows] - w_ref)) <= WEIGHT_TOL, what + ": weights"
+
+
+@pytest.mark.slow
+def test_layer_one_token_two_router_units(h):
+    """One token with more router units (40 row groups x 8 column chunks = 320)
+    than the routing launch has CTAs on a 152-SM GPU (304): the first CTAs own
+    two units, the second loaded after the norm. The 2 GB bank is placed by the
+    device filler and regenerated per selected expert for the oracle."""
+    import torch
+    H, E, I, k, N_in, K_out = 8192, 320, 128, 8, 264, 256
+    L = Layer(H, N_in, K_out, E, I, k, base=6700)
+    n = E * I * H
+    Wg = torch.empty((E, I, H), dtype=torch.bfloat16, device="cuda")
+    Wu = torch.empty_like(Wg)
+    Wd = torch.empty((E, H, I), dtype=torch.bfloat16, device="cuda")
+    for t, tid in ((Wg, synth.W_G), (Wu, synth.W_U), (Wd, synth.W_D)):
+        synth.fill_bf16_dev(t.data_ptr(), n, 0, tid, 0, 0.02)
+    sh_bits = (synth.bf16(I * H, SEED, 6710, 0, 0.05).reshape(I, H), synth.bf16(I * H, SEED, 6711, 0, 0.05).reshape(I, H),
+               synth.bf16(H * I, SEED, 6712, 0, 0.05).reshape(H, I))
+    dev_w = L.device(Wg, Wu, Wd, tuple(dev_bf16(a, a.shape) for a in sh_bits))
+    bank = HostBank(E, H, I)
+    for rep in range(2):
+        hbits, _ = gap_rows(L.scores, 1, H, k, base=6720 + rep)
+        hid, tr = _run(h, L, dev_w, hbits)
+        ref = L.oracle(hbits, bank, sh_bits)
+        _check_layer(tr, hid, ref, slice(None), f"layer one token two units rep={rep}", L)
+    del Wg, Wu, Wd
+    torch.cuda.empty_cache()
 
 
 def _check_layer(tr, hid, ref, rows, what, L=None):
