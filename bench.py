@@ -52,6 +52,28 @@ EXPERT_BYTES = 3 * I * H * 2
 DENSE_BYTES = N_IN * H * 2 + H * K_OUT * 2 + E * H * 4 + 2 * H * 2
 
 
+SHARD = 1
+
+
+def set_shard(s: int) -> None:
+    """Per-GPU shapes of an s-way tensor-parallel deployment of the layer (the
+    pages' TP8 / TP16): the input projection split over its outputs (N_in / s),
+    the out-projection over its inputs (K_out / s) and every expert over its
+    intermediate size (I / s); hidden size, router (replicated) and top-k
+    unchanged. The exchange steps of a TP group (all-reduces) have no one-GPU
+    counterpart and are not run."""
+    global SHARD, N_IN, K_OUT, I, EXPERT_BYTES, WORKLOAD
+    SHARD = int(s)
+    N_IN, K_OUT, I = 12288 // SHARD, 8192 // SHARD, 2048 // SHARD
+    EXPERT_BYTES = 3 * I * H * 2
+    set_experts(E)
+    if SHARD > 1:
+        WORKLOAD = (f"decode layer step at TP{SHARD} per-GPU shapes: RMSNorm -> input projection (K={H}, "
+                    f"N={N_IN}) -> out-projection (K={K_OUT}, N={H}) + residual -> RMSNorm -> MoE (router "
+                    f"W_r[{E},{H}] fp32 replicated, sigmoid, top-{TOPK} renormalised; {E} routed + 1 shared "
+                    f"SwiGLU experts {H}->{I}->{H}), bf16; no all-reduce")
+
+
 def set_experts(n: int) -> None:
     """Routed experts in the bank (384 for the workload; fewer only for small profiling captures)."""
     global E, DENSE_BYTES
@@ -199,6 +221,19 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- our arm
+def layer_copies() -> int:
+    """Weight copies the bench rotates through. At full shapes a step reads
+    1.1-25 GB, far above the 129 MB L2, and two dense copies suffice (the router
+    and shared expert are re-read only after about 1 GB of other traffic). The
+    sharded steps read 80-150 MB, so every weight, router and expert bank
+    included, gets enough copies that a step's bytes come back only after four
+    times L2 of traffic."""
+    if SHARD == 1:
+        return 2
+    step_m1 = DENSE_BYTES + (TOPK + 1) * EXPERT_BYTES
+    return max(2, -(-4 * 129_000_000 // step_m1))
+
+
 def build_weights(dev: str, copies: int = 2):
     import torch
     import moe_layers_gb300 as ML
@@ -209,16 +244,23 @@ def build_weights(dev: str, copies: int = 2):
         synth.fill_bf16_dev(t.data_ptr(), t.numel(), 0, tid, 0, sigma)
         return t
 
-    Wg = fill_bf16((E, I, H), synth.W_G, 0.02)
-    Wu = fill_bf16((E, I, H), synth.W_U, 0.02)
-    Wd = fill_bf16((E, H, I), synth.W_D, 0.02)
-    Ws = (fill_bf16((I, H), synth.W_G_S, 0.02), fill_bf16((I, H), synth.W_U_S, 0.02),
-          fill_bf16((H, I), synth.W_D_S, 0.02))
-    Wr = torch.empty((E, H), dtype=torch.float32, device=dev)
-    synth.fill_f32_dev(Wr.data_ptr(), Wr.numel(), 0, synth.W_R, 0, 0.01)
+    def moe_weights():
+        Wg = fill_bf16((E, I, H), synth.W_G, 0.02)
+        Wu = fill_bf16((E, I, H), synth.W_U, 0.02)
+        Wd = fill_bf16((E, H, I), synth.W_D, 0.02)
+        Ws = (fill_bf16((I, H), synth.W_G_S, 0.02), fill_bf16((I, H), synth.W_U_S, 0.02),
+              fill_bf16((H, I), synth.W_D_S, 0.02))
+        Wr = torch.empty((E, H), dtype=torch.float32, device=dev)
+        synth.fill_f32_dev(Wr.data_ptr(), Wr.numel(), 0, synth.W_R, 0, 0.01)
+        return Wg, Wu, Wd, Ws, Wr
+
     ones = torch.ones(H, dtype=torch.bfloat16, device=dev)
     layers = []
+    moe = moe_weights()
     for c in range(copies):
+        if c > 0 and SHARD > 1:
+            moe = moe_weights()  # sharded steps are small: nothing may stay in L2 from step to step
+        Wg, Wu, Wd, Ws, Wr = moe
         W_in = fill_bf16((N_IN, H), synth.W_IN, 0.02)
         W_o = fill_bf16((H, K_OUT), synth.W_O, 0.02)
         layers.append(ML.LayerWeights(gamma1=ones, W_in=W_in, W_o=W_o, gamma2=ones, W_r=Wr, Wg=Wg, Wu=Wu, Wd=Wd,
@@ -242,7 +284,7 @@ def run_ours(args, rank, local, world):
     if args.l2_ahead is not None:
         h.set_l2_ahead(args.l2_ahead)
     h.set_one_token_shared(args.shared_in_routing)
-    layers = build_weights(dev)
+    layers = build_weights(dev, layer_copies())
     cws = [L.c_struct() for L in layers]
     stream = torch.cuda.current_stream()
     peaks = measured_peaks()
@@ -262,7 +304,7 @@ def run_ours(args, rank, local, world):
         idx_all = torch.empty((K, M, TOPK), dtype=torch.int32, device=dev)
 
         def step(i, trace=None):
-            ML.decode_layer(h, layers[i % 2], hidden, trace=trace, ws=ws, _cw=cws[i % 2])
+            ML.decode_layer(h, layers[i % len(layers)], hidden, trace=trace, ws=ws, _cw=cws[i % len(layers)])
 
         for i in range(args.warmup):
             step(i)
@@ -299,7 +341,8 @@ def run_ours(args, rank, local, world):
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=gs):
                 for i in range(K):
-                    ML.decode_layer(h, layers[i % 2], hidden, trace={"idx": idx_all[i]}, ws=ws, _cw=cws[i % 2],
+                    ML.decode_layer(h, layers[i % len(layers)], hidden, trace={"idx": idx_all[i]}, ws=ws,
+                                    _cw=cws[i % len(layers)],
                                     stream=gs)
             hidden.copy_(host_in)
             graph.replay()
@@ -372,6 +415,7 @@ def run_ours(args, rank, local, world):
            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
            "data": "synthetic: seeded random-init weights of the workload's shapes, seeded N(0,1) activations",
            "config": {"workload": WORKLOAD if E == 384 else WORKLOAD + f" (profiling variant: {E} routed experts)",
+                      "weight_copies": len(layers),
                       "batch": args.batch, "parallelism": "replicas" if world > 1 else "1 GPU",
                       "l2": "inputs larger than L2: each step reads >= 1.1 GB (L2 129 MB); dense weights alternate "
                             "between 2 copies; routing changes every step",
@@ -498,10 +542,13 @@ def main(argv=None):
                     help="bytes per CTA the small-matrix kernels keep requested into L2 ahead (default: library's)")
     ap.add_argument("--prefetch-shared", action="store_true",
                     help="at batch 1, pull the shared expert into L2 during the router phase (off: measured slower)")
+    ap.add_argument("--shard", type=int, choices=(1, 8, 16), default=1,
+                    help="per-GPU shapes of a TP8 / TP16 deployment (1: the full layer)")
     ap.add_argument("--experts", type=int, default=E,
                     help="routed experts in the bank (default 384, the workload; smaller only for ncu captures)")
     args = ap.parse_args(argv)
     set_experts(args.experts)
+    set_shard(args.shard)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.steps < 2:

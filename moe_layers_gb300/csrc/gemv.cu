@@ -167,6 +167,110 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
   }
 }
 
+// Narrow rows (K <= 1024: K / 8 <= TPR <= 128 vectors): TPR threads share a
+// row, one 16-byte vector each, so a CTA works on 256 / TPR rows at a time
+// instead of leaving most of its threads idle. Each group of TPR threads takes
+// RB rows per step (one vector per row per thread; the next step's loads are
+// issued before this step's FMAs); groups interleave so that the CTA's
+// concurrent rows are adjacent in memory. Groups of up to 32 threads reduce
+// with shuffles alone; wider groups add one shared-memory pass over their
+// warps. No RMSNorm here (the input projection's rows are wide).
+template <int M, int TPR>
+__global__ void __launch_bounds__(kGemvThreads, 2)
+    gemv_narrow_kernel(const uint16_t* x, long long ldx, const uint16_t* __restrict__ W, const uint16_t* res,
+                       long long ldr, uint16_t* y, long long ldy, int N, int K, int ahead) {
+  constexpr int NG = kGemvThreads / TPR;  // row groups
+  constexpr int RB = M == 1 ? 8 : 4;      // rows per group per step
+  constexpr int WPG = TPR > 32 ? TPR / 32 : 1;  // warps per group
+  static_assert(TPR >= RB * M, "a group's threads write its RB x M outputs");
+  const int t = threadIdx.x, g = t / TPR, j = t % TPR, lane = t & 31;
+  const int K8 = K >> 3;
+  const long long G = gridDim.x;
+  const int r0 = (int)((long long)blockIdx.x * N / G);
+  const int r1 = (int)((long long)(blockIdx.x + 1) * N / G);
+  constexpr int STEP = NG * RB;  // rows per CTA step
+  __shared__ float red[2][kGemvThreads / 32][TPR > 32 ? RB * M : 1];
+  const uint64_t pol = policy_evict_first();
+  pdl_trigger();
+
+  // row of group g, slot r, in the step starting at rb
+  auto row_of = [&](int rb, int r) { return rb + g + NG * r; };
+  uint4 wa[RB];
+  auto load_rows = [&](uint4(&w)[RB], int rb) {
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const int rr = row_of(rb, r);
+      w[r] = (rr < r1 && j < K8) ? ld_stream(W + (size_t)rr * K + (size_t)j * 8, pol) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  if (r0 < r1) load_rows(wa, r0);
+  const size_t rowb = (size_t)K * sizeof(uint16_t);
+  const int ahead_rows = ahead > 0 ? max(STEP, (int)((size_t)ahead / rowb)) : 0;
+  int pf = r0 + STEP;
+  auto request = [&](int upto) {
+    upto = min(upto, r1);
+    if (ahead_rows > 0 && upto > pf) {
+      if (t == 0) request_l2(W + (size_t)pf * K, (size_t)(upto - pf) * rowb);
+      pf = upto;
+    }
+  };
+  request(r0 + STEP + ahead_rows);
+  pdl_wait();
+  uint4 xr[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) xr[m] = j < K8 ? ld_act16(x + (size_t)m * ldx + (size_t)j * 8) : make_uint4(0, 0, 0, 0);
+
+  int buf = 0;
+  for (int rb = r0; rb < r1; rb += STEP) {
+    uint4 wb[RB];
+    const bool more = rb + STEP < r1;
+    if (more) load_rows(wb, rb + STEP);
+    request(rb + 2 * STEP + ahead_rows);
+    float acc[RB][M];
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+      for (int m = 0; m < M; ++m) acc[r][m] = dot8(wa[r], xr[m], 0.f);
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int o = (TPR < 32 ? TPR : 32) / 2; o > 0; o >>= 1)
+          acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], o);
+    float val = 0.f;  // thread j < RB * M of the group: output (r, m) = (j / M, j % M)
+    if (TPR > 32) {
+      if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+#pragma unroll
+          for (int m = 0; m < M; ++m) red[buf][t >> 5][r * M + m] = acc[r][m];
+      }
+      __syncthreads();
+      if (j < RB * M)
+        for (int w = 0; w < WPG; ++w) val += red[buf][g * WPG + w][j];
+    } else {
+#pragma unroll
+      for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int m = 0; m < M; ++m)
+          if (j == r * M + m) val = acc[r][m];
+    }
+    if (j < RB * M) {
+      const int r = j / M, m = j % M, row = row_of(rb, r);
+      if (row < r1) {
+        if (res != nullptr) val += bf2f(ld_act_u16(res + (size_t)m * ldr + row));
+        y[(size_t)m * ldy + row] = f2bf(val);
+      }
+    }
+    buf ^= 1;
+    if (more) {
+#pragma unroll
+      for (int r = 0; r < RB; ++r) wa[r] = wb[r];
+    }
+  }
+}
+
 bool gemv_supported(int M, int K) { return M >= 1 && M <= 4 && K >= 8 && K % 8 == 0 && K <= 8 * 8 * kGemvThreads; }
 
 template <int M>
@@ -177,6 +281,12 @@ static cudaError_t gemv_m(dec_handle* h, const uint16_t* x, long long ldx, const
   const int grid = (int)std::min<long long>((long long)N, 2LL * h->sms);
   const dim3 g(grid > 0 ? grid : 1), b(kGemvThreads);
   const int a = h->l2_ahead;
+  if (gamma == nullptr && K8 <= 128) {
+    if (K8 <= 16) return launch_k(h, gemv_narrow_kernel<M, 16>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, a);
+    if (K8 <= 32) return launch_k(h, gemv_narrow_kernel<M, 32>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, a);
+    if (K8 <= 64) return launch_k(h, gemv_narrow_kernel<M, 64>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, a);
+    return launch_k(h, gemv_narrow_kernel<M, 128>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, a);
+  }
   if (K8 <= kGemvThreads)
     return launch_k(h, gemv_kernel<M, 1>, g, b, 0, s, x, ldx, W, res, ldr, y, ldy, N, K, gamma, eps, a);
   if (K8 <= 2 * kGemvThreads)

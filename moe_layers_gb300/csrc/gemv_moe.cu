@@ -367,6 +367,104 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_kernel(
   }
 }
 
+// Narrow rows (K = I <= 256, K / 8 <= TPR in {16, 32}): as the kernel above,
+// but a group of TPR threads owns a whole output row (one 16-byte vector of
+// each of the NP matrices' row per thread), so a CTA works on 256 / TPR rows
+// at a time and a row is reduced by shuffles alone, with no barrier in the
+// loop. Groups take the CTA's rows interleaved (group g: n0 + g, n0 + g + NG,
+// ...); the next row's NP vectors are loaded while this one's are consumed.
+template <int NP, int TPR, bool SHARED>
+__global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_narrow_kernel(
+    const uint16_t* __restrict__ Wd, long long rows_bank, const uint16_t* __restrict__ Wd_s, int H, int K,
+    const uint16_t* hbuf, const uint16_t* hs, const int* table, int E, int k, const float* w, const uint16_t* res,
+    uint16_t* out, int routing_ready, int ahead) {
+  constexpr int NR = SHARED ? NP - 1 : NP;
+  constexpr int NG = kGmThreads / TPR;
+  const int t = threadIdx.x, g = t / TPR, j = t % TPR;
+  const int K8 = K >> 3;
+  const uint64_t pol = policy_evict_first();
+  pdl_trigger();
+  const long long G = gridDim.x, c = blockIdx.x;
+  const int n0 = (int)(c * H / G), n1 = (int)((c + 1) * H / G);
+  if (n0 >= n1) return;  // (before any barrier)
+  const TableLayout L(E, k);
+  __shared__ const uint16_t* s_rowbase[NP];
+  __shared__ const uint16_t* s_xrow[NP];
+  __shared__ float s_w[NP];
+  auto routing = [&](bool cg) {
+    if (t < NP) {
+      if (SHARED && t == NP - 1) {
+        s_rowbase[t] = Wd_s;
+        s_xrow[t] = hs;
+        s_w[t] = 1.f;
+      } else {
+        const int slot = cg ? ld_cg_s32(table + L.entry_slot() + t) : ld_act_s32(table + L.entry_slot() + t);
+        const long long e = cg ? ld_cg_s32(table + L.expert() + slot) : ld_act_s32(table + L.expert() + slot);
+        s_rowbase[t] = Wd + e * rows_bank * K;
+        s_xrow[t] = hbuf + (size_t)slot * K;
+        s_w[t] = cg ? ld_cg_f32(w + t) : ld_act_f32(w + t);
+      }
+    }
+    __syncthreads();
+  };
+  // Loads are unconditional at clamped, in-range addresses (a lane past the
+  // row's vectors reads the row's last one and meets a zero activation; a
+  // group past the CTA's rows reads its last row and writes nothing), so the
+  // register ring holds no second copies.
+  const int jj = min(j, K8 - 1);
+  uint4 ring[NP];
+  auto load_row = [&](int n) {
+    const int nn = min(n, n1 - 1);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) ring[q] = ld_stream(s_rowbase[q] + (size_t)nn * K + (size_t)jj * 8, pol);
+  };
+  const int rowb = K * (int)sizeof(uint16_t);
+  const int ahead_rows = ahead > 0 ? max(1, ahead / (NP * rowb)) : 0;
+  int pf = n0 + NG;
+  auto request = [&](int upto) {
+    upto = min(upto, n1);
+    if (ahead_rows > 0 && upto > pf) {
+      if (t < NP) request_l2(s_rowbase[t] + (size_t)pf * K, (size_t)(upto - pf) * rowb);
+      pf = upto;
+    }
+  };
+  if (routing_ready) {
+    routing(true);
+    load_row(n0 + g);
+    request(n0 + NG + ahead_rows);
+  }
+  pdl_wait();
+  if (!routing_ready) {
+    routing(false);
+    load_row(n0 + g);
+    request(n0 + NG + ahead_rows);
+  }
+  uint4 xr[NP];
+#pragma unroll
+  for (int q = 0; q < NP; ++q) xr[q] = j < K8 ? ld_act16(s_xrow[q] + (size_t)j * 8) : make_uint4(0, 0, 0, 0);
+  for (int n = n0 + g; n < n1; n += NG) {
+    if (g == 0) request(n + 2 * NG + ahead_rows);  // (only threads t < NP issue)
+    float a = 0.f;
+    const int nn = min(n + NG, n1 - 1);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+      const uint4 wv = ring[q];
+      ring[q] = ld_stream(s_rowbase[q] + (size_t)nn * K + (size_t)jj * 8, pol);
+      const float d = dot8(wv, xr[q], 0.f);
+      if (SHARED && q == NP - 1)
+        a += d;
+      else
+        a = fmaf(s_w[q], d, a);
+    }
+#pragma unroll
+    for (int o = TPR / 2; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    if (j == 0) {
+      if (res != nullptr) a += bf2f(ld_act_u16(res + n));
+      out[n] = f2bf(a);
+    }
+  }
+}
+
 // Rows of up to 2048 elements (one vector per thread per row, activations in registers).
 bool gemv_down_combine_supported(int k, int I) { return k == 8 && I >= 8 && I % 8 == 0 && I <= 8 * kGmThreads; }
 
@@ -376,12 +474,25 @@ cudaError_t launch_gemv_down_combine(dec_handle* h, const uint16_t* Wd, long lon
                                      cudaStream_t s, bool routing_ready) {
   if (!gemv_down_combine_supported(k, I)) return cudaErrorInvalidValue;
   const dim3 g(std::max(1, 2 * sms)), b(kGmThreads);
-  const size_t smem = 0;
+  const int rr = (int)routing_ready, a = h->l2_ahead;
+  const int K8 = I / 8;
+  if (K8 <= 32) {
+    // narrow rows: a group of 16 or 32 threads per output row
+    if (Wd_s != nullptr)
+      return K8 <= 16 ? launch_k(h, gemv_down_combine_narrow_kernel<9, 16, true>, g, b, 0, s, Wd, rows_bank, Wd_s, H,
+                                 I, hbuf, hs, table, E, k, w, res, out, rr, a)
+                      : launch_k(h, gemv_down_combine_narrow_kernel<9, 32, true>, g, b, 0, s, Wd, rows_bank, Wd_s, H,
+                                 I, hbuf, hs, table, E, k, w, res, out, rr, a);
+    return K8 <= 16 ? launch_k(h, gemv_down_combine_narrow_kernel<8, 16, false>, g, b, 0, s, Wd, rows_bank, Wd_s, H, I,
+                               hbuf, hs, table, E, k, w, res, out, rr, a)
+                    : launch_k(h, gemv_down_combine_narrow_kernel<8, 32, false>, g, b, 0, s, Wd, rows_bank, Wd_s, H, I,
+                               hbuf, hs, table, E, k, w, res, out, rr, a);
+  }
   if (Wd_s != nullptr)
-    return launch_k(h, gemv_down_combine_kernel<9, 1, true>, g, b, smem, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs,
-                    table, E, k, w, res, out, (int)routing_ready, h->l2_ahead);
-  return launch_k(h, gemv_down_combine_kernel<8, 1, false>, g, b, smem, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs, table,
-                  E, k, w, res, out, (int)routing_ready, h->l2_ahead);
+    return launch_k(h, gemv_down_combine_kernel<9, 1, true>, g, b, 0, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs, table,
+                    E, k, w, res, out, rr, a);
+  return launch_k(h, gemv_down_combine_kernel<8, 1, false>, g, b, 0, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs, table, E,
+                  k, w, res, out, rr, a);
 }
 
 bool gemv_moe_supported(int K) { return K >= 8 && K % 8 == 0 && K <= 8 * 4 * kGmThreads; }

@@ -204,3 +204,44 @@ def test_layer_full_size(h, full_bank, full_layer, M):
     s_all = L.scores(hbits)
     i_all, _ = oracle.topk(s_all, K_FULL)
     assert np.array_equal(tr["idx"].cpu().numpy(), i_all)
+
+
+# ---------------------------------------------------------------------------- TP-shard shapes
+@pytest.fixture(scope="module", params=[8, 16], ids=["tp8", "tp16"])
+def tp_layer(request):
+    """Per-GPU shapes of the layer in an s-way tensor-parallel deployment: the
+    input projection split over its outputs, the out-projection over its
+    inputs and every expert over its intermediate size; 384 experts, the
+    router replicated. The bank is placed by the device filler."""
+    import torch
+    sh = request.param
+    H, E, k = H_FULL, E_FULL, K_FULL
+    N_in, K_out, I = N_IN_FULL // sh, K_OUT_FULL // sh, I_FULL // sh
+    L = Layer(H, N_in, K_out, E, I, k, base=7100 + sh, gamma_noise=True)
+    n = E * I * H
+    Wg = torch.empty((E, I, H), dtype=torch.bfloat16, device="cuda")
+    Wu = torch.empty_like(Wg)
+    Wd = torch.empty((E, H, I), dtype=torch.bfloat16, device="cuda")
+    ids = (synth.W_G, synth.W_U, synth.W_D)
+    for t, tid in zip((Wg, Wu, Wd), ids):
+        synth.fill_bf16_dev(t.data_ptr(), n, 0, tid, 0, 0.02)
+    sh_bits = tuple(synth.bf16(I * H, SEED, 7150 + q, 0, 0.02).reshape(shape)
+                    for q, shape in enumerate(((I, H), (I, H), (H, I))))
+    dev_w = L.device(Wg, Wu, Wd, tuple(dev_bf16(a, a.shape) for a in sh_bits))
+    yield sh, L, dev_w, HostBank(E, H, I), sh_bits
+    del Wg, Wu, Wd, dev_w
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M", [1, 4, 64])
+def test_layer_tp_shapes(h, tp_layer, M):
+    sh, L, dev_w, bank, sh_bits = tp_layer
+    hbits, _ = gap_rows(L.scores, M, L.H, L.k, base=synth.X_BASE + 60 + sh)
+    hid, tr = _run(h, L, dev_w, hbits)
+    tokens = sorted(set([0, M // 2, M - 1]))
+    ref = L.oracle(hbits, bank, sh_bits, tokens=tokens)
+    _check_layer(tr, hid, ref, tokens, f"layer TP{sh} M={M}", L)
+    s_all = L.scores(hbits)
+    i_all, _ = oracle.topk(s_all, L.k)
+    assert np.array_equal(tr["idx"].cpu().numpy(), i_all)

@@ -32,7 +32,9 @@ def _mats(M, N, K, tid, sx=1.0, sw=0.02):
 
 
 SMALL = [(1, 200, 72), (2, 300, 136), (1, 7, 8), (2, 1, 4096), (3, 257, 520), (4, 130, 64), (5, 128, 1000),
-         (16, 384, 704), (17, 129, 136), (33, 640, 1032), (48, 256, 512), (64, 520, 704), (64, 1, 64)]
+         (16, 384, 704), (17, 129, 136), (33, 640, 1032), (48, 256, 512), (64, 520, 704), (64, 1, 64),
+         # narrow rows (K <= 1024: 16 to 128 threads per row), incl. the TP8 / TP16 out-projection shapes
+         (1, 7168, 1024), (1, 3001, 512), (2, 1000, 256), (4, 333, 1024), (3, 77, 128), (1, 7168, 512)]
 
 
 @pytest.mark.parametrize("M,N,K", SMALL)
