@@ -285,6 +285,13 @@ def run_ours(args, rank, local, world):
         h.set_l2_ahead(args.l2_ahead)
     h.set_one_token_shared(args.shared_in_routing)
     layers = build_weights(dev, layer_copies())
+    if args.prefetch_next:
+        # Cross-layer prefetch: while layer l routes, the next layer's input
+        # projection is pulled into L2 (up to the given bytes).
+        for li, L in enumerate(layers):
+            nxt = layers[(li + 1) % len(layers)].W_in
+            L.prefetch_next = nxt
+            L.prefetch_bytes = min(int(args.prefetch_next), nxt.numel() * 2) // 16 * 16
     cws = [L.c_struct() for L in layers]
     stream = torch.cuda.current_stream()
     peaks = measured_peaks()
@@ -542,6 +549,8 @@ def main(argv=None):
                     help="bytes per CTA the small-matrix kernels keep requested into L2 ahead (default: library's)")
     ap.add_argument("--prefetch-shared", action="store_true",
                     help="at batch 1, pull the shared expert into L2 during the router phase (off: measured slower)")
+    ap.add_argument("--prefetch-next", type=int, default=0,
+                    help="bytes of the next layer's input projection to pull into L2 during the routing (0: none)")
     ap.add_argument("--shard", type=int, choices=(1, 8, 16), default=1,
                     help="per-GPU shapes of a TP8 / TP16 deployment (1: the full layer)")
     ap.add_argument("--experts", type=int, default=E,
