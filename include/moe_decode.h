@@ -63,7 +63,8 @@ typedef enum dec_status {
 
 /* Kernel families of the projections [K3 P1§1]. */
 typedef enum dec_variant {
-  DEC_VARIANT_AUTO = 0,    /* choose by batch: SMALL_M for M = 1, SPLIT_K above (measured faster at M = 2) */
+  DEC_VARIANT_AUTO = 0,    /* choose by batch and size (measured on GB300): SMALL_M for M <= 2, and for
+                              M <= 4 when the weight matrix is at most 48 MB; SPLIT_K otherwise */
   DEC_VARIANT_SMALL_M = 1, /* CUDA-core small-matrix kernel: each CTA streams whole weight rows */
   DEC_VARIANT_SPLIT_K = 2  /* tcgen05 kernel; the weight k-blocks are split evenly over all SMs */
 } dec_variant;

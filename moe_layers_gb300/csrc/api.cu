@@ -92,11 +92,19 @@ bool linear_shape_ok(int M, int N, int K, int ldx) {
   return M >= 1 && M <= kMaxM && N >= 1 && K >= 8 && K % 8 == 0 && ldx >= K && ldx % 8 == 0;
 }
 
-int choose_variant(const dec_handle* h, int M, int K) {
+int choose_variant(const dec_handle* h, int M, int N, int K) {
   if (h->force_variant == DEC_VARIANT_SMALL_M || h->force_variant == DEC_VARIANT_SPLIT_K) return h->force_variant;
-  // Measured on GB300 (CUDA-graph replay, 115-240 MB weights): the small-matrix kernel streams at
-  // 6.7-6.9 TB/s with one token but 3.9-4.9 TB/s with two, where the split-K kernel reaches 5.8-6.2.
-  return (M == 1 && gemv_supported(M, K)) ? DEC_VARIANT_SMALL_M : DEC_VARIANT_SPLIT_K;
+  // Measured on GB300 (CUDA-graph replay of back-to-back launches, weights rotated past L2): with
+  // its L2 request-ahead the small-matrix kernel streams 115-174 MB weights at 6.9-7.0 TB/s with
+  // one token and 6.1-6.3 TB/s with two, where the split-K kernel reaches 4.6-5.7; with three or
+  // four tokens it drops to 1.8-3.8 TB/s (its FMA and unpacking work grows with the tokens)
+  // against the split-K kernel's 4.6-5.5. But the split-K kernel costs about 15 us per launch
+  // beyond its bytes, so small matrices (the tensor-parallel shard shapes) stay on the
+  // small-matrix kernel up to four tokens.
+  if (!gemv_supported(M, K)) return DEC_VARIANT_SPLIT_K;
+  const double bytes = (double)N * K * 2.0;
+  if (M <= 2 || bytes <= 48e6) return DEC_VARIANT_SMALL_M;
+  return DEC_VARIANT_SPLIT_K;
 }
 
 // gamma (small-matrix kernel, one token only): the input row is RMS-normalised
@@ -104,7 +112,7 @@ int choose_variant(const dec_handle* h, int M, int K) {
 dec_status linear_impl(dec_handle* h, const uint16_t* x, int ldx, const uint16_t* W, const uint16_t* r, uint16_t* y,
                        int M, int N, int K, EngineRegion eng, cudaStream_t s, const char* tag = "linear",
                        const uint16_t* gamma = nullptr, float eps = 0.f) {
-  const int v = choose_variant(h, M, K);
+  const int v = choose_variant(h, M, N, K);
   cudaError_t e;
   LaunchScope scope(h, tag, s);
   if (v == DEC_VARIANT_SMALL_M) {
@@ -572,7 +580,7 @@ static dec_status linear_entry(dec_handle* h, const dec_bf16* x, int ldx, const 
   if (!al16(x) || !al16(W) || !al16(out) || (r != nullptr && !al16(r))) return DEC_ERR_INVALID_ARG;
   if (!linear_shape_ok(M, N, K, ldx)) return DEC_ERR_INVALID_ARG;
   EngineRegion eng;
-  if (choose_variant(h, M, K) == DEC_VARIANT_SPLIT_K) {
+  if (choose_variant(h, M, N, K) == DEC_VARIANT_SPLIT_K) {
     size_t need = 0;
     dec_linear_workspace_size(h, M, N, K, &need);
     if (ws == nullptr || !al16(ws) || ws_bytes < need) return DEC_ERR_INVALID_ARG;
@@ -720,7 +728,7 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
 
   // One token with the small-matrix kernel: the first RMSNorm runs inside the
   // input projection (same arithmetic, one launch fewer).
-  const bool fuse_norm1 = M == 1 && choose_variant(h, M, H) == DEC_VARIANT_SMALL_M;
+  const bool fuse_norm1 = M == 1 && choose_variant(h, M, L.N_in, H) == DEC_VARIANT_SMALL_M;
   if (!fuse_norm1) {
     LaunchScope scope(h, "rmsnorm1", s);
     if (launch_rmsnorm(h, hidden, L.gamma1, w.a, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;

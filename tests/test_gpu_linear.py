@@ -123,8 +123,22 @@ def test_input_projection_batch_sweep(h, w_in, M):
     x = synth.bf16_rows(synth.X_BASE, range(M), 7168, SEED)
     Wd = dev_bf16(w_in, (12288, 7168))
     y = ML.dec_linear(h, dev_bf16(x, (M, 7168)), Wd)
-    assert h.last_variant == (ML.VARIANT_SMALL_M if M == 1 else ML.VARIANT_SPLIT_K)
+    # automatic choice: the small-matrix kernel up to two tokens (a 176 MB matrix), split-K above
+    assert h.last_variant == (ML.VARIANT_SMALL_M if M <= 2 else ML.VARIANT_SPLIT_K)
     assert_bf16_close(host_bits(y), oracle.linear(x, w_in), f"in-proj M={M}")
+
+
+def test_automatic_choice_by_size(h):
+    """Up to four tokens a matrix of at most 48 MB stays on the small-matrix
+    kernel (the split-K kernel's per-launch cost outweighs its rate there)."""
+    import moe_layers_gb300 as ML
+    for (M, N, K, want) in [(3, 1536, 7168, ML.VARIANT_SMALL_M), (4, 7168, 1024, ML.VARIANT_SMALL_M),
+                            (3, 7168, 8192, ML.VARIANT_SPLIT_K), (5, 1536, 7168, ML.VARIANT_SPLIT_K)]:
+        x = synth.bf16(M * K, SEED, 950 + M, 0, 1.0).reshape(M, K)
+        W = synth.bf16(N * K, SEED, 951, 0, 0.02).reshape(N, K)
+        y = ML.dec_linear(h, dev_bf16(x, (M, K)), dev_bf16(W, (N, K)))
+        assert h.last_variant == want, (M, N, K)
+        assert_bf16_close(host_bits(y), oracle.linear(x, W), f"auto M={M} N={N} K={K}")
 
 
 @pytest.mark.parametrize("M", [1, 4, 16, 64])

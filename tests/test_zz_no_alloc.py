@@ -25,7 +25,9 @@ def test_no_alloc_entry_point_matches_workspace_entry_point():
     assert torch.cuda.is_available()
     ML.build()
     with ML.Handle(0) as h:
-        cases = [(8, 1000, 520, False), (3, 4096, 4096, True)]  # two calls in a row, second with a residual
+        # two calls in a row, second with a residual; both shapes are split-K shapes under the
+        # automatic choice (batch 8; batch 3 with a 67 MB matrix)
+        cases = [(8, 1000, 520, False), (3, 4096, 8192, True)]
         for i, (M, N, K, resid) in enumerate(cases):
             x = synth.bf16(M * K, SEED, 9100 + i, 0, 1.0).reshape(M, K)
             W = synth.bf16(N * K, SEED, 9110 + i, 0, 0.02).reshape(N, K)
