@@ -188,6 +188,22 @@ bool experts_small(const dec_handle* h, int M, int H, int I) {
   return M == 1 && h->force_variant != DEC_VARIANT_SPLIT_K && gemv_moe_supported(H) && gemv_moe_supported(I);
 }
 
+// A few tokens: the small-matrix kernels over one problem per (token, expert)
+// entry (an expert chosen by several tokens is read once per entry), unless
+// the split-K family is forced. Measured on GB300 (layer step, graph replay):
+// at two tokens with 2048-wide expert rows 296.7 us against 311.8 on the
+// split-K family; at four tokens 545.8 against 523.9 (6% more expert bytes,
+// the shared down projection read once per token); with the narrow rows of
+// the tensor-parallel shard shapes slower at two and four tokens (the grouped
+// down projection has no narrow-row form). So: two tokens, wide rows; with
+// the small-matrix family forced, two to four tokens at any width.
+bool experts_few(const dec_handle* h, int M, int k, int E, int H, int I) {
+  if (M < 2 || M > 4 || !gemv_moe_supported(H) || !gemv_moe_supported(I) || !route_shared_supported(h, M, H, E, k))
+    return false;
+  if (h->force_variant == DEC_VARIANT_SMALL_M) return true;
+  return h->force_variant == DEC_VARIANT_AUTO && M == 2 && I >= 2048;
+}
+
 // SM shares of the shared and the routed experts ("the schedule controls how
 // many GPU resources each op uses", Kimi K3 article, Part 1 §3).
 //  - automatic (h->shared_ctas == 0, default): the shared expert keeps its
@@ -312,6 +328,38 @@ dec_status moe_small(dec_handle* h, const uint16_t* x, long long ldx, const floa
   {
     LaunchScope scope(h, "combine", s);
     DEC_CUDA(launch_combine(h, ws.y, ws.table, w, 1, k, E, has_shared ? ws.ys : nullptr, residual, out, H, s));
+  }
+  return DEC_OK;
+}
+
+// Two to four tokens after the routing launch (route_shared: entry table,
+// normalised rows x [M][H], and the shared expert's h_s [M][I] when there is
+// one): gate/up over the M k entries (each reads its token's row), down over
+// the shared expert applied to the M rows of h_s plus the entries, then the
+// weighted combine with the shared output and the residual.
+dec_status moe_few(dec_handle* h, int M, const uint16_t* x, const float* w, int k, const uint16_t* Wg,
+                   const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I, const uint16_t* Wd_s,
+                   const uint16_t* residual, uint16_t* out, const MoeWs& ws, cudaStream_t s) {
+  const int n = M * k;
+  h->last_expert_variant = DEC_VARIANT_SMALL_M;
+  {
+    // late trigger: the next routing launch reuses this launch's predecessor's row queue
+    LaunchScope scope(h, "gate_up", s);
+    DEC_CUDA(launch_gemv_moe(h, true, Wg, Wu, I, I, H, x, H, ws.table, E, n, ws.hbuf, I, h->sms, s, nullptr, n,
+                             true, true));
+  }
+  GemvMoeShared sdn{Wd_s, nullptr, ws.hs, ws.ys};
+  sdn.n = M;
+  sdn.ldx = I;
+  sdn.ldo = H;
+  {
+    LaunchScope scope(h, "down", s);
+    DEC_CUDA(launch_gemv_moe(h, false, Wd, nullptr, H, H, I, ws.hbuf, I, ws.table, E, n, ws.y, H, h->sms, s,
+                             Wd_s != nullptr ? &sdn : nullptr, n, false, false));
+  }
+  {
+    LaunchScope scope(h, "combine", s);
+    DEC_CUDA(launch_combine(h, ws.y, ws.table, w, M, k, E, Wd_s != nullptr ? ws.ys : nullptr, residual, out, H, s));
   }
   return DEC_OK;
 }
@@ -743,7 +791,8 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   // the top-k and the routing table are one launch (router_select), and the
   // experts read the normalised row for every slot (no gather).
   const bool one_token = experts_small(h, M, H, L.I);
-  if (!one_token) {
+  const bool few_tokens = !one_token && experts_few(h, M, L.k, L.E, H, L.I);
+  if (!one_token && !few_tokens) {
     LaunchScope scope(h, "rmsnorm2", s);
     if (launch_rmsnorm(h, h1, L.gamma2, w.b, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
   }
@@ -774,18 +823,31 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   if (one_token) {
     // With a shared expert the routing launch also streams its gate/up.
     const bool fuse_shared = L.Wg_s != nullptr && h->fuse_shared_routing &&
-                             route_shared_supported(h, H, L.E, L.k);
+                             route_shared_supported(h, 1, H, L.E, L.k);
     {
       LaunchScope scope(h, "router", s);
       if (fuse_shared)
-        DEC_CUDA(launch_route_shared(h, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx, wt,
-                                     scores, w.moe.table, L.Wg_s, L.Wu_s, L.I, w.moe.hs, s));
+        DEC_CUDA(launch_route_shared(h, 1, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx,
+                                     wt, scores, w.moe.table, L.Wg_s, L.Wu_s, L.I, w.moe.hs, s));
       else
         DEC_CUDA(launch_router_select(h, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx,
                                       wt, scores, w.moe.table, s));
     }
     st = moe_small(h, w.b, 0, wt, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, h1, hidden, w.moe, s,
                    fuse_shared);
+    if (st != DEC_OK) return st;
+    if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
+    return DEC_OK;
+  }
+  if (few_tokens) {
+    // Two to four tokens: the second RMSNorm, router, top-k, routing table (one
+    // problem per entry) and the shared expert's gate/up in one launch.
+    {
+      LaunchScope scope(h, "router", s);
+      DEC_CUDA(launch_route_shared(h, M, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx,
+                                   wt, scores, w.moe.table, L.Wg_s, L.Wu_s, L.Wg_s ? L.I : 0, w.moe.hs, s));
+    }
+    st = moe_few(h, M, w.b, wt, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wd_s, h1, hidden, w.moe, s);
     if (st != DEC_OK) return st;
     if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
     return DEC_OK;

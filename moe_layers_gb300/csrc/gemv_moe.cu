@@ -29,12 +29,15 @@ namespace dec {
 constexpr int kGmThreads = 256;
 
 struct GemvMoeParams {
-  // Optional extra problem 0: a dense expert (the shared expert) with its own
-  // weights, activation row and output row; routed problems follow it.
+  // Optional leading dense problems 0 .. ns-1: one dense expert (the shared
+  // expert) applied to ns activation rows (sx + p * sldx -> sout + p * sldo);
+  // the routed problems follow them.
   const uint16_t* sA;
   const uint16_t* sA2;
   const uint16_t* sx;
   void* sout;
+  int ns;
+  long long sldx, sldo;
   const uint16_t* A;   // first weight matrix (gate or down), row-major [rows][K]
   const uint16_t* A2;  // up matrix (SwiGLU) or unused
   long long rows_per_prob_bank;  // row distance between experts in the bank (0: one dense problem)
@@ -46,6 +49,7 @@ struct GemvMoeParams {
   int E, n_entries;
   void* out;           // SwiGLU: bf16 [slots][ldo]; down: fp32 [slots][ldo]
   long long ldo;
+  int x_by_token;      // routed activation row: the slot's token (x + token * ldx), else the slot's own row
   int nprob_known;     // routed problems if known at launch (one token: k), else 0
   int ahead;           // weight bytes per CTA requested into L2 ahead of the register loads (0: none)
   int late_trigger;    // trigger dependents after the dependency wait (they may then read the routing early)
@@ -63,15 +67,16 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_kernel(const GemvMoePa
 
   // Problem bookkeeping (the routed table is read only after the dependency wait).
   const TableLayout L(P.E, P.n_entries);
-  const int ns = P.sA != nullptr ? 1 : 0;  // leading dense problem
+  const int ns = P.sA != nullptr ? P.ns : 0;  // leading dense problems
   auto nprob = [&]() -> long long { return (P.table ? ld_act_s32(P.table + L.U()) : 1) + ns; };
   // Problem p: -1 marks the leading dense problem; otherwise the expert id.
   auto expert_of = [&](int p) -> long long {
     if (p < ns) return -1;
     return P.table ? ld_act_s32(P.table + L.expert() + (p - ns)) : 0;
   };
+  // Problem p's row: for a dense problem its index, for a routed one its slot.
   auto slot_of = [&](int p) -> long long {
-    if (p < ns) return 0;
+    if (p < ns) return p;
     return P.table ? ld_act_s32(P.table + L.offset() + (p - ns)) : 0;
   };
 
@@ -143,7 +148,8 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_kernel(const GemvMoePa
   uint4 xr[VPT];
   long long slot = slot_of(p);
   auto load_x = [&]() {
-    const uint16_t* xrow = e < 0 ? P.sx : P.x + slot * P.ldx;
+    const long long xr_row = (e >= 0 && P.x_by_token && P.table) ? ld_act_s32(P.table + L.slot_token() + slot) : slot;
+    const uint16_t* xrow = e < 0 ? P.sx + slot * P.sldx : P.x + xr_row * P.ldx;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int v = t + kGmThreads * i;
@@ -208,7 +214,7 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_kernel(const GemvMoePa
         if (SWIGLU) up += red[buf][w][t * NR + 1];
       }
       void* dst = e < 0 ? P.sout : P.out;
-      const long long o = (e < 0 ? 0 : slot * P.ldo) + r + t;
+      const long long o = slot * (e < 0 ? P.sldo : P.ldo) + r + t;
       if (SWIGLU)
         reinterpret_cast<uint16_t*>(dst)[o] = f2bf(g / (1.0f + expf(-g)) * up);
       else
@@ -509,13 +515,18 @@ static cudaError_t launch_mode(dec_handle* h, const GemvMoeParams& P, int grid, 
 cudaError_t launch_gemv_moe(dec_handle* h, bool swiglu, const uint16_t* A, const uint16_t* A2,
                             long long rows_per_prob_bank, int R, int K, const uint16_t* x, long long ldx,
                             const int* table, int E, int n_entries, void* out, long long ldo, int sms,
-                            cudaStream_t s, const GemvMoeShared* shared, int nprob_known, bool late_trigger) {
+                            cudaStream_t s, const GemvMoeShared* shared, int nprob_known, bool late_trigger,
+                            bool x_by_token) {
   if (!gemv_moe_supported(K)) return cudaErrorInvalidValue;
   GemvMoeParams P;
   P.sA = shared ? shared->A : nullptr;
   P.sA2 = shared ? (shared->A2 ? shared->A2 : shared->A) : nullptr;
   P.sx = shared ? shared->x : nullptr;
   P.sout = shared ? shared->out : nullptr;
+  P.ns = shared ? std::max(1, shared->n) : 0;
+  P.sldx = shared ? shared->ldx : 0;
+  P.sldo = shared ? shared->ldo : 0;
+  P.x_by_token = x_by_token ? 1 : 0;
   P.A = A;
   P.A2 = A2 ? A2 : A;
   P.rows_per_prob_bank = rows_per_prob_bank;

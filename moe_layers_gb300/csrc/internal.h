@@ -101,17 +101,21 @@ bool gemv_supported(int M, int K);
 // table, or one dense expert when table is null.
 // A dense expert processed as problem 0 of the same launch (the shared
 // expert at batch 1): its weights, its activation row and its output row.
+// The shared expert as the leading dense problem(s) of a grouped launch: n
+// activation rows x + t * ldx, outputs out + t * ldo.
 struct GemvMoeShared {
   const uint16_t* A;
   const uint16_t* A2;
   const uint16_t* x;
   void* out;
+  int n = 1;
+  long long ldx = 0, ldo = 0;
 };
 cudaError_t launch_gemv_moe(dec_handle* h, bool swiglu, const uint16_t* A, const uint16_t* A2,
                             long long rows_per_prob_bank, int R, int K, const uint16_t* x, long long ldx,
                             const int* table, int E, int n_entries, void* out, long long ldo, int sms,
                             cudaStream_t s, const GemvMoeShared* shared = nullptr, int nprob_known = 0,
-                            bool late_trigger = false);
+                            bool late_trigger = false, bool x_by_token = false);
 bool gemv_moe_supported(int K);
 // One token: down projection of the k routed (+ shared) experts fused with the
 // weighted combine and the residual, written straight to out (bf16 [H]).
@@ -136,11 +140,13 @@ cudaError_t launch_router_select(dec_handle* h, const uint16_t* x, const uint16_
 // One token: the routing table with entry j as problem j on slot j (expert idx[j]).
 // One token: launch_router_select's work plus the shared expert's gate/up
 // (h_s = bf16(silu(W_g,s b) * (W_u,s b))) streamed by the same CTAs; ctr: 3 ints, zero on entry and on return.
-bool route_shared_supported(const dec_handle* h, int H, int E, int k);
-cudaError_t launch_route_shared(dec_handle* h, const uint16_t* h1, const uint16_t* gamma, float eps, const float* Wr,
-                                int H, int E, int k, uint16_t* xn, float* parts, int* ctr, int32_t* idx, float* w,
-                                float* scores, int* table, const uint16_t* Wg_s, const uint16_t* Wu_s, int I,
-                                uint16_t* hs, cudaStream_t s);
+// M = 2..4 tokens: the same with one routing-table problem per (token, expert) entry (U = M k,
+// slot p = t k + j), h_s [M][I] and xn [M][H]; without a shared expert (Wg_s null) routing only.
+bool route_shared_supported(const dec_handle* h, int M, int H, int E, int k);
+cudaError_t launch_route_shared(dec_handle* h, int M, const uint16_t* h1, const uint16_t* gamma, float eps,
+                                const float* Wr, int H, int E, int k, uint16_t* xn, float* parts, int* ctr,
+                                int32_t* idx, float* w, float* scores, int* table, const uint16_t* Wg_s,
+                                const uint16_t* Wu_s, int I, uint16_t* hs, cudaStream_t s);
 cudaError_t launch_one_token_table(dec_handle* h, const int32_t* idx, int E, int k, int* table, cudaStream_t s);
 cudaError_t launch_route_table(dec_handle* h, const int32_t* idx, int M, int k, int E, const uint16_t* x, int H,
                                int* table, uint16_t* xs, cudaStream_t s);

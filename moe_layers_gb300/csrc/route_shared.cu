@@ -42,6 +42,7 @@ struct RouteSharedParams {
   float eps;
   const float* Wr;        // router weights fp32 [E][H]
   int H, E, k;
+  int M;                  // tokens (the multi-token kernel)
   int nunits;             // ceil(E / 8) * ceil(H / 1024)
   uint16_t* xn;           // normalised row out [H]
   float* parts;           // logit pieces [ceil(H / 1024)][E]
@@ -254,6 +255,236 @@ __global__ void __launch_bounds__(kThreads, 2) route_shared_kernel(const RouteSh
   }
 }
 
+// M = 2 .. MT tokens: the same launch for a few tokens. Every CTA
+// normalises the M rows (two passes over them: sums of squares, then the
+// normalised rows into shared memory; CTA 0 writes them out), adds its router
+// units' logit pieces for every token, and arrives; in the last CTA warp t
+// takes token t's top-k (warp_topk) and writes its k entries of the routing
+// table (one problem per (token, expert) entry). The shared expert's gate/up
+// rows stream from the queue meanwhile, each row pair applied to the M rows
+// held in shared memory.
+template <int J, int VPT, int MT>
+__global__ void __launch_bounds__(kThreads, 2) route_shared_multi_kernel(const RouteSharedParams P) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int H = P.H, H8 = H >> 3, M = P.M;
+  const int ngrp = (P.E + 7) / 8;
+  const int ksplit = (H + kUnitCols - 1) / kUnitCols;
+  extern __shared__ __align__(16) uint16_t sx[];  // the normalised rows [MT][H]
+  __shared__ float s_norm[kThreads / 32][MT];
+  __shared__ float red[2][kThreads / 32][2 * MT];
+  __shared__ int s_row[2];
+  __shared__ int s_next[2];
+  __shared__ int s_last;
+  const uint64_t pol = policy_evict_first();
+  pdl_trigger();
+
+  float4 wv[kUnitCols / 128];
+  auto load_unit = [&](int u) {
+    const int e = (u % ngrp) * 8 + warp, k0 = (u / ngrp) * kUnitCols;
+    const int kn = min(kUnitCols, H - k0);
+#pragma unroll
+    for (int i = 0; i < kUnitCols / 128; ++i) {
+      const int kk = 4 * (lane + 32 * i);
+      wv[i] = (u < P.nunits && e < P.E && kk < kn)
+                  ? __ldg(reinterpret_cast<const float4*>(P.Wr + (size_t)e * H + k0 + kk))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  load_unit(c);
+  const bool has_shared = P.Wg != nullptr && P.I > 0;
+  int base = 0;
+  if (t == 0 && has_shared) {
+    base = atomicAdd(&P.ctr[1], 3);
+    for (int q = 0; q < 3; ++q)
+      if (base + q < P.I) {
+        request_l2(P.Wg + (size_t)(base + q) * H, (size_t)H * 2);
+        request_l2(P.Wu + (size_t)(base + q) * H, (size_t)H * 2);
+      }
+  }
+  uint4 gv[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = t + kThreads * i;
+    gv[i] = v < H8 ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+  }
+  pdl_wait();
+
+  // RMSNorm of the M rows (each row's sum of squares in the RMSNorm kernel's order)
+  {
+    float ss[MT];
+#pragma unroll
+    for (int q = 0; q < MT; ++q) {
+      ss[q] = 0.f;
+      if (q < M) {
+        uint4 hv[VPT];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = t + kThreads * i;
+          hv[i] = v < H8 ? ld_act16(P.h1 + (size_t)q * H + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < VPT; ++i)
+          if (t + kThreads * i < H8) ss[q] = sumsq8(hv[i], ss[q]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss[q] += __shfl_xor_sync(0xffffffffu, ss[q], o);
+      if (lane == 0) s_norm[warp][q] = ss[q];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < MT; ++q) {
+      if (q < M) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) tot += s_norm[w][q];
+        const float r = rsqrtf(tot / (float)H + P.eps);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = t + kThreads * i;
+          if (v < H8) {
+            const uint4 y = norm8(ld_act16(P.h1 + (size_t)q * H + (size_t)v * 8), gv[i], r);
+            *reinterpret_cast<uint4*>(&sx[(size_t)q * H + v * 8]) = y;
+            if (c == 0) *reinterpret_cast<uint4*>(P.xn + (size_t)q * H + (size_t)v * 8) = y;
+          }
+        }
+      }
+    }
+  }
+  int pending = base + 2;  // (thread 0)
+  __syncthreads();
+
+  // router logit pieces of this CTA's units for every token, then the hand-off
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int u = c + m * G;
+    if (m == 1 && u < P.nunits) load_unit(u);
+    if (u < P.nunits) {
+      const int e = (u % ngrp) * 8 + warp, ks = u / ngrp, k0 = ks * kUnitCols;
+      const int kn = min(kUnitCols, H - k0);
+      float acc[MT];
+#pragma unroll
+      for (int q = 0; q < MT; ++q) acc[q] = 0.f;
+#pragma unroll
+      for (int i = 0; i < kUnitCols / 128; ++i) {
+        const int kk = 4 * (lane + 32 * i);
+        if (kk < kn) {
+#pragma unroll
+          for (int q = 0; q < MT; ++q) {
+            if (q < M) {
+              const uint2 xv = *reinterpret_cast<const uint2*>(&sx[(size_t)q * H + k0 + kk]);
+              float a = acc[q];
+              a = fmaf(wv[i].x, bf_lo(xv.x), a);
+              a = fmaf(wv[i].y, bf_hi(xv.x), a);
+              a = fmaf(wv[i].z, bf_lo(xv.y), a);
+              a = fmaf(wv[i].w, bf_hi(xv.y), a);
+              acc[q] = a;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < MT; ++q) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+        if (lane == 0 && e < P.E && q < M) P.parts[((size_t)ks * M + q) * P.E + e] = acc[q];
+      }
+    }
+  }
+  if (t == 0) {
+    s_row[0] = has_shared ? base : P.I;
+    s_row[1] = has_shared ? base + 1 : P.I;
+  }
+  __syncthreads();
+  if (t == 0) s_last = atom_add_acq_rel_gpu(&P.ctr[0], 1) == G - 1;
+  __syncthreads();
+  if (s_last) {
+    if (warp < M) {
+      int se = 0;
+      float sw = 0.f;
+      warp_topk<8 * J>(P.parts, ksplit, M, warp, P.E, P.k, P.idx, P.w, P.scores, &se, &sw);
+      write_entry_table(P.table, P.E, M, P.k, warp, se);
+    }
+    if (t == 0) P.ctr[0] = 0;  // leave the workspace reusable
+  }
+
+  // shared-expert gate/up rows from the queue, each applied to the M rows
+  if (!has_shared) return;
+  uint4 wa[2][VPT], wb[2][VPT];
+  auto load = [&](uint4(&wr)[2][VPT], int row) {
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = t + kThreads * i;
+        wr[a][i] = v < H8 ? ld_stream((a == 0 ? P.Wg : P.Wu) + (size_t)row * H + (size_t)v * 8, pol)
+                          : make_uint4(0, 0, 0, 0);
+      }
+  };
+  int cur = s_row[0], nxt = s_row[1];
+  if (cur < P.I) load(wa, cur);
+  int buf = 0;
+  while (cur < P.I) {
+    if (nxt < P.I) load(wb, nxt);
+    float g[MT], up[MT];
+#pragma unroll
+    for (int q = 0; q < MT; ++q) {
+      g[q] = 0.f;
+      up[q] = 0.f;
+      if (q < M) {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = t + kThreads * i;
+          if (v < H8) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(&sx[(size_t)q * H + v * 8]);
+            g[q] = dot8(wa[0][i], xv, g[q]);
+            up[q] = dot8(wa[1][i], xv, up[q]);
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        g[q] += __shfl_xor_sync(0xffffffffu, g[q], o);
+        up[q] += __shfl_xor_sync(0xffffffffu, up[q], o);
+      }
+      if (lane == 0) {
+        red[buf][warp][2 * q] = g[q];
+        red[buf][warp][2 * q + 1] = up[q];
+      }
+    }
+    if (t == 0) {
+      s_next[buf] = pending;
+      if (pending < P.I) {
+        request_l2(P.Wg + (size_t)pending * H, (size_t)H * 2);
+        request_l2(P.Wu + (size_t)pending * H, (size_t)H * 2);
+        pending = atomicAdd(&P.ctr[1], 1);
+      }
+    }
+    __syncthreads();
+    if (t < M) {
+      float gs = 0.f, us = 0.f;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) {
+        gs += red[buf][w][2 * t];
+        us += red[buf][w][2 * t + 1];
+      }
+      P.hs[(size_t)t * P.I + cur] = f2bf(gs / (1.0f + expf(-gs)) * us);
+    }
+    const int nn = s_next[buf];
+    cur = nxt;
+    nxt = nn;
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) wa[a][i] = wb[a][i];
+    buf ^= 1;
+  }
+  if (t == 0 && atom_add_acq_rel_gpu(&P.ctr[2], 1) == G - 1) {
+    P.ctr[1] = 0;
+    P.ctr[2] = 0;
+  }
+}
+
 template <int J>
 cudaError_t launch_j(dec_handle* h, const RouteSharedParams& P, int vpt, cudaStream_t s) {
   const dim3 g(2 * h->sms), b(kThreads);
@@ -263,22 +494,41 @@ cudaError_t launch_j(dec_handle* h, const RouteSharedParams& P, int vpt, cudaStr
   return launch_k(h, route_shared_kernel<J, 4>, g, b, smem, s, P);
 }
 
+template <int J, int MT>
+cudaError_t launch_multi(dec_handle* h, const RouteSharedParams& P, int vpt, cudaStream_t s) {
+  const dim3 g(2 * h->sms), b(kThreads);
+  const size_t smem = (size_t)MT * P.H * sizeof(uint16_t);
+  auto go = [&](auto kern) -> cudaError_t {
+    if (smem > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    return launch_k(h, kern, g, b, smem, s, P);
+  };
+  if (vpt == 1) return go(route_shared_multi_kernel<J, 1, MT>);
+  if (vpt == 2) return go(route_shared_multi_kernel<J, 2, MT>);
+  return go(route_shared_multi_kernel<J, 4, MT>);
+}
+
 }  // namespace
 
 // Rows of up to 8192 elements (four vectors per thread); E up to 1024; at
-// most two router units per CTA.
-bool route_shared_supported(const dec_handle* h, int H, int E, int k) {
+// most two router units per CTA; up to 4 tokens (their normalised rows in
+// shared memory, two CTAs per SM).
+bool route_shared_supported(const dec_handle* h, int M, int H, int E, int k) {
   const long long units = (long long)((E + 7) / 8) * ((H + kUnitCols - 1) / kUnitCols);
-  return H >= 8 && H % 8 == 0 && H <= 8 * 4 * kThreads && E >= 1 && E <= 1024 && k >= 1 && k <= 16 && k <= E &&
-         units <= 2LL * 2 * h->sms;
+  return M >= 1 && M <= 4 && H >= 8 && H % 8 == 0 && H <= 8 * 4 * kThreads && E >= 1 && E <= 1024 && k >= 1 &&
+         k <= 16 && k <= E && units <= 2LL * 2 * h->sms && (size_t)(M <= 1 ? 1 : (M <= 2 ? 2 : 4)) * H * 2 <= 100000;
 }
 
-cudaError_t launch_route_shared(dec_handle* h, const uint16_t* h1, const uint16_t* gamma, float eps, const float* Wr,
-                                int H, int E, int k, uint16_t* xn, float* parts, int* ctr, int32_t* idx, float* w,
-                                float* scores, int* table, const uint16_t* Wg_s, const uint16_t* Wu_s, int I,
-                                uint16_t* hs, cudaStream_t s) {
-  if (!route_shared_supported(h, H, E, k)) return cudaErrorInvalidValue;
+cudaError_t launch_route_shared(dec_handle* h, int M, const uint16_t* h1, const uint16_t* gamma, float eps,
+                                const float* Wr, int H, int E, int k, uint16_t* xn, float* parts, int* ctr,
+                                int32_t* idx, float* w, float* scores, int* table, const uint16_t* Wg_s,
+                                const uint16_t* Wu_s, int I, uint16_t* hs, cudaStream_t s) {
+  if (!route_shared_supported(h, M, H, E, k)) return cudaErrorInvalidValue;
+  if (M == 1 && Wg_s == nullptr) return cudaErrorInvalidValue;  // (one token without a shared expert: router_select)
   RouteSharedParams P;
+  P.M = M;
   P.h1 = h1;
   P.gamma = gamma;
   P.eps = eps;
@@ -300,9 +550,19 @@ cudaError_t launch_route_shared(dec_handle* h, const uint16_t* h1, const uint16_
   P.hs = hs;
   const int H8 = H / 8, vpt = H8 <= kThreads ? 1 : (H8 <= 2 * kThreads ? 2 : 4);
   const int Ew = (E + 7) / 8;
-  if (Ew <= 32) return launch_j<1>(h, P, vpt, s);
-  if (Ew <= 64) return launch_j<2>(h, P, vpt, s);
-  return launch_j<4>(h, P, vpt, s);
+  if (M == 1) {
+    if (Ew <= 32) return launch_j<1>(h, P, vpt, s);
+    if (Ew <= 64) return launch_j<2>(h, P, vpt, s);
+    return launch_j<4>(h, P, vpt, s);
+  }
+  if (M == 2) {
+    if (Ew <= 32) return launch_multi<1, 2>(h, P, vpt, s);
+    if (Ew <= 64) return launch_multi<2, 2>(h, P, vpt, s);
+    return launch_multi<4, 2>(h, P, vpt, s);
+  }
+  if (Ew <= 32) return launch_multi<1, 4>(h, P, vpt, s);
+  if (Ew <= 64) return launch_multi<2, 4>(h, P, vpt, s);
+  return launch_multi<4, 4>(h, P, vpt, s);
 }
 
 }  // namespace dec

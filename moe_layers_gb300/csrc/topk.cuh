@@ -141,3 +141,94 @@ __device__ __forceinline__ void write_one_token_table(int* table, int E, int k, 
 }
 
 }  // namespace dec
+
+namespace dec {
+
+// Top-k of token t by one warp (up to 8 tokens of a CTA in parallel). Lane l
+// holds the experts l, l + 32, ... (JW >= E / 32 per lane). logits = sum of
+// the split partials in split order (read at L2: other CTAs wrote them),
+// s = 1 / (1 + exp(-logit)), k rounds of warp arg-max (score descending,
+// expert id ascending), weights = selected scores over their sum: the rule
+// and arithmetic of block_topk. On return lane r < k holds the r-th selection
+// in *sel_e, *sel_w (idx, w, scores are written here).
+template <int JW>
+__device__ __forceinline__ void warp_topk(const float* parts, int ks, int M, int t, int E, int k, int32_t* idx,
+                                          float* w, float* scores, int* sel_e, float* sel_w) {
+  const int lane = threadIdx.x & 31;
+  float sv[JW];
+  int ev[JW];
+#pragma unroll
+  for (int i = 0; i < JW; ++i) {
+    ev[i] = lane + 32 * i;
+    sv[i] = 0.f;
+  }
+  for (int s = 0; s < ks; ++s) {
+#pragma unroll
+    for (int i = 0; i < JW; ++i)
+      if (ev[i] < E) sv[i] += __ldcg(parts + ((size_t)s * M + t) * E + ev[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < JW; ++i) {
+    if (ev[i] < E) {
+      sv[i] = 1.0f / (1.0f + expf(-sv[i]));
+      if (scores != nullptr) scores[(size_t)t * E + ev[i]] = sv[i];
+    } else {
+      sv[i] = -FLT_MAX;
+      ev[i] = INT_MAX;
+    }
+  }
+  float fv = 0.f;
+  int fi = 0;
+  for (int r = 0; r < k; ++r) {
+    float bv = -FLT_MAX;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < JW; ++i)
+      if (sv[i] > bv || (sv[i] == bv && ev[i] < bi)) {
+        bv = sv[i];
+        bi = ev[i];
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < JW; ++i)
+      if (ev[i] == bi) sv[i] = -FLT_MAX;  // ids are unique: only the owner matches
+    if (lane == r) {
+      fv = bv;
+      fi = bi;
+    }
+  }
+  float sum = 0.f;
+  for (int r = 0; r < k; ++r) sum += __shfl_sync(0xffffffffu, fv, r);
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = fi;
+    w[(size_t)t * k + lane] = fv / sum;
+  }
+  *sel_e = fi;
+  *sel_w = fv / sum;
+}
+
+// M tokens: the routing table with entry p = t * k + j as problem p on slot p
+// (expert idx[t][j], token t), U = M * k. Called by warp t for its token.
+__device__ __forceinline__ void write_entry_table(int* table, int E, int M, int k, int t, int sel_e) {
+  const int lane = threadIdx.x & 31;
+  const TableLayout L(E, M * k);
+  if (lane < k) {
+    const int p = t * k + lane;
+    table[L.expert() + p] = sel_e;
+    table[L.offset() + p] = p;
+    table[L.count() + p] = 1;
+    table[L.slot_token() + p] = t;
+    table[L.entry_slot() + p] = p;
+  }
+  if (t == 0 && lane == 0) table[L.U()] = M * k;
+}
+
+}  // namespace dec

@@ -168,6 +168,39 @@ def test_layer_one_token_two_router_units(h):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("M", [2, 3, 4])
+@pytest.mark.parametrize("I,shared", [(128, True), (256, False), (256, True)])
+def test_layer_few_tokens(h, M, I, shared):
+    """Two to four tokens on the small-matrix family (forced): one routing
+    launch (second RMSNorm, router, warp-per-token top-k, a routing table with
+    one problem per (token, expert) entry, and the shared expert's gate/up),
+    gate/up over the entries, down over the shared expert's M rows plus the
+    entries, then the combine."""
+    import moe_layers_gb300 as ML
+    H, N_in, K_out, E, k = 1152, 264, 256, 40, 8
+    L = Layer(H, N_in, K_out, E, I, k, base=6800 + I + M)
+    n = E * I * H
+    g = synth.bf16(n, SEED, 6810, 0, 0.05).reshape(E, I, H)
+    u = synth.bf16(n, SEED, 6811, 0, 0.05).reshape(E, I, H)
+    d = synth.bf16(n, SEED, 6812, 0, 0.05).reshape(E, H, I)
+    sh = None
+    if shared:
+        sh = (synth.bf16(I * H, SEED, 6813, 0, 0.05).reshape(I, H), synth.bf16(I * H, SEED, 6814, 0, 0.05).reshape(I, H),
+              synth.bf16(H * I, SEED, 6815, 0, 0.05).reshape(H, I))
+    dev_w = L.device(dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
+                     None if sh is None else tuple(dev_bf16(a, a.shape) for a in sh))
+    h.set_force_variant(ML.VARIANT_SMALL_M)
+    try:
+        for rep in range(2):  # the counters must be back at zero after every call
+            hbits, _ = gap_rows(L.scores, M, H, k, base=6900 + 10 * M + I + rep)
+            hid, tr = _run(h, L, dev_w, hbits)
+            assert h.last_expert_variant == ML.VARIANT_SMALL_M
+            ref = L.oracle(hbits, lambda e: (g[e], u[e], d[e]), sh)
+            _check_layer(tr, hid, ref, slice(None), f"layer few tokens M={M} I={I} rep={rep}", L)
+    finally:
+        h.set_force_variant(ML.VARIANT_AUTO)
+
+
 def _check_layer(tr, hid, ref, rows, what, L=None):
     assert np.array_equal(tr["idx"].cpu().numpy()[rows], ref["idx"]), what + ": top-k indices"
     h1g = oracle.bf16_to_f64(host_bits(tr["h1"])[rows])

@@ -37,6 +37,8 @@ def small_layer():
 
 
 def _defaults(h):
+    import moe_layers_gb300 as ML
+    h.set_force_variant(ML.VARIANT_AUTO)
     h.set_shared_sms(0)
     h.set_pdl(True)
     h.set_l2_ahead(49152)
@@ -54,10 +56,12 @@ SETTINGS = {
     "shared_fixed_4": {"shared_sms": 4},
     "prefetch_shared": {"prefetch_shared": True},
     "prefetch_next": {"prefetch_next": True},
+    "split_k_family": {"force": "split_k"},
+    "small_m_family": {"force": "small_m"},
 }
 
 
-@pytest.mark.parametrize("M", [1, 3])
+@pytest.mark.parametrize("M", [1, 3, 8])
 @pytest.mark.parametrize("name", list(SETTINGS))
 def test_layer_settings_change_schedule_not_result(h, small_layer, M, name):
     import moe_layers_gb300 as ML
@@ -79,6 +83,12 @@ def test_layer_settings_change_schedule_not_result(h, small_layer, M, name):
             h.set_shared_sms(cfg["shared_sms"])
         if "prefetch_shared" in cfg:
             h.set_prefetch_shared(cfg["prefetch_shared"])
+        if cfg.get("force") == "split_k":
+            h.set_force_variant(ML.VARIANT_SPLIT_K)
+        if cfg.get("force") == "small_m":
+            if M > 4:
+                pytest.skip("the small-matrix family covers up to four tokens")
+            h.set_force_variant(ML.VARIANT_SMALL_M)
         for rep in range(2):
             hbits, _ = gap_rows(L.scores, M, L.H, L.k, base=8100 + 10 * M + rep)
             hid, tr = _run(h, L, dev_w, hbits)
@@ -95,6 +105,8 @@ def test_profiling_reports_every_launch(h, small_layer):
     expect = {
         1: {"in_proj", "out_proj", "router", "gate_up", "down"},
         3: {"rmsnorm1", "in_proj", "out_proj", "rmsnorm2", "router", "topk", "route_table", "gate_up", "down",
+            "shared_gate_up", "shared_down", "combine"},
+        8: {"rmsnorm1", "in_proj", "out_proj", "rmsnorm2", "router", "topk", "route_table", "gate_up", "down",
             "shared_gate_up", "shared_down", "combine"},
     }
     for M, tags in expect.items():
