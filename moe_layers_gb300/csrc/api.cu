@@ -107,8 +107,8 @@ int choose_variant(const dec_handle* h, int M, int N, int K) {
   return DEC_VARIANT_SPLIT_K;
 }
 
-// gamma (small-matrix kernel, one token only): the input row is RMS-normalised
-// inside the projection kernel.
+// gamma (small-matrix kernel): the input rows are RMS-normalised inside the
+// projection kernel.
 dec_status linear_impl(dec_handle* h, const uint16_t* x, int ldx, const uint16_t* W, const uint16_t* r, uint16_t* y,
                        int M, int N, int K, EngineRegion eng, cudaStream_t s, const char* tag = "linear",
                        const uint16_t* gamma = nullptr, float eps = 0.f) {
@@ -774,9 +774,9 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   float* scores = trace ? trace->scores : nullptr;
   const int H = L.H;
 
-  // One token with the small-matrix kernel: the first RMSNorm runs inside the
-  // input projection (same arithmetic, one launch fewer).
-  const bool fuse_norm1 = M == 1 && choose_variant(h, M, L.N_in, H) == DEC_VARIANT_SMALL_M;
+  // Small-matrix input projection (up to four tokens): the first RMSNorm runs
+  // inside it (same arithmetic, one launch fewer).
+  const bool fuse_norm1 = M <= 4 && choose_variant(h, M, L.N_in, H) == DEC_VARIANT_SMALL_M;
   if (!fuse_norm1) {
     LaunchScope scope(h, "rmsnorm1", s);
     if (launch_rmsnorm(h, hidden, L.gamma1, w.a, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;

@@ -77,9 +77,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
     }
   };
   request(r0 + RB + ahead_rows);
-  // Optional RMSNorm of the (single) input row, fused: gains are static weights.
+  // Optional RMSNorm of the input rows, fused: gains are static weights.
   uint4 gv[VPT];
-  if (M == 1 && gamma != nullptr) {
+  if (gamma != nullptr) {
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int v = t + kGemvThreads * i;
@@ -96,26 +96,32 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
       const int v = t + kGemvThreads * i;
       xr[m][i] = (v < K8) ? ld_act16(x + (size_t)m * ldx + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
     }
-  if (M == 1 && gamma != nullptr) {
-    // a = bf16(x / sqrt(mean(x^2) + eps) * gamma), in the reduction order of
-    // the stand-alone RMSNorm kernel (so the result is the same bits).
-    __shared__ float rred[kGemvThreads / 32];
-    float ss = 0.f;
+  if (gamma != nullptr) {
+    // a_m = bf16(x_m / sqrt(mean(x_m^2) + eps) * gamma) for every row m, in
+    // the reduction order of the stand-alone RMSNorm kernel (the same bits).
+    __shared__ float rred[kGemvThreads / 32][M];
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = t + kGemvThreads * i;
-      if (v < K8) ss = sumsq8(xr[0][i], ss);
+    for (int m = 0; m < M; ++m) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = t + kGemvThreads * i;
+        if (v < K8) ss = sumsq8(xr[m][i], ss);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) rred[warp][m] = ss;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) rred[warp] = ss;
     __syncthreads();
-    float tot = 0.f;
 #pragma unroll
-    for (int q = 0; q < kGemvThreads / 32; ++q) tot += rred[q];
-    const float rs = rsqrtf(tot / (float)K + eps);
+    for (int m = 0; m < M; ++m) {
+      float tot = 0.f;
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) xr[0][i] = norm8(xr[0][i], gv[i], rs);
+      for (int q = 0; q < kGemvThreads / 32; ++q) tot += rred[q][m];
+      const float rs = rsqrtf(tot / (float)K + eps);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) xr[m][i] = norm8(xr[m][i], gv[i], rs);
+    }
   }
 
   int buf = 0;
@@ -299,12 +305,11 @@ static cudaError_t gemv_m(dec_handle* h, const uint16_t* x, long long ldx, const
 cudaError_t launch_gemv(dec_handle* h, const uint16_t* x, long long ldx, const uint16_t* W, const uint16_t* res,
                         long long ldr, uint16_t* y, long long ldy, int M, int N, int K, cudaStream_t s,
                         const uint16_t* gamma, float eps) {
-  if (gamma != nullptr && M != 1) return cudaErrorInvalidValue;
   switch (M) {
     case 1: return gemv_m<1>(h, x, ldx, W, res, ldr, y, ldy, N, K, s, gamma, eps);
-    case 2: return gemv_m<2>(h, x, ldx, W, res, ldr, y, ldy, N, K, s, nullptr, 0.f);
-    case 3: return gemv_m<3>(h, x, ldx, W, res, ldr, y, ldy, N, K, s, nullptr, 0.f);
-    case 4: return gemv_m<4>(h, x, ldx, W, res, ldr, y, ldy, N, K, s, nullptr, 0.f);
+    case 2: return gemv_m<2>(h, x, ldx, W, res, ldr, y, ldy, N, K, s, gamma, eps);
+    case 3: return gemv_m<3>(h, x, ldx, W, res, ldr, y, ldy, N, K, s, gamma, eps);
+    case 4: return gemv_m<4>(h, x, ldx, W, res, ldr, y, ldy, N, K, s, gamma, eps);
     default: return cudaErrorInvalidValue;
   }
 }
