@@ -284,6 +284,8 @@ def run_ours(args, rank, local, world):
     if args.l2_ahead is not None:
         h.set_l2_ahead(args.l2_ahead)
     h.set_one_token_shared(args.shared_in_routing)
+    h.set_force_variant({"auto": ML.VARIANT_AUTO, "small_m": ML.VARIANT_SMALL_M,
+                         "split_k": ML.VARIANT_SPLIT_K}[args.family])
     layers = build_weights(dev, layer_copies())
     if args.prefetch_next:
         # Cross-layer prefetch: while layer l routes, the next layer's input
@@ -543,6 +545,8 @@ def main(argv=None):
                          "and report the replay time as the value)")
     ap.add_argument("--shared-sms", type=int, default=0,
                     help="SMs for the shared expert: 0 automatic share (default), -1 every SM overlapped, n fixed")
+    ap.add_argument("--family", choices=("auto", "small_m", "split_k"), default="auto",
+                    help="kernel family (auto: by batch and size; small_m covers batch <= 4)")
     ap.add_argument("--shared-in-routing", type=int, choices=(0, 1), default=1,
                     help="batch 1: shared expert gate/up inside the routing launch (1) or the gate/up launch (0)")
     ap.add_argument("--l2-ahead", type=int, default=None,

@@ -190,18 +190,17 @@ bool experts_small(const dec_handle* h, int M, int H, int I) {
 
 // A few tokens: the small-matrix kernels over one problem per (token, expert)
 // entry (an expert chosen by several tokens is read once per entry), unless
-// the split-K family is forced. Measured on GB300 (layer step, graph replay):
-// at two tokens with 2048-wide expert rows 296.7 us against 311.8 on the
-// split-K family; at four tokens 545.8 against 523.9 (6% more expert bytes,
-// the shared down projection read once per token); with the narrow rows of
-// the tensor-parallel shard shapes slower at two and four tokens (the grouped
-// down projection has no narrow-row form). So: two tokens, wide rows; with
-// the small-matrix family forced, two to four tokens at any width.
+// the split-K family is forced. Measured on GB300 (layer step, graph replay,
+// this path against the split-K experts): at two tokens 297 against 312 us
+// (full shapes), 74 against 77 (TP8 shard shapes), 54 against 67 (TP16); at
+// three and four tokens mixed or slower (up to 6% more expert bytes, the
+// shared down projection read once per token). So: two tokens; with the
+// small-matrix family forced, two to four.
 bool experts_few(const dec_handle* h, int M, int k, int E, int H, int I) {
   if (M < 2 || M > 4 || !gemv_moe_supported(H) || !gemv_moe_supported(I) || !route_shared_supported(h, M, H, E, k))
     return false;
   if (h->force_variant == DEC_VARIANT_SMALL_M) return true;
-  return h->force_variant == DEC_VARIANT_AUTO && M == 2 && I >= 2048;
+  return h->force_variant == DEC_VARIANT_AUTO && M == 2;
 }
 
 // SM shares of the shared and the routed experts ("the schedule controls how

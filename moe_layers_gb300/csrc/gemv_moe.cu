@@ -448,7 +448,11 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_narrow_kernel
   uint4 xr[NP];
 #pragma unroll
   for (int q = 0; q < NP; ++q) xr[q] = j < K8 ? ld_act16(s_xrow[q] + (size_t)j * 8) : make_uint4(0, 0, 0, 0);
-  for (int n = n0 + g; n < n1; n += NG) {
+  // The loop runs the same number of steps in every group (a group past the
+  // CTA's rows computes on its clamped last row and writes nothing), so the
+  // whole-warp shuffles below never meet diverged lanes.
+  for (int nb = n0; nb < n1; nb += NG) {
+    const int n = nb + g;
     if (g == 0) request(n + 2 * NG + ahead_rows);  // (only threads t < NP issue)
     float a = 0.f;
     const int nn = min(n + NG, n1 - 1);
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_narrow_kernel
     }
 #pragma unroll
     for (int o = TPR / 2; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-    if (j == 0) {
+    if (j == 0 && n < n1) {
       if (res != nullptr) a += bf2f(ld_act_u16(res + n));
       out[n] = f2bf(a);
     }
@@ -503,10 +507,132 @@ cudaError_t launch_gemv_down_combine(dec_handle* h, const uint16_t* Wd, long lon
 
 bool gemv_moe_supported(int K) { return K >= 8 && K % 8 == 0 && K <= 8 * 4 * kGmThreads; }
 
+// Narrow rows (K <= 256: K / 8 <= TPR in {16, 32} vectors): the problems of
+// gemv_moe_kernel with a group of TPR threads per unit, so that a CTA is
+// 256 / TPR independent "virtual CTAs". Each group takes its own equal,
+// contiguous range of the unit sequence, walks it RB units per step (one
+// vector of each of the unit's rows per thread; the next step's loads are
+// issued before this step's FMAs) and reduces by shuffles only: no barrier.
+template <bool SWIGLU, int TPR>
+__global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_narrow_kernel(const GemvMoeParams P) {
+  constexpr int NR = SWIGLU ? 2 : 1;
+  constexpr int RB = 4;
+  constexpr int NG = kGmThreads / TPR;
+  const int t = threadIdx.x, g = t / TPR, j = t % TPR;
+  // Groups walk ranges of their own, so two 16-thread groups of one warp may
+  // diverge: every shuffle names only its own group's lanes.
+  const unsigned gmask = TPR == 32 ? 0xffffffffu : (0xffffu << (t & 16));
+  const int K8 = P.K >> 3;
+  const int jj = min(j, K8 - 1);  // lanes past the row read its last vector and meet a zero activation
+  const uint64_t pol = policy_evict_first();
+  if (!P.late_trigger) pdl_trigger();
+  const TableLayout L(P.E, P.n_entries);
+  const int ns = P.sA != nullptr ? P.ns : 0;
+  auto expert_of = [&](int p) -> long long {
+    if (p < ns) return -1;
+    return P.table ? ld_act_s32(P.table + L.expert() + (p - ns)) : 0;
+  };
+  auto slot_of = [&](int p) -> long long {
+    if (p < ns) return p;
+    return P.table ? ld_act_s32(P.table + L.offset() + (p - ns)) : 0;
+  };
+  auto mat0 = [&](long long e) { return e < 0 ? P.sA : P.A + e * P.rows_per_prob_bank * P.K; };
+  auto mat1 = [&](long long e) { return e < 0 ? P.sA2 : P.A2 + e * P.rows_per_prob_bank * P.K; };
+  const long long VG = (long long)gridDim.x * NG, vg = (long long)blockIdx.x * NG + g;
+  pdl_wait();
+  if (P.late_trigger) pdl_trigger();
+  const long long T = ((P.table ? ld_act_s32(P.table + L.U()) : 1) + ns) * (long long)P.R;
+  const long long q0 = vg * T / VG, q1 = (vg + 1) * T / VG;
+  if (q0 >= q1) return;  // (no barrier in this kernel)
+  int p = (int)(q0 / P.R), r = (int)(q0 % P.R);
+  long long left = q1 - q0;
+  long long e = expert_of(p);
+  const uint16_t* A0 = mat0(e);
+  const uint16_t* A1 = mat1(e);
+  uint4 wa[RB][NR];
+  auto load_units = [&](uint4(&w)[RB][NR], const uint16_t* a0, const uint16_t* a1, int rr, int nu) {
+#pragma unroll
+    for (int u = 0; u < RB; ++u)
+#pragma unroll
+      for (int a = 0; a < NR; ++a) {
+        const int row = rr + min(u, nu - 1);  // past nu: re-read the last unit (in range), discarded
+        w[u][a] = ld_stream((a == 0 ? a0 : a1) + (size_t)row * P.K + (size_t)jj * 8, pol);
+      }
+  };
+  int nu = (int)min((long long)min(RB, P.R - r), left);
+  load_units(wa, A0, A1, r, nu);
+  uint4 xr;
+  long long slot = slot_of(p);
+  auto load_x = [&]() {
+    const long long xr_row = (e >= 0 && P.x_by_token && P.table) ? ld_act_s32(P.table + L.slot_token() + slot) : slot;
+    const uint16_t* xrow = e < 0 ? P.sx + slot * P.sldx : P.x + xr_row * P.ldx;
+    xr = j < K8 ? ld_act16(xrow + (size_t)j * 8) : make_uint4(0, 0, 0, 0);
+  };
+  load_x();
+  while (left > 0) {
+    int pn = p, rn = r + nu;
+    long long en = e;
+    const uint16_t *N0 = A0, *N1 = A1;
+    const long long leftn = left - nu;
+    if (rn == P.R) {
+      pn = p + 1;
+      rn = 0;
+      if (leftn > 0) {
+        en = expert_of(pn);
+        N0 = mat0(en);
+        N1 = mat1(en);
+      }
+    }
+    const int nun = (int)min((long long)min(RB, P.R - rn), leftn);
+    uint4 wb[RB][NR];
+    if (nun > 0) load_units(wb, N0, N1, rn, nun);
+    float acc[RB][NR];
+#pragma unroll
+    for (int u = 0; u < RB; ++u)
+#pragma unroll
+      for (int a = 0; a < NR; ++a) {
+        float sum = dot8(wa[u][a], xr, 0.f);
+#pragma unroll
+        for (int o = TPR / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(gmask, sum, o);
+        acc[u][a] = sum;
+      }
+    // lane u of the group writes unit u
+#pragma unroll
+    for (int u = 0; u < RB; ++u)
+      if (j == u && u < nu) {
+        void* dst = e < 0 ? P.sout : P.out;
+        const long long o = slot * (e < 0 ? P.sldo : P.ldo) + r + u;
+        if (SWIGLU) {
+          const float gg = acc[u][0], up = acc[u][NR - 1];
+          reinterpret_cast<uint16_t*>(dst)[o] = f2bf(gg / (1.0f + expf(-gg)) * up);
+        } else {
+          reinterpret_cast<float*>(dst)[o] = acc[u][0];
+        }
+      }
+    left = leftn;
+    if (pn != p && left > 0) {
+      p = pn;
+      e = en;
+      A0 = N0;
+      A1 = N1;
+      slot = slot_of(p);
+      load_x();
+    }
+    r = rn;
+    nu = nun;
+#pragma unroll
+    for (int u = 0; u < RB; ++u)
+#pragma unroll
+      for (int a = 0; a < NR; ++a) wa[u][a] = wb[u][a];
+  }
+}
+
 template <bool SWIGLU>
 static cudaError_t launch_mode(dec_handle* h, const GemvMoeParams& P, int grid, cudaStream_t s) {
   const int K8 = P.K / 8;
   const dim3 g(grid), b(kGmThreads);
+  if (K8 <= 16) return launch_k(h, gemv_moe_narrow_kernel<SWIGLU, 16>, g, b, 0, s, P);
+  if (K8 <= 32) return launch_k(h, gemv_moe_narrow_kernel<SWIGLU, 32>, g, b, 0, s, P);
   if (K8 <= kGmThreads) return launch_k(h, gemv_moe_kernel<SWIGLU, 1>, g, b, 0, s, P);
   if (K8 <= 2 * kGmThreads) return launch_k(h, gemv_moe_kernel<SWIGLU, 2>, g, b, 0, s, P);
   return launch_k(h, gemv_moe_kernel<SWIGLU, 4>, g, b, 0, s, P);
