@@ -305,7 +305,11 @@ def run_ours(args, rank, local, world):
     for M in sweep:
         ws = h.workspace(("bench", M), ML.decode_layer_workspace_size(h, layers[0], M),
                          ("layer", M))
-        x0 = synth.bf16_rows(synth.X_BASE + 100, range(M), H, 0)
+        if args.verify > 1:
+            # speculative-verify batch: groups of `verify` related rows (one request's drafts)
+            x0 = synth.correlated_rows(synth.X_BASE + 100, range(M), args.verify, H, 0, args.verify_noise)
+        else:
+            x0 = synth.bf16_rows(synth.X_BASE + 100, range(M), H, 0)
         host_in = torch.from_numpy(x0.view(np.int16)).view(torch.bfloat16).reshape(M, H).pin_memory()
         host_out = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
         hidden = host_in.to(dev)
@@ -425,6 +429,8 @@ def run_ours(args, rank, local, world):
            "data": "synthetic: seeded random-init weights of the workload's shapes, seeded N(0,1) activations",
            "config": {"workload": WORKLOAD if E == 384 else WORKLOAD + f" (profiling variant: {E} routed experts)",
                       "weight_copies": len(layers),
+                      "token_rows": ("independent" if args.verify <= 1 else
+                                     f"speculative verify: groups of {args.verify} related rows, noise {args.verify_noise}"),
                       "batch": args.batch, "parallelism": "replicas" if world > 1 else "1 GPU",
                       "l2": "inputs larger than L2: each step reads >= 1.1 GB (L2 129 MB); dense weights alternate "
                             "between 2 copies; routing changes every step",
@@ -555,6 +561,10 @@ def main(argv=None):
                     help="at batch 1, pull the shared expert into L2 during the router phase (off: measured slower)")
     ap.add_argument("--prefetch-next", type=int, default=0,
                     help="bytes of the next layer's input projection to pull into L2 during the routing (0: none)")
+    ap.add_argument("--verify", type=int, default=1,
+                    help="speculative-verify batch: groups of this many related token rows (1: independent rows)")
+    ap.add_argument("--verify-noise", type=float, default=0.5,
+                    help="per-token deviation from the group's row (rows of a group correlate at 1/(1+x^2))")
     ap.add_argument("--shard", type=int, choices=(1, 8, 16), default=1,
                     help="per-GPU shapes of a TP8 / TP16 deployment (1: the full layer)")
     ap.add_argument("--experts", type=int, default=E,

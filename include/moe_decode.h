@@ -99,7 +99,12 @@ dec_status dec_set_pdl(dec_handle* h, int enable);
 /* How the shared expert and the routed experts share the SMs [K3 P1§3: the
  * schedule sets how many GPU resources each operation uses]. The shared
  * expert is always launched first, beside the router / top-k phase.
- *  0 (default): it keeps its share of the expected weight bytes (rounded up);
+ *  0 (default): it keeps its share of the expected weight bytes (rounded
+ *     up), except from four tokens on with a shared expert of at least 48 MB,
+ *     where it acts as -1 (measured on GB300: as fast with independent
+ *     tokens, up to 17% faster when tokens share experts, as the drafts of a
+ *     speculative-verify batch do; with a small shared expert the byte share
+ *     is faster);
  * -1: it starts on every SM and the routed experts take SMs as it finishes;
  *  n > 0: it keeps n SMs. */
 dec_status dec_set_shared_sms(dec_handle* h, int sms);

@@ -205,26 +205,38 @@ bool experts_few(const dec_handle* h, int M, int k, int E, int H, int I) {
 
 // SM shares of the shared and the routed experts ("the schedule controls how
 // many GPU resources each op uses", Kimi K3 article, Part 1 §3).
-//  - automatic (h->shared_ctas == 0, default): the shared expert keeps its
-//    share of the expected weight bytes, rounded up with a 25% margin so that
-//    it never finishes after the routed experts (at least one SM, at most
-//    half). Expected distinct experts for uniform routing: E (1 - (1 - k/E)^M).
 //  - overlap (h->shared_ctas < 0): both use every SM; the hardware hands SMs
 //    to the routed kernels as the shared expert's CTAs finish.
+//  - byte share: the shared expert keeps its share of the expected weight
+//    bytes, rounded up with a 25% margin (at least one SM, at most half).
+//    Expected distinct experts for uniform routing: E (1 - (1 - k/E)^M).
+//  - automatic (h->shared_ctas == 0, default): overlap from four tokens on
+//    when the shared expert is large (at least 48 MB of weights), the byte
+//    share otherwise.
 //  - fixed (h->shared_ctas > 0): that many SMs for the shared expert.
-// Measured on GB300 (layer step, CUDA-graph replay): the automatic share is
-// best or within 3% at M = 1..64 except M = 16, where overlap is 6-8% faster.
-int shared_grid(const dec_handle* h, int M, int k, int E) {
+// Measured on GB300 (layer step, CUDA-graph replay): with independent tokens
+// overlap is within -0.7% / +0.3% of the byte share from four tokens on and
+// 1.6% slower at three; with related tokens (speculative-verify groups of 8
+// drafts) routing is far from uniform, U far below the expectation, and the
+// byte share starves the shared expert: overlap is 8% faster at 8 tokens and
+// 17% at 16. But a small shared expert (the tensor-parallel shard shapes:
+// 11 MB) is mostly the split-K kernel's fixed per-launch cost, and on every
+// SM it holds the whole GPU for it: there the byte share is 1.4-1.9x faster.
+bool shared_overlap_auto(const dec_handle* h, int M, int H, int I) {
+  return h->shared_ctas == 0 && M >= 4 && 3.0 * I * H * 2.0 >= 48e6;
+}
+
+int shared_grid(const dec_handle* h, int M, int k, int E, int H, int I) {
   if (h->shared_ctas > 0) return std::min(h->shared_ctas, h->sms - 1);
-  if (h->shared_ctas < 0) return h->sms;
+  if (h->shared_ctas < 0 || shared_overlap_auto(h, M, H, I)) return h->sms;
   const double eu = E * (1.0 - std::pow(1.0 - (double)k / E, (double)M));
   const int g = (int)std::ceil(1.25 * h->sms / (1.0 + eu));
   return std::max(1, std::min(g, h->sms / 2));
 }
 
-int routed_grid(const dec_handle* h, int M, int k, int E, bool has_shared) {
-  if (!has_shared || h->shared_ctas < 0) return h->sms;
-  return h->sms - shared_grid(h, M, k, E);
+int routed_grid(const dec_handle* h, int M, int k, int E, int H, int I, bool has_shared) {
+  if (!has_shared || h->shared_ctas < 0 || shared_overlap_auto(h, M, H, I)) return h->sms;
+  return h->sms - shared_grid(h, M, k, E, H, I);
 }
 
 // The shared expert on the handle's side stream, forked from `s` now. It does
@@ -235,7 +247,7 @@ dec_status moe_shared_fork(dec_handle* h, const uint16_t* x, int M, int k, int E
                            const uint16_t* Wg_s, const uint16_t* Wu_s, const uint16_t* Wd_s, const MoeWs& ws,
                            cudaStream_t s) {
   const bool has_shared = Wg_s != nullptr;
-  const int g1 = has_shared ? shared_grid(h, M, k, E) : 0;
+  const int g1 = has_shared ? shared_grid(h, M, k, E, H, I) : 0;
   // At one token the shared expert is problem 0 of the routed launches (see moe_routed).
   if (experts_small(h, M, H, I)) return DEC_OK;
   if (has_shared) {
@@ -369,7 +381,7 @@ dec_status moe_routed(dec_handle* h, const uint16_t* x, const int32_t* idx, cons
                       uint16_t* out, const MoeWs& ws, cudaStream_t s) {
   const bool has_shared = Wg_s != nullptr;
   const int n = M * k;
-  const int g0 = routed_grid(h, M, k, E, has_shared);
+  const int g0 = routed_grid(h, M, k, E, H, I, has_shared);
   if (experts_small(h, M, H, I)) {
     {
       LaunchScope scope(h, "route_table", s);

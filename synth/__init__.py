@@ -150,6 +150,31 @@ def bf16_rows(base: int, rows, cols: int, seed: int, sigma: float = 1.0, attempt
     return out
 
 
+def correlated_rows(base: int, rows, group: int, cols: int, seed: int, eps: float, attempts=None) -> np.ndarray:
+    """Activation rows in groups of `group` related rows (the draft tokens of
+    one request in a speculative-verify batch): row r is
+    bf16(b + eps * n_r), b the group's N(0, 1) row (row_tensor_id(base, r // group)),
+    n_r an N(0, 1) row of its own (row_tensor_id(base + 1, r, attempt)), rounded
+    to nearest-even bf16. Two rows of one group have correlation 1 / (1 + eps^2)."""
+    rows = list(rows)
+    attempts = [0] * len(rows) if attempts is None else list(attempts)
+    out = np.empty((len(rows), cols), dtype=np.uint16)
+    for i, (r, a) in enumerate(zip(rows, attempts)):
+        b = _bits_to_f32(bf16(cols, seed, row_tensor_id(base, r // group, 0), 0, 1.0))
+        n = _bits_to_f32(bf16(cols, seed, row_tensor_id(base + 1, r, a), 0, 1.0))
+        out[i] = _f32_to_bf16_bits(b + np.float32(eps) * n)
+    return out
+
+
+def _bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def _f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
 def fill_bf16_dev(ptr: int, n: int, seed: int, tensor_id: int, offset: int = 0, sigma: float = 1.0,
                   stream: int = 0) -> None:
     """Fill n bf16 elements at device address ptr (same bits as bf16())."""

@@ -113,6 +113,30 @@ def gap_rows(score_fn: Callable[[np.ndarray], np.ndarray], M: int, H: int, k: in
     return bits, attempts
 
 
+def gap_correlated_rows(score_fn: Callable[[np.ndarray], np.ndarray], M: int, H: int, k: int, base: int, group: int,
+                        eps: float, seed: int = SEED, gap: float = GAP, max_attempts: int = 200):
+    """As gap_rows, for a speculative-verify batch: groups of `group` related
+    rows (synth.correlated_rows); a row that misses the gap rule redraws its
+    own deviation (attempt counter), its group's shared row stays."""
+    bits = np.empty((M, H), dtype=np.uint16)
+    attempts = [0] * M
+    pending = list(range(M))
+    while pending:
+        cand = synth.correlated_rows(base, pending, group, H, seed, eps, [attempts[r] for r in pending])
+        sc = score_fn(cand)
+        nxt = []
+        for i, r in enumerate(pending):
+            if gap_ok(sc[i], k, gap):
+                bits[r] = cand[i]
+            else:
+                attempts[r] += 1
+                if attempts[r] > max_attempts:
+                    raise RuntimeError("gap rule: too many redraws")
+                nxt.append(r)
+        pending = nxt
+    return bits, attempts
+
+
 # ---------------------------------------------------------------------------- expert banks
 class HostBank:
     """Host view of a seeded expert bank: regenerates expert e's weights on demand."""

@@ -6,7 +6,8 @@ import pytest
 
 import oracle
 import synth
-from _util import SCORE_TOL, SEED, WEIGHT_TOL, HostBank, assert_bf16_close, dev_bf16, dev_f32, gap_rows, host_bits
+from _util import (SCORE_TOL, SEED, WEIGHT_TOL, HostBank, assert_bf16_close, dev_bf16, dev_f32, gap_correlated_rows,
+                   gap_rows, host_bits)
 from conftest import E_FULL, H_FULL, I_FULL, K_FULL, K_OUT_FULL, N_IN_FULL
 
 pytestmark = pytest.mark.gpu
@@ -166,6 +167,31 @@ def test_layer_one_token_two_router_units(h):
         _check_layer(tr, hid, ref, slice(None), f"layer one token two units rep={rep}", L)
     del Wg, Wu, Wd
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("M,group", [(2, 2), (16, 8), (64, 8)])
+def test_layer_speculative_verify_batch(h, M, group):
+    """A speculative-verify batch: groups of related token rows (one request's
+    drafts) route largely to the same experts, so the split-K family's expert
+    tiles carry several tokens and U is well below the independent-token case."""
+    H, N_in, K_out, E, I, k = 256, 264, 256, 128, 128, 8
+    L = Layer(H, N_in, K_out, E, I, k, base=6950 + M)
+    n = E * I * H
+    g = synth.bf16(n, SEED, 6960, 0, 0.05).reshape(E, I, H)
+    u = synth.bf16(n, SEED, 6961, 0, 0.05).reshape(E, I, H)
+    d = synth.bf16(n, SEED, 6962, 0, 0.05).reshape(E, H, I)
+    sh = (synth.bf16(I * H, SEED, 6963, 0, 0.05).reshape(I, H), synth.bf16(I * H, SEED, 6964, 0, 0.05).reshape(I, H),
+          synth.bf16(H * I, SEED, 6965, 0, 0.05).reshape(H, I))
+    dev_w = L.device(dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
+                     tuple(dev_bf16(a, a.shape) for a in sh))
+    hbits, _ = gap_correlated_rows(L.scores, M, H, k, base=7000 + M, group=group, eps=0.3)
+    hid, tr = _run(h, L, dev_w, hbits)
+    ref = L.oracle(hbits, lambda e: (g[e], u[e], d[e]), sh)
+    _check_layer(tr, hid, ref, slice(None), f"layer verify batch M={M} group={group}", L)
+    idx = tr["idx"].cpu().numpy()
+    U = len(np.unique(idx))
+    if M >= 16:  # related rows share experts: well below the independent-token expectation
+        assert U < 0.8 * E * (1 - (1 - k / E) ** M), U
 
 
 @pytest.mark.parametrize("M", [2, 3, 4])

@@ -105,3 +105,23 @@ def test_splitmix_stream_definition():
     for key in (0, 1, 0xDEADBEEF12345678, M):
         for n in (0, 1, 2, 1000, 1 << 40):
             assert synth.stream_u64(key, n) == mix((key + (n + 1) * 0x9E3779B97F4A7C15) & M)
+
+
+def test_correlated_rows_groups():
+    """Rows of a group share their base row: correlated within a group,
+    independent across groups, deterministic, and bf16 of the stated sum."""
+    import numpy as np
+    H = 4096
+    r = synth.correlated_rows(1000, range(16), 8, H, 0, 0.5)
+    assert r.shape == (16, H) and r.dtype == np.uint16
+    assert np.array_equal(r, synth.correlated_rows(1000, range(16), 8, H, 0, 0.5))
+    f = (r.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    c = np.corrcoef(f)
+    within = [c[i, j] for i in range(16) for j in range(16) if i != j and i // 8 == j // 8]
+    across = [c[i, j] for i in range(16) for j in range(16) if i // 8 != j // 8]
+    assert min(within) > 0.75 and max(abs(x) for x in across) < 0.1  # 1 / (1 + 0.25) = 0.8
+    b = (synth.bf16(H, 0, synth.row_tensor_id(1000, 0, 0), 0, 1.0).astype(np.uint32) << 16).view(np.float32)
+    n = (synth.bf16(H, 0, synth.row_tensor_id(1001, 3, 0), 0, 1.0).astype(np.uint32) << 16).view(np.float32)
+    want = (b + np.float32(0.5) * n).astype(np.float32)
+    got = (r[3].astype(np.uint32) << 16).view(np.float32)
+    assert np.all(np.abs(got - want) <= np.abs(want) * 2.0 ** -8 + 1e-30)  # within half a bf16 ulp
