@@ -798,9 +798,10 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   if (st != DEC_OK) return st;
   st = linear_impl(h, w.yin, L.N_in, L.W_o, hidden, h1, M, H, L.K_out, w.moe.r0, s, "out_proj");
   if (st != DEC_OK) return st;
-  // One token with the small-matrix experts: the second RMSNorm, the router,
-  // the top-k and the routing table are one launch (router_select), and the
-  // experts read the normalised row for every slot (no gather).
+  // One to a few tokens on the small-matrix experts: the second RMSNorm, the
+  // router, the top-k and the routing table are one launch (route_shared /
+  // router_select), and the experts read the normalised rows by token (no
+  // gather). Otherwise the split-K family's chain of launches.
   const bool one_token = experts_small(h, M, H, L.I);
   const bool few_tokens = !one_token && experts_few(h, M, L.k, L.E, H, L.I);
   if (!one_token && !few_tokens) {
