@@ -95,10 +95,10 @@ def step_bytes(M: int, U: float) -> float:
 # gate/up launch reads the k selected experts whatever the bank size, so a
 # capture on a 32-expert bank gives the full workload's traffic.
 NCU_TRAFFIC = {
-    ("gate_up", 1): {"bytes": 469823232 + 3301632,
+    ("gate_up", 1): {"bytes": 469825280 + 3002368,
                      "sources": ("moe_layers_gb300/csrc/gemv_moe.cu", "moe_layers_gb300/csrc/common.cuh",
                                  "moe_layers_gb300/csrc/api.cu", "moe_layers_gb300/csrc/route_shared.cu"),
-                     "sha256": "f0dd2bac432164c815222f147ceaa7f872ac9ea041ce4062685fcb755a65004c"},
+                     "sha256": "340362af0906b9ebc0afe900040147f4705f65a6291392b5ffcd7ded7da37b9f"},
 }
 
 
