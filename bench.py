@@ -91,14 +91,15 @@ def step_bytes(M: int, U: float) -> float:
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # one ncu capture of a kernel, reported while its sources are unchanged (the
-# sha256 of the listed files at capture time); null otherwise. At batch 1 the
-# gate/up launch reads the k selected experts whatever the bank size, so a
-# capture on a 32-expert bank gives the full workload's traffic.
+# sha256 of the listed files at capture time); null otherwise.
 NCU_TRAFFIC = {
-    ("gate_up", 1): {"bytes": 469825280 + 3002368,
-                     "sources": ("moe_layers_gb300/csrc/gemv_moe.cu", "moe_layers_gb300/csrc/common.cuh",
-                                 "moe_layers_gb300/csrc/api.cu", "moe_layers_gb300/csrc/route_shared.cu"),
-                     "sha256": "340362af0906b9ebc0afe900040147f4705f65a6291392b5ffcd7ded7da37b9f"},
+    # one-token MoE front launch, full workload: dram__bytes_read.sum + dram__bytes_write.sum,
+    # mean of two launches of one ncu capture (read 539.66 / 539.70 MB, write 3.32 / 0.53 MB)
+    ("moe_front", 1): {"bytes": (539658240 + 539695104) // 2 + (3324160 + 525568) // 2,
+                       "sources": ("moe_layers_gb300/csrc/route_shared.cu", "moe_layers_gb300/csrc/topk.cuh",
+                                   "moe_layers_gb300/csrc/common.cuh", "moe_layers_gb300/csrc/internal.h",
+                                   "moe_layers_gb300/csrc/api.cu"),
+                       "sha256": "c83f135480575e25f4d8a574fca0016c584e315b4b0484e1d2b660de16f242fe"},
 }
 
 
@@ -118,8 +119,9 @@ def captured_traffic(tag: str, M: int):
 def kernel_bytes(tag: str, M: int, U: float, shared_in: str | None = None) -> float:
     """Algorithmic bytes of one launch of a kernel of the step. shared_in names
     where the one-token schedule runs the shared expert's gate/up ("router":
-    inside the routing launch; "gate_up": problem 0 of the gate/up launch); its
-    down projection then is part of the down launch. None: the shared expert
+    inside the routing launch; "gate_up": problem 0 of the gate/up launch;
+    "front": one launch of the routing and both gate/ups); its down projection
+    then is part of the down launch. None: the shared expert
     has launches of its own (batch >= 2)."""
     b = {
         "in_proj": N_IN * H * 2 + M * H * 2 + M * N_IN * 2,
@@ -130,7 +132,10 @@ def kernel_bytes(tag: str, M: int, U: float, shared_in: str | None = None) -> fl
         "shared_gate_up": 2 * I * H * 2 + M * (H + I) * 2,
         "shared_down": H * I * 2 + M * (I * 2 + H * 4),
     }
-    if shared_in is not None:
+    if shared_in == "front":  # one launch: routing, the shared and the routed gate/up
+        b["moe_front"] = b["router"] + b["gate_up"] + 2 * I * H * 2 + M * I * 2
+        b["down"] += H * I * 2
+    elif shared_in is not None:
         b[shared_in] += 2 * I * H * 2 + M * I * 2
         b["down"] += H * I * 2
     return b.get(tag, 0.0)
@@ -433,7 +438,8 @@ def run_ours(args, rank, local, world):
         b = step_bytes(M, U)
         kern = {}
         # batch 1: the shared expert runs inside the routing (or gate/up) and down launches
-        shared_in = None if "shared_gate_up" in prof else ("router" if args.shared_in_routing else "gate_up")
+        shared_in = (None if "shared_gate_up" in prof else "front" if "moe_front" in prof else
+                     "router" if args.shared_in_routing else "gate_up")
         for tag, (n, ms) in prof.items():
             avg_us = ms * 1000.0 / max(n, 1)
             kb = kernel_bytes(tag, M, U_prof, shared_in)
@@ -449,7 +455,7 @@ def run_ours(args, rank, local, world):
         raise RuntimeError("device error word set during the benchmark")
 
     hl = results[args.batch]
-    dom = max((t for t in hl["kernels"] if kernel_bytes(t, args.batch, 1.0) > 0),
+    dom = max((t for t in hl["kernels"] if hl["kernels"][t]["GBps"]),  # (kernels with algorithmic bytes)
               key=lambda t: hl["kernels"][t]["avg_us"] * hl["kernels"][t]["launches_per_step"])
     dk = hl["kernels"][dom]
     achieved = dk["GBps"]
@@ -587,8 +593,9 @@ def main(argv=None):
                     help="SMs for the shared expert: 0 automatic share (default), -1 every SM overlapped, n fixed")
     ap.add_argument("--family", choices=("auto", "small_m", "split_k"), default="auto",
                     help="kernel family (auto: by batch and size; small_m covers batch <= 4)")
-    ap.add_argument("--shared-in-routing", type=int, choices=(0, 1), default=1,
-                    help="batch 1: shared expert gate/up inside the routing launch (1) or the gate/up launch (0)")
+    ap.add_argument("--shared-in-routing", type=int, choices=(0, 1, 2), default=2,
+                    help="batch 1: one launch of the routing and both gate/ups (2, default), the shared "
+                         "expert's gate/up inside the routing launch (1) or the gate/up launch (0)")
     ap.add_argument("--l2-ahead", type=int, default=None,
                     help="bytes per CTA the small-matrix kernels keep requested into L2 ahead (default: library's)")
     ap.add_argument("--prefetch-shared", action="store_true",

@@ -195,8 +195,11 @@ class Handle:
     def set_prefetch_shared(self, enable: bool) -> None:
         _check(_load().dec_set_prefetch_shared(self._h, 1 if enable else 0), "dec_set_prefetch_shared")
 
-    def set_one_token_shared(self, in_routing: bool) -> None:
-        _check(_load().dec_set_one_token_shared(self._h, 1 if in_routing else 0), "dec_set_one_token_shared")
+    def set_one_token_shared(self, in_routing) -> None:
+        """False / True: the shared gate/up in the routed launch / the routing
+        launch; 2: one MoE front launch (routing, shared and routed gate/up)."""
+        v = int(in_routing) if not isinstance(in_routing, bool) else (1 if in_routing else 0)
+        _check(_load().dec_set_one_token_shared(self._h, v), "dec_set_one_token_shared")
 
     def set_l2_ahead(self, nbytes: int) -> None:
         _check(_load().dec_set_l2_ahead(self._h, int(nbytes)), "dec_set_l2_ahead")

@@ -460,7 +460,7 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
 
 // ---------------------------------------------------------------- decode layer workspace
 struct LayerWs {
-  int* sel_counter = nullptr;  // the one-token routing launch's counters (hand-off, row queue, done)
+  int* sel_counter = nullptr;  // the one-token routing launch's counters (hand-off, row queue, done, routing flag, tail queue)
   uint16_t* a = nullptr;
   uint16_t* yin = nullptr;
   uint16_t* h1 = nullptr;
@@ -482,7 +482,7 @@ bool layer_ok(const dec_layer_weights* L, int M) {
 void carve_layer(Carver& c, const dec_handle* h, const dec_layer_weights* L, int M, LayerWs* w) {
   const int H = L->H;
   const long long dense_tiles = std::max<long long>((L->N_in + kTileN - 1) / kTileN, H / kTileN);
-  w->sel_counter = c.take<int>(4);
+  w->sel_counter = c.take<int>(8);
   carve_moe_counters(c, L->E, H, L->I, dense_tiles, &w->moe);
   w->a = c.take<uint16_t>((size_t)M * H);
   w->yin = c.take<uint16_t>((size_t)M * L->N_in);
@@ -587,7 +587,7 @@ dec_status dec_set_prefetch_shared(dec_handle* h, int enable) {
 }
 
 dec_status dec_set_one_token_shared(dec_handle* h, int in_routing) {
-  if (h == nullptr || (in_routing != 0 && in_routing != 1)) return DEC_ERR_INVALID_ARG;
+  if (h == nullptr || in_routing < 0 || in_routing > 2) return DEC_ERR_INVALID_ARG;
   h->fuse_shared_routing = in_routing;
   return DEC_OK;
 }
@@ -836,6 +836,23 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
     // With a shared expert the routing launch also streams its gate/up.
     const bool fuse_shared = L.Wg_s != nullptr && h->fuse_shared_routing &&
                              route_shared_supported(h, 1, H, L.E, L.k);
+    if (fuse_shared && h->fuse_shared_routing == 2 && gemv_down_combine_supported(L.k, L.I)) {
+      // One MoE front launch (routing, shared gate/up, routed gate/up), then
+      // the down projection with the combine and the residual.
+      h->last_expert_variant = DEC_VARIANT_SMALL_M;
+      {
+        LaunchScope scope(h, "moe_front", s);
+        DEC_CUDA(launch_moe_front(h, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.parts, w.sel_counter, idx, wt, scores,
+                                  w.moe.table, L.Wg_s, L.Wu_s, L.I, w.moe.hs, L.Wg, L.Wu, w.moe.hbuf, s));
+      }
+      {
+        LaunchScope scope(h, "down", s);
+        DEC_CUDA(launch_gemv_down_combine(h, L.Wd, H, L.Wd_s, H, L.I, w.moe.hbuf, w.moe.hs, w.moe.table, L.E, L.k, wt,
+                                          h1, hidden, h->sms, s, true));
+      }
+      if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
+      return DEC_OK;
+    }
     {
       LaunchScope scope(h, "router", s);
       if (fuse_shared)

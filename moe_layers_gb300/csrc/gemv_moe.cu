@@ -259,7 +259,6 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_kernel(
     const uint16_t* __restrict__ Wd, long long rows_bank, const uint16_t* __restrict__ Wd_s, int H, int K,
     const uint16_t* hbuf, const uint16_t* hs, const int* table, int E, int k, const float* w, const uint16_t* res,
     uint16_t* out, int routing_ready, int ahead) {
-  constexpr int NR = SHARED ? NP - 1 : NP;  // routed rows per unit
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int K8 = K >> 3;
   __shared__ __align__(16) float red[2][kGmThreads / 32];
@@ -384,7 +383,6 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_narrow_kernel
     const uint16_t* __restrict__ Wd, long long rows_bank, const uint16_t* __restrict__ Wd_s, int H, int K,
     const uint16_t* hbuf, const uint16_t* hs, const int* table, int E, int k, const float* w, const uint16_t* res,
     uint16_t* out, int routing_ready, int ahead) {
-  constexpr int NR = SHARED ? NP - 1 : NP;
   constexpr int NG = kGmThreads / TPR;
   const int t = threadIdx.x, g = t / TPR, j = t % TPR;
   const int K8 = K >> 3;

@@ -24,7 +24,7 @@ struct dec_handle {
   int last_variant = 0;
   int last_expert_variant = 0;      // kernel family of the most recent expert launches
   int shared_ctas = 0;              // CTAs for the shared expert's kernels (0 = default)
-  int fuse_shared_routing = 1;      // batch 1: the routing launch also streams the shared gate/up
+  int fuse_shared_routing = 2;      // batch 1: 1 the routing launch also streams the shared gate/up, 2 and the routed
   int l2_ahead = 49152;             // small-matrix kernels: weight bytes per CTA requested into L2 ahead
   int prefetch_shared = 0;          // batch 1: pull the shared expert into L2 during the router phase
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -143,6 +143,12 @@ cudaError_t launch_router_select(dec_handle* h, const uint16_t* x, const uint16_
 // M = 2..4 tokens: the same with one routing-table problem per (token, expert) entry (U = M k,
 // slot p = t k + j), h_s [M][I] and xn [M][H]; without a shared expert (Wg_s null) routing only.
 bool route_shared_supported(const dec_handle* h, int M, int H, int E, int k);
+// One token: routing + shared gate/up + the k routed experts' gate/up in one
+// launch (hbuf [k][I], slot j = entry j); counters ctr[5] zero between launches.
+cudaError_t launch_moe_front(dec_handle* h, const uint16_t* h1, const uint16_t* gamma, float eps, const float* Wr,
+                             int H, int E, int k, float* parts, int* ctr, int32_t* idx, float* w, float* scores,
+                             int* table, const uint16_t* Wg_s, const uint16_t* Wu_s, int I, uint16_t* hs,
+                             const uint16_t* Wg, const uint16_t* Wu, uint16_t* hbuf, cudaStream_t s);
 cudaError_t launch_route_shared(dec_handle* h, int M, const uint16_t* h1, const uint16_t* gamma, float eps,
                                 const float* Wr, int H, int E, int k, uint16_t* xn, float* parts, int* ctr,
                                 int32_t* idx, float* w, float* scores, int* table, const uint16_t* Wg_s,

@@ -23,6 +23,12 @@
 //     h_s[r] = bf16(silu(g) * u)) taken from a row queue (an atomic counter),
 //     so the CTA that ran the top-k simply takes fewer rows. The queue and a
 //     "done" counter are reset by the last CTA to finish.
+//
+// The MoE front kernel (the default at one token) goes on: once the top-k CTA
+// has published the routing (a release flag), every CTA streams the k routed
+// experts' gate/up rows as well, so the routing, the shared expert and the
+// routed experts take one launch and the down projection follows directly.
+// Two to four tokens: route_shared_multi_kernel, one warp's top-k per token.
 #include <algorithm>
 
 #include "common.cuh"
@@ -55,6 +61,12 @@ struct RouteSharedParams {
   const uint16_t* Wu;     // shared up [I][H]
   int I;
   uint16_t* hs;           // shared SwiGLU output bf16 [I]
+  // the MoE front kernel only: the routed gate/up
+  const uint16_t* Wgb;    // routed gate bank [E][I][H]
+  const uint16_t* Wub;    // routed up bank [E][I][H]
+  uint16_t* hbuf;         // routed SwiGLU outputs bf16 [k][I] (slot j: entry j)
+  int* err;               // device error word
+  unsigned long long wait_ns;
 };
 
 template <int J, int VPT>
@@ -485,6 +497,345 @@ __global__ void __launch_bounds__(kThreads, 2) route_shared_multi_kernel(const R
   }
 }
 
+// One token: the MoE front in one launch: the routing launch above (RMSNorm,
+// router, top-k, routing table), then one row queue over the shared expert's
+// gate/up rows followed by the k routed experts' rows. The routing is
+// published by the last CTA to reach the hand-off (it waits for nothing), so
+// a CTA that waits for it waits only until every CTA has started.
+template <int J, int VPT>
+__global__ void __launch_bounds__(kThreads, 2) moe_front_kernel(const RouteSharedParams P) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int H = P.H, H8 = H >> 3;
+  const int ngrp = (P.E + 7) / 8;
+  extern __shared__ __align__(16) uint16_t sx[];  // the normalised row [H]
+  __shared__ float s_norm[kThreads / 32];
+  __shared__ float red[2][kThreads / 32][2];
+  __shared__ int s_row[2];
+  __shared__ int s_next[2];
+  __shared__ int s_last;
+  __shared__ int s_ok;
+  const uint64_t pol = policy_evict_first();
+
+  float4 wv[kUnitCols / 128];
+  auto load_unit = [&](int u) {
+    const int e = (u % ngrp) * 8 + warp, k0 = (u / ngrp) * kUnitCols;
+    const int kn = min(kUnitCols, H - k0);
+#pragma unroll
+    for (int i = 0; i < kUnitCols / 128; ++i) {
+      const int kk = 4 * (lane + 32 * i);
+      wv[i] = (u < P.nunits && e < P.E && kk < kn)
+                  ? __ldg(reinterpret_cast<const float4*>(P.Wr + (size_t)e * H + k0 + kk))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  load_unit(c);
+  int base = 0;
+  if (t == 0) {
+    base = atomicAdd(&P.ctr[1], 3);
+    for (int q = 0; q < 3; ++q)
+      if (base + q < P.I) {
+        request_l2(P.Wg + (size_t)(base + q) * H, (size_t)H * 2);
+        request_l2(P.Wu + (size_t)(base + q) * H, (size_t)H * 2);
+      }
+  }
+  uint4 xr[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = t + kThreads * i;
+    xr[i] = v < H8 ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+  }
+  pdl_wait();
+  {
+    uint4 hv[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = t + kThreads * i;
+      hv[i] = v < H8 ? ld_act16(P.h1 + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+      if (t + kThreads * i < H8) ss = sumsq8(hv[i], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) s_norm[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int q = 0; q < kThreads / 32; ++q) tot += s_norm[q];
+    const float r = rsqrtf(tot / (float)H + P.eps);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = t + kThreads * i;
+      xr[i] = norm8(hv[i], xr[i], r);
+      if (v < H8) *reinterpret_cast<uint4*>(&sx[v * 8]) = xr[i];
+    }
+  }
+  int pending = base + 2;
+  __syncthreads();
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int u = c + m * G;
+    if (m == 1 && u < P.nunits) load_unit(u);
+    if (u < P.nunits) {
+      const int e = (u % ngrp) * 8 + warp, ks = u / ngrp, k0 = ks * kUnitCols;
+      const int kn = min(kUnitCols, H - k0);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < kUnitCols / 128; ++i) {
+        const int kk = 4 * (lane + 32 * i);
+        if (kk < kn) {
+          const uint2 xv = *reinterpret_cast<const uint2*>(&sx[k0 + kk]);
+          acc = fmaf(wv[i].x, bf_lo(xv.x), acc);
+          acc = fmaf(wv[i].y, bf_hi(xv.x), acc);
+          acc = fmaf(wv[i].z, bf_lo(xv.y), acc);
+          acc = fmaf(wv[i].w, bf_hi(xv.y), acc);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0 && e < P.E) P.parts[(size_t)ks * P.E + e] = acc;
+    }
+  }
+  __syncthreads();
+  if (t == 0) s_last = atom_add_acq_rel_gpu(&P.ctr[0], 1) == G - 1;
+  __syncthreads();
+  if (s_last) {
+    int se = 0;
+    float sw = 0.f;
+    block_topk<J, true>(P.parts, (H + kUnitCols - 1) / kUnitCols, 1, 0, P.E, P.k, P.idx, P.w, P.scores, &se, &sw);
+    if (warp == 0) {
+      write_one_token_table(P.table, P.E, P.k, se);
+      __syncwarp();
+      if (lane == 0) {
+        P.ctr[0] = 0;
+        P.ctr[5] = c;                  // this CTA's static share goes to the tail queue
+        st_release_gpu(&P.ctr[3], 1);  // the routing is written
+      }
+    }
+  }
+
+  // Three streams of row pairs, one after the other: the shared expert's
+  // rows from the row queue until it runs dry; then this CTA's static
+  // contiguous share of the routed rows (7/8 of them split evenly; routed row
+  // q is row q mod I of entry q / I, with the one token's row for every
+  // problem); then routed rows from a tail queue, so that CTAs that started
+  // late or stream slower end together with the rest. Each queue grab is
+  // made an iteration before its value is needed. Before its first routed
+  // row a CTA waits for the routing (thread 0, acquire, bounded by the
+  // wall-clock limit: past it the device error word is raised and the CTA
+  // stops); dependents are triggered once the routing is seen, so the down
+  // kernel may read it before its dependency wait.
+  const int I = P.I, T = P.k * P.I;
+  const int bulk = T * 7 / 8 / G, tail0 = G * bulk;
+  uint4 wa[2][VPT], wb[2][VPT];
+  auto load_rows = [&](uint4(&wr)[2][VPT], const uint16_t* g0, const uint16_t* u0) {
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = t + kThreads * i;
+        wr[a][i] = v < H8 ? ld_stream((a == 0 ? g0 : u0) + (size_t)v * 8, pol) : make_uint4(0, 0, 0, 0);
+      }
+  };
+  auto dot_pair = [&](int b) {
+    float g = 0.f, up = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      // the normalised row from shared memory (registers hold the weight stream)
+      const int v = t + kThreads * i;
+      const uint4 xv = v < H8 ? *reinterpret_cast<const uint4*>(&sx[v * 8]) : make_uint4(0, 0, 0, 0);
+      g = dot8(wa[0][i], xv, g);
+      up = dot8(wa[1][i], xv, up);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      g += __shfl_xor_sync(0xffffffffu, g, o);
+      up += __shfl_xor_sync(0xffffffffu, up, o);
+    }
+    if (lane == 0) {
+      red[b][warp][0] = g;
+      red[b][warp][1] = up;
+    }
+  };
+  auto swiglu_out = [&](int b) {  // thread 0, after the barrier
+    float gs = 0.f, us = 0.f;
+#pragma unroll
+    for (int q = 0; q < kThreads / 32; ++q) {
+      gs += red[b][q][0];
+      us += red[b][q][1];
+    }
+    return f2bf(gs / (1.0f + expf(-gs)) * us);
+  };
+  auto shift = [&]() {
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) wa[a][i] = wb[a][i];
+  };
+  int buf = 0;
+  if (t == 0) {
+    s_row[0] = base;
+    s_row[1] = base + 1;
+  }
+  __syncthreads();
+  {  // the shared expert's rows
+    int cur = s_row[0], nxt = s_row[1];
+    if (cur < I) load_rows(wa, P.Wg + (size_t)cur * H, P.Wu + (size_t)cur * H);
+    while (cur < I) {
+      if (nxt < I) load_rows(wb, P.Wg + (size_t)nxt * H, P.Wu + (size_t)nxt * H);
+      dot_pair(buf);
+      if (t == 0) {
+        s_next[buf] = pending;
+        if (pending < I) {
+          request_l2(P.Wg + (size_t)pending * H, (size_t)H * 2);
+          request_l2(P.Wu + (size_t)pending * H, (size_t)H * 2);
+          pending = atomicAdd(&P.ctr[1], 1);
+        }
+      }
+      __syncthreads();
+      if (t == 0) P.hs[cur] = swiglu_out(buf);
+      const int nn = s_next[buf];
+      cur = nxt;
+      nxt = nn;
+      shift();
+      buf ^= 1;
+    }
+  }
+
+  // the routing
+  __shared__ const uint16_t* s_g[32];
+  __shared__ const uint16_t* s_u[32];
+  if (t == 0) {
+    const unsigned long long t0 = globaltimer();
+    int ok = 1;
+    while (ld_acquire_gpu(&P.ctr[3]) == 0) {
+      if (globaltimer() - t0 > P.wait_ns) {
+        atomicOr(P.err, DEV_ERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (s_ok) {
+    __shared__ int s_tb, s_cstar;
+    if (t < P.k) {
+      const long long e = ld_cg_s32(P.table + TableLayout(P.E, P.k).expert() + t);
+      s_g[t] = P.Wgb + e * I * H;
+      s_u[t] = P.Wub + e * I * H;
+    }
+    if (t == 0) s_cstar = ld_cg_s32(&P.ctr[5]);
+    __syncthreads();
+    pdl_trigger();
+    const int cstar = s_cstar;
+    // tail unit v: the top-k CTA's share first, then the rows after the shares
+    auto tail_row = [&](int v) { return v < bulk ? cstar * bulk + v : tail0 + v - bulk; };
+    const int ntail = bulk + T - tail0;
+    auto rows = [&](int q, const uint16_t*& g0, const uint16_t*& u0) {
+      const int e = q / I, r = q - e * I;
+      g0 = s_g[e] + (size_t)r * H;
+      u0 = s_u[e] + (size_t)r * H;
+    };
+    int tb = 0;  // (thread 0) the first of three tail units grabbed together, published in s_tb
+    const int q0 = c * bulk, q1 = c == cstar ? q0 : q0 + bulk;
+    if (q1 - q0 < 4) {
+      if (t == 0) {
+        tb = atomicAdd(&P.ctr[4], 3);
+        s_tb = tb;
+      }
+      __syncthreads();
+    }
+    bool wa_loaded = false;
+    if (q0 < q1) {  // this CTA's static share
+      int e = q0 / I, r = q0 - (q0 / I) * I;
+      load_rows(wa, s_g[e] + (size_t)r * H, s_u[e] + (size_t)r * H);
+      for (int q = q0; q < q1; ++q) {
+        int en = e, rn = r + 1;
+        if (rn == I) {
+          ++en;
+          rn = 0;
+        }
+        if (q + 1 < q1) {
+          load_rows(wb, s_g[en] + (size_t)rn * H, s_u[en] + (size_t)rn * H);
+        } else if (s_tb < ntail) {  // the first tail row follows without a gap
+          const uint16_t *g0, *u0;
+          rows(tail_row(s_tb), g0, u0);
+          load_rows(wb, g0, u0);
+          wa_loaded = true;
+        }
+        if (t == 0) {
+          if (q + 2 < q1) {  // the row after next into L2
+            const int e2 = rn + 1 == I ? en + 1 : en, r2 = rn + 1 == I ? 0 : rn + 1;
+            request_l2(s_g[e2] + (size_t)r2 * H, (size_t)H * 2);
+            request_l2(s_u[e2] + (size_t)r2 * H, (size_t)H * 2);
+          }
+          if (q + 3 == q1 && q1 - q0 >= 4) tb = atomicAdd(&P.ctr[4], 3);  // the tail grab
+          if (q + 2 == q1 && q1 - q0 >= 4) {
+            s_tb = tb;  // published at this iteration's barrier
+            for (int v = tb; v < tb + 2 && v < ntail; ++v) {
+              const uint16_t *g2, *u2;
+              rows(tail_row(v), g2, u2);
+              request_l2(g2, (size_t)H * 2);
+              request_l2(u2, (size_t)H * 2);
+            }
+          }
+        }
+        dot_pair(buf);
+        __syncthreads();
+        if (t == 0) P.hbuf[q] = swiglu_out(buf);
+        e = en;
+        r = rn;
+        shift();
+        buf ^= 1;
+      }
+    }
+    {  // the tail queue
+      const int v0 = s_tb;
+      int cur = v0, nxt = v0 + 1;
+      if (t == 0) pending = v0 + 2;
+      const uint16_t *g0, *u0;
+      if (cur < ntail && !wa_loaded) {
+        rows(tail_row(cur), g0, u0);
+        load_rows(wa, g0, u0);
+      }
+      while (cur < ntail) {
+        if (nxt < ntail) {
+          rows(tail_row(nxt), g0, u0);
+          load_rows(wb, g0, u0);
+        }
+        dot_pair(buf);
+        if (t == 0) {
+          s_next[buf] = pending;
+          if (pending < ntail) {
+            const uint16_t *g2, *u2;
+            rows(tail_row(pending), g2, u2);
+            request_l2(g2, (size_t)H * 2);
+            request_l2(u2, (size_t)H * 2);
+            pending = atomicAdd(&P.ctr[4], 1);
+          }
+        }
+        __syncthreads();
+        if (t == 0) P.hbuf[tail_row(cur)] = swiglu_out(buf);
+        const int nn = s_next[buf];
+        cur = nxt;
+        nxt = nn;
+        shift();
+        buf ^= 1;
+      }
+    }
+  }
+  if (t == 0 && atom_add_acq_rel_gpu(&P.ctr[2], 1) == G - 1) {
+    P.ctr[1] = 0;
+    P.ctr[2] = 0;
+    P.ctr[3] = 0;
+    P.ctr[4] = 0;
+  }
+}
+
 template <int J>
 cudaError_t launch_j(dec_handle* h, const RouteSharedParams& P, int vpt, cudaStream_t s) {
   const dim3 g(2 * h->sms), b(kThreads);
@@ -492,6 +843,15 @@ cudaError_t launch_j(dec_handle* h, const RouteSharedParams& P, int vpt, cudaStr
   if (vpt == 1) return launch_k(h, route_shared_kernel<J, 1>, g, b, smem, s, P);
   if (vpt == 2) return launch_k(h, route_shared_kernel<J, 2>, g, b, smem, s, P);
   return launch_k(h, route_shared_kernel<J, 4>, g, b, smem, s, P);
+}
+
+template <int J>
+cudaError_t launch_front_j(dec_handle* h, const RouteSharedParams& P, int vpt, cudaStream_t s) {
+  const dim3 g(2 * h->sms), b(kThreads);
+  const size_t smem = (size_t)P.H * sizeof(uint16_t);
+  if (vpt == 1) return launch_k(h, moe_front_kernel<J, 1>, g, b, smem, s, P);
+  if (vpt == 2) return launch_k(h, moe_front_kernel<J, 2>, g, b, smem, s, P);
+  return launch_k(h, moe_front_kernel<J, 4>, g, b, smem, s, P);
 }
 
 template <int J, int MT>
@@ -563,6 +923,44 @@ cudaError_t launch_route_shared(dec_handle* h, int M, const uint16_t* h1, const 
   if (Ew <= 32) return launch_multi<1, 4>(h, P, vpt, s);
   if (Ew <= 64) return launch_multi<2, 4>(h, P, vpt, s);
   return launch_multi<4, 4>(h, P, vpt, s);
+}
+
+cudaError_t launch_moe_front(dec_handle* h, const uint16_t* h1, const uint16_t* gamma, float eps, const float* Wr,
+                             int H, int E, int k, float* parts, int* ctr, int32_t* idx, float* w, float* scores,
+                             int* table, const uint16_t* Wg_s, const uint16_t* Wu_s, int I, uint16_t* hs,
+                             const uint16_t* Wg, const uint16_t* Wu, uint16_t* hbuf, cudaStream_t s) {
+  if (!route_shared_supported(h, 1, H, E, k) || Wg_s == nullptr || k > 32) return cudaErrorInvalidValue;
+  RouteSharedParams P;
+  P.M = 1;
+  P.h1 = h1;
+  P.gamma = gamma;
+  P.eps = eps;
+  P.Wr = Wr;
+  P.H = H;
+  P.E = E;
+  P.k = k;
+  P.nunits = ((E + 7) / 8) * ((H + kUnitCols - 1) / kUnitCols);
+  P.xn = nullptr;
+  P.parts = parts;
+  P.ctr = ctr;
+  P.idx = idx;
+  P.w = w;
+  P.scores = scores;
+  P.table = table;
+  P.Wg = Wg_s;
+  P.Wu = Wu_s;
+  P.I = I;
+  P.hs = hs;
+  P.Wgb = Wg;
+  P.Wub = Wu;
+  P.hbuf = hbuf;
+  P.err = h->d_err;
+  P.wait_ns = h->wait_ns;
+  const int H8 = H / 8, vpt = H8 <= kThreads ? 1 : (H8 <= 2 * kThreads ? 2 : 4);
+  const int Ew = (E + 7) / 8;
+  if (Ew <= 32) return launch_front_j<1>(h, P, vpt, s);
+  if (Ew <= 64) return launch_front_j<2>(h, P, vpt, s);
+  return launch_front_j<4>(h, P, vpt, s);
 }
 
 }  // namespace dec

@@ -12,104 +12,81 @@ namespace dec {
 constexpr int kTopkSplitsInRegs = 16;  // split partials per expert loaded together (H <= 16384)
 
 // Top-k of token t, one 256-thread block. logits = sum of the split partials
-// in split order, s = 1 / (1 + exp(-logit)). Each of the 8 warps takes a
-// contiguous eighth of the experts (J per lane, in registers), keeps its local
-// top-k by k rounds of warp arg-max (score descending, expert id ascending),
-// and warp 0 merges the 8k candidates the same way; weights are the selected
-// scores over their sum. All partial-sum loads are issued before any is used.
-// CG: read the partials at L2 (written by other CTAs of the running kernel).
-// On return lane r < k of warp 0 holds the r-th selection in *sel_e, *sel_w.
+// in split order, s = 1 / (1 + exp(-logit)) (thread t owns experts t, t + 256,
+// ...; all partial-sum loads are issued before any is used). Warp 0 then
+// selects over all E scores from shared memory (lane l holds experts l,
+// l + 32, ...): k rounds of arg-max (score descending, expert id ascending),
+// each round one warp max of the scores' bit patterns (positive floats order
+// as their bits; +1 keeps 0 for "taken") and one warp min of the ids that
+// reach it. Weights are the selected scores over their sum. CG: read the
+// partials at L2 (written by other CTAs of the running kernel). On return
+// lane r < k of warp 0 holds the r-th selection in *sel_e, *sel_w.
 template <int J, bool CG>
 __device__ __forceinline__ void block_topk(const float* parts, int ks, int M, int t, int E, int k, int32_t* idx,
                                            float* w, float* scores, int* sel_e, float* sel_w) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Ew = (E + 7) / 8;
-  __shared__ float cv[8][16];
-  __shared__ int ci[8][16];
-  float sv[J];
-  int ev[J];
-  bool ok[J];
+  constexpr int JT = J;      // experts per thread (E <= 256 J)
+  constexpr int JW = 8 * J;  // experts per lane of warp 0
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ float s_sc[256 * J];
+  float sv[JT];
 #pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const int off = lane + 32 * j;
-    ev[j] = warp * Ew + off;
-    ok[j] = off < Ew && ev[j] < E;
-    sv[j] = 0.f;
-  }
+  for (int j = 0; j < JT; ++j) sv[j] = 0.f;
   auto ld = [&](const float* p) { return CG ? ld_cg_f32(p) : ld_act_f32(p); };
   for (int s0 = 0; s0 < ks; s0 += kTopkSplitsInRegs) {
-    float tmp[kTopkSplitsInRegs][J];
+    float tmp[kTopkSplitsInRegs][JT];
 #pragma unroll
     for (int q = 0; q < kTopkSplitsInRegs; ++q)
 #pragma unroll
-      for (int j = 0; j < J; ++j)
-        tmp[q][j] = (s0 + q < ks && ok[j]) ? ld(parts + ((size_t)(s0 + q) * M + t) * E + ev[j]) : 0.f;
+      for (int j = 0; j < JT; ++j) {
+        const int e = tid + 256 * j;
+        tmp[q][j] = (s0 + q < ks && e < E) ? ld(parts + ((size_t)(s0 + q) * M + t) * E + e) : 0.f;
+      }
 #pragma unroll
     for (int q = 0; q < kTopkSplitsInRegs; ++q)
 #pragma unroll
-      for (int j = 0; j < J; ++j)
+      for (int j = 0; j < JT; ++j)
         if (s0 + q < ks) sv[j] += tmp[q][j];
   }
 #pragma unroll
-  for (int j = 0; j < J; ++j) {
-    if (ok[j]) {
-      sv[j] = 1.0f / (1.0f + expf(-sv[j]));
-      if (scores != nullptr) scores[(size_t)t * E + ev[j]] = sv[j];
-    } else {
-      sv[j] = -FLT_MAX;
-      ev[j] = INT_MAX;
+  for (int j = 0; j < JT; ++j) {
+    const int e = tid + 256 * j;
+    if (e < E) {
+      const float sc = 1.0f / (1.0f + expf(-sv[j]));
+      if (scores != nullptr) scores[(size_t)t * E + e] = sc;
+      s_sc[e] = sc;
     }
-  }
-  // k rounds of warp arg-max; returns the r-th selection in lane r.
-  auto select = [&](float* v, int* id, int n, float& out_v, int& out_i) {
-    for (int r = 0; r < k; ++r) {
-      float bv = -FLT_MAX;
-      int bi = INT_MAX;
-      for (int j = 0; j < n; ++j)
-        if (v[j] > bv || (v[j] == bv && id[j] < bi)) {
-          bv = v[j];
-          bi = id[j];
-        }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      for (int j = 0; j < n; ++j)
-        if (id[j] == bi) v[j] = -FLT_MAX;  // ids are unique: only the owner matches
-      if (lane == r) {
-        out_v = bv;
-        out_i = bi;
-      }
-    }
-  };
-  float mv = -FLT_MAX;
-  int mi = INT_MAX;
-  select(sv, ev, J, mv, mi);
-  if (lane < k) {
-    cv[warp][lane] = mv;
-    ci[warp][lane] = mi;
   }
   __syncthreads();
   if (warp == 0) {
-    // the 8k candidates, up to four per lane
-    float v2[4];
-    int i2[4];
+    unsigned key[JW];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int q = lane + 32 * j;  // candidate index in [0, 8k)
-      const int wq = q / k, rq = q - wq * k;
-      const bool okq = q < 8 * k;
-      v2[j] = okq ? cv[wq][rq] : -FLT_MAX;
-      i2[j] = okq ? ci[wq][rq] : INT_MAX;
+    for (int i = 0; i < JW; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = e < E ? __float_as_uint(s_sc[e]) + 1u : 0u;
     }
     float fv = 0.f;
     int fi = 0;
-    select(v2, i2, 4, fv, fi);
+    for (int r = 0; r < k; ++r) {
+      unsigned bk = 0u;
+      int bi = 0;
+#pragma unroll
+      for (int i = 0; i < JW; ++i)
+        if (key[i] > bk) {  // strict: the lowest id among a lane's equal scores
+          bk = key[i];
+          bi = i;
+        }
+      const unsigned m = __reduce_max_sync(0xffffffffu, bk);
+      const unsigned win = __reduce_min_sync(0xffffffffu, bk == m && m != 0u ? (unsigned)(lane + 32 * bi) : 0xffffffffu);
+      if ((int)(win & 31u) == lane) {
+#pragma unroll
+        for (int i = 0; i < JW; ++i)
+          if (i == (int)(win >> 5)) key[i] = 0u;
+      }
+      if (lane == r) {
+        fv = __uint_as_float(m - 1u);
+        fi = (int)win;
+      }
+    }
     float sum = 0.f;
     for (int r = 0; r < k; ++r) sum += __shfl_sync(0xffffffffu, fv, r);
     if (lane < k) {

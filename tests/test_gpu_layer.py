@@ -93,7 +93,7 @@ def test_layer_small(h, M, shared):
     _check_layer(tr, hid, ref, slice(None), f"layer M={M}", L)
 
 
-@pytest.mark.parametrize("in_routing", [True, False])
+@pytest.mark.parametrize("in_routing", [True, False, 2])
 @pytest.mark.parametrize("H,E,k,shared", [(1152, 37, 5, True), (1152, 37, 5, False), (256, 9, 8, True),
                                           (2048, 300, 8, True)])
 def test_layer_one_token_shapes(h, H, E, k, shared, in_routing):
@@ -101,7 +101,8 @@ def test_layer_one_token_shapes(h, H, E, k, shared, in_routing):
     a router row split into a full and a ragged chunk (H = 1152), with a
     number of experts that leaves a partial row group, k = 8 (the fused down
     projection + combine) over only 9 experts, and 300 experts; the shared
-    expert's gate/up in the routing launch and in the routed gate/up launch."""
+    expert's gate/up in the routing launch, in the routed gate/up launch, and
+    the MoE front launch (routing, shared and routed gate/up)."""
     N_in, K_out, I = 264, 256, 128
     L = Layer(H, N_in, K_out, E, I, k, base=6500 + E)
     n = E * I * H
@@ -120,7 +121,7 @@ def test_layer_one_token_shapes(h, H, E, k, shared, in_routing):
         try:
             hid, tr = _run(h, L, dev_w, hbits)
         finally:
-            h.set_one_token_shared(True)
+            h.set_one_token_shared(2)
         ref = L.oracle(hbits, lambda e: (g[e], u[e], d[e]), sh)
         _check_layer(tr, hid, ref, slice(None), f"layer one token H={H} E={E} rep={rep}", L)
 
@@ -246,12 +247,18 @@ def full_layer():
                  gamma_noise=False)
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
-def test_layer_full_size(h, full_bank, full_layer, M):
+@pytest.mark.parametrize("M,sched", [(1, 1), (1, 2), (1, 0), (2, 1), (4, 1), (8, 1), (16, 1), (32, 1), (64, 1)])
+def test_layer_full_size(h, full_bank, full_layer, M, sched):
+    """The full-size layer; at one token also the two other schedules of the
+    shared expert (sched: set_one_token_shared)."""
     Wg, Wu, Wd, sh = full_bank
     L = full_layer
     hbits, _ = gap_rows(L.scores, M, H_FULL, K_FULL, base=synth.X_BASE + 30)
-    hid, tr = _run(h, L, L.device(Wg, Wu, Wd, sh), hbits)
+    h.set_one_token_shared(sched)
+    try:
+        hid, tr = _run(h, L, L.device(Wg, Wu, Wd, sh), hbits)
+    finally:
+        h.set_one_token_shared(2)
     bank = HostBank(E_FULL, H_FULL, I_FULL)
     shared = tuple(oracle.bf16_to_f64(synth.bf16(I_FULL * H_FULL, SEED, tid, 0, 0.02)).reshape(shape)
                    for tid, shape in ((synth.W_G_S, (I_FULL, H_FULL)), (synth.W_U_S, (I_FULL, H_FULL)),

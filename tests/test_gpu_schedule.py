@@ -42,7 +42,7 @@ def _defaults(h):
     h.set_shared_sms(0)
     h.set_pdl(True)
     h.set_l2_ahead(49152)
-    h.set_one_token_shared(True)
+    h.set_one_token_shared(2)
     h.set_prefetch_shared(False)
 
 
@@ -52,6 +52,7 @@ SETTINGS = {
     "no_l2_ahead": {"l2_ahead": 0},
     "big_l2_ahead": {"l2_ahead": 1 << 20},
     "shared_in_gate_up": {"one_token_shared": False},
+    "shared_in_routing": {"one_token_shared": True},
     "shared_overlap": {"shared_sms": -1},
     "shared_fixed_4": {"shared_sms": 4},
     "prefetch_shared": {"prefetch_shared": True},
@@ -103,7 +104,8 @@ def test_profiling_reports_every_launch(h, small_layer):
     L, _, (gd, ud, dd, shd) = small_layer
     dev_w = L.device(gd, ud, dd, shd)
     expect = {
-        1: {"in_proj", "out_proj", "router", "gate_up", "down"},
+        # one token: the MoE front launch (routing, shared and routed gate/up), then down + combine
+        1: {"in_proj", "out_proj", "moe_front", "down"},
         # three tokens on a small matrix: small-matrix input projection with the RMSNorm inside,
         # split-K experts
         3: {"in_proj", "out_proj", "rmsnorm2", "router", "topk", "route_table", "gate_up", "down",
