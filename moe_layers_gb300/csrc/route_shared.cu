@@ -270,9 +270,9 @@ __global__ void __launch_bounds__(kThreads, 2) route_shared_kernel(const RouteSh
 // M = 2 .. MT tokens: the same launch for a few tokens. Every CTA
 // normalises the M rows (two passes over them: sums of squares, then the
 // normalised rows into shared memory; CTA 0 writes them out), adds its router
-// units' logit pieces for every token, and arrives; in the last CTA warp t
-// takes token t's top-k (warp_topk) and writes its k entries of the routing
-// table (one problem per (token, expert) entry). The shared expert's gate/up
+// units' logit pieces for every token, and arrives; the last CTA scores all
+// tokens and warp t takes token t's top-k and writes its k entries of the
+// routing table (block_topk_tokens; one problem per (token, expert) entry). The shared expert's gate/up
 // rows stream from the queue meanwhile, each row pair applied to the M rows
 // held in shared memory.
 template <int J, int VPT, int MT>
@@ -411,12 +411,7 @@ __global__ void __launch_bounds__(kThreads, 2) route_shared_multi_kernel(const R
   if (t == 0) s_last = atom_add_acq_rel_gpu(&P.ctr[0], 1) == G - 1;
   __syncthreads();
   if (s_last) {
-    if (warp < M) {
-      int se = 0;
-      float sw = 0.f;
-      warp_topk<8 * J>(P.parts, ksplit, M, warp, P.E, P.k, P.idx, P.w, P.scores, &se, &sw);
-      write_entry_table(P.table, P.E, M, P.k, warp, se);
-    }
+    block_topk_tokens<J, MT>(P.parts, ksplit, M, P.E, P.k, P.idx, P.w, P.scores, P.table);
     if (t == 0) P.ctr[0] = 0;  // leave the workspace reusable
   }
 
