@@ -119,13 +119,15 @@ dec_status dec_set_prefetch_shared(dec_handle* h, int enable);
 /* Where decode_layer runs the shared expert's gate/up at batch 1
  * [K3 P1§3, §4]: 1 inside the routing launch, whose CTAs stream it while the
  * router / top-k chain runs; 0 as problem 0 of the routed gate/up launch;
- * 2 (default) inside one MoE front launch that also streams the k routed
+ * 2 (default) inside one MoE front launch that also streams the routed
  * experts' gate/up once its top-k CTA has published the routing (its CTAs wait
  * for that with the handle's wait limit, raising DEC_ERR_TIMEOUT in the device
- * error word past it), leaving four launches per layer. All compute the same
- * layer (fp32 sums of the routed rows may run in another order); the switch
- * exists to measure and test the schedules. in_routing in {0, 1, 2}, else
- * DEC_ERR_INVALID_ARG. */
+ * error word past it), leaving four launches per layer. At two to four tokens
+ * on the small-matrix family the routing launch always streams the shared
+ * gate/up, and 2 also folds the entries' gate/up into it (at most 32 (token,
+ * expert) entries). All compute the same layer (fp32 sums of the routed rows
+ * may run in another order); the switch exists to measure and test the
+ * schedules. in_routing in {0, 1, 2}, else DEC_ERR_INVALID_ARG. */
 dec_status dec_set_one_token_shared(dec_handle* h, int in_routing);
 
 /* The small-matrix kernels (batch 1) keep about `bytes` of each CTA's

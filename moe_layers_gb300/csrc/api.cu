@@ -345,15 +345,17 @@ dec_status moe_small(dec_handle* h, const uint16_t* x, long long ldx, const floa
 
 // Two to four tokens after the routing launch (route_shared: entry table,
 // normalised rows x [M][H], and the shared expert's h_s [M][I] when there is
-// one): gate/up over the M k entries (each reads its token's row), down over
-// the shared expert applied to the M rows of h_s plus the entries, then the
-// weighted combine with the shared output and the residual.
+// one): gate/up over the M k entries (each reads its token's row; skipped when
+// the MoE front launch has written them, gate_up_done), down over the shared
+// expert applied to the M rows of h_s plus the entries, then the weighted
+// combine with the shared output and the residual.
 dec_status moe_few(dec_handle* h, int M, const uint16_t* x, const float* w, int k, const uint16_t* Wg,
                    const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I, const uint16_t* Wd_s,
-                   const uint16_t* residual, uint16_t* out, const MoeWs& ws, cudaStream_t s) {
+                   const uint16_t* residual, uint16_t* out, const MoeWs& ws, cudaStream_t s,
+                   bool gate_up_done = false) {
   const int n = M * k;
   h->last_expert_variant = DEC_VARIANT_SMALL_M;
-  {
+  if (!gate_up_done) {
     // late trigger: the next routing launch reuses this launch's predecessor's row queue
     LaunchScope scope(h, "gate_up", s);
     DEC_CUDA(launch_gemv_moe(h, true, Wg, Wu, I, I, H, x, H, ws.table, E, n, ws.hbuf, I, h->sms, s, nullptr, n,
@@ -870,7 +872,20 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   }
   if (few_tokens) {
     // Two to four tokens: the second RMSNorm, router, top-k, routing table (one
-    // problem per entry) and the shared expert's gate/up in one launch.
+    // problem per entry) and the shared expert's gate/up in one launch; with
+    // the MoE front schedule the entries' gate/up as well.
+    if (L.Wg_s != nullptr && h->fuse_shared_routing == 2 && M * L.k <= 32) {
+      {
+        LaunchScope scope(h, "moe_front", s);
+        DEC_CUDA(launch_moe_front_multi(h, M, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.parts, w.sel_counter, idx, wt,
+                                        scores, w.moe.table, L.Wg_s, L.Wu_s, L.I, w.moe.hs, L.Wg, L.Wu, w.moe.hbuf,
+                                        s));
+      }
+      st = moe_few(h, M, w.b, wt, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wd_s, h1, hidden, w.moe, s, true);
+      if (st != DEC_OK) return st;
+      if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
+      return DEC_OK;
+    }
     {
       LaunchScope scope(h, "router", s);
       DEC_CUDA(launch_route_shared(h, M, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx,

@@ -831,6 +831,400 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_kernel(const RouteShare
   }
 }
 
+// Two to four tokens: the MoE front in one launch. The routing and the
+// shared gate/up of route_shared_multi_kernel (the M rows normalised into
+// shared memory, every CTA's router units for every token, the last CTA's
+// top-k of all tokens and entry table; the shared expert's row pairs from the
+// queue, each applied to the M rows), then the routed entries' gate/up as in
+// moe_front_kernel: once the routing flag is seen, each CTA's static share
+// of the M k I row pairs, then the tail queue. Routed row q is row q mod I of
+// entry p = q / I (token p / k, its normalised row from shared memory);
+// outputs go to hbuf[q] (slot p's row at hbuf + p I).
+template <int J, int VPT, int MT>
+__global__ void __launch_bounds__(kThreads, 2) moe_front_multi_kernel(const RouteSharedParams P) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int H = P.H, H8 = H >> 3, M = P.M;
+  const int ngrp = (P.E + 7) / 8;
+  const int ksplit = (H + kUnitCols - 1) / kUnitCols;
+  extern __shared__ __align__(16) uint16_t sx[];  // the normalised rows [MT][H]
+  __shared__ float s_norm[kThreads / 32][MT];
+  __shared__ float red[2][kThreads / 32][2 * MT];
+  __shared__ int s_row[2];
+  __shared__ int s_next[2];
+  __shared__ int s_last;
+  __shared__ int s_ok;
+  const uint64_t pol = policy_evict_first();
+
+  float4 wv[kUnitCols / 128];
+  auto load_unit = [&](int u) {
+    const int e = (u % ngrp) * 8 + warp, k0 = (u / ngrp) * kUnitCols;
+    const int kn = min(kUnitCols, H - k0);
+#pragma unroll
+    for (int i = 0; i < kUnitCols / 128; ++i) {
+      const int kk = 4 * (lane + 32 * i);
+      wv[i] = (u < P.nunits && e < P.E && kk < kn)
+                  ? __ldg(reinterpret_cast<const float4*>(P.Wr + (size_t)e * H + k0 + kk))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  load_unit(c);
+  // (a grab that races the previous launch's reset finds the queue exhausted
+  // or already reset: that launch's CTAs trigger this one's predecessors only
+  // after their shared rows)
+  int base = 0;
+  if (t == 0) {
+    base = atomicAdd(&P.ctr[1], 3);
+    for (int q = 0; q < 3; ++q)
+      if (base + q < P.I) {
+        request_l2(P.Wg + (size_t)(base + q) * H, (size_t)H * 2);
+        request_l2(P.Wu + (size_t)(base + q) * H, (size_t)H * 2);
+      }
+  }
+  uint4 gv[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = t + kThreads * i;
+    gv[i] = v < H8 ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+  }
+  pdl_wait();
+
+  // RMSNorm of the M rows (each row's sum of squares in the RMSNorm kernel's order)
+  {
+    float ss[MT];
+#pragma unroll
+    for (int q = 0; q < MT; ++q) {
+      ss[q] = 0.f;
+      if (q < M) {
+        uint4 hv[VPT];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = t + kThreads * i;
+          hv[i] = v < H8 ? ld_act16(P.h1 + (size_t)q * H + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < VPT; ++i)
+          if (t + kThreads * i < H8) ss[q] = sumsq8(hv[i], ss[q]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss[q] += __shfl_xor_sync(0xffffffffu, ss[q], o);
+      if (lane == 0) s_norm[warp][q] = ss[q];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < MT; ++q) {
+      if (q < M) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) tot += s_norm[w][q];
+        const float r = rsqrtf(tot / (float)H + P.eps);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = t + kThreads * i;
+          if (v < H8)
+            *reinterpret_cast<uint4*>(&sx[(size_t)q * H + v * 8]) =
+                norm8(ld_act16(P.h1 + (size_t)q * H + (size_t)v * 8), gv[i], r);
+        }
+      }
+    }
+  }
+  int pending = base + 2;  // (thread 0)
+  __syncthreads();
+
+  // router logit pieces of this CTA's units for every token, then the hand-off
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int u = c + m * G;
+    if (m == 1 && u < P.nunits) load_unit(u);
+    if (u < P.nunits) {
+      const int e = (u % ngrp) * 8 + warp, ks = u / ngrp, k0 = ks * kUnitCols;
+      const int kn = min(kUnitCols, H - k0);
+      float acc[MT];
+#pragma unroll
+      for (int q = 0; q < MT; ++q) acc[q] = 0.f;
+#pragma unroll
+      for (int i = 0; i < kUnitCols / 128; ++i) {
+        const int kk = 4 * (lane + 32 * i);
+        if (kk < kn) {
+#pragma unroll
+          for (int q = 0; q < MT; ++q) {
+            if (q < M) {
+              const uint2 xv = *reinterpret_cast<const uint2*>(&sx[(size_t)q * H + k0 + kk]);
+              float a = acc[q];
+              a = fmaf(wv[i].x, bf_lo(xv.x), a);
+              a = fmaf(wv[i].y, bf_hi(xv.x), a);
+              a = fmaf(wv[i].z, bf_lo(xv.y), a);
+              a = fmaf(wv[i].w, bf_hi(xv.y), a);
+              acc[q] = a;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < MT; ++q) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+        if (lane == 0 && e < P.E && q < M) P.parts[((size_t)ks * M + q) * P.E + e] = acc[q];
+      }
+    }
+  }
+  if (t == 0) {
+    s_row[0] = base;
+    s_row[1] = base + 1;
+  }
+  __syncthreads();
+  if (t == 0) s_last = atom_add_acq_rel_gpu(&P.ctr[0], 1) == G - 1;
+  __syncthreads();
+  if (s_last) {
+    block_topk_tokens<J, MT>(P.parts, ksplit, M, P.E, P.k, P.idx, P.w, P.scores, P.table);
+    __syncthreads();  // every warp's entries are written before the release
+    if (t == 0) {
+      P.ctr[0] = 0;
+      P.ctr[5] = c;                  // this CTA's static share goes to the tail queue
+      st_release_gpu(&P.ctr[3], 1);  // the routing is written
+    }
+  }
+
+  uint4 wa[2][VPT];
+  auto load_rows = [&](uint4(&wr)[2][VPT], const uint16_t* g0, const uint16_t* u0) {
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = t + kThreads * i;
+        wr[a][i] = v < H8 ? ld_stream((a == 0 ? g0 : u0) + (size_t)v * 8, pol) : make_uint4(0, 0, 0, 0);
+      }
+  };
+  auto shift = [&](const uint4(&wb)[2][VPT]) {
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) wa[a][i] = wb[a][i];
+  };
+  int buf = 0;
+  const int I = P.I;
+  {  // the shared expert's rows, each applied to the M rows
+    int cur = s_row[0], nxt = s_row[1];
+    if (cur < I) load_rows(wa, P.Wg + (size_t)cur * H, P.Wu + (size_t)cur * H);
+    while (cur < I) {
+      uint4 wb[2][VPT];
+      if (nxt < I) load_rows(wb, P.Wg + (size_t)nxt * H, P.Wu + (size_t)nxt * H);
+      float g[MT], up[MT];
+#pragma unroll
+      for (int q = 0; q < MT; ++q) {
+        g[q] = 0.f;
+        up[q] = 0.f;
+        if (q < M) {
+#pragma unroll
+          for (int i = 0; i < VPT; ++i) {
+            const int v = t + kThreads * i;
+            if (v < H8) {
+              const uint4 xv = *reinterpret_cast<const uint4*>(&sx[(size_t)q * H + v * 8]);
+              g[q] = dot8(wa[0][i], xv, g[q]);
+              up[q] = dot8(wa[1][i], xv, up[q]);
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          g[q] += __shfl_xor_sync(0xffffffffu, g[q], o);
+          up[q] += __shfl_xor_sync(0xffffffffu, up[q], o);
+        }
+        if (lane == 0) {
+          red[buf][warp][2 * q] = g[q];
+          red[buf][warp][2 * q + 1] = up[q];
+        }
+      }
+      if (t == 0) {
+        s_next[buf] = pending;
+        if (pending < I) {
+          request_l2(P.Wg + (size_t)pending * H, (size_t)H * 2);
+          request_l2(P.Wu + (size_t)pending * H, (size_t)H * 2);
+          pending = atomicAdd(&P.ctr[1], 1);
+        }
+      }
+      __syncthreads();
+      if (t < M) {
+        float gs = 0.f, us = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+          gs += red[buf][w][2 * t];
+          us += red[buf][w][2 * t + 1];
+        }
+        P.hs[(size_t)t * I + cur] = f2bf(gs / (1.0f + expf(-gs)) * us);
+      }
+      const int nn = s_next[buf];
+      cur = nxt;
+      nxt = nn;
+      shift(wb);
+      buf ^= 1;
+    }
+  }
+
+  // the routing
+  __shared__ const uint16_t* s_g[32];
+  __shared__ const uint16_t* s_u[32];
+  if (t == 0) {
+    const unsigned long long t0 = globaltimer();
+    int ok = 1;
+    while (ld_acquire_gpu(&P.ctr[3]) == 0) {
+      if (globaltimer() - t0 > P.wait_ns) {
+        atomicOr(P.err, DEV_ERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (s_ok) {
+    __shared__ int s_tb, s_cstar;
+    const int n = M * P.k;  // entries
+    if (t < n) {
+      const long long e = ld_cg_s32(P.table + TableLayout(P.E, n).expert() + t);
+      s_g[t] = P.Wgb + e * I * H;
+      s_u[t] = P.Wub + e * I * H;
+    }
+    if (t == 0) s_cstar = ld_cg_s32(&P.ctr[5]);
+    __syncthreads();
+    pdl_trigger();
+    const int T = n * I;
+    const int bulk = T * 7 / 8 / G, tail0 = G * bulk;
+    const int cstar = s_cstar;
+    auto tail_row = [&](int v) { return v < bulk ? cstar * bulk + v : tail0 + v - bulk; };
+    const int ntail = bulk + T - tail0;
+    // one routed row pair: the dot products with its entry's token row, reduced and stored
+    auto routed_step = [&](int q, int e) {
+      const uint16_t* xrow = sx + (size_t)(e / P.k) * H;
+      float g = 0.f, up = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = t + kThreads * i;
+        const uint4 xv = v < H8 ? *reinterpret_cast<const uint4*>(&xrow[v * 8]) : make_uint4(0, 0, 0, 0);
+        g = dot8(wa[0][i], xv, g);
+        up = dot8(wa[1][i], xv, up);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        g += __shfl_xor_sync(0xffffffffu, g, o);
+        up += __shfl_xor_sync(0xffffffffu, up, o);
+      }
+      if (lane == 0) {
+        red[buf][warp][0] = g;
+        red[buf][warp][1] = up;
+      }
+      __syncthreads();
+      if (t == 0) {
+        float gs = 0.f, us = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+          gs += red[buf][w][0];
+          us += red[buf][w][1];
+        }
+        P.hbuf[q] = f2bf(gs / (1.0f + expf(-gs)) * us);
+      }
+      buf ^= 1;
+    };
+    auto rows = [&](int q, const uint16_t*& g0, const uint16_t*& u0) {
+      const int e = q / I, r = q - e * I;
+      g0 = s_g[e] + (size_t)r * H;
+      u0 = s_u[e] + (size_t)r * H;
+    };
+    int tb = 0;  // (thread 0) the first of three tail rows grabbed together, published in s_tb
+    const int q0 = c * bulk, q1 = c == cstar ? q0 : q0 + bulk;
+    if (q1 - q0 < 4) {
+      if (t == 0) {
+        tb = atomicAdd(&P.ctr[4], 3);
+        s_tb = tb;
+      }
+      __syncthreads();
+    }
+    bool wa_loaded = false;
+    if (q0 < q1) {  // this CTA's static share
+      int e = q0 / I, r = q0 - (q0 / I) * I;
+      load_rows(wa, s_g[e] + (size_t)r * H, s_u[e] + (size_t)r * H);
+      for (int q = q0; q < q1; ++q) {
+        int en = e, rn = r + 1;
+        if (rn == I) {
+          ++en;
+          rn = 0;
+        }
+        uint4 wb[2][VPT];
+        if (q + 1 < q1) {
+          load_rows(wb, s_g[en] + (size_t)rn * H, s_u[en] + (size_t)rn * H);
+        } else if (s_tb < ntail) {  // the first tail row follows without a gap
+          const uint16_t *g0, *u0;
+          rows(tail_row(s_tb), g0, u0);
+          load_rows(wb, g0, u0);
+          wa_loaded = true;
+        }
+        if (t == 0) {
+          if (q + 2 < q1) {  // the row after next into L2
+            const int e2 = rn + 1 == I ? en + 1 : en, r2 = rn + 1 == I ? 0 : rn + 1;
+            request_l2(s_g[e2] + (size_t)r2 * H, (size_t)H * 2);
+            request_l2(s_u[e2] + (size_t)r2 * H, (size_t)H * 2);
+          }
+          if (q + 3 == q1 && q1 - q0 >= 4) tb = atomicAdd(&P.ctr[4], 3);  // the tail grab
+          if (q + 2 == q1 && q1 - q0 >= 4) {
+            s_tb = tb;  // published at this iteration's barrier
+            for (int v = tb; v < tb + 2 && v < ntail; ++v) {
+              const uint16_t *g2, *u2;
+              rows(tail_row(v), g2, u2);
+              request_l2(g2, (size_t)H * 2);
+              request_l2(u2, (size_t)H * 2);
+            }
+          }
+        }
+        routed_step(q, e);
+        e = en;
+        r = rn;
+        shift(wb);
+      }
+    }
+    {  // the tail queue
+      const int v0 = s_tb;
+      int cur = v0, nxt = v0 + 1;
+      if (t == 0) pending = v0 + 2;
+      const uint16_t *g0, *u0;
+      if (cur < ntail && !wa_loaded) {
+        rows(tail_row(cur), g0, u0);
+        load_rows(wa, g0, u0);
+      }
+      while (cur < ntail) {
+        uint4 wb[2][VPT];
+        if (nxt < ntail) {
+          rows(tail_row(nxt), g0, u0);
+          load_rows(wb, g0, u0);
+        }
+        const int b0 = buf;
+        if (t == 0) {
+          s_next[b0] = pending;
+          if (pending < ntail) {
+            const uint16_t *g2, *u2;
+            rows(tail_row(pending), g2, u2);
+            request_l2(g2, (size_t)H * 2);
+            request_l2(u2, (size_t)H * 2);
+            pending = atomicAdd(&P.ctr[4], 1);
+          }
+        }
+        const int q = tail_row(cur);
+        routed_step(q, q / I);
+        const int nn = s_next[b0];
+        cur = nxt;
+        nxt = nn;
+        shift(wb);
+      }
+    }
+  }
+  if (t == 0 && atom_add_acq_rel_gpu(&P.ctr[2], 1) == G - 1) {
+    P.ctr[1] = 0;
+    P.ctr[2] = 0;
+    P.ctr[3] = 0;
+    P.ctr[4] = 0;
+  }
+}
+
 template <int J>
 cudaError_t launch_j(dec_handle* h, const RouteSharedParams& P, int vpt, cudaStream_t s) {
   const dim3 g(2 * h->sms), b(kThreads);
@@ -847,6 +1241,22 @@ cudaError_t launch_front_j(dec_handle* h, const RouteSharedParams& P, int vpt, c
   if (vpt == 1) return launch_k(h, moe_front_kernel<J, 1>, g, b, smem, s, P);
   if (vpt == 2) return launch_k(h, moe_front_kernel<J, 2>, g, b, smem, s, P);
   return launch_k(h, moe_front_kernel<J, 4>, g, b, smem, s, P);
+}
+
+template <int J, int MT>
+cudaError_t launch_front_multi(dec_handle* h, const RouteSharedParams& P, int vpt, cudaStream_t s) {
+  const dim3 g(2 * h->sms), b(kThreads);
+  const size_t smem = (size_t)MT * P.H * sizeof(uint16_t);
+  auto go = [&](auto kern) -> cudaError_t {
+    if (smem > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    return launch_k(h, kern, g, b, smem, s, P);
+  };
+  if (vpt == 1) return go(moe_front_multi_kernel<J, 1, MT>);
+  if (vpt == 2) return go(moe_front_multi_kernel<J, 2, MT>);
+  return go(moe_front_multi_kernel<J, 4, MT>);
 }
 
 template <int J, int MT>
@@ -956,6 +1366,51 @@ cudaError_t launch_moe_front(dec_handle* h, const uint16_t* h1, const uint16_t* 
   if (Ew <= 32) return launch_front_j<1>(h, P, vpt, s);
   if (Ew <= 64) return launch_front_j<2>(h, P, vpt, s);
   return launch_front_j<4>(h, P, vpt, s);
+}
+
+cudaError_t launch_moe_front_multi(dec_handle* h, int M, const uint16_t* h1, const uint16_t* gamma, float eps,
+                                   const float* Wr, int H, int E, int k, float* parts, int* ctr, int32_t* idx, float* w,
+                                   float* scores, int* table, const uint16_t* Wg_s, const uint16_t* Wu_s, int I,
+                                   uint16_t* hs, const uint16_t* Wg, const uint16_t* Wu, uint16_t* hbuf,
+                                   cudaStream_t s) {
+  if (M < 2 || M > 4 || !route_shared_supported(h, M, H, E, k) || Wg_s == nullptr || M * k > 32)
+    return cudaErrorInvalidValue;
+  RouteSharedParams P;
+  P.M = M;
+  P.h1 = h1;
+  P.gamma = gamma;
+  P.eps = eps;
+  P.Wr = Wr;
+  P.H = H;
+  P.E = E;
+  P.k = k;
+  P.nunits = ((E + 7) / 8) * ((H + kUnitCols - 1) / kUnitCols);
+  P.xn = nullptr;
+  P.parts = parts;
+  P.ctr = ctr;
+  P.idx = idx;
+  P.w = w;
+  P.scores = scores;
+  P.table = table;
+  P.Wg = Wg_s;
+  P.Wu = Wu_s;
+  P.I = I;
+  P.hs = hs;
+  P.Wgb = Wg;
+  P.Wub = Wu;
+  P.hbuf = hbuf;
+  P.err = h->d_err;
+  P.wait_ns = h->wait_ns;
+  const int H8 = H / 8, vpt = H8 <= kThreads ? 1 : (H8 <= 2 * kThreads ? 2 : 4);
+  const int Ew = (E + 7) / 8;
+  if (M == 2) {
+    if (Ew <= 32) return launch_front_multi<1, 2>(h, P, vpt, s);
+    if (Ew <= 64) return launch_front_multi<2, 2>(h, P, vpt, s);
+    return launch_front_multi<4, 2>(h, P, vpt, s);
+  }
+  if (Ew <= 32) return launch_front_multi<1, 4>(h, P, vpt, s);
+  if (Ew <= 64) return launch_front_multi<2, 4>(h, P, vpt, s);
+  return launch_front_multi<4, 4>(h, P, vpt, s);
 }
 
 }  // namespace dec

@@ -195,14 +195,16 @@ def test_layer_speculative_verify_batch(h, M, group):
         assert U < 0.8 * E * (1 - (1 - k / E) ** M), U
 
 
+@pytest.mark.parametrize("sched", [2, 1])
 @pytest.mark.parametrize("M", [2, 3, 4])
 @pytest.mark.parametrize("I,shared", [(128, True), (256, False), (256, True)])
-def test_layer_few_tokens(h, M, I, shared):
+def test_layer_few_tokens(h, M, I, shared, sched):
     """Two to four tokens on the small-matrix family (forced): one routing
-    launch (second RMSNorm, router, warp-per-token top-k, a routing table with
-    one problem per (token, expert) entry, and the shared expert's gate/up),
-    gate/up over the entries, down over the shared expert's M rows plus the
-    entries, then the combine."""
+    launch (second RMSNorm, router, per-token top-k, a routing table with one
+    problem per (token, expert) entry, and the shared expert's gate/up), the
+    entries' gate/up (sched 2, with a shared expert: inside that launch, the
+    MoE front; sched 1: a launch of its own), down over the shared expert's M
+    rows plus the entries, then the combine."""
     import moe_layers_gb300 as ML
     H, N_in, K_out, E, k = 1152, 264, 256, 40, 8
     L = Layer(H, N_in, K_out, E, I, k, base=6800 + I + M)
@@ -217,15 +219,17 @@ def test_layer_few_tokens(h, M, I, shared):
     dev_w = L.device(dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
                      None if sh is None else tuple(dev_bf16(a, a.shape) for a in sh))
     h.set_force_variant(ML.VARIANT_SMALL_M)
+    h.set_one_token_shared(sched)
     try:
         for rep in range(2):  # the counters must be back at zero after every call
             hbits, _ = gap_rows(L.scores, M, H, k, base=6900 + 10 * M + I + rep)
             hid, tr = _run(h, L, dev_w, hbits)
             assert h.last_expert_variant == ML.VARIANT_SMALL_M
             ref = L.oracle(hbits, lambda e: (g[e], u[e], d[e]), sh)
-            _check_layer(tr, hid, ref, slice(None), f"layer few tokens M={M} I={I} rep={rep}", L)
+            _check_layer(tr, hid, ref, slice(None), f"layer few tokens M={M} I={I} sched={sched} rep={rep}", L)
     finally:
         h.set_force_variant(ML.VARIANT_AUTO)
+        h.set_one_token_shared(2)
 
 
 def _check_layer(tr, hid, ref, rows, what, L=None):
@@ -247,10 +251,10 @@ def full_layer():
                  gamma_noise=False)
 
 
-@pytest.mark.parametrize("M,sched", [(1, 1), (1, 2), (1, 0), (2, 1), (4, 1), (8, 1), (16, 1), (32, 1), (64, 1)])
+@pytest.mark.parametrize("M,sched", [(1, 2), (1, 1), (1, 0), (2, 2), (2, 1), (4, 2), (8, 2), (16, 2), (32, 2), (64, 2)])
 def test_layer_full_size(h, full_bank, full_layer, M, sched):
-    """The full-size layer; at one token also the two other schedules of the
-    shared expert (sched: set_one_token_shared)."""
+    """The full-size layer; at one and two tokens also the other schedules of
+    the shared expert (sched: set_one_token_shared)."""
     Wg, Wu, Wd, sh = full_bank
     L = full_layer
     hbits, _ = gap_rows(L.scores, M, H_FULL, K_FULL, base=synth.X_BASE + 30)
