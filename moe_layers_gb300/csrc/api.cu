@@ -361,6 +361,16 @@ dec_status moe_few(dec_handle* h, int M, const uint16_t* x, const float* w, int 
     DEC_CUDA(launch_gemv_moe(h, true, Wg, Wu, I, I, H, x, H, ws.table, E, n, ws.hbuf, I, h->sms, s, nullptr, n,
                              true, true));
   }
+  if (M == 2 && gemv_down_combine2_supported(k, I)) {
+    // two tokens: down, weighted combine and residual in one kernel (the shared
+    // W_d read once for both rows); the routing is read before the dependency
+    // wait, as the launch before triggers its dependents only once the routing
+    // is written
+    LaunchScope scope(h, "down", s);
+    DEC_CUDA(launch_gemv_down_combine2(h, Wd, H, Wd_s, H, I, ws.hbuf, ws.hs, ws.table, E, k, w, residual, out, h->sms,
+                                       s, true));
+    return DEC_OK;
+  }
   GemvMoeShared sdn{Wd_s, nullptr, ws.hs, ws.ys};
   sdn.n = M;
   sdn.ldx = I;

@@ -474,6 +474,153 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine_narrow_kernel
 }
 
 // Rows of up to 2048 elements (one vector per thread per row, activations in registers).
+// Two tokens: the down projection of the 2 k entries and of the shared
+// expert, the weighted combine and the residual in one kernel (the one-token
+// kernel above, extended). Output row n of token m:
+//   out[m][n] = res[m][n] + sum_j w_j (W_d[e_j] h_j)[n] + (W_d_s h_s[m])[n]
+// over token m's entries j (slots m k .. m k + k - 1). Unit: output row n of
+// every selected matrix (row n of the shared W_d is read once and applied to
+// both tokens' h_s rows). Thread t owns column vector t of every row; its
+// activation vectors (one per entry, two for the shared expert) sit in
+// shared memory (each thread reads only its own), which leaves the
+// registers to the ring of weight vectors.
+template <int NE, bool SHARED>
+__global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine2_kernel(
+    const uint16_t* __restrict__ Wd, long long rows_bank, const uint16_t* __restrict__ Wd_s, int H, int K,
+    const uint16_t* hbuf, const uint16_t* hs, const int* table, int E, int k, const float* w, const uint16_t* res,
+    uint16_t* out, int routing_ready, int ahead) {
+  constexpr int NP = SHARED ? NE + 1 : NE;  // matrices per unit
+  constexpr int NX = SHARED ? NE + 2 : NE;  // activation vectors per thread
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int K8 = K >> 3;
+  __shared__ __align__(16) float red[2][kGmThreads / 32][2];
+  extern __shared__ __align__(16) uint4 sxv[];  // [NX][kGmThreads]
+  const uint64_t pol = policy_evict_first();
+  pdl_trigger();
+  const long long G = gridDim.x, c = blockIdx.x;
+  const int n0 = (int)(c * H / G), n1 = (int)((c + 1) * H / G);
+  if (n0 >= n1) return;  // (before any barrier)
+  const TableLayout L(E, NE);
+  __shared__ const uint16_t* s_rowbase[NP];
+  __shared__ float s_w[NE];
+  auto routing = [&](bool cg) {
+    if (t < NP) {
+      if (SHARED && t == NE) {
+        s_rowbase[t] = Wd_s;
+      } else {
+        // entry t on slot t (one problem per entry)
+        const long long e = cg ? ld_cg_s32(table + L.expert() + t) : ld_act_s32(table + L.expert() + t);
+        s_rowbase[t] = Wd + e * rows_bank * K;
+        s_w[t] = cg ? ld_cg_f32(w + t) : ld_act_f32(w + t);
+      }
+    }
+    __syncthreads();
+  };
+  uint4 ring[NP];
+  auto load1 = [&](int j, int n) {
+    return t < K8 ? ld_stream(s_rowbase[j] + (size_t)n * K + (size_t)t * 8, pol) : make_uint4(0, 0, 0, 0);
+  };
+  const int rowb = K * (int)sizeof(uint16_t);
+  const int ahead_rows = ahead > 0 ? max(1, ahead / (NP * rowb)) : 0;
+  int pf = n0 + 1;
+  auto request = [&](int upto) {
+    upto = min(upto, n1);
+    if (ahead_rows > 0 && upto > pf) {
+      if (t < NP) request_l2(s_rowbase[t] + (size_t)pf * K, (size_t)(upto - pf) * rowb);
+      pf = upto;
+    }
+  };
+  if (routing_ready) {
+    routing(true);
+#pragma unroll
+    for (int j = 0; j < NP; ++j) ring[j] = load1(j, n0);
+    request(n0 + 1 + ahead_rows);
+  }
+  pdl_wait();
+  if (!routing_ready) {
+    routing(false);
+#pragma unroll
+    for (int j = 0; j < NP; ++j) ring[j] = load1(j, n0);
+    request(n0 + 1 + ahead_rows);
+  }
+  // this thread's activation vectors: the entries' rows, then the two shared rows
+#pragma unroll
+  for (int j = 0; j < NX; ++j) {
+    const uint16_t* row = j < NE ? hbuf + (size_t)j * K : hs + (size_t)(j - NE) * K;
+    sxv[j * kGmThreads + t] = t < K8 ? ld_act16(row + (size_t)t * 8) : make_uint4(0, 0, 0, 0);
+  }
+  __shared__ float s_res[2][64];
+  for (int q = t; q < 2 * 64; q += kGmThreads) {
+    const int m = q / 64, r = q % 64;
+    if (r < n1 - n0) s_res[m][r] = res ? bf2f(ld_act_u16(res + (size_t)m * H + n0 + r)) : 0.f;
+  }
+  __syncthreads();
+  const int kk = NE / 2;  // entries per token
+  int buf = 0;
+  for (int n = n0; n < n1; ++n) {
+    const bool more = n + 1 < n1;
+    request(n + 2 + ahead_rows);
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < NE; ++j) {
+      const uint4 wv = ring[j];
+      if (more) ring[j] = load1(j, n + 1);
+      const float d = dot8(wv, sxv[j * kGmThreads + t], 0.f);
+      if (j < kk)
+        a0 = fmaf(s_w[j], d, a0);
+      else
+        a1 = fmaf(s_w[j], d, a1);
+    }
+    if constexpr (SHARED) {
+      const uint4 wv = ring[NE];
+      if (more) ring[NE] = load1(NE, n + 1);
+      a0 += dot8(wv, sxv[NE * kGmThreads + t], 0.f);
+      a1 += dot8(wv, sxv[(NE + 1) * kGmThreads + t], 0.f);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+      a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+    }
+    if (lane == 0) {
+      red[buf][warp][0] = a0;
+      red[buf][warp][1] = a1;
+    }
+    __syncthreads();
+    if (t < 2) {
+      float y = 0.f;
+#pragma unroll
+      for (int q = 0; q < kGmThreads / 32; ++q) y += red[buf][q][t];
+      if (res != nullptr) y += (n - n0 < 64) ? s_res[t][n - n0] : bf2f(ld_act_u16(res + (size_t)t * H + n));
+      out[(size_t)t * H + n] = f2bf(y);
+    }
+    buf ^= 1;
+  }
+}
+
+bool gemv_down_combine2_supported(int k, int I) {
+  return k == 8 && I >= 8 && I % 8 == 0 && I / 8 > 32 && I <= 8 * kGmThreads;
+}
+
+cudaError_t launch_gemv_down_combine2(dec_handle* h, const uint16_t* Wd, long long rows_bank, const uint16_t* Wd_s,
+                                      int H, int I, const uint16_t* hbuf, const uint16_t* hs, const int* table, int E,
+                                      int k, const float* w, const uint16_t* res, uint16_t* out, int sms,
+                                      cudaStream_t s, bool routing_ready) {
+  if (!gemv_down_combine2_supported(k, I)) return cudaErrorInvalidValue;
+  const dim3 g(std::max(1, 2 * sms)), b(kGmThreads);
+  const int rr = (int)routing_ready, a = h->l2_ahead;
+  auto go = [&](auto kern, int nx) -> cudaError_t {
+    const size_t smem = (size_t)nx * kGmThreads * sizeof(uint4);
+    if (smem > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    return launch_k(h, kern, g, b, smem, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs, table, E, k, w, res, out, rr, a);
+  };
+  if (Wd_s != nullptr) return go(gemv_down_combine2_kernel<16, true>, 18);
+  return go(gemv_down_combine2_kernel<16, false>, 16);
+}
+
 bool gemv_down_combine_supported(int k, int I) { return k == 8 && I >= 8 && I % 8 == 0 && I <= 8 * kGmThreads; }
 
 cudaError_t launch_gemv_down_combine(dec_handle* h, const uint16_t* Wd, long long rows_bank, const uint16_t* Wd_s,

@@ -197,14 +197,16 @@ def test_layer_speculative_verify_batch(h, M, group):
 
 @pytest.mark.parametrize("sched", [2, 1])
 @pytest.mark.parametrize("M", [2, 3, 4])
-@pytest.mark.parametrize("I,shared", [(128, True), (256, False), (256, True)])
+@pytest.mark.parametrize("I,shared", [(128, True), (256, False), (256, True), (384, True), (512, False)])
 def test_layer_few_tokens(h, M, I, shared, sched):
     """Two to four tokens on the small-matrix family (forced): one routing
     launch (second RMSNorm, router, per-token top-k, a routing table with one
     problem per (token, expert) entry, and the shared expert's gate/up), the
     entries' gate/up (sched 2, with a shared expert: inside that launch, the
     MoE front; sched 1: a launch of its own), down over the shared expert's M
-    rows plus the entries, then the combine."""
+    rows plus the entries, then the combine. At two tokens with I > 256 the
+    down, the combine and the residual are one kernel (I = 384: a ragged
+    thread count; I = 512 without a shared expert)."""
     import moe_layers_gb300 as ML
     H, N_in, K_out, E, k = 1152, 264, 256, 40, 8
     L = Layer(H, N_in, K_out, E, I, k, base=6800 + I + M)
