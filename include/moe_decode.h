@@ -338,6 +338,15 @@ uint64_t dec_launch_count(const dec_handle* h);
  * that timeouts surface as DEC_ERR_TIMEOUT with the context still usable. */
 dec_status dec_test_wait_timeout(dec_handle* h, cudaStream_t stream);
 
+/* Run the MoE front launch (tokens: 1, or 2 for the few-token kernel) on a
+ * small zeroed problem whose routing hand-off can never complete (its arrival
+ * counter starts past the grid size), so the routing flag is never set: every
+ * CTA's wait for it must give up after the handle's wait limit and set the
+ * device error word. Allocates and frees its own buffers and synchronises
+ * `stream`. Used to test that the routing wait surfaces as DEC_ERR_TIMEOUT
+ * with the context still usable. tokens outside {1, 2}: DEC_ERR_INVALID_ARG. */
+dec_status dec_test_routing_wait_timeout(dec_handle* h, int tokens, cudaStream_t stream);
+
 /* Copy `bytes` from src to dst on `stream` after spinning for delay_ns
  * (bounded by the clock): a slow producer for ordering tests of the
  * programmatic-dependent-launch path. */

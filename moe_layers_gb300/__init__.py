@@ -84,6 +84,7 @@ def _load():
         "decode_layer": [P, ctypes.POINTER(_LayerWeights), P, I, ctypes.POINTER(_LayerTrace), P, Z, P],
         "dec_prefetch_l2": [P, P, Z, P],
         "dec_test_wait_timeout": [P, P],
+        "dec_test_routing_wait_timeout": [P, I, P],
         "dec_test_delayed_copy": [P, P, P, Z, U64, P],
         "dec_set_profiling": [P, I],
         "dec_profile_read": [P, ctypes.POINTER(_KernelTime), I, ctypes.POINTER(I)],
@@ -427,6 +428,10 @@ def dec_prefetch_l2(h: Handle, t, nbytes: Optional[int] = None, stream=None) -> 
 
 def test_wait_timeout(h: Handle, stream=None) -> None:
     _check(_load().dec_test_wait_timeout(h.ptr, _stream(stream)), "dec_test_wait_timeout")
+
+def test_routing_wait_timeout(h: Handle, tokens: int = 1, stream=None) -> None:
+    _check(_load().dec_test_routing_wait_timeout(h.ptr, int(tokens), _stream(stream)),
+           "dec_test_routing_wait_timeout")
 
 
 def test_delayed_copy(h: Handle, dst, src, delay_ns: int, stream=None) -> None:

@@ -971,6 +971,59 @@ dec_status dec_test_wait_timeout(dec_handle* h, cudaStream_t stream) {
   return launch_wait_timeout_probe(h, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
 }
 
+dec_status dec_test_routing_wait_timeout(dec_handle* h, int tokens, cudaStream_t stream) {
+  if (h == nullptr || (tokens != 1 && tokens != 2)) return DEC_ERR_INVALID_ARG;
+  const int H = 256, E = 16, k = 4, I = 64, M = tokens;
+  // one zeroed allocation carved into every buffer of the launch (16-byte aligned pieces)
+  const size_t n_bank = (size_t)E * I * H, n_sh = (size_t)I * H;
+  size_t off = 0;
+  auto piece = [&](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + 255) / 256 * 256;
+    return at;
+  };
+  const size_t o_h1 = piece((size_t)M * H * 2), o_g = piece((size_t)H * 2), o_wr = piece((size_t)E * H * 4),
+               o_parts = piece((size_t)M * E * 4), o_ctr = piece(8 * 4), o_idx = piece((size_t)M * k * 4),
+               o_w = piece((size_t)M * k * 4), o_sc = piece((size_t)M * E * 4),
+               o_tab = piece((size_t)TableLayout(E, M * k).words() * 4), o_gs = piece(n_sh * 2),
+               o_us = piece(n_sh * 2), o_hs = piece((size_t)M * I * 2), o_gb = piece(n_bank * 2),
+               o_ub = piece(n_bank * 2), o_hb = piece((size_t)M * k * I * 2);
+  char* base = nullptr;
+  if (cudaMalloc(&base, off) != cudaSuccess) return DEC_ERR_CUDA;
+  dec_status st = DEC_OK;
+  const int past = 1 << 30;  // the hand-off count starts past any grid size
+  if (cudaMemsetAsync(base, 0, off, stream) != cudaSuccess ||
+      cudaMemcpyAsync(base + o_ctr, &past, sizeof(int), cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+    st = DEC_ERR_CUDA;
+  } else {
+    LaunchScope scope(h, "test_routing_wait", stream);
+    const uint16_t* h1 = reinterpret_cast<const uint16_t*>(base + o_h1);
+    const uint16_t* g = reinterpret_cast<const uint16_t*>(base + o_g);
+    const float* wr = reinterpret_cast<const float*>(base + o_wr);
+    float* parts = reinterpret_cast<float*>(base + o_parts);
+    int* ctr = reinterpret_cast<int*>(base + o_ctr);
+    int32_t* idx = reinterpret_cast<int32_t*>(base + o_idx);
+    float* w = reinterpret_cast<float*>(base + o_w);
+    float* sc = reinterpret_cast<float*>(base + o_sc);
+    int* tab = reinterpret_cast<int*>(base + o_tab);
+    const uint16_t* gs = reinterpret_cast<const uint16_t*>(base + o_gs);
+    const uint16_t* us = reinterpret_cast<const uint16_t*>(base + o_us);
+    uint16_t* hs = reinterpret_cast<uint16_t*>(base + o_hs);
+    const uint16_t* gb = reinterpret_cast<const uint16_t*>(base + o_gb);
+    const uint16_t* ub = reinterpret_cast<const uint16_t*>(base + o_ub);
+    uint16_t* hb = reinterpret_cast<uint16_t*>(base + o_hb);
+    const cudaError_t e =
+        tokens == 1 ? launch_moe_front(h, h1, g, 1e-6f, wr, H, E, k, parts, ctr, idx, w, sc, tab, gs, us, I, hs, gb, ub,
+                                       hb, stream)
+                    : launch_moe_front_multi(h, M, h1, g, 1e-6f, wr, H, E, k, parts, ctr, idx, w, sc, tab, gs, us, I,
+                                             hs, gb, ub, hb, stream);
+    if (e != cudaSuccess) st = DEC_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(stream) != cudaSuccess) st = DEC_ERR_CUDA;
+  cudaFree(base);
+  return st;
+}
+
 dec_status dec_test_delayed_copy(dec_handle* h, void* dst, const void* src, size_t bytes, uint64_t delay_ns,
                                  cudaStream_t stream) {
   if (h == nullptr || dst == nullptr || src == nullptr || !al16(dst) || !al16(src) || bytes % 16 != 0 ||

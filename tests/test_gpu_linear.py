@@ -204,6 +204,28 @@ def test_wait_timeout_surfaces_as_status(h, torch_cuda):
     assert_bf16_close(host_bits(y), oracle.linear(x, W), "after timeout")
 
 
+@pytest.mark.parametrize("tokens", [1, 2])
+def test_routing_wait_timeout_surfaces_as_status(h, torch_cuda, tokens):
+    """The MoE front's CTAs wait for the routing flag with a bounded wait: on a
+    problem whose hand-off never completes (nothing sets the flag) every CTA
+    gives up after the limit, the error word reads DEC_ERR_TIMEOUT, and the
+    context stays usable."""
+    import moe_layers_gb300 as ML
+    assert h.check_device_error() == ML.DEC_OK
+    h.set_wait_limit_ns(2_000_000)
+    try:
+        ML.test_routing_wait_timeout(h, tokens)
+        assert h.check_device_error() == ML.DEC_ERR_TIMEOUT
+        assert h.check_device_error() == ML.DEC_OK  # cleared
+    finally:
+        h.set_wait_limit_ns(500_000_000)
+    with pytest.raises(ML.DecodeError):
+        ML.test_routing_wait_timeout(h, 3)
+    x, W = _mats(2, 256, 512, 1310)
+    y = ML.dec_linear(h, dev_bf16(x, (2, 512)), dev_bf16(W, (256, 512)))
+    assert_bf16_close(host_bits(y), oracle.linear(x, W), "after the routing timeout")
+
+
 def test_bad_arguments_launch_nothing(h, torch_cuda):
     import moe_layers_gb300 as ML
     torch = torch_cuda
