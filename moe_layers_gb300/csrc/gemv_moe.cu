@@ -598,8 +598,120 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine2_kernel(
   }
 }
 
+// Two tokens on narrow rows (K / 8 <= TPR <= 32 vectors): the kernel above in
+// the layout of gemv_down_combine_narrow_kernel. A group of TPR threads owns
+// an output row (256 / TPR rows at a time), thread j of a group column vector
+// j of every selected matrix's row. The activation vectors (column j of the 16
+// entries' rows and of both h_s rows) are the same for every group, so they
+// sit once in shared memory. Loads are unconditional at clamped, in-range
+// addresses (a lane past the row's vectors meets a zero activation; a group
+// past the CTA's rows computes on its last row and writes nothing), and every
+// group runs the same steps, so whole-warp shuffles never meet diverged lanes.
+template <int NE, int TPR, bool SHARED>
+__global__ void __launch_bounds__(kGmThreads, 2) gemv_down_combine2_narrow_kernel(
+    const uint16_t* __restrict__ Wd, long long rows_bank, const uint16_t* __restrict__ Wd_s, int H, int K,
+    const uint16_t* hbuf, const uint16_t* hs, const int* table, int E, int k, const float* w, const uint16_t* res,
+    uint16_t* out, int routing_ready, int ahead) {
+  constexpr int NP = SHARED ? NE + 1 : NE;
+  constexpr int NX = SHARED ? NE + 2 : NE;
+  constexpr int NG = kGmThreads / TPR;
+  const int t = threadIdx.x, g = t / TPR, j = t % TPR;
+  const int K8 = K >> 3;
+  const uint64_t pol = policy_evict_first();
+  pdl_trigger();
+  const long long G = gridDim.x, c = blockIdx.x;
+  const int n0 = (int)(c * H / G), n1 = (int)((c + 1) * H / G);
+  if (n0 >= n1) return;  // (before any barrier)
+  const TableLayout L(E, NE);
+  __shared__ const uint16_t* s_rowbase[NP];
+  __shared__ float s_w[NE];
+  __shared__ __align__(16) uint4 sx[NX][TPR];
+  auto routing = [&](bool cg) {
+    if (t < NP) {
+      if (SHARED && t == NE) {
+        s_rowbase[t] = Wd_s;
+      } else {
+        const long long e = cg ? ld_cg_s32(table + L.expert() + t) : ld_act_s32(table + L.expert() + t);
+        s_rowbase[t] = Wd + e * rows_bank * K;
+        s_w[t] = cg ? ld_cg_f32(w + t) : ld_act_f32(w + t);
+      }
+    }
+    __syncthreads();
+  };
+  const int jj = min(j, K8 - 1);
+  uint4 ring[NP];
+  auto load_row = [&](int n) {
+    const int nn = min(n, n1 - 1);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) ring[q] = ld_stream(s_rowbase[q] + (size_t)nn * K + (size_t)jj * 8, pol);
+  };
+  const int rowb = K * (int)sizeof(uint16_t);
+  const int ahead_rows = ahead > 0 ? max(1, ahead / (NP * rowb)) : 0;
+  int pf = n0 + NG;
+  auto request = [&](int upto) {
+    upto = min(upto, n1);
+    if (ahead_rows > 0 && upto > pf) {
+      if (t < NP) request_l2(s_rowbase[t] + (size_t)pf * K, (size_t)(upto - pf) * rowb);
+      pf = upto;
+    }
+  };
+  if (routing_ready) {
+    routing(true);
+    load_row(n0 + g);
+    request(n0 + NG + ahead_rows);
+  }
+  pdl_wait();
+  if (!routing_ready) {
+    routing(false);
+    load_row(n0 + g);
+    request(n0 + NG + ahead_rows);
+  }
+  for (int q = t; q < NX * TPR; q += kGmThreads) {
+    const int r = q / TPR, jx = q % TPR;
+    const uint16_t* row = r < NE ? hbuf + (size_t)r * K : hs + (size_t)(r - NE) * K;
+    sx[r][jx] = jx < K8 ? ld_act16(row + (size_t)jx * 8) : make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  constexpr int KK = NE / 2;  // entries per token
+  for (int nb = n0; nb < n1; nb += NG) {
+    const int n = nb + g;
+    if (g == 0) request(n + 2 * NG + ahead_rows);  // (only threads t < NP issue)
+    float a0 = 0.f, a1 = 0.f;
+    const int nn = min(n + NG, n1 - 1);
+#pragma unroll
+    for (int q = 0; q < NE; ++q) {
+      const uint4 wv = ring[q];
+      ring[q] = ld_stream(s_rowbase[q] + (size_t)nn * K + (size_t)jj * 8, pol);
+      const float d = dot8(wv, sx[q][j], 0.f);
+      if (q < KK)
+        a0 = fmaf(s_w[q], d, a0);
+      else
+        a1 = fmaf(s_w[q], d, a1);
+    }
+    if constexpr (SHARED) {
+      const uint4 wv = ring[NE];
+      ring[NE] = ld_stream(s_rowbase[NE] + (size_t)nn * K + (size_t)jj * 8, pol);
+      a0 += dot8(wv, sx[NE][j], 0.f);
+      a1 += dot8(wv, sx[NE + 1][j], 0.f);
+    }
+#pragma unroll
+    for (int o = TPR / 2; o > 0; o >>= 1) {
+      a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+      a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+    }
+    if (j == 0 && n < n1) {
+      if (res != nullptr) {
+        a0 += bf2f(ld_act_u16(res + n));
+        a1 += bf2f(ld_act_u16(res + (size_t)H + n));
+      }
+      out[n] = f2bf(a0);
+      out[(size_t)H + n] = f2bf(a1);
+    }
+  }
+}
+
 bool gemv_down_combine2_supported(int k, int I) {
-  return k == 8 && I >= 8 && I % 8 == 0 && I / 8 > 32 && I <= 8 * kGmThreads;
+  return k == 8 && I >= 8 && I % 8 == 0 && I <= 8 * kGmThreads;
 }
 
 cudaError_t launch_gemv_down_combine2(dec_handle* h, const uint16_t* Wd, long long rows_bank, const uint16_t* Wd_s,
@@ -617,6 +729,18 @@ cudaError_t launch_gemv_down_combine2(dec_handle* h, const uint16_t* Wd, long lo
     }
     return launch_k(h, kern, g, b, smem, s, Wd, rows_bank, Wd_s, H, I, hbuf, hs, table, E, k, w, res, out, rr, a);
   };
+  if (I / 8 <= 32) {  // narrow rows: a group of 16 or 32 threads per output row
+    const bool n16 = I / 8 <= 16;
+    if (Wd_s != nullptr)
+      return n16 ? launch_k(h, gemv_down_combine2_narrow_kernel<16, 16, true>, g, b, 0, s, Wd, rows_bank, Wd_s, H, I,
+                            hbuf, hs, table, E, k, w, res, out, rr, a)
+                 : launch_k(h, gemv_down_combine2_narrow_kernel<16, 32, true>, g, b, 0, s, Wd, rows_bank, Wd_s, H, I,
+                            hbuf, hs, table, E, k, w, res, out, rr, a);
+    return n16 ? launch_k(h, gemv_down_combine2_narrow_kernel<16, 16, false>, g, b, 0, s, Wd, rows_bank, Wd_s, H, I,
+                          hbuf, hs, table, E, k, w, res, out, rr, a)
+               : launch_k(h, gemv_down_combine2_narrow_kernel<16, 32, false>, g, b, 0, s, Wd, rows_bank, Wd_s, H, I,
+                          hbuf, hs, table, E, k, w, res, out, rr, a);
+  }
   if (Wd_s != nullptr) return go(gemv_down_combine2_kernel<16, true>, 18);
   return go(gemv_down_combine2_kernel<16, false>, 16);
 }

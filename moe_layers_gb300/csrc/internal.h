@@ -120,8 +120,8 @@ bool gemv_moe_supported(int K);
 // One token: down projection of the k routed (+ shared) experts fused with the
 // weighted combine and the residual, written straight to out (bf16 [H]).
 bool gemv_down_combine_supported(int k, int I);
-// Two tokens, k = 8, 256 < I <= 2048: down of the 16 entries and the shared
-// expert, weighted combine and residual in one kernel (out, res [2][H]).
+// Two tokens, k = 8, I <= 2048: down of the 16 entries and the shared expert,
+// weighted combine and residual in one kernel (out, res [2][H]).
 bool gemv_down_combine2_supported(int k, int I);
 cudaError_t launch_gemv_down_combine2(dec_handle* h, const uint16_t* Wd, long long rows_bank, const uint16_t* Wd_s,
                                       int H, int I, const uint16_t* hbuf, const uint16_t* hs, const int* table, int E,

@@ -306,7 +306,7 @@ def tp_layer(request):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("M", [1, 4, 64])
+@pytest.mark.parametrize("M", [1, 2, 4, 64])
 def test_layer_tp_shapes(h, tp_layer, M):
     sh, L, dev_w, bank, sh_bits = tp_layer
     hbits, _ = gap_rows(L.scores, M, L.H, L.k, base=synth.X_BASE + 60 + sh)
