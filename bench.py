@@ -24,6 +24,7 @@ Reported (one JSON line, rank 0):
   roofline     dominant kernel of the --batch step: algorithmic bytes / its
                event-timed duration, against the measured HBM copy bandwidth
   cpu_baseline the fp64 oracle on the host cores, on one token of the step
+               (single_core: the same with one BLAS/OpenMP thread, in a child process)
 With --impl reference the fp64 oracle is the timed arm.
 
 Multi-GPU (torchrun, --gpus N): the decode layer does not shard across GPUs
@@ -551,9 +552,31 @@ def cpu_baseline(M: int, steps: int = 1) -> dict:
     s.prepare()
     secs = [s.run() for _ in range(max(1, steps))]
     per_token_us = statistics.median(secs) * 1e6
-    return {"value": round(per_token_us * M, 1), "unit": "us/step", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"1 token of the M={M} decode-layer step (fp64 numpy oracle, weights widened inside), "
-                      f"scaled by M; median of {len(secs)} run(s)"}
+    out = {"value": round(per_token_us * M, 1), "unit": "us/step", "cores": blas_threads(), "kind": "oracle",
+           "sample": f"1 token of the M={M} decode-layer step (fp64 numpy oracle, weights widened inside), "
+                     f"scaled by M; median of {len(secs)} run(s)"}
+    one = oracle_one_thread(M)
+    if one is not None:
+        out["single_core"] = {"value": one, "unit": "us/step", "cores": 1}
+    return out
+
+
+def oracle_one_thread(M: int):
+    """The same sample in a child process whose BLAS and OpenMP pools hold one
+    thread (the pools are fixed when numpy loads); None if it fails."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-thread", str(M)], env=env,
+                           capture_output=True, text=True, timeout=600)
+        return round(float(json.loads(r.stdout.strip().splitlines()[-1])["us"]) * M, 1)
+    except Exception:
+        return None
+
+
+def _oracle_one_thread_main(M: int) -> None:
+    s = _OracleSample(M)
+    s.prepare()
+    print(json.dumps({"us": s.run() * 1e6}), flush=True)
 
 
 def run_reference(args, rank, world):
@@ -578,6 +601,9 @@ def run_reference(args, rank, world):
 
 
 def main(argv=None):
+    if argv is None and len(sys.argv) == 3 and sys.argv[1] == "--oracle-one-thread":
+        _oracle_one_thread_main(int(sys.argv[2]))
+        return
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
