@@ -293,15 +293,17 @@ dec_status decode_layer_workspace_size(const dec_handle* h, const dec_layer_weig
  *   idx, w = top-k(sigmoid(b W_r^T))                                    [K3 P1§3]
  *   h  = h1 + sum_j w_j E_idx_j(b) + S(b)
  * The attention core, which the pages do not define, is read as the identity
- * on the first K_out columns of y. At M = 1 the layer is five launches on
+ * on the first K_out columns of y. At M = 1 the layer is four launches on
  * `stream`: in-projection with the first RMSNorm, out-projection with the
- * residual, one routing launch (second RMSNorm, router, top-k, routing
- * table, and the shared expert's gate/up streamed meanwhile), gate/up of the
- * selected experts, and the down projection (selected and shared experts)
- * fused with the combine and the residual. For M >= 2 the shared
- * expert runs on the handle's side stream [K3 P1§3]. While the router and
- * top-k run, the `prefetch_next` region (if any) is pulled into L2 on a
- * second side stream [K3 P1§4]. trace may be NULL. */
+ * residual, the MoE front (second RMSNorm, router, top-k, routing table, the
+ * shared expert's gate/up streamed meanwhile, then the selected experts'
+ * gate/up), and the down projection (selected and shared experts) fused with
+ * the combine and the residual; M = 2 is the same with two rows. For M >= 3
+ * the split-K family runs the shared expert on the handle's side stream
+ * [K3 P1§3]. While the router and top-k run, the `prefetch_next` region (if
+ * any) is pulled into L2 [K3 P1§4]: by the MoE front's CTAs while they wait
+ * for the routing, else by a kernel on a second side stream. trace may be
+ * NULL. */
 dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hidden, int M,
                         const dec_layer_trace* trace, void* ws, size_t ws_bytes, cudaStream_t stream);
 

@@ -824,8 +824,18 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   // memory idle, a side-stream kernel pulls weights that come next into L2:
   // at one token the shared expert (it runs inside the routed launches), and
   // the caller's next-operator region if given.
+  // The MoE front launches (one token; two to four on the small-matrix
+  // family) pull the next-operator region themselves, from the CTAs that wait
+  // for the routing, so the side stream then carries only the shared expert.
+  const bool front1 = one_token && L.Wg_s != nullptr && h->fuse_shared_routing == 2 &&
+                      route_shared_supported(h, 1, H, L.E, L.k) && gemv_down_combine_supported(L.k, L.I);
+  const bool front_few = few_tokens && L.Wg_s != nullptr && h->fuse_shared_routing == 2 && M * L.k <= 32;
+  const bool next_in_front = (front1 || front_few) && L.prefetch_next != nullptr && L.prefetch_bytes > 0;
   const bool pf_shared = L.Wg_s != nullptr && experts_small(h, M, H, L.I) && h->prefetch_shared;
-  const bool pf = (L.prefetch_next != nullptr && L.prefetch_bytes > 0) || pf_shared;
+  const bool pf_next_side = L.prefetch_next != nullptr && L.prefetch_bytes > 0 && !next_in_front;
+  const bool pf = pf_next_side || pf_shared;
+  const void* pf_front = next_in_front ? L.prefetch_next : nullptr;
+  const size_t pf_front_bytes = next_in_front ? L.prefetch_bytes : 0;
   if (pf) {
     DEC_CUDA(cudaEventRecord(h->ev_pf_fork, s));
     DEC_CUDA(cudaStreamWaitEvent(h->pf, h->ev_pf_fork, 0));
@@ -837,8 +847,7 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
         DEC_CUDA(launch_prefetch(h, L.Wu_s, mat, 16, h->pf));
         DEC_CUDA(launch_prefetch(h, L.Wd_s, mat, 16, h->pf));
       }
-      if (L.prefetch_next != nullptr && L.prefetch_bytes > 0)
-        DEC_CUDA(launch_prefetch(h, L.prefetch_next, L.prefetch_bytes, 16, h->pf));
+      if (pf_next_side) DEC_CUDA(launch_prefetch(h, L.prefetch_next, L.prefetch_bytes, 16, h->pf));
     }
     DEC_CUDA(cudaEventRecord(h->ev_pf_join, h->pf));
   }
@@ -848,14 +857,15 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
     // With a shared expert the routing launch also streams its gate/up.
     const bool fuse_shared = L.Wg_s != nullptr && h->fuse_shared_routing &&
                              route_shared_supported(h, 1, H, L.E, L.k);
-    if (fuse_shared && h->fuse_shared_routing == 2 && gemv_down_combine_supported(L.k, L.I)) {
+    if (front1) {
       // One MoE front launch (routing, shared gate/up, routed gate/up), then
       // the down projection with the combine and the residual.
       h->last_expert_variant = DEC_VARIANT_SMALL_M;
       {
         LaunchScope scope(h, "moe_front", s);
         DEC_CUDA(launch_moe_front(h, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.parts, w.sel_counter, idx, wt, scores,
-                                  w.moe.table, L.Wg_s, L.Wu_s, L.I, w.moe.hs, L.Wg, L.Wu, w.moe.hbuf, s));
+                                  w.moe.table, L.Wg_s, L.Wu_s, L.I, w.moe.hs, L.Wg, L.Wu, w.moe.hbuf, s, pf_front,
+                                  pf_front_bytes));
       }
       {
         LaunchScope scope(h, "down", s);
@@ -884,12 +894,12 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
     // Two to four tokens: the second RMSNorm, router, top-k, routing table (one
     // problem per entry) and the shared expert's gate/up in one launch; with
     // the MoE front schedule the entries' gate/up as well.
-    if (L.Wg_s != nullptr && h->fuse_shared_routing == 2 && M * L.k <= 32) {
+    if (front_few) {
       {
         LaunchScope scope(h, "moe_front", s);
         DEC_CUDA(launch_moe_front_multi(h, M, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.parts, w.sel_counter, idx, wt,
                                         scores, w.moe.table, L.Wg_s, L.Wu_s, L.I, w.moe.hs, L.Wg, L.Wu, w.moe.hbuf,
-                                        s));
+                                        s, pf_front, pf_front_bytes));
       }
       st = moe_few(h, M, w.b, wt, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wd_s, h1, hidden, w.moe, s, true);
       if (st != DEC_OK) return st;

@@ -152,17 +152,20 @@ cudaError_t launch_router_select(dec_handle* h, const uint16_t* x, const uint16_
 bool route_shared_supported(const dec_handle* h, int M, int H, int E, int k);
 // One token: routing + shared gate/up + the k routed experts' gate/up in one
 // launch (hbuf [k][I], slot j = entry j); counters ctr[5] zero between launches.
+// pf / pf_bytes (16-byte aligned, multiple of 16): pulled into L2 by the CTAs
+// while they wait for the routing.
 cudaError_t launch_moe_front(dec_handle* h, const uint16_t* h1, const uint16_t* gamma, float eps, const float* Wr,
                              int H, int E, int k, float* parts, int* ctr, int32_t* idx, float* w, float* scores,
                              int* table, const uint16_t* Wg_s, const uint16_t* Wu_s, int I, uint16_t* hs,
-                             const uint16_t* Wg, const uint16_t* Wu, uint16_t* hbuf, cudaStream_t s);
+                             const uint16_t* Wg, const uint16_t* Wu, uint16_t* hbuf, cudaStream_t s,
+                             const void* pf = nullptr, size_t pf_bytes = 0);
 // Two to four tokens: routing + shared gate/up + the M k entries' gate/up in
 // one launch (hbuf [M k][I], slot p = entry p); counters ctr[5] zero between launches.
 cudaError_t launch_moe_front_multi(dec_handle* h, int M, const uint16_t* h1, const uint16_t* gamma, float eps,
                                    const float* Wr, int H, int E, int k, float* parts, int* ctr, int32_t* idx, float* w,
                                    float* scores, int* table, const uint16_t* Wg_s, const uint16_t* Wu_s, int I,
                                    uint16_t* hs, const uint16_t* Wg, const uint16_t* Wu, uint16_t* hbuf,
-                                   cudaStream_t s);
+                                   cudaStream_t s, const void* pf = nullptr, size_t pf_bytes = 0);
 cudaError_t launch_route_shared(dec_handle* h, int M, const uint16_t* h1, const uint16_t* gamma, float eps,
                                 const float* Wr, int H, int E, int k, uint16_t* xn, float* parts, int* ctr,
                                 int32_t* idx, float* w, float* scores, int* table, const uint16_t* Wg_s,

@@ -67,6 +67,9 @@ struct RouteSharedParams {
   uint16_t* hbuf;         // routed SwiGLU outputs bf16 [k][I] (slot j: entry j)
   int* err;               // device error word
   unsigned long long wait_ns;
+  const char* pf = nullptr;  // the MoE fronts: a region pulled into L2 while the routing is awaited
+  size_t pf_bytes = 0;       // (16-byte multiple; 0 for none)
+  size_t pf_per = 0;         // bytes per CTA (16-byte multiple)
 };
 
 template <int J, int VPT>
@@ -703,6 +706,15 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_kernel(const RouteShare
   __shared__ const uint16_t* s_g[32];
   __shared__ const uint16_t* s_u[32];
   if (t == 0) {
+    // Cross-layer prefetch: a CTA that reaches the wait pulls its slice of the
+    // next operator's weights into L2 (memory otherwise idle until the routing).
+    if (P.pf_bytes > 0) {
+      const size_t off = (size_t)c * P.pf_per;
+      if (off < P.pf_bytes) {
+        const size_t n = P.pf_bytes - off < P.pf_per ? P.pf_bytes - off : P.pf_per;
+        request_l2(P.pf + off, n);
+      }
+    }
     const unsigned long long t0 = globaltimer();
     int ok = 1;
     while (ld_acquire_gpu(&P.ctr[3]) == 0) {
@@ -1065,6 +1077,15 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_multi_kernel(const Rout
   __shared__ const uint16_t* s_g[32];
   __shared__ const uint16_t* s_u[32];
   if (t == 0) {
+    // Cross-layer prefetch: a CTA that reaches the wait pulls its slice of the
+    // next operator's weights into L2 (memory otherwise idle until the routing).
+    if (P.pf_bytes > 0) {
+      const size_t off = (size_t)c * P.pf_per;
+      if (off < P.pf_bytes) {
+        const size_t n = P.pf_bytes - off < P.pf_per ? P.pf_bytes - off : P.pf_per;
+        request_l2(P.pf + off, n);
+      }
+    }
     const unsigned long long t0 = globaltimer();
     int ok = 1;
     while (ld_acquire_gpu(&P.ctr[3]) == 0) {
@@ -1333,7 +1354,8 @@ cudaError_t launch_route_shared(dec_handle* h, int M, const uint16_t* h1, const 
 cudaError_t launch_moe_front(dec_handle* h, const uint16_t* h1, const uint16_t* gamma, float eps, const float* Wr,
                              int H, int E, int k, float* parts, int* ctr, int32_t* idx, float* w, float* scores,
                              int* table, const uint16_t* Wg_s, const uint16_t* Wu_s, int I, uint16_t* hs,
-                             const uint16_t* Wg, const uint16_t* Wu, uint16_t* hbuf, cudaStream_t s) {
+                             const uint16_t* Wg, const uint16_t* Wu, uint16_t* hbuf, cudaStream_t s, const void* pf,
+                             size_t pf_bytes) {
   if (!route_shared_supported(h, 1, H, E, k) || Wg_s == nullptr || k > 32) return cudaErrorInvalidValue;
   RouteSharedParams P;
   P.M = 1;
@@ -1361,6 +1383,9 @@ cudaError_t launch_moe_front(dec_handle* h, const uint16_t* h1, const uint16_t* 
   P.hbuf = hbuf;
   P.err = h->d_err;
   P.wait_ns = h->wait_ns;
+  P.pf = static_cast<const char*>(pf);
+  P.pf_bytes = pf != nullptr ? pf_bytes : 0;
+  P.pf_per = (P.pf_bytes / (2 * h->sms) + 15) / 16 * 16;
   const int H8 = H / 8, vpt = H8 <= kThreads ? 1 : (H8 <= 2 * kThreads ? 2 : 4);
   const int Ew = (E + 7) / 8;
   if (Ew <= 32) return launch_front_j<1>(h, P, vpt, s);
@@ -1372,7 +1397,7 @@ cudaError_t launch_moe_front_multi(dec_handle* h, int M, const uint16_t* h1, con
                                    const float* Wr, int H, int E, int k, float* parts, int* ctr, int32_t* idx, float* w,
                                    float* scores, int* table, const uint16_t* Wg_s, const uint16_t* Wu_s, int I,
                                    uint16_t* hs, const uint16_t* Wg, const uint16_t* Wu, uint16_t* hbuf,
-                                   cudaStream_t s) {
+                                   cudaStream_t s, const void* pf, size_t pf_bytes) {
   if (M < 2 || M > 4 || !route_shared_supported(h, M, H, E, k) || Wg_s == nullptr || M * k > 32)
     return cudaErrorInvalidValue;
   RouteSharedParams P;
@@ -1401,6 +1426,9 @@ cudaError_t launch_moe_front_multi(dec_handle* h, int M, const uint16_t* h1, con
   P.hbuf = hbuf;
   P.err = h->d_err;
   P.wait_ns = h->wait_ns;
+  P.pf = static_cast<const char*>(pf);
+  P.pf_bytes = pf != nullptr ? pf_bytes : 0;
+  P.pf_per = (P.pf_bytes / (2 * h->sms) + 15) / 16 * 16;
   const int H8 = H / 8, vpt = H8 <= kThreads ? 1 : (H8 <= 2 * kThreads ? 2 : 4);
   const int Ew = (E + 7) / 8;
   if (M == 2) {
