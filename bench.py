@@ -95,12 +95,12 @@ def step_bytes(M: int, U: float) -> float:
 # sha256 of the listed files at capture time); null otherwise.
 NCU_TRAFFIC = {
     # one-token MoE front launch, full workload: dram__bytes_read.sum + dram__bytes_write.sum,
-    # mean of two launches of one ncu capture (read 539.64 / 539.63 MB, write 3.35 / 0.14 MB)
-    ("moe_front", 1): {"bytes": (539636736 + 539634944) // 2 + (3345920 + 138752) // 2,
+    # mean of two launches of one ncu capture (read 539.64 / 539.64 MB, write 3.40 / 0.14 MB)
+    ("moe_front", 1): {"bytes": (539637248 + 539639808) // 2 + (3399424 + 139776) // 2,
                        "sources": ("moe_layers_gb300/csrc/route_shared.cu", "moe_layers_gb300/csrc/topk.cuh",
                                    "moe_layers_gb300/csrc/common.cuh", "moe_layers_gb300/csrc/internal.h",
                                    "moe_layers_gb300/csrc/api.cu"),
-                       "sha256": "27ea7a67fee220af51f5ce9540fea70683a3965e1ac8c1cc7374408825051236"},
+                       "sha256": "5e7ab66b9728094a3c858870ae4be5b7b5982eff810c4a70dfaa19bc5aa790ea"},
 }
 
 
