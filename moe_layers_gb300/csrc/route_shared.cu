@@ -528,6 +528,9 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_kernel(const RouteShare
     }
   };
   load_unit(c);
+  // (a grab that races the previous launch's reset finds the queue exhausted
+  // or already reset: that launch's CTAs trigger this one's predecessors only
+  // after their shared rows)
   int base = 0;
   if (t == 0) {
     base = atomicAdd(&P.ctr[1], 3);
