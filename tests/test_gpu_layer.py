@@ -126,6 +126,41 @@ def test_layer_one_token_shapes(h, H, E, k, shared, in_routing):
         _check_layer(tr, hid, ref, slice(None), f"layer one token H={H} E={E} rep={rep}", L)
 
 
+def test_layer_batch_rows_match_single_tokens(h):
+    """M-invariance across the kernel families: the same 8 token rows as one
+    batch (split-K family), as four batches of two (the few-token MoE front)
+    and one by one (the one-token MoE front) give bit-identical top-k indices
+    and outputs within the bf16 rule of each other (and of the oracle)."""
+    H, N_in, K_out, E, I, k = 512, 520, 384, 40, 256, 8
+    L = Layer(H, N_in, K_out, E, I, k, base=7600)
+    n = E * I * H
+    g = synth.bf16(n, SEED, 7610, 0, 0.05).reshape(E, I, H)
+    u = synth.bf16(n, SEED, 7611, 0, 0.05).reshape(E, I, H)
+    d = synth.bf16(n, SEED, 7612, 0, 0.05).reshape(E, H, I)
+    sh = (synth.bf16(I * H, SEED, 7613, 0, 0.05).reshape(I, H), synth.bf16(I * H, SEED, 7614, 0, 0.05).reshape(I, H),
+          synth.bf16(H * I, SEED, 7615, 0, 0.05).reshape(H, I))
+    dev_w = L.device(dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
+                     tuple(dev_bf16(a, a.shape) for a in sh))
+    hbits, _ = gap_rows(L.scores, 8, H, k, base=7700)
+    ref = L.oracle(hbits, lambda e: (g[e], u[e], d[e]), sh)
+    hid8, tr8 = _run(h, L, dev_w, hbits)
+    out8, idx8, h1_8 = host_bits(hid8), tr8["idx"].cpu().numpy(), oracle.bf16_to_f64(host_bits(tr8["h1"]))
+    for size in (2, 1):
+        for r0 in range(0, 8, size):
+            rows = slice(r0, r0 + size)
+            hid, tr = _run(h, L, dev_w, hbits[rows])
+            what = f"rows {r0}..{r0 + size - 1} as a batch of {size}"
+            assert np.array_equal(tr["idx"].cpu().numpy(), idx8[rows]), what + ": top-k against the batch of 8"
+            got = oracle.bf16_to_f64(host_bits(hid))
+            # (each side may round its residual h1 one ulp apart: that difference passes through)
+            dh1 = np.abs(oracle.bf16_to_f64(host_bits(tr["h1"])) - h1_8[rows])
+            assert_bf16_close(host_bits(hid), oracle.bf16_to_f64(out8[rows]), what + " against the batch of 8",
+                              tol=2e-2, passthrough=dh1)
+            assert_bf16_close(host_bits(hid), ref["out"][rows], what + " against the oracle",
+                              passthrough=np.abs(oracle.bf16_to_f64(host_bits(tr["h1"])) - ref["h1"][rows]))
+            assert np.isfinite(got).all()
+
+
 def _check_router_stage(L, tr, rows, what):
     """Router scores and weights on the layer's own input: the oracle's RMSNorm
     and router applied to the h1 the GPU produced. h1 is a bf16 activation
