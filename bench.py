@@ -100,7 +100,7 @@ NCU_TRAFFIC = {
                        "sources": ("moe_layers_gb300/csrc/route_shared.cu", "moe_layers_gb300/csrc/topk.cuh",
                                    "moe_layers_gb300/csrc/common.cuh", "moe_layers_gb300/csrc/internal.h",
                                    "moe_layers_gb300/csrc/api.cu"),
-                       "sha256": "af73981d01cc386bb80ae5cd6fb9be844f6ddf4a3f4a385f71c0faf5b82ab71d"},
+                       "sha256": "7cf579a0bfede19da93d049016e68f13fc581dcc104bb370310bf7361821d986"},
 }
 
 

@@ -28,7 +28,10 @@
 // has published the routing (a release flag), every CTA streams the k routed
 // experts' gate/up rows as well, so the routing, the shared expert and the
 // routed experts take one launch and the down projection follows directly.
-// Two to four tokens: route_shared_multi_kernel, one warp's top-k per token.
+// Two to four tokens: route_shared_multi_kernel (the routing launch for M
+// rows; the last CTA scores every token and each warp selects one token's
+// experts) and moe_front_multi_kernel (that launch plus the (token, expert)
+// entries' gate/up, the default).
 #include <algorithm>
 
 #include "common.cuh"
