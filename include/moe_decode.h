@@ -165,9 +165,10 @@ dec_status dec_check_device_error(dec_handle* h);
 dec_status dec_linear_workspace_size(const dec_handle* h, int M, int N, int K, size_t* bytes);
 
 /* y[M][N] = x[M][K] W[N][K]^T  (bf16 in, fp32 accumulate, bf16 out).
- * [K3 P1§1], [hu-sum]: the small-matrix kernel at M = 1, the split-K tcgen05
- * kernel above (or as forced; the pages use the small-matrix kernel at batch
- * 1-2, but on GB300 the split-K kernel measured faster at batch 2). x has row stride ldx >= K elements (ldx = K
+ * [K3 P1§1], [hu-sum]: the small-matrix kernel at M <= 2 (and up to M = 4
+ * for matrices of at most 48 MB, where the split-K kernel's fixed cost per
+ * launch dominates), the split-K tcgen05 kernel above (or as forced with
+ * dec_set_force_variant). x has row stride ldx >= K elements (ldx = K
  * for a dense matrix; a larger stride reads the leading K columns of a wider
  * activation). 1 <= M <= 64, N >= 1, 8 <= K, K % 8 == 0, ldx % 8 == 0.
  * y must not overlap x or W. */
