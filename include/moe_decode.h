@@ -193,13 +193,19 @@ dec_status dec_linear_residual(dec_handle* h, const dec_bf16* x, int ldx, const 
  * of split-K partial sums and 4 KiB of tile counters) in one static device
  * array that every GPU loading the library holds until the process exits.
  * - The first call on a device looks up that array's address
- *   (cudaGetSymbolAddress, with the handle's device made current); make that
- *   first call before any stream capture.
+ *   (cudaGetSymbolAddress, with the handle's device made current, then the
+ *   caller's device restored) and keeps it for the process; make that first
+ *   call before any stream capture. A device reset (cudaDeviceReset) after
+ *   that first call is not supported: the kept address may no longer be the
+ *   array's. A call that fails with DEC_ERR_CUDA drops the kept address, so
+ *   the next call looks it up again.
  * - Every call shares the array and it keeps the last call's contents: each
  *   call clears the counters it uses, and calls that overlap on the GPU (for
  *   instance on two streams at once) race on it.
- * - Limits: 1 <= M <= 64 and N <= 131072 (DEC_ERR_UNSUPPORTED beyond), plus
- *   the shape rules of dec_linear. r may be NULL; out may alias r exactly.
+ * - Sizes: the shape rules of dec_linear apply (M outside 1..64, K or ldx
+ *   not a multiple of 8 and the like return DEC_ERR_INVALID_ARG); N above
+ *   131072, the array's limit, returns DEC_ERR_UNSUPPORTED. r may be NULL;
+ *   out may alias r exactly.
  * - Calls no cudaMalloc, cudaFree or other allocating routine. */
 dec_status dec_linear_noalloc(dec_handle* h, const dec_bf16* x, int ldx, const dec_bf16* W, const dec_bf16* r,
                               dec_bf16* out, int M, int N, int K, cudaStream_t stream);
@@ -349,6 +355,14 @@ dec_status dec_test_wait_timeout(dec_handle* h, cudaStream_t stream);
  * `stream`. Used to test that the routing wait surfaces as DEC_ERR_TIMEOUT
  * with the context still usable. tokens outside {1, 2}: DEC_ERR_INVALID_ARG. */
 dec_status dec_test_routing_wait_timeout(dec_handle* h, int tokens, cudaStream_t stream);
+
+/* Hold `ctas` SMs (1 <= ctas <= the device's SM count) for hold_ns
+ * nanoseconds (at most 2 s) with a kernel on `stream`: one CTA per SM that
+ * takes the whole per-block shared memory, so nothing else fits beside it,
+ * and sleeps on the global timer. It writes nothing. Used to test that the
+ * MoE fronts complete when another stream's kernel holds part of the SMs, so
+ * that not all of their CTAs can be resident at once. */
+dec_status dec_test_occupy_sms(dec_handle* h, int ctas, uint64_t hold_ns, cudaStream_t stream);
 
 /* Copy `bytes` from src to dst on `stream` after spinning for delay_ns
  * (bounded by the clock): a slow producer for ordering tests of the

@@ -86,6 +86,7 @@ def _load():
         "dec_test_wait_timeout": [P, P],
         "dec_test_routing_wait_timeout": [P, I, P],
         "dec_test_delayed_copy": [P, P, P, Z, U64, P],
+        "dec_test_occupy_sms": [P, I, U64, P],
         "dec_set_profiling": [P, I],
         "dec_profile_read": [P, ctypes.POINTER(_KernelTime), I, ctypes.POINTER(I)],
     }
@@ -432,6 +433,11 @@ def test_wait_timeout(h: Handle, stream=None) -> None:
 def test_routing_wait_timeout(h: Handle, tokens: int = 1, stream=None) -> None:
     _check(_load().dec_test_routing_wait_timeout(h.ptr, int(tokens), _stream(stream)),
            "dec_test_routing_wait_timeout")
+
+
+def test_occupy_sms(h: Handle, ctas: int, hold_ns: int, stream=None) -> None:
+    """Hold `ctas` SMs for hold_ns with a sleeping kernel on `stream` (a test hook)."""
+    _check(_load().dec_test_occupy_sms(h.ptr, int(ctas), int(hold_ns), _stream(stream)), "dec_test_occupy_sms")
 
 
 def test_delayed_copy(h: Handle, dst, src, delay_ns: int, stream=None) -> None:

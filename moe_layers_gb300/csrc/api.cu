@@ -23,37 +23,6 @@ inline size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
     if ((expr) != cudaSuccess) return DEC_ERR_CUDA; \
   } while (0)
 
-cudaEvent_t pool_event(dec_handle* h) {
-  if (!h->event_pool.empty()) {
-    cudaEvent_t e = h->event_pool.back();
-    h->event_pool.pop_back();
-    return e;
-  }
-  cudaEvent_t e = nullptr;
-  cudaEventCreate(&e);
-  return e;
-}
-
-// Counts every kernel launch; when profiling, brackets it with events on its stream.
-struct LaunchScope {
-  dec_handle* h;
-  cudaStream_t s;
-  int rec = -1;
-  LaunchScope(dec_handle* h_, const char* tag, cudaStream_t s_) : h(h_), s(s_) {
-    h->launches++;
-    if (h->profiling) {
-      dec_handle::ProfRec r{tag, pool_event(h), pool_event(h)};
-      if (r.a && r.b && cudaEventRecord(r.a, s) == cudaSuccess) {
-        h->prof.push_back(r);
-        rec = (int)h->prof.size() - 1;
-      }
-    }
-  }
-  ~LaunchScope() {
-    if (rec >= 0) cudaEventRecord(h->prof[rec].b, s);
-  }
-};
-
 // Split a workspace into 256-byte-aligned pieces.
 struct Carver {
   char* base;
@@ -1032,6 +1001,12 @@ dec_status dec_test_routing_wait_timeout(dec_handle* h, int tokens, cudaStream_t
   if (cudaStreamSynchronize(stream) != cudaSuccess) st = DEC_ERR_CUDA;
   cudaFree(base);
   return st;
+}
+
+dec_status dec_test_occupy_sms(dec_handle* h, int ctas, uint64_t hold_ns, cudaStream_t stream) {
+  if (h == nullptr || ctas < 1 || ctas > h->sms || hold_ns > 2000000000ull) return DEC_ERR_INVALID_ARG;
+  LaunchScope scope(h, "test_occupy", stream);
+  return launch_occupy(h, ctas, hold_ns, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
 }
 
 dec_status dec_test_delayed_copy(dec_handle* h, void* dst, const void* src, size_t bytes, uint64_t delay_ns,

@@ -177,8 +177,40 @@ cudaError_t launch_combine(dec_handle* h, const float* y, const int* table, cons
                            const float* ys, const uint16_t* res, uint16_t* out, int H, cudaStream_t s);
 cudaError_t launch_prefetch(dec_handle* h, const void* p, size_t bytes, int ctas, cudaStream_t s);
 cudaError_t launch_wait_timeout_probe(dec_handle* h, cudaStream_t s);
+cudaError_t launch_occupy(dec_handle* h, int ctas, uint64_t hold_ns, cudaStream_t s);
 cudaError_t launch_delayed_copy(dec_handle* h, void* dst, const void* src, size_t bytes, uint64_t delay_ns,
                                 cudaStream_t s);
+
+inline cudaEvent_t pool_event(dec_handle* h) {
+  if (!h->event_pool.empty()) {
+    cudaEvent_t e = h->event_pool.back();
+    h->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Counts every kernel launch; when profiling, brackets it with events on its stream.
+struct LaunchScope {
+  dec_handle* h;
+  cudaStream_t s;
+  int rec = -1;
+  LaunchScope(dec_handle* h_, const char* tag, cudaStream_t s_) : h(h_), s(s_) {
+    h->launches++;
+    if (h->profiling) {
+      dec_handle::ProfRec r{tag, pool_event(h), pool_event(h)};
+      if (r.a && r.b && cudaEventRecord(r.a, s) == cudaSuccess) {
+        h->prof.push_back(r);
+        rec = (int)h->prof.size() - 1;
+      }
+    }
+  }
+  ~LaunchScope() {
+    if (rec >= 0) cudaEventRecord(h->prof[rec].b, s);
+  }
+};
 
 // Launch with the handle's programmatic-dependent-launch setting.
 template <typename... KArgs, typename... Args>

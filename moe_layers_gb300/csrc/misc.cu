@@ -108,6 +108,27 @@ __global__ void delayed_copy_kernel(uint4* dst, const uint4* src, size_t n16, un
     dst[i] = src[i];
 }
 
+// Test hook: one 32-thread CTA per SM on `ctas` SMs (each asks for the whole
+// per-block shared memory, so no other CTA fits beside it) that sleeps until
+// hold_ns have passed on the global timer, then exits. It writes nothing.
+constexpr int kOccupySmem = 227 * 1024;
+__global__ void __launch_bounds__(32) occupy_kernel(unsigned long long hold_ns) {
+  extern __shared__ uint8_t occupy_smem[];
+  if (threadIdx.x == 0) {
+    occupy_smem[0] = 0;
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < hold_ns) __nanosleep(4000);
+  }
+  __syncwarp();
+}
+
+cudaError_t launch_occupy(dec_handle* h, int ctas, uint64_t hold_ns, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(occupy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kOccupySmem);
+  if (e != cudaSuccess) return e;
+  occupy_kernel<<<ctas, 32, kOccupySmem, s>>>((unsigned long long)hold_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rmsnorm(dec_handle* h, const uint16_t* x, const uint16_t* gamma, uint16_t* y, int M, int H,
                            float eps, cudaStream_t s) {
   const int H8 = H / 8;

@@ -26,7 +26,8 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on `device`, looked up once per device
-// with that device current.
+// with that device current; the caller's current device is restored (a
+// failure to restore it is returned as an error).
 cudaError_t scratch_address(int device, void** out) {
   if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -37,12 +38,23 @@ cudaError_t scratch_address(int device, void** out) {
     if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess) return e;
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (prev != device) cudaSetDevice(prev);
+    if (prev != device) {
+      const cudaError_t r = cudaSetDevice(prev);
+      if (e == cudaSuccess) e = r;
+    }
     if (e != cudaSuccess) return e;
     g_scratch_addr[device] = p;
   }
   *out = g_scratch_addr[device];
   return cudaSuccess;
+}
+
+// Forget a device's address after a failed call, so that the next call looks
+// it up again.
+void forget_scratch_address(int device) {
+  if (device < 0 || device >= kMaxDevices) return;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_scratch_addr[device] = nullptr;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -63,8 +75,6 @@ extern "C" dec_status dec_linear_noalloc(dec_handle* h, const dec_bf16* x, int l
   if (scratch_address(h->device, &base) != cudaSuccess) return DEC_ERR_CUDA;
   int* counters = static_cast<int*>(base);
   float* partials = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kNoAllocCounterBytes);
-  // The array keeps whatever the previous call left; the counters must start at zero.
-  if (cudaMemsetAsync(counters, 0, (size_t)tiles * sizeof(int), stream) != cudaSuccess) return DEC_ERR_CUDA;
 
   EngineLaunch L;
   L.epi = EPI_LINEAR;
@@ -83,7 +93,17 @@ extern "C" dec_status dec_linear_noalloc(dec_handle* h, const dec_bf16* x, int l
   L.partials = partials;
   L.counters = counters;
   L.grid = h->sms < kNoAllocMaxCtas ? h->sms : kNoAllocMaxCtas;
-  h->launches++;
   h->last_variant = DEC_VARIANT_SPLIT_K;
-  return launch_engine(h, L, stream) == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
+  cudaError_t e;
+  {
+    // The array keeps whatever the previous call left; the counters must start at zero.
+    LaunchScope scope(h, "linear_noalloc", stream);
+    e = cudaMemsetAsync(counters, 0, (size_t)tiles * sizeof(int), stream);
+    if (e == cudaSuccess) e = launch_engine(h, L, stream);
+  }
+  if (e != cudaSuccess) {
+    forget_scratch_address(h->device);
+    return DEC_ERR_CUDA;
+  }
+  return DEC_OK;
 }

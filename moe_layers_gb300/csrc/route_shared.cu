@@ -28,6 +28,10 @@
 // has published the routing (a release flag), every CTA streams the k routed
 // experts' gate/up rows as well, so the routing, the shared expert and the
 // routed experts take one launch and the down projection follows directly.
+// Because its CTAs wait for that flag, the front does not own router units by
+// block index as in step 1: a CTA takes units from a ticket counter
+// (take_unit) and the hand-off counts units, so the routing never waits for a
+// CTA that the SMs cannot hold yet.
 // Two to four tokens: route_shared_multi_kernel (the routing launch for M
 // rows; the last CTA scores every token and each warp selects one token's
 // experts) and moe_front_multi_kernel (that launch plus the (token, expert)
@@ -74,6 +78,19 @@ struct RouteSharedParams {
   size_t pf_bytes = 0;       // (16-byte multiple; 0 for none)
   size_t pf_per = 0;         // bytes per CTA (16-byte multiple)
 };
+
+// The MoE fronts hand out their router units from a counter (ctr[6]) that
+// cycles through nunits + G values: a CTA takes tickets until one is past the
+// last unit, so every launch takes exactly nunits + G tickets and leaves the
+// counter where it found it (a launch's CTAs take their tickets before they
+// trigger the next launch, so launches never interleave on it). A unit is
+// therefore computed by whichever running CTA took it, and the routing
+// hand-off completes once the CTAs that are resident have computed all units,
+// whether or not every CTA of the grid can be resident at once (another
+// stream's kernels may hold SMs). The hand-off counts units, not CTAs.
+__device__ __forceinline__ int take_unit(int* ctr, int nunits, int G) {
+  return (int)atomicInc(reinterpret_cast<unsigned*>(ctr + 6), (unsigned)(nunits + G - 1));
+}
 
 template <int J, int VPT>
 __global__ void __launch_bounds__(kThreads, 2) route_shared_kernel(const RouteSharedParams P) {
@@ -501,8 +518,10 @@ __global__ void __launch_bounds__(kThreads, 2) route_shared_multi_kernel(const R
 // One token: the MoE front in one launch: the routing launch above (RMSNorm,
 // router, top-k, routing table), then one row queue over the shared expert's
 // gate/up rows followed by the k routed experts' rows. The routing is
-// published by the last CTA to reach the hand-off (it waits for nothing), so
-// a CTA that waits for it waits only until every CTA has started.
+// published by the CTA whose arrival completes the last router unit, and it
+// waits for nothing. Units go to whichever CTAs are running (take_unit), so
+// a CTA that waits for the routing depends only on CTAs that have started,
+// however many of the grid's CTAs the SMs can hold beside other kernels.
 template <int J, int VPT>
 __global__ void __launch_bounds__(kThreads, 2) moe_front_kernel(const RouteSharedParams P) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -530,7 +549,12 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_kernel(const RouteShare
                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
-  load_unit(c);
+  // this CTA's first router unit (take_unit): its fp32 rows load before the wait
+  __shared__ int s_unit;
+  if (t == 0) s_unit = take_unit(P.ctr, P.nunits, G);
+  __syncthreads();
+  int u = s_unit;
+  load_unit(u);
   // (a grab that races the previous launch's reset finds the queue exhausted
   // or already reset: that launch's CTAs trigger this one's predecessors only
   // after their shared rows)
@@ -578,10 +602,10 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_kernel(const RouteShare
   }
   int pending = base + 2;
   __syncthreads();
-#pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    const int u = c + m * G;
-    if (m == 1 && u < P.nunits) load_unit(u);
+  // Router units: the CTA's ticket, then further tickets while units remain.
+  // Every computed unit arrives on the hand-off (ctr[0] counts units); the
+  // arrival that completes the last unit takes the top-k.
+  for (;;) {
     if (u < P.nunits) {
       const int e = (u % ngrp) * 8 + warp, ks = u / ngrp, k0 = ks * kUnitCols;
       const int kn = min(kUnitCols, H - k0);
@@ -601,23 +625,31 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_kernel(const RouteShare
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if (lane == 0 && e < P.E) P.parts[(size_t)ks * P.E + e] = acc;
     }
-  }
-  __syncthreads();
-  if (t == 0) s_last = atom_add_acq_rel_gpu(&P.ctr[0], 1) == G - 1;
-  __syncthreads();
-  if (s_last) {
-    int se = 0;
-    float sw = 0.f;
-    block_topk<J, true>(P.parts, (H + kUnitCols - 1) / kUnitCols, 1, 0, P.E, P.k, P.idx, P.w, P.scores, &se, &sw);
-    if (warp == 0) {
-      write_one_token_table(P.table, P.E, P.k, se);
-      __syncwarp();
-      if (lane == 0) {
-        P.ctr[0] = 0;
-        P.ctr[5] = c;                  // this CTA's static share goes to the tail queue
-        st_release_gpu(&P.ctr[3], 1);  // the routing is written
+    // The barrier orders the unit's stores before thread 0's acquire-release
+    // add; in the last arrival the barrier after it orders every read after it.
+    __syncthreads();
+    if (t == 0) {
+      s_last = u < P.nunits && atom_add_acq_rel_gpu(&P.ctr[0], 1) == P.nunits - 1;
+      s_unit = u < P.nunits ? take_unit(P.ctr, P.nunits, G) : P.nunits;
+    }
+    __syncthreads();
+    if (s_last) {
+      int se = 0;
+      float sw = 0.f;
+      block_topk<J, true>(P.parts, (H + kUnitCols - 1) / kUnitCols, 1, 0, P.E, P.k, P.idx, P.w, P.scores, &se, &sw);
+      if (warp == 0) {
+        write_one_token_table(P.table, P.E, P.k, se);
+        __syncwarp();
+        if (lane == 0) {
+          P.ctr[0] = 0;
+          P.ctr[5] = c;                  // this CTA's static share goes to the tail queue
+          st_release_gpu(&P.ctr[3], 1);  // the routing is written
+        }
       }
     }
+    u = s_unit;
+    if (u >= P.nunits) break;  // (the last arrival's next ticket is always past the units)
+    load_unit(u);
   }
 
   // Three streams of row pairs, one after the other: the shared expert's
@@ -886,7 +918,12 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_multi_kernel(const Rout
                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
-  load_unit(c);
+  // this CTA's first router unit (take_unit): its fp32 rows load before the wait
+  __shared__ int s_unit;
+  if (t == 0) s_unit = take_unit(P.ctr, P.nunits, G);
+  __syncthreads();
+  int u = s_unit;
+  load_unit(u);
   // (a grab that races the previous launch's reset finds the queue exhausted
   // or already reset: that launch's CTAs trigger this one's predecessors only
   // after their shared rows)
@@ -949,11 +986,14 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_multi_kernel(const Rout
   int pending = base + 2;  // (thread 0)
   __syncthreads();
 
-  // router logit pieces of this CTA's units for every token, then the hand-off
-#pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    const int u = c + m * G;
-    if (m == 1 && u < P.nunits) load_unit(u);
+  if (t == 0) {
+    s_row[0] = base;
+    s_row[1] = base + 1;
+  }
+  // Router units for every token: the CTA's ticket, then further tickets
+  // while units remain. Every computed unit arrives on the hand-off (ctr[0]
+  // counts units); the arrival that completes the last unit takes the top-k.
+  for (;;) {
     if (u < P.nunits) {
       const int e = (u % ngrp) * 8 + warp, ks = u / ngrp, k0 = ks * kUnitCols;
       const int kn = min(kUnitCols, H - k0);
@@ -985,22 +1025,24 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_multi_kernel(const Rout
         if (lane == 0 && e < P.E && q < M) P.parts[((size_t)ks * M + q) * P.E + e] = acc[q];
       }
     }
-  }
-  if (t == 0) {
-    s_row[0] = base;
-    s_row[1] = base + 1;
-  }
-  __syncthreads();
-  if (t == 0) s_last = atom_add_acq_rel_gpu(&P.ctr[0], 1) == G - 1;
-  __syncthreads();
-  if (s_last) {
-    block_topk_tokens<J, MT>(P.parts, ksplit, M, P.E, P.k, P.idx, P.w, P.scores, P.table);
-    __syncthreads();  // every warp's entries are written before the release
+    __syncthreads();  // the unit's stores before thread 0's acquire-release add
     if (t == 0) {
-      P.ctr[0] = 0;
-      P.ctr[5] = c;                  // this CTA's static share goes to the tail queue
-      st_release_gpu(&P.ctr[3], 1);  // the routing is written
+      s_last = u < P.nunits && atom_add_acq_rel_gpu(&P.ctr[0], 1) == P.nunits - 1;
+      s_unit = u < P.nunits ? take_unit(P.ctr, P.nunits, G) : P.nunits;
     }
+    __syncthreads();
+    if (s_last) {
+      block_topk_tokens<J, MT>(P.parts, ksplit, M, P.E, P.k, P.idx, P.w, P.scores, P.table);
+      __syncthreads();  // every warp's entries are written before the release
+      if (t == 0) {
+        P.ctr[0] = 0;
+        P.ctr[5] = c;                  // this CTA's static share goes to the tail queue
+        st_release_gpu(&P.ctr[3], 1);  // the routing is written
+      }
+    }
+    u = s_unit;
+    if (u >= P.nunits) break;  // (the last arrival's next ticket is always past the units)
+    load_unit(u);
   }
 
   uint4 wa[2][VPT];

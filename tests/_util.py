@@ -142,9 +142,12 @@ class HostBank:
     """Host view of a seeded expert bank: regenerates expert e's weights on demand."""
 
     def __init__(self, E: int, H: int, I: int, seed: int = SEED, ids=(synth.W_G, synth.W_U, synth.W_D),
-                 sigma: float = 0.02):
+                 sigma: float = 0.02, cache: int = 16):
+        """cache: experts whose bits are kept (a full-size expert is 88 MB), so
+        that a second oracle pass over the same experts does not regenerate them."""
         self.E, self.H, self.I, self.seed, self.ids, self.sigma = E, H, I, seed, ids, sigma
         self._cache = {}
+        self._cap = int(cache)
 
     def bits(self, e: int):
         if e not in self._cache:
@@ -152,7 +155,7 @@ class HostBank:
             g = synth.bf16(n, self.seed, self.ids[0], e * n, self.sigma).reshape(self.I, self.H)
             u = synth.bf16(n, self.seed, self.ids[1], e * n, self.sigma).reshape(self.I, self.H)
             d = synth.bf16(n, self.seed, self.ids[2], e * n, self.sigma).reshape(self.H, self.I)
-            if len(self._cache) > 16:
+            if len(self._cache) >= self._cap:
                 self._cache.clear()
             self._cache[e] = (g, u, d)
         return self._cache[e]

@@ -125,7 +125,8 @@ def test_experts_full_size(h, full_bank, M, family):
     shared = tuple(oracle.bf16_to_f64(synth.bf16(I_FULL * H_FULL, SEED, tid, 0, 0.02)).reshape(shape)
                    for tid, shape in ((synth.W_G_S, (I_FULL, H_FULL)), (synth.W_U_S, (I_FULL, H_FULL)),
                                       (synth.W_D_S, (H_FULL, I_FULL))))
-    tokens = sorted(set([0, M - 1, M // 2]))  # sampled tokens; each is a full output row
+    # every token up to 16, else 16 tokens spread over the batch; each is a full output row
+    tokens = list(range(M)) if M <= 16 else sorted(set(int(round(v)) for v in np.linspace(0, M - 1, 16)))
     ref = oracle.moe(x, idx, w, bank, shared, tokens=tokens)
     got = host_bits(out)[tokens]
     assert_bf16_close(got, ref, f"moe full M={M}")

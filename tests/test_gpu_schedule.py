@@ -93,8 +93,9 @@ def test_layer_settings_change_schedule_not_result(h, small_layer, M, name):
         for rep in range(2):
             hbits, _ = gap_rows(L.scores, M, L.H, L.k, base=8100 + 10 * M + rep)
             hid, tr = _run(h, L, dev_w, hbits)
-            ref = L.oracle(hbits, lambda e: (g[e], u[e], d[e]), sh)
-            _check_layer(tr, hid, ref, slice(None), f"layer {name} M={M} rep={rep}", L)
+            ex = lambda e: (g[e], u[e], d[e])
+            ref = L.oracle(hbits, ex, sh)
+            _check_layer(tr, hid, ref, slice(None), f"layer {name} M={M} rep={rep}", L, ex, sh)
         assert h.check_device_error() == ML.DEC_OK
     finally:
         _defaults(h)

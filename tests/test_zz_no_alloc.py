@@ -60,3 +60,9 @@ def test_no_alloc_rejects_sizes_beyond_its_scratch():
         with pytest.raises(ML.DecodeError) as e:
             ML.dec_linear_noalloc(h, x, W)
         assert e.value.status == ML.DEC_ERR_UNSUPPORTED
+        # M above 64 breaks the shape rules every projection entry point shares
+        x65 = torch.zeros((65, 64), dtype=torch.bfloat16, device="cuda")
+        W1 = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(ML.DecodeError) as e:
+            ML.dec_linear_noalloc(h, x65, W1)
+        assert e.value.status == ML.DEC_ERR_INVALID_ARG
