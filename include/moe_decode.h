@@ -254,6 +254,46 @@ dec_status moe_experts(dec_handle* h, const dec_bf16* x, const int32_t* idx, con
                        const dec_bf16* Wg_s, const dec_bf16* Wu_s, const dec_bf16* Wd_s, const dec_bf16* residual,
                        dec_bf16* out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------ MoE layer */
+
+/* Weights and shape of one MoE layer. */
+typedef struct dec_moe_weights {
+  int H;                /* hidden size */
+  int E;                /* routed experts */
+  int k;                /* experts per token */
+  int I;                /* expert intermediate size */
+  float eps;            /* RMSNorm epsilon (used with gamma) */
+  const dec_bf16* gamma;  /* [H] RMSNorm gains applied to the input first, or NULL for none */
+  const float* W_r;     /* [E][H] fp32 router */
+  const dec_bf16* Wg;   /* [E][I][H] */
+  const dec_bf16* Wu;   /* [E][I][H] */
+  const dec_bf16* Wd;   /* [E][H][I] */
+  const dec_bf16* Wg_s; /* [I][H] or NULL (no shared expert) */
+  const dec_bf16* Wu_s; /* [I][H] */
+  const dec_bf16* Wd_s; /* [H][I] */
+} dec_moe_weights;
+
+dec_status moe_layer_workspace_size(const dec_handle* h, const dec_moe_weights* Wt, int M, size_t* bytes);
+
+/* The MoE layer of a decode step in one call [K3 P1§3, §4]: routing and the
+ * experts with the schedule of decode_layer's MoE block:
+ *   b       = gamma ? RMSNorm(x; gamma, eps) : x
+ *   idx, w  = top-k(sigmoid(b W_r^T)), renormalised
+ *   out     = [residual +] sum_j w_j E_idx_j(b) [+ S(b)]
+ * x bf16 [M][H]; residual bf16 [M][H] or NULL; out bf16 [M][H] (may alias
+ * residual, not x); idx int32 [M][k], w fp32 [M][k] and scores fp32 [M][E]
+ * receive the routing when given (each may be NULL). At one token (and two,
+ * with a shared expert) the routing, the shared expert's gate/up and the
+ * selected experts' gate/up are one launch whose CTAs wait, with the handle's
+ * limit, for the routing that one of them publishes; the down projection
+ * follows with the combine and the residual. Above, the split-K family runs
+ * the shared expert on the handle's side stream. Same shape rules as
+ * moe_experts (1 <= M <= 64, 1 <= k <= 16, k <= E <= 1024, H and I multiples
+ * of 128). */
+dec_status moe_layer(dec_handle* h, const dec_moe_weights* Wt, const dec_bf16* x, const dec_bf16* residual,
+                     dec_bf16* out, int M, int32_t* idx, float* w, float* scores, void* ws, size_t ws_bytes,
+                     cudaStream_t stream);
+
 /* ------------------------------------------------------------------ decode layer */
 
 /* Weights and shape of one decode layer. */

@@ -42,6 +42,12 @@ class _LayerWeights(ctypes.Structure):
                [("prefetch_bytes", ctypes.c_size_t)]
 
 
+class _MoeWeights(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int), ("I", ctypes.c_int),
+                ("eps", ctypes.c_float)] + \
+               [(n, ctypes.c_void_p) for n in ("gamma", "W_r", "Wg", "Wu", "Wd", "Wg_s", "Wu_s", "Wd_s")]
+
+
 class _KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
 
@@ -80,6 +86,8 @@ def _load():
         "moe_route_topk": [P, P, P, I, I, I, I, P, P, P, P, Z, P],
         "moe_experts_workspace_size": [P, I, I, I, I, I, ctypes.POINTER(Z)],
         "moe_experts": [P, P, P, P, I, I, P, P, P, I, I, I, P, P, P, P, P, P, Z, P],
+        "moe_layer_workspace_size": [P, ctypes.POINTER(_MoeWeights), I, ctypes.POINTER(Z)],
+        "moe_layer": [P, ctypes.POINTER(_MoeWeights), P, P, P, I, P, P, P, P, Z, P],
         "decode_layer_workspace_size": [P, ctypes.POINTER(_LayerWeights), I, ctypes.POINTER(Z)],
         "decode_layer": [P, ctypes.POINTER(_LayerWeights), P, I, ctypes.POINTER(_LayerTrace), P, Z, P],
         "dec_prefetch_l2": [P, P, Z, P],
@@ -348,6 +356,67 @@ def moe_experts(h: Handle, x, idx, w, Wg, Wu, Wd, shared: Optional[Sequence] = N
                            _ptr(sg), _ptr(su), _ptr(sd), _ptr(residual), _ptr(out), _ptr(ws), ws.numel(),
                            _stream(stream)), "moe_experts")
     return out
+
+
+@dataclass
+class MoeWeights:
+    """Device tensors of one MoE layer (see dec_moe_weights); gamma None: no RMSNorm."""
+    W_r: object
+    Wg: object
+    Wu: object
+    Wd: object
+    Wg_s: object = None
+    Wu_s: object = None
+    Wd_s: object = None
+    gamma: object = None
+    k: int = 8
+    eps: float = 1e-6
+
+    def c_struct(self) -> _MoeWeights:
+        E, I, H = self.Wg.shape
+        s = _MoeWeights()
+        s.H, s.E, s.k, s.I, s.eps = H, E, self.k, I, self.eps
+        for n in ("gamma", "W_r", "Wg", "Wu", "Wd", "Wg_s", "Wu_s", "Wd_s"):
+            setattr(s, n, _ptr(getattr(self, n)))
+        return s
+
+
+def moe_layer_workspace_size(h: Handle, weights: MoeWeights, M: int) -> int:
+    nb = ctypes.c_size_t()
+    cw = weights.c_struct()
+    _check(_load().moe_layer_workspace_size(h.ptr, ctypes.byref(cw), int(M), ctypes.byref(nb)),
+           "moe_layer_workspace_size")
+    return nb.value
+
+
+def moe_layer(h: Handle, weights: MoeWeights, x, residual=None, out=None, trace=False, stream=None, ws=None,
+              _cw=None):
+    """out = [residual +] MoE([RMSNorm](x)) (bf16 [M,H]): routing and experts in one call.
+
+    trace=True also returns a dict of new device tensors with the routing
+    (idx, w, scores); trace may be a dict of preallocated tensors (any of those
+    keys). Returns out, or (out, trace dict)."""
+    import torch
+    lib = _load()
+    _require(x, torch.bfloat16, "x", 2)
+    M = x.shape[0]
+    cw = weights.c_struct() if _cw is None else _cw
+    if out is None:
+        out = torch.empty_like(x)
+    if ws is None:
+        ws = h.workspace(("moe_layer", id(stream)), moe_layer_workspace_size(h, weights, M),
+                         ("moe_layer", M, cw.H, cw.E, cw.k, cw.I))
+    tr = None
+    if trace is True:
+        tr = dict(idx=torch.empty((M, cw.k), dtype=torch.int32, device=x.device),
+                  w=torch.empty((M, cw.k), dtype=torch.float32, device=x.device),
+                  scores=torch.empty((M, cw.E), dtype=torch.float32, device=x.device))
+    elif isinstance(trace, dict):
+        tr = trace
+    g = (lambda n: None) if tr is None else tr.get
+    _check(lib.moe_layer(h.ptr, ctypes.byref(cw), _ptr(x), _ptr(residual), _ptr(out), M, _ptr(g("idx")),
+                         _ptr(g("w")), _ptr(g("scores")), _ptr(ws), ws.numel(), _stream(stream)), "moe_layer")
+    return out if tr is None else (out, tr)
 
 
 @dataclass

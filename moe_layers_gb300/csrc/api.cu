@@ -439,18 +439,38 @@ dec_status moe_impl(dec_handle* h, const uint16_t* x, const int32_t* idx, const 
   return moe_routed(h, x, idx, w, M, k, Wg, Wu, Wd, E, H, I, Wg_s, Wu_s, Wd_s, residual, out, ws, s);
 }
 
-// ---------------------------------------------------------------- decode layer workspace
-struct LayerWs {
-  int* sel_counter = nullptr;  // the one-token routing launch's counters (hand-off, row queue, done, routing flag, tail queue)
-  uint16_t* a = nullptr;
-  uint16_t* yin = nullptr;
-  uint16_t* h1 = nullptr;
-  uint16_t* b = nullptr;
+// ---------------------------------------------------------------- MoE layer / decode layer workspaces
+struct MoeLayerWs {
+  int* sel_counter = nullptr;  // the routing launches' counters (hand-off, row queue, done, routing flag, tail queue,
+                               // tail owner, router-unit tickets)
+  uint16_t* b = nullptr;       // the normalised rows (when a launch writes them out)
   float* parts = nullptr;
   int32_t* idx = nullptr;
   float* w = nullptr;
   MoeWs moe;
 };
+
+struct LayerWs {
+  uint16_t* a = nullptr;
+  uint16_t* yin = nullptr;
+  uint16_t* h1 = nullptr;
+  MoeLayerWs ml;
+};
+
+// Counters first: the routing counters, then the split-K tile counters
+// (extra_tiles: room for the dense projections' tiles as well).
+void carve_moe_layer_head(Carver& c, int E, int H, int I, long long extra_tiles, MoeLayerWs* w) {
+  w->sel_counter = c.take<int>(8);
+  carve_moe_counters(c, E, H, I, extra_tiles, &w->moe);
+}
+
+void carve_moe_layer_data(Carver& c, const dec_handle* h, int M, int k, int E, int H, int I, MoeLayerWs* w) {
+  w->b = c.take<uint16_t>((size_t)M * H);
+  w->parts = c.take<float>((size_t)router_ksplit(H) * M * E);
+  w->idx = c.take<int32_t>((size_t)M * k);
+  w->w = c.take<float>((size_t)M * k);
+  carve_moe_data(c, h, M, k, E, H, I, &w->moe);
+}
 
 bool layer_ok(const dec_layer_weights* L, int M) {
   if (!L || M < 1 || M > kMaxM) return false;
@@ -463,16 +483,160 @@ bool layer_ok(const dec_layer_weights* L, int M) {
 void carve_layer(Carver& c, const dec_handle* h, const dec_layer_weights* L, int M, LayerWs* w) {
   const int H = L->H;
   const long long dense_tiles = std::max<long long>((L->N_in + kTileN - 1) / kTileN, H / kTileN);
-  w->sel_counter = c.take<int>(8);
-  carve_moe_counters(c, L->E, H, L->I, dense_tiles, &w->moe);
+  carve_moe_layer_head(c, L->E, H, L->I, dense_tiles, &w->ml);
   w->a = c.take<uint16_t>((size_t)M * H);
   w->yin = c.take<uint16_t>((size_t)M * L->N_in);
   w->h1 = c.take<uint16_t>((size_t)M * H);
-  w->b = c.take<uint16_t>((size_t)M * H);
-  w->parts = c.take<float>((size_t)router_ksplit(H) * M * L->E);
-  w->idx = c.take<int32_t>((size_t)M * L->k);
-  w->w = c.take<float>((size_t)M * L->k);
-  carve_moe_data(c, h, M, L->k, L->E, H, L->I, &w->moe);
+  carve_moe_layer_data(c, h, M, L->k, L->E, H, L->I, &w->ml);
+}
+
+// ---------------------------------------------------------------- MoE layer
+struct MoeLayerArgs {
+  const uint16_t* x = nullptr;      // [M][H] the layer's input rows
+  const uint16_t* gamma = nullptr;  // RMSNorm gains applied to x first, or null
+  float eps = 0.f;
+  const float* Wr = nullptr;
+  int M = 0, k = 0, E = 0, H = 0, I = 0;
+  const uint16_t *Wg = nullptr, *Wu = nullptr, *Wd = nullptr;
+  const uint16_t *Wg_s = nullptr, *Wu_s = nullptr, *Wd_s = nullptr;
+  const uint16_t* residual = nullptr;  // or null
+  uint16_t* out = nullptr;
+  int32_t* idx = nullptr;
+  float* w = nullptr;
+  float* scores = nullptr;             // or null
+  const void* pf = nullptr;            // a region to pull into L2 during the routing (Part 1 §4), or null
+  size_t pf_bytes = 0;
+};
+
+// The MoE layer: [RMSNorm,] router, top-k, routing table, routed and shared
+// experts, combine [+ residual]; the kernel schedule by batch.
+dec_status moe_layer_impl(dec_handle* h, const MoeLayerArgs& A, const MoeLayerWs& w, cudaStream_t s) {
+  const int M = A.M, H = A.H;
+  // One to a few tokens on the small-matrix experts: the RMSNorm, the router,
+  // the top-k and the routing table are one launch (route_shared /
+  // router_select / the MoE fronts), and the experts read the normalised rows
+  // by token (no gather). Otherwise the split-K family's chain of launches.
+  const bool one_token = experts_small(h, M, H, A.I);
+  const bool few_tokens = !one_token && experts_few(h, M, A.k, A.E, H, A.I);
+  // the rows the experts read: the routing launch writes them out when it normalises
+  const uint16_t* b = A.gamma != nullptr ? w.b : A.x;
+  if (!one_token && !few_tokens && A.gamma != nullptr) {
+    LaunchScope scope(h, "rmsnorm2", s);
+    if (launch_rmsnorm(h, A.x, A.gamma, w.b, M, H, A.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
+  }
+  // Kimi K3 article, Part 1 §4: while the router / top-k phase leaves the
+  // memory idle, a side-stream kernel pulls weights that come next into L2:
+  // at one token the shared expert (it runs inside the routed launches), and
+  // the caller's next-operator region if given.
+  // The MoE front launches (one token; two to four on the small-matrix
+  // family) pull the next-operator region themselves, from the CTAs that wait
+  // for the routing, so the side stream then carries only the shared expert.
+  const bool front1 = one_token && A.Wg_s != nullptr && h->fuse_shared_routing == 2 &&
+                      route_shared_supported(h, 1, H, A.E, A.k) && gemv_down_combine_supported(A.k, A.I);
+  const bool front_few = few_tokens && A.Wg_s != nullptr && h->fuse_shared_routing == 2 && M * A.k <= 32;
+  const bool next_in_front = (front1 || front_few) && A.pf != nullptr && A.pf_bytes > 0;
+  const bool pf_shared = A.Wg_s != nullptr && one_token && h->prefetch_shared;
+  const bool pf_next_side = A.pf != nullptr && A.pf_bytes > 0 && !next_in_front;
+  const bool pf = pf_next_side || pf_shared;
+  const void* pf_front = next_in_front ? A.pf : nullptr;
+  const size_t pf_front_bytes = next_in_front ? A.pf_bytes : 0;
+  if (pf) {
+    DEC_CUDA(cudaEventRecord(h->ev_pf_fork, s));
+    DEC_CUDA(cudaStreamWaitEvent(h->pf, h->ev_pf_fork, 0));
+    {
+      LaunchScope scope(h, "prefetch", h->pf);
+      if (pf_shared) {
+        const size_t mat = (size_t)A.I * H * sizeof(uint16_t);
+        DEC_CUDA(launch_prefetch(h, A.Wg_s, mat, 16, h->pf));
+        DEC_CUDA(launch_prefetch(h, A.Wu_s, mat, 16, h->pf));
+        DEC_CUDA(launch_prefetch(h, A.Wd_s, mat, 16, h->pf));
+      }
+      if (pf_next_side) DEC_CUDA(launch_prefetch(h, A.pf, A.pf_bytes, 16, h->pf));
+    }
+    DEC_CUDA(cudaEventRecord(h->ev_pf_join, h->pf));
+  }
+  dec_status st = DEC_OK;
+  // The router / top-k phase is latency-bound; the shared expert and the
+  // prefetch stream use the idle bandwidth meanwhile.
+  if (one_token) {
+    // With a shared expert the routing launch also streams its gate/up.
+    const bool fuse_shared = A.Wg_s != nullptr && h->fuse_shared_routing && route_shared_supported(h, 1, H, A.E, A.k);
+    if (front1) {
+      // One MoE front launch (routing, shared gate/up, routed gate/up), then
+      // the down projection with the combine and the residual.
+      h->last_expert_variant = DEC_VARIANT_SMALL_M;
+      {
+        LaunchScope scope(h, "moe_front", s);
+        DEC_CUDA(launch_moe_front(h, A.x, A.gamma, A.eps, A.Wr, H, A.E, A.k, w.parts, w.sel_counter, A.idx, A.w,
+                                  A.scores, w.moe.table, A.Wg_s, A.Wu_s, A.I, w.moe.hs, A.Wg, A.Wu, w.moe.hbuf, s,
+                                  pf_front, pf_front_bytes));
+      }
+      {
+        LaunchScope scope(h, "down", s);
+        DEC_CUDA(launch_gemv_down_combine(h, A.Wd, H, A.Wd_s, H, A.I, w.moe.hbuf, w.moe.hs, w.moe.table, A.E, A.k, A.w,
+                                          A.residual, A.out, h->sms, s, true));
+      }
+      if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
+      return DEC_OK;
+    }
+    {
+      LaunchScope scope(h, "router", s);
+      if (fuse_shared)
+        DEC_CUDA(launch_route_shared(h, 1, A.x, A.gamma, A.eps, A.Wr, H, A.E, A.k, w.b, w.parts, w.sel_counter, A.idx,
+                                     A.w, A.scores, w.moe.table, A.Wg_s, A.Wu_s, A.I, w.moe.hs, s));
+      else
+        DEC_CUDA(launch_router_select(h, A.x, A.gamma, A.eps, A.Wr, H, A.E, A.k, w.b, w.parts, w.sel_counter, A.idx,
+                                      A.w, A.scores, w.moe.table, s));
+    }
+    st = moe_small(h, b, 0, A.w, A.k, A.Wg, A.Wu, A.Wd, A.E, H, A.I, A.Wg_s, A.Wu_s, A.Wd_s, A.residual, A.out, w.moe,
+                   s, fuse_shared);
+    if (st != DEC_OK) return st;
+    if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
+    return DEC_OK;
+  }
+  if (few_tokens) {
+    // Two to four tokens: the RMSNorm, router, top-k, routing table (one
+    // problem per entry) and the shared expert's gate/up in one launch; with
+    // the MoE front schedule the entries' gate/up as well.
+    if (front_few) {
+      {
+        LaunchScope scope(h, "moe_front", s);
+        DEC_CUDA(launch_moe_front_multi(h, M, A.x, A.gamma, A.eps, A.Wr, H, A.E, A.k, w.parts, w.sel_counter, A.idx,
+                                        A.w, A.scores, w.moe.table, A.Wg_s, A.Wu_s, A.I, w.moe.hs, A.Wg, A.Wu,
+                                        w.moe.hbuf, s, pf_front, pf_front_bytes));
+      }
+      st = moe_few(h, M, w.b, A.w, A.k, A.Wg, A.Wu, A.Wd, A.E, H, A.I, A.Wd_s, A.residual, A.out, w.moe, s, true);
+      if (st != DEC_OK) return st;
+      if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
+      return DEC_OK;
+    }
+    {
+      LaunchScope scope(h, "router", s);
+      DEC_CUDA(launch_route_shared(h, M, A.x, A.gamma, A.eps, A.Wr, H, A.E, A.k, w.b, w.parts, w.sel_counter, A.idx,
+                                   A.w, A.scores, w.moe.table, A.Wg_s, A.Wu_s, A.Wg_s ? A.I : 0, w.moe.hs, s));
+    }
+    // (the routing launch writes its rows, normalised or as they are, to w.b)
+    st = moe_few(h, M, w.b, A.w, A.k, A.Wg, A.Wu, A.Wd, A.E, H, A.I, A.Wd_s, A.residual, A.out, w.moe, s);
+    if (st != DEC_OK) return st;
+    if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
+    return DEC_OK;
+  }
+  st = moe_shared_fork(h, b, M, A.k, A.E, H, A.I, A.Wg_s, A.Wu_s, A.Wd_s, w.moe, s);
+  if (st != DEC_OK) return st;
+  {
+    LaunchScope scope(h, "router", s);
+    if (launch_router(h, b, A.Wr, M, H, A.E, w.parts, s) != cudaSuccess) return DEC_ERR_CUDA;
+  }
+  {
+    LaunchScope scope(h, "topk", s);
+    if (launch_topk(h, w.parts, router_ksplit(H), M, A.E, A.k, A.idx, A.w, A.scores, s) != cudaSuccess)
+      return DEC_ERR_CUDA;
+  }
+  st = moe_routed(h, b, A.idx, A.w, M, A.k, A.Wg, A.Wu, A.Wd, A.E, H, A.I, A.Wg_s, A.Wu_s, A.Wd_s, A.residual, A.out,
+                  w.moe, s);
+  if (st != DEC_OK) return st;
+  if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
+  return DEC_OK;
 }
 
 }  // namespace
@@ -761,9 +925,6 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
   LayerWs w;
   carve_layer(c, h, Wt, M, &w);
   uint16_t* h1 = (trace && trace->h1) ? trace->h1 : w.h1;
-  int32_t* idx = (trace && trace->idx) ? trace->idx : w.idx;
-  float* wt = (trace && trace->w) ? trace->w : w.w;
-  float* scores = trace ? trace->scores : nullptr;
   const int H = L.H;
 
   // Small-matrix input projection (up to four tokens): the first RMSNorm runs
@@ -773,133 +934,95 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
     LaunchScope scope(h, "rmsnorm1", s);
     if (launch_rmsnorm(h, hidden, L.gamma1, w.a, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
   }
-  dec_status st = fuse_norm1 ? linear_impl(h, hidden, H, L.W_in, nullptr, w.yin, M, L.N_in, H, w.moe.r0, s, "in_proj",
+  EngineRegion dense = w.ml.moe.r0;
+  dec_status st = fuse_norm1 ? linear_impl(h, hidden, H, L.W_in, nullptr, w.yin, M, L.N_in, H, dense, s, "in_proj",
                                            L.gamma1, L.eps)
-                             : linear_impl(h, w.a, H, L.W_in, nullptr, w.yin, M, L.N_in, H, w.moe.r0, s, "in_proj");
+                             : linear_impl(h, w.a, H, L.W_in, nullptr, w.yin, M, L.N_in, H, dense, s, "in_proj");
   if (st != DEC_OK) return st;
-  st = linear_impl(h, w.yin, L.N_in, L.W_o, hidden, h1, M, H, L.K_out, w.moe.r0, s, "out_proj");
+  st = linear_impl(h, w.yin, L.N_in, L.W_o, hidden, h1, M, H, L.K_out, dense, s, "out_proj");
   if (st != DEC_OK) return st;
-  // One to a few tokens on the small-matrix experts: the second RMSNorm, the
-  // router, the top-k and the routing table are one launch (route_shared /
-  // router_select), and the experts read the normalised rows by token (no
-  // gather). Otherwise the split-K family's chain of launches.
-  const bool one_token = experts_small(h, M, H, L.I);
-  const bool few_tokens = !one_token && experts_few(h, M, L.k, L.E, H, L.I);
-  if (!one_token && !few_tokens) {
-    LaunchScope scope(h, "rmsnorm2", s);
-    if (launch_rmsnorm(h, h1, L.gamma2, w.b, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
-  }
-  // Kimi K3 article, Part 1 §4: while the router / top-k phase leaves the
-  // memory idle, a side-stream kernel pulls weights that come next into L2:
-  // at one token the shared expert (it runs inside the routed launches), and
-  // the caller's next-operator region if given.
-  // The MoE front launches (one token; two to four on the small-matrix
-  // family) pull the next-operator region themselves, from the CTAs that wait
-  // for the routing, so the side stream then carries only the shared expert.
-  const bool front1 = one_token && L.Wg_s != nullptr && h->fuse_shared_routing == 2 &&
-                      route_shared_supported(h, 1, H, L.E, L.k) && gemv_down_combine_supported(L.k, L.I);
-  const bool front_few = few_tokens && L.Wg_s != nullptr && h->fuse_shared_routing == 2 && M * L.k <= 32;
-  const bool next_in_front = (front1 || front_few) && L.prefetch_next != nullptr && L.prefetch_bytes > 0;
-  const bool pf_shared = L.Wg_s != nullptr && experts_small(h, M, H, L.I) && h->prefetch_shared;
-  const bool pf_next_side = L.prefetch_next != nullptr && L.prefetch_bytes > 0 && !next_in_front;
-  const bool pf = pf_next_side || pf_shared;
-  const void* pf_front = next_in_front ? L.prefetch_next : nullptr;
-  const size_t pf_front_bytes = next_in_front ? L.prefetch_bytes : 0;
-  if (pf) {
-    DEC_CUDA(cudaEventRecord(h->ev_pf_fork, s));
-    DEC_CUDA(cudaStreamWaitEvent(h->pf, h->ev_pf_fork, 0));
-    {
-      LaunchScope scope(h, "prefetch", h->pf);
-      if (pf_shared) {
-        const size_t mat = (size_t)L.I * H * sizeof(uint16_t);
-        DEC_CUDA(launch_prefetch(h, L.Wg_s, mat, 16, h->pf));
-        DEC_CUDA(launch_prefetch(h, L.Wu_s, mat, 16, h->pf));
-        DEC_CUDA(launch_prefetch(h, L.Wd_s, mat, 16, h->pf));
-      }
-      if (pf_next_side) DEC_CUDA(launch_prefetch(h, L.prefetch_next, L.prefetch_bytes, 16, h->pf));
-    }
-    DEC_CUDA(cudaEventRecord(h->ev_pf_join, h->pf));
-  }
-  // The router / top-k phase is latency-bound; the shared expert and the
-  // prefetch stream use the idle bandwidth meanwhile.
-  if (one_token) {
-    // With a shared expert the routing launch also streams its gate/up.
-    const bool fuse_shared = L.Wg_s != nullptr && h->fuse_shared_routing &&
-                             route_shared_supported(h, 1, H, L.E, L.k);
-    if (front1) {
-      // One MoE front launch (routing, shared gate/up, routed gate/up), then
-      // the down projection with the combine and the residual.
-      h->last_expert_variant = DEC_VARIANT_SMALL_M;
-      {
-        LaunchScope scope(h, "moe_front", s);
-        DEC_CUDA(launch_moe_front(h, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.parts, w.sel_counter, idx, wt, scores,
-                                  w.moe.table, L.Wg_s, L.Wu_s, L.I, w.moe.hs, L.Wg, L.Wu, w.moe.hbuf, s, pf_front,
-                                  pf_front_bytes));
-      }
-      {
-        LaunchScope scope(h, "down", s);
-        DEC_CUDA(launch_gemv_down_combine(h, L.Wd, H, L.Wd_s, H, L.I, w.moe.hbuf, w.moe.hs, w.moe.table, L.E, L.k, wt,
-                                          h1, hidden, h->sms, s, true));
-      }
-      if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
-      return DEC_OK;
-    }
-    {
-      LaunchScope scope(h, "router", s);
-      if (fuse_shared)
-        DEC_CUDA(launch_route_shared(h, 1, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx,
-                                     wt, scores, w.moe.table, L.Wg_s, L.Wu_s, L.I, w.moe.hs, s));
-      else
-        DEC_CUDA(launch_router_select(h, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx,
-                                      wt, scores, w.moe.table, s));
-    }
-    st = moe_small(h, w.b, 0, wt, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, h1, hidden, w.moe, s,
-                   fuse_shared);
-    if (st != DEC_OK) return st;
-    if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
-    return DEC_OK;
-  }
-  if (few_tokens) {
-    // Two to four tokens: the second RMSNorm, router, top-k, routing table (one
-    // problem per entry) and the shared expert's gate/up in one launch; with
-    // the MoE front schedule the entries' gate/up as well.
-    if (front_few) {
-      {
-        LaunchScope scope(h, "moe_front", s);
-        DEC_CUDA(launch_moe_front_multi(h, M, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.parts, w.sel_counter, idx, wt,
-                                        scores, w.moe.table, L.Wg_s, L.Wu_s, L.I, w.moe.hs, L.Wg, L.Wu, w.moe.hbuf,
-                                        s, pf_front, pf_front_bytes));
-      }
-      st = moe_few(h, M, w.b, wt, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wd_s, h1, hidden, w.moe, s, true);
-      if (st != DEC_OK) return st;
-      if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
-      return DEC_OK;
-    }
-    {
-      LaunchScope scope(h, "router", s);
-      DEC_CUDA(launch_route_shared(h, M, h1, L.gamma2, L.eps, L.W_r, H, L.E, L.k, w.b, w.parts, w.sel_counter, idx,
-                                   wt, scores, w.moe.table, L.Wg_s, L.Wu_s, L.Wg_s ? L.I : 0, w.moe.hs, s));
-    }
-    st = moe_few(h, M, w.b, wt, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wd_s, h1, hidden, w.moe, s);
-    if (st != DEC_OK) return st;
-    if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
-    return DEC_OK;
-  }
-  st = moe_shared_fork(h, w.b, M, L.k, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, w.moe, s);
-  if (st != DEC_OK) return st;
-  {
-    LaunchScope scope(h, "router", s);
-    if (launch_router(h, w.b, L.W_r, M, H, L.E, w.parts, s) != cudaSuccess) return DEC_ERR_CUDA;
-  }
-  {
-    LaunchScope scope(h, "topk", s);
-    if (launch_topk(h, w.parts, router_ksplit(H), M, L.E, L.k, idx, wt, scores, s) != cudaSuccess)
-      return DEC_ERR_CUDA;
-  }
-  st = moe_routed(h, w.b, idx, wt, M, L.k, L.Wg, L.Wu, L.Wd, L.E, H, L.I, L.Wg_s, L.Wu_s, L.Wd_s, h1, hidden, w.moe, s);
-  if (st != DEC_OK) return st;
-  if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
+  // The MoE block, pre-norm with its own residual: hidden = h1 + MoE(RMSNorm(h1)).
+  MoeLayerArgs A;
+  A.x = h1;
+  A.gamma = L.gamma2;
+  A.eps = L.eps;
+  A.Wr = L.W_r;
+  A.M = M;
+  A.k = L.k;
+  A.E = L.E;
+  A.H = H;
+  A.I = L.I;
+  A.Wg = L.Wg;
+  A.Wu = L.Wu;
+  A.Wd = L.Wd;
+  A.Wg_s = L.Wg_s;
+  A.Wu_s = L.Wu_s;
+  A.Wd_s = L.Wd_s;
+  A.residual = h1;
+  A.out = hidden;
+  A.idx = (trace && trace->idx) ? trace->idx : w.ml.idx;
+  A.w = (trace && trace->w) ? trace->w : w.ml.w;
+  A.scores = trace ? trace->scores : nullptr;
+  A.pf = L.prefetch_next;
+  A.pf_bytes = L.prefetch_next != nullptr ? L.prefetch_bytes : 0;
+  return moe_layer_impl(h, A, w.ml, s);
+}
+
+dec_status moe_layer_workspace_size(const dec_handle* h, const dec_moe_weights* Wt, int M, size_t* bytes) {
+  if (h == nullptr || Wt == nullptr || bytes == nullptr || !moe_shape_ok(M, Wt->k, Wt->E, Wt->H, Wt->I))
+    return DEC_ERR_INVALID_ARG;
+  Carver c(nullptr);
+  MoeLayerWs w;
+  carve_moe_layer_head(c, Wt->E, Wt->H, Wt->I, 0, &w);
+  carve_moe_layer_data(c, h, M, Wt->k, Wt->E, Wt->H, Wt->I, &w);
+  *bytes = c.used;
   return DEC_OK;
+}
+
+dec_status moe_layer(dec_handle* h, const dec_moe_weights* Wt, const dec_bf16* x, const dec_bf16* residual,
+                     dec_bf16* out, int M, int32_t* idx, float* w, float* scores, void* ws, size_t ws_bytes,
+                     cudaStream_t s) {
+  if (h == nullptr || Wt == nullptr || x == nullptr || out == nullptr) return DEC_ERR_INVALID_ARG;
+  const dec_moe_weights& L = *Wt;
+  if (!moe_shape_ok(M, L.k, L.E, L.H, L.I) || !L.W_r || !L.Wg || !L.Wu || !L.Wd || !(L.eps >= 0.f))
+    return DEC_ERR_INVALID_ARG;
+  const bool any_s = L.Wg_s || L.Wu_s || L.Wd_s, all_s = L.Wg_s && L.Wu_s && L.Wd_s;
+  if (any_s && !all_s) return DEC_ERR_INVALID_ARG;
+  for (const void* p : {(const void*)x, (const void*)residual, (const void*)out, (const void*)L.gamma,
+                        (const void*)L.W_r, (const void*)L.Wg, (const void*)L.Wu, (const void*)L.Wd,
+                        (const void*)L.Wg_s, (const void*)L.Wu_s, (const void*)L.Wd_s, (const void*)idx,
+                        (const void*)w, (const void*)scores, (const void*)ws})
+    if (p != nullptr && !al16(p)) return DEC_ERR_INVALID_ARG;
+  if (out == x) return DEC_ERR_INVALID_ARG;
+  size_t need = 0;
+  moe_layer_workspace_size(h, Wt, M, &need);
+  if (ws == nullptr || ws_bytes < need) return DEC_ERR_INVALID_ARG;
+  Carver c(ws);
+  MoeLayerWs mw;
+  carve_moe_layer_head(c, L.E, L.H, L.I, 0, &mw);
+  carve_moe_layer_data(c, h, M, L.k, L.E, L.H, L.I, &mw);
+  MoeLayerArgs A;
+  A.x = x;
+  A.gamma = L.gamma;
+  A.eps = L.eps;
+  A.Wr = L.W_r;
+  A.M = M;
+  A.k = L.k;
+  A.E = L.E;
+  A.H = L.H;
+  A.I = L.I;
+  A.Wg = L.Wg;
+  A.Wu = L.Wu;
+  A.Wd = L.Wd;
+  A.Wg_s = L.Wg_s;
+  A.Wu_s = L.Wu_s;
+  A.Wd_s = L.Wd_s;
+  A.residual = residual;
+  A.out = out;
+  A.idx = idx != nullptr ? idx : mw.idx;
+  A.w = w != nullptr ? w : mw.w;
+  A.scores = scores;
+  return moe_layer_impl(h, A, mw, s);
 }
 
 dec_status dec_prefetch_l2(dec_handle* h, const void* ptr, size_t bytes, cudaStream_t stream) {

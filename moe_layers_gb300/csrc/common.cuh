@@ -154,6 +154,43 @@ __device__ __forceinline__ uint4 norm8(const uint4& a, const uint4& g, float r) 
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// This thread's partial sum of squares over the vectors it holds of a row:
+// v[i] is vector t + T i (those below H8), taken in ascending i.
+template <int NV, int T>
+__device__ __forceinline__ float thread_sumsq(const uint4 (&v)[NV], int H8, float ss = 0.f) {
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+    if ((int)threadIdx.x + T * i < H8) ss = sumsq8(v[i], ss);
+  return ss;
+}
+
+// The RMSNorm scale 1 / sqrt(mean(x^2) + eps) of a row of H elements from each
+// thread's partial sum of squares, reduced in the one order that every kernel
+// here that normalises a row uses: warp shuffles (xor 16, 8, 4, 2, 1), then the
+// NW warps' sums in warp order. A row normalised by any of them therefore has
+// the same bits. red: NW floats of shared memory that no other thread is
+// still reading; one barrier.
+template <int NW>
+__device__ __forceinline__ float block_rms_scale(float ss, int H, float eps, float* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int q = 0; q < NW; ++q) tot += red[q];
+  return rsqrtf(tot / (float)H + eps);
+}
+
+// ---------------------------------------------------------------- SwiGLU, sigmoid
+// One SwiGLU output from its gate and up sums, rounded once to bf16:
+// silu(g) * u = g / (1 + e^-g) * u.
+__device__ __forceinline__ uint16_t swiglu_bf16(float g, float u) { return f2bf(g / (1.0f + expf(-g)) * u); }
+
+// Router score of a logit: 1 / (1 + e^-z).
+__device__ __forceinline__ float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
+
 // ---------------------------------------------------------------- PDL
 // Programmatic dependent launch: a kernel may start while its predecessor on
 // the stream drains. Everything before pdl_wait() may touch only memory that

@@ -99,26 +99,11 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
   if (gamma != nullptr) {
     // a_m = bf16(x_m / sqrt(mean(x_m^2) + eps) * gamma) for every row m, in
     // the reduction order of the stand-alone RMSNorm kernel (the same bits).
-    __shared__ float rred[kGemvThreads / 32][M];
+    __shared__ float rred[M][kGemvThreads / 32];
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-      float ss = 0.f;
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int v = t + kGemvThreads * i;
-        if (v < K8) ss = sumsq8(xr[m][i], ss);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) rred[warp][m] = ss;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-      float tot = 0.f;
-#pragma unroll
-      for (int q = 0; q < kGemvThreads / 32; ++q) tot += rred[q][m];
-      const float rs = rsqrtf(tot / (float)K + eps);
+      const float rs =
+          block_rms_scale<kGemvThreads / 32>(thread_sumsq<VPT, kGemvThreads>(xr[m], K8), K, eps, rred[m]);
 #pragma unroll
       for (int i = 0; i < VPT; ++i) xr[m][i] = norm8(xr[m][i], gv[i], rs);
     }

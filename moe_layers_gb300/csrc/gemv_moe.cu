@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_kernel(const GemvMoePa
       void* dst = e < 0 ? P.sout : P.out;
       const long long o = slot * (e < 0 ? P.sldo : P.ldo) + r + t;
       if (SWIGLU)
-        reinterpret_cast<uint16_t*>(dst)[o] = f2bf(g / (1.0f + expf(-g)) * up);
+        reinterpret_cast<uint16_t*>(dst)[o] = swiglu_bf16(g, up);
       else
         reinterpret_cast<float*>(dst)[o] = g;
     }
@@ -873,7 +873,7 @@ __global__ void __launch_bounds__(kGmThreads, 2) gemv_moe_narrow_kernel(const Ge
         const long long o = slot * (e < 0 ? P.sldo : P.ldo) + r + u;
         if (SWIGLU) {
           const float gg = acc[u][0], up = acc[u][NR - 1];
-          reinterpret_cast<uint16_t*>(dst)[o] = f2bf(gg / (1.0f + expf(-gg)) * up);
+          reinterpret_cast<uint16_t*>(dst)[o] = swiglu_bf16(gg, up);
         } else {
           reinterpret_cast<float*>(dst)[o] = acc[u][0];
         }

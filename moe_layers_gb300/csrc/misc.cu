@@ -17,7 +17,7 @@ namespace dec {
 template <int VPT>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const uint16_t* __restrict__ gamma,
                                                       uint16_t* y, int H, float eps) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const uint16_t* xr = x + (size_t)blockIdx.x * H;
   uint16_t* yr = y + (size_t)blockIdx.x * H;
   __shared__ float red[8];
@@ -38,13 +38,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, const u
   } else {
     for (int v = tid; v < H8; v += blockDim.x) ss = sumsq8(ld_act16(xr + (size_t)v * 8), ss);
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) red[warp] = ss;
-  __syncthreads();
-  float tot = 0.f;
-  for (int q = 0; q < (int)(blockDim.x >> 5); ++q) tot += red[q];
-  const float r = rsqrtf(tot / (float)H + eps);
+  const float r = block_rms_scale<8>(ss, H, eps, red);
   auto put = [&](int v, const uint4& a) {
     const uint4 g = *reinterpret_cast<const uint4*>(gamma + (size_t)v * 8);
     *reinterpret_cast<uint4*>(yr + (size_t)v * 8) = norm8(a, g, r);

@@ -92,6 +92,63 @@ __device__ __forceinline__ int take_unit(int* ctr, int nunits, int G) {
   return (int)atomicInc(reinterpret_cast<unsigned*>(ctr + 6), (unsigned)(nunits + G - 1));
 }
 
+// The token's row into xr (registers) and sx (shared memory), RMS-normalised
+// with the gains that xr holds on entry, or as it is without gains (has_gamma
+// false); also to xn when given. Normalising takes one barrier.
+template <int VPT>
+__device__ __forceinline__ void norm_row(const uint16_t* row, bool has_gamma, float eps, int H, uint4 (&xr)[VPT],
+                                         uint16_t* sx, float* red, uint16_t* xn) {
+  const int t = threadIdx.x, H8 = H >> 3;
+  uint4 hv[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = t + kThreads * i;
+    hv[i] = v < H8 ? ld_act16(row + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+  }
+  float r = 0.f;
+  if (has_gamma) r = block_rms_scale<kThreads / 32>(thread_sumsq<VPT, kThreads>(hv, H8), H, eps, red);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = t + kThreads * i;
+    xr[i] = has_gamma ? norm8(hv[i], xr[i], r) : hv[i];
+    if (v < H8) {
+      *reinterpret_cast<uint4*>(&sx[v * 8]) = xr[i];
+      if (xn != nullptr) *reinterpret_cast<uint4*>(xn + (size_t)v * 8) = xr[i];
+    }
+  }
+}
+
+// M <= MT token rows [M][H] into sx [MT][H] (and xn when given), each
+// RMS-normalised with the gains gv, or as they are without gains. One barrier
+// per row when normalising (red: [MT][8] floats).
+template <int VPT, int MT>
+__device__ __forceinline__ void norm_rows(const uint16_t* rows, int M, bool has_gamma, const uint4 (&gv)[VPT],
+                                          float eps, int H, uint16_t* sx, float (*red)[kThreads / 32], uint16_t* xn) {
+  const int t = threadIdx.x, H8 = H >> 3;
+#pragma unroll
+  for (int q = 0; q < MT; ++q) {
+    if (q < M) {
+      uint4 hv[VPT];
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = t + kThreads * i;
+        hv[i] = v < H8 ? ld_act16(rows + (size_t)q * H + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+      }
+      float r = 0.f;
+      if (has_gamma) r = block_rms_scale<kThreads / 32>(thread_sumsq<VPT, kThreads>(hv, H8), H, eps, red[q]);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = t + kThreads * i;
+        if (v < H8) {
+          const uint4 y = has_gamma ? norm8(hv[i], gv[i], r) : hv[i];
+          *reinterpret_cast<uint4*>(&sx[(size_t)q * H + v * 8]) = y;
+          if (xn != nullptr) *reinterpret_cast<uint4*>(xn + (size_t)q * H + (size_t)v * 8) = y;
+        }
+      }
+    }
+  }
+}
+
 template <int J, int VPT>
 __global__ void __launch_bounds__(kThreads, 2) route_shared_kernel(const RouteSharedParams P) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -141,40 +198,13 @@ __global__ void __launch_bounds__(kThreads, 2) route_shared_kernel(const RouteSh
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int v = t + kThreads * i;
-    xr[i] = v < H8 ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+    xr[i] = (P.gamma != nullptr && v < H8) ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8)
+                                           : make_uint4(0, 0, 0, 0);
   }
   pdl_wait();
 
   // 2. RMSNorm of the row (xr holds the gains until normalised)
-  {
-    uint4 hv[VPT];
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = t + kThreads * i;
-      hv[i] = v < H8 ? ld_act16(P.h1 + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < VPT; ++i)
-      if (t + kThreads * i < H8) ss = sumsq8(hv[i], ss);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) s_norm[warp] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int q = 0; q < kThreads / 32; ++q) tot += s_norm[q];
-    const float r = rsqrtf(tot / (float)H + P.eps);
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = t + kThreads * i;
-      xr[i] = norm8(hv[i], xr[i], r);
-      if (v < H8) {
-        *reinterpret_cast<uint4*>(&sx[v * 8]) = xr[i];
-        if (c == 0) *reinterpret_cast<uint4*>(P.xn + (size_t)v * 8) = xr[i];
-      }
-    }
-  }
+  norm_row<VPT>(P.h1, P.gamma != nullptr, P.eps, H, xr, sx, s_norm, c == 0 ? P.xn : nullptr);
   int pending = base + 2;  // (thread 0) the third row; the first two are published at the hand-off
   __syncthreads();
 
@@ -271,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 2) route_shared_kernel(const RouteSh
         gs += red[buf][q][0];
         us += red[buf][q][1];
       }
-      P.hs[cur] = f2bf(gs / (1.0f + expf(-gs)) * us);
+      P.hs[cur] = swiglu_bf16(gs, us);
     }
     const int nn = s_next[buf];
     cur = nxt;
@@ -306,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 2) route_shared_multi_kernel(const R
   const int ngrp = (P.E + 7) / 8;
   const int ksplit = (H + kUnitCols - 1) / kUnitCols;
   extern __shared__ __align__(16) uint16_t sx[];  // the normalised rows [MT][H]
-  __shared__ float s_norm[kThreads / 32][MT];
+  __shared__ float s_norm[MT][kThreads / 32];
   __shared__ float red[2][kThreads / 32][2 * MT];
   __shared__ int s_row[2];
   __shared__ int s_next[2];
@@ -341,51 +371,13 @@ __global__ void __launch_bounds__(kThreads, 2) route_shared_multi_kernel(const R
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int v = t + kThreads * i;
-    gv[i] = v < H8 ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+    gv[i] = (P.gamma != nullptr && v < H8) ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8)
+                                           : make_uint4(0, 0, 0, 0);
   }
   pdl_wait();
 
   // RMSNorm of the M rows (each row's sum of squares in the RMSNorm kernel's order)
-  {
-    float ss[MT];
-#pragma unroll
-    for (int q = 0; q < MT; ++q) {
-      ss[q] = 0.f;
-      if (q < M) {
-        uint4 hv[VPT];
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-          const int v = t + kThreads * i;
-          hv[i] = v < H8 ? ld_act16(P.h1 + (size_t)q * H + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int i = 0; i < VPT; ++i)
-          if (t + kThreads * i < H8) ss[q] = sumsq8(hv[i], ss[q]);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss[q] += __shfl_xor_sync(0xffffffffu, ss[q], o);
-      if (lane == 0) s_norm[warp][q] = ss[q];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int q = 0; q < MT; ++q) {
-      if (q < M) {
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) tot += s_norm[w][q];
-        const float r = rsqrtf(tot / (float)H + P.eps);
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-          const int v = t + kThreads * i;
-          if (v < H8) {
-            const uint4 y = norm8(ld_act16(P.h1 + (size_t)q * H + (size_t)v * 8), gv[i], r);
-            *reinterpret_cast<uint4*>(&sx[(size_t)q * H + v * 8]) = y;
-            if (c == 0) *reinterpret_cast<uint4*>(P.xn + (size_t)q * H + (size_t)v * 8) = y;
-          }
-        }
-      }
-    }
-  }
+  norm_rows<VPT, MT>(P.h1, M, P.gamma != nullptr, gv, P.eps, H, sx, s_norm, c == 0 ? P.xn : nullptr);
   int pending = base + 2;  // (thread 0)
   __syncthreads();
 
@@ -498,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 2) route_shared_multi_kernel(const R
         gs += red[buf][w][2 * t];
         us += red[buf][w][2 * t + 1];
       }
-      P.hs[(size_t)t * P.I + cur] = f2bf(gs / (1.0f + expf(-gs)) * us);
+      P.hs[(size_t)t * P.I + cur] = swiglu_bf16(gs, us);
     }
     const int nn = s_next[buf];
     cur = nxt;
@@ -571,35 +563,11 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_kernel(const RouteShare
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int v = t + kThreads * i;
-    xr[i] = v < H8 ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+    xr[i] = (P.gamma != nullptr && v < H8) ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8)
+                                           : make_uint4(0, 0, 0, 0);
   }
   pdl_wait();
-  {
-    uint4 hv[VPT];
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = t + kThreads * i;
-      hv[i] = v < H8 ? ld_act16(P.h1 + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < VPT; ++i)
-      if (t + kThreads * i < H8) ss = sumsq8(hv[i], ss);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) s_norm[warp] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int q = 0; q < kThreads / 32; ++q) tot += s_norm[q];
-    const float r = rsqrtf(tot / (float)H + P.eps);
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = t + kThreads * i;
-      xr[i] = norm8(hv[i], xr[i], r);
-      if (v < H8) *reinterpret_cast<uint4*>(&sx[v * 8]) = xr[i];
-    }
-  }
+  norm_row<VPT>(P.h1, P.gamma != nullptr, P.eps, H, xr, sx, s_norm, nullptr);
   int pending = base + 2;
   __syncthreads();
   // Router units: the CTA's ticket, then further tickets while units remain.
@@ -702,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_kernel(const RouteShare
       gs += red[b][q][0];
       us += red[b][q][1];
     }
-    return f2bf(gs / (1.0f + expf(-gs)) * us);
+    return swiglu_bf16(gs, us);
   };
   auto shift = [&]() {
 #pragma unroll
@@ -898,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_multi_kernel(const Rout
   const int ngrp = (P.E + 7) / 8;
   const int ksplit = (H + kUnitCols - 1) / kUnitCols;
   extern __shared__ __align__(16) uint16_t sx[];  // the normalised rows [MT][H]
-  __shared__ float s_norm[kThreads / 32][MT];
+  __shared__ float s_norm[MT][kThreads / 32];
   __shared__ float red[2][kThreads / 32][2 * MT];
   __shared__ int s_row[2];
   __shared__ int s_next[2];
@@ -940,49 +908,13 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_multi_kernel(const Rout
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int v = t + kThreads * i;
-    gv[i] = v < H8 ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+    gv[i] = (P.gamma != nullptr && v < H8) ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8)
+                                           : make_uint4(0, 0, 0, 0);
   }
   pdl_wait();
 
   // RMSNorm of the M rows (each row's sum of squares in the RMSNorm kernel's order)
-  {
-    float ss[MT];
-#pragma unroll
-    for (int q = 0; q < MT; ++q) {
-      ss[q] = 0.f;
-      if (q < M) {
-        uint4 hv[VPT];
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-          const int v = t + kThreads * i;
-          hv[i] = v < H8 ? ld_act16(P.h1 + (size_t)q * H + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int i = 0; i < VPT; ++i)
-          if (t + kThreads * i < H8) ss[q] = sumsq8(hv[i], ss[q]);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss[q] += __shfl_xor_sync(0xffffffffu, ss[q], o);
-      if (lane == 0) s_norm[warp][q] = ss[q];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int q = 0; q < MT; ++q) {
-      if (q < M) {
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) tot += s_norm[w][q];
-        const float r = rsqrtf(tot / (float)H + P.eps);
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-          const int v = t + kThreads * i;
-          if (v < H8)
-            *reinterpret_cast<uint4*>(&sx[(size_t)q * H + v * 8]) =
-                norm8(ld_act16(P.h1 + (size_t)q * H + (size_t)v * 8), gv[i], r);
-        }
-      }
-    }
-  }
+  norm_rows<VPT, MT>(P.h1, M, P.gamma != nullptr, gv, P.eps, H, sx, s_norm, nullptr);
   int pending = base + 2;  // (thread 0)
   __syncthreads();
 
@@ -1111,7 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_multi_kernel(const Rout
           gs += red[buf][w][2 * t];
           us += red[buf][w][2 * t + 1];
         }
-        P.hs[(size_t)t * I + cur] = f2bf(gs / (1.0f + expf(-gs)) * us);
+        P.hs[(size_t)t * I + cur] = swiglu_bf16(gs, us);
       }
       const int nn = s_next[buf];
       cur = nxt;
@@ -1191,7 +1123,7 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_multi_kernel(const Rout
           gs += red[buf][w][0];
           us += red[buf][w][1];
         }
-        P.hbuf[q] = f2bf(gs / (1.0f + expf(-gs)) * us);
+        P.hbuf[q] = swiglu_bf16(gs, us);
       }
       buf ^= 1;
     };

@@ -152,13 +152,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(const uint16_t* xin,
     for (int j = 0; j < 4; ++j)
       if (tid + 256 * j < H8) ss = sumsq8(hv[j], ss);
     for (int v = tid + 1024; v < H8; v += 256) ss = sumsq8(ld_act16(xin + (size_t)v * 8), ss);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    float tot = 0.f;
-    for (int q = 0; q < (int)(blockDim.x >> 5); ++q) tot += red[q];
-    const float r = rsqrtf(tot / (float)H + eps);
+    const float r = block_rms_scale<8>(ss, H, eps, red);
     if (owner) {
       const int jj = ks >> 1;
       const uint4 xv = jj == 0 ? hv[0] : jj == 1 ? hv[1] : jj == 2 ? hv[2] : jj == 3 ? hv[3]

@@ -132,7 +132,7 @@ __device__ __forceinline__ void block_scores(const float* parts, int ks, int M, 
     for (int j = 0; j < J; ++j) {
       const int e = tid + 256 * j;
       if (m < nt && e < E) {
-        const float sc = 1.0f / (1.0f + expf(-sv[m][j]));
+        const float sc = sigmoid_f(sv[m][j]);
         if (scores != nullptr) scores[(size_t)(t0 + m) * E + e] = sc;
         s_sc[m][e] = sc;
       }
@@ -179,7 +179,7 @@ __device__ __forceinline__ void block_topk(const float* parts, int ks, int M, in
   for (int j = 0; j < JT; ++j) {
     const int e = tid + 256 * j;
     if (e < E) {
-      const float sc = 1.0f / (1.0f + expf(-sv[j]));
+      const float sc = sigmoid_f(sv[j]);
       if (scores != nullptr) scores[(size_t)t * E + e] = sc;
       s_sc[e] = sc;
     }

@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
         for (int i = 0; i < 16; ++i)
           if (i < jn) {
             const float g = v0[i];
-            out16[((long long)pr.off + ch * 16 + i) * P.ldo + n] = f2bf(g / (1.0f + expf(-g)) * v1[i]);
+            out16[((long long)pr.off + ch * 16 + i) * P.ldo + n] = swiglu_bf16(g, v1[i]);
           }
       } else {
 #pragma unroll

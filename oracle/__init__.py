@@ -199,6 +199,38 @@ def moe(x, idx, w, expert: ExpertFn, shared: Optional[Sequence] = None, residual
     return out
 
 
+# ----------------------------------------------------------------------------- MoE layer
+def moe_layer(x, gamma, Wr, k: int, expert: ExpertFn, shared: Optional[Sequence] = None, residual=None,
+              eps: float = RMS_EPS, tokens: Optional[Sequence[int]] = None, storage: str = "bf16"):
+    """The MoE layer as one step: optional RMSNorm, router, top-k, experts.
+
+    b = RMSNorm(x; gamma) (x itself when gamma is None); logits, scores =
+    router(b); idx, w = top-k; out = [residual +] moe(b, idx, w) [+ S(b)].
+    Kimi K3 article, Part 1 §3 (router scores, then the routed experts and the
+    shared expert). With ``storage`` "bf16" (default) the normalised rows b,
+    a stored activation, are rounded to bf16 before the router and the
+    experts read them; "f64" rounds nothing.
+
+    Returns a dict with b, logits, scores, idx, w and ``out`` (unrounded),
+    and ``b_unrounded`` (b before its storage rounding); ``tokens`` limits all
+    of it to some rows.
+    """
+    if storage not in ("bf16", "f64"):
+        raise ValueError("storage must be 'bf16' or 'f64'")
+    st = round_bf16 if storage == "bf16" else (lambda v: v)
+    x = as_f64(x)
+    rows = list(range(x.shape[0])) if tokens is None else [int(t) for t in tokens]
+    x = x[rows]
+    b_unrounded = rmsnorm(x, gamma, eps) if gamma is not None else x
+    b = st(b_unrounded)
+    logits, scores = router_scores(b, Wr)
+    idx, w = topk(scores, k)
+    out = moe(b, idx, w, expert, shared)
+    if residual is not None:
+        out = out + as_f64(residual)[rows]
+    return dict(b=b, b_unrounded=b_unrounded, logits=logits, scores=scores, idx=idx, w=w, out=out)
+
+
 # ----------------------------------------------------------------------------- decode layer
 def decode_layer(h, gamma1, W_in, W_o, gamma2, Wr, k: int, expert: ExpertFn, shared: Optional[Sequence],
                  k_out: Optional[int] = None, eps: float = RMS_EPS, tokens: Optional[Sequence[int]] = None,
@@ -210,7 +242,8 @@ def decode_layer(h, gamma1, W_in, W_o, gamma2, Wr, k: int, expert: ExpertFn, sha
     out-projection; the plainest reading that keeps the data dependency is to
     feed the first ``k_out`` columns of the input projection (K of the
     out-projection) straight to the out-projection. The MoE block is pre-norm
-    with its own residual: out = h1 + MoE(RMSNorm(h1)).
+    with its own residual: out = h1 + MoE(RMSNorm(h1)) (``moe_layer`` with
+    gamma2 and the residual h1).
 
     ``storage``: the layer's activations are bf16 tensors, so with "bf16"
     (default) the output of each operation (a, y_in, h1, b) is rounded to bf16
@@ -219,8 +252,10 @@ def decode_layer(h, gamma1, W_in, W_o, gamma2, Wr, k: int, expert: ExpertFn, sha
     the layer defines. "f64" rounds nothing.
 
     Returns a dict with the intermediates (a, y_in, h1, b, logits, scores,
-    idx, w) and the output ``out`` (unrounded); ``tokens`` limits all of it to
-    some rows.
+    idx, w), the output ``out`` (unrounded), and ``unrounded``: the values of
+    a, y_in, h1 and b before their storage rounding (each the exact result of
+    its operation on the stored inputs); ``tokens`` limits all of it to some
+    rows.
     """
     if storage not in ("bf16", "f64"):
         raise ValueError("storage must be 'bf16' or 'f64'")
@@ -230,11 +265,12 @@ def decode_layer(h, gamma1, W_in, W_o, gamma2, Wr, k: int, expert: ExpertFn, sha
     h = h[rows]
     W_o64 = as_f64(W_o)
     k_out = W_o64.shape[1] if k_out is None else k_out
-    a = st(rmsnorm(h, gamma1, eps))
-    y_in = st(linear(a, W_in))
-    h1 = st(linear_residual(y_in[:, :k_out], W_o64, h))
-    b = st(rmsnorm(h1, gamma2, eps))
-    logits, scores = router_scores(b, Wr)
-    idx, w = topk(scores, k)
-    out = h1 + moe(b, idx, w, expert, shared)
-    return dict(a=a, y_in=y_in, h1=h1, b=b, logits=logits, scores=scores, idx=idx, w=w, out=out)
+    a_x = rmsnorm(h, gamma1, eps)
+    a = st(a_x)
+    y_x = linear(a, W_in)
+    y_in = st(y_x)
+    h1_x = linear_residual(y_in[:, :k_out], W_o64, h)
+    h1 = st(h1_x)
+    m = moe_layer(h1, gamma2, Wr, k, expert, shared, residual=h1, eps=eps, storage=storage)
+    return dict(a=a, y_in=y_in, h1=h1, b=m["b"], logits=m["logits"], scores=m["scores"], idx=m["idx"], w=m["w"],
+                out=m["out"], unrounded=dict(a=a_x, y_in=y_x, h1=h1_x, b=m["b_unrounded"]))

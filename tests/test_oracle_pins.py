@@ -346,9 +346,46 @@ def pin_decode_layer(o):
     assert np.allclose(sub["out"], full["out"][[3, 0]], rtol=1e-12, atol=1e-12)
 
 
+def pin_moe_layer(o):
+    rng = np.random.default_rng(11)
+    E, H, I, k = 10, 16, 8, 3
+    Wg, Wu, Wd = _bank(rng, E, H, I)
+    Ws = tuple(a[0] for a in _bank(rng, 1, H, I))
+    Wr = rng.standard_normal((E, H))
+    ex = lambda e: (Wg[e], Wu[e], Wd[e])
+    x = rng.standard_normal((5, H))
+    r = rng.standard_normal((5, H))
+    g = 1.0 + 0.1 * rng.standard_normal(H)
+    # without gains the rows are read as they are
+    plain = o.moe_layer(x, None, Wr, k, ex, Ws, storage="f64")
+    assert np.array_equal(plain["b"], x)
+    # the residual enters once, unchanged
+    with_r = o.moe_layer(x, None, Wr, k, ex, Ws, residual=r, storage="f64")
+    assert np.allclose(with_r["out"] - plain["out"], r, rtol=0, atol=1e-12)
+    # with gains the rows are normalised first: invariant under a positive row scale (eps 0)
+    a = o.moe_layer(x, g, Wr, k, ex, Ws, eps=0.0, storage="f64")
+    b = o.moe_layer(x * np.array([[0.5], [2.0], [3.0], [0.25], [7.0]]), g, Wr, k, ex, Ws, eps=0.0, storage="f64")
+    assert np.array_equal(a["idx"], b["idx"])
+    assert np.allclose(a["out"], b["out"], rtol=1e-9, atol=1e-9)
+    assert not np.allclose(a["out"], plain["out"], rtol=1e-3, atol=1e-3)
+    # identical experts: the renormalised weights sum to one, so the routed part is that expert
+    same = lambda e: (Wg[0], Wu[0], Wd[0])
+    one = o.moe_layer(x, None, Wr, k, same, None, storage="f64")
+    assert np.allclose(one["out"], o.swiglu_expert(x, Wg[0], Wu[0], Wd[0]), rtol=1e-12, atol=1e-12)
+    # bf16 storage rounds the normalised rows once; the unrounded value is kept beside them
+    st = o.moe_layer(x, g, Wr, k, ex, Ws, eps=0.0)
+    assert np.array_equal(st["b"], o.round_bf16(st["b_unrounded"]))
+    assert np.array_equal(st["b_unrounded"], a["b"])
+    # the decode layer's stored activations and their unrounded values
+    L = _tiny_layer(rng)
+    d = o.decode_layer(rng.standard_normal((3, 16)), **L)
+    for key in ("a", "y_in", "h1", "b"):
+        assert np.array_equal(d[key], o.round_bf16(d["unrounded"][key])), key
+
+
 PINS = [pin_linear_bruteforce, pin_linear_integer_exact, pin_linear_orientation, pin_linear_linearity,
         pin_linear_residual, pin_rmsnorm, pin_router_golden, pin_router_properties, pin_swiglu_golden,
-        pin_swiglu_odd_part, pin_moe_properties, pin_round_bf16, pin_decode_layer]
+        pin_swiglu_odd_part, pin_moe_properties, pin_round_bf16, pin_decode_layer, pin_moe_layer]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -437,6 +474,12 @@ def _mut_layer_no_moe_residual(mp):
     mp.setattr(oracle, "decode_layer", dl)
 
 
+def _mut_moe_layer_always_normalises(mp):
+    orig = oracle.moe_layer
+    mp.setattr(oracle, "moe_layer", lambda x, gamma, *a, **kw: orig(
+        x, np.ones(np.asarray(x).shape[1]) if gamma is None else gamma, *a, **kw))
+
+
 def _mut_round_half_up(mp):
     mp.setattr(oracle, "round_bf16", lambda a: (lambda v, e: np.ldexp(np.floor(np.ldexp(v, 8 - e) + 0.5), e - 8))(
         np.asarray(a, dtype=np.float64), np.maximum(np.frexp(np.asarray(a, dtype=np.float64))[1], -125)))
@@ -445,7 +488,7 @@ def _mut_round_half_up(mp):
 MUTATIONS = [_mut_round_half_up, _mut_linear_transposed, _mut_linear_dropped_term, _mut_residual_sign, _mut_rms_sum,
              _mut_rms_eps_outside, _mut_sigmoid_sign, _mut_softmax_scores, _mut_tie_high_id, _mut_no_renorm,
              _mut_silu_as_sigmoid, _mut_gate_up_swapped, _mut_moe_unweighted, _mut_moe_no_shared,
-             _mut_layer_no_moe_residual]
+             _mut_layer_no_moe_residual, _mut_moe_layer_always_normalises]
 
 
 @pytest.mark.parametrize("mutate", MUTATIONS, ids=[m.__name__[5:] for m in MUTATIONS])
