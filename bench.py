@@ -13,8 +13,9 @@ every step; the dense weights alternate between two copies. Every step reads
 
 Reported (one JSON line, rank 0):
   value        device-timed microseconds per step at --batch (CUDA events, inputs resident):
-               the K steps captured once as a CUDA graph and replayed (the stream-launched
-               time of the same K steps is reported beside it as us_per_step_stream)
+               the K steps captured once as a CUDA graph and replayed --repeats times, the
+               median (min/max in the sweep; the stream-launched time of the same K steps is
+               reported beside it as us_per_step_stream)
   e2e          same through the C ABI (stream-launched steps) with every step's input
                copied from pinned host memory and its output copied back inside the
                timed region; the copies run on a copy stream over two alternating
@@ -23,8 +24,13 @@ Reported (one JSON line, rank 0):
                unique bytes the step must read, incl. the actual distinct experts U)
   roofline     dominant kernel of the --batch step: algorithmic bytes / its
                event-timed duration, against the measured HBM copy bandwidth
-  cpu_baseline the fp64 oracle on the host cores, on one token of the step
-               (single_core: the same with one BLAS/OpenMP thread, in a child process)
+  workloads    the workload's other configurations, each alone through its entry point
+               (--configs): the 4096x4096 projection at one token, the input projection at
+               M = 1..64, the out-projection with its residual at M = 1, 4, 16, 64, and the MoE
+               layer (moe_layer) at M = 1, 8, 64; µs per call, GB/s and the fraction of the
+               measured copy peak, with every kernel's event-timed GB/s beside it
+  cpu_baseline the fp64 oracle on the host cores, on one token of the step, median of three
+               runs (single_core: the same with one BLAS/OpenMP thread, in a child process)
 With --impl reference the fp64 oracle is the timed arm.
 
 Multi-GPU (torchrun, --gpus N): the decode layer does not shard across GPUs
@@ -242,7 +248,11 @@ def layer_copies() -> int:
     return max(2, -(-4 * 129_000_000 // step_m1))
 
 
-def build_weights(dev: str, copies: int = 2):
+def build_weights(dev: str, copies: int = 2, distinct: bool = False):
+    """`copies` layers' weights. distinct: every layer has its own seeded
+    values (tensor id + 100 l for layer l: its own projections, router and
+    expert banks, about 34.5 GB each at full shapes); otherwise the copies hold
+    the same values and only make every step stream its weights from HBM."""
     import torch
     import moe_layers_gb300 as ML
     import synth
@@ -252,67 +262,98 @@ def build_weights(dev: str, copies: int = 2):
         synth.fill_bf16_dev(t.data_ptr(), t.numel(), 0, tid, 0, sigma)
         return t
 
-    def moe_weights():
-        Wg = fill_bf16((E, I, H), synth.W_G, 0.02)
-        Wu = fill_bf16((E, I, H), synth.W_U, 0.02)
-        Wd = fill_bf16((E, H, I), synth.W_D, 0.02)
-        Ws = (fill_bf16((I, H), synth.W_G_S, 0.02), fill_bf16((I, H), synth.W_U_S, 0.02),
-              fill_bf16((H, I), synth.W_D_S, 0.02))
+    def moe_weights(l):
+        Wg = fill_bf16((E, I, H), synth.W_G + 100 * l, 0.02)
+        Wu = fill_bf16((E, I, H), synth.W_U + 100 * l, 0.02)
+        Wd = fill_bf16((E, H, I), synth.W_D + 100 * l, 0.02)
+        Ws = (fill_bf16((I, H), synth.W_G_S + 100 * l, 0.02), fill_bf16((I, H), synth.W_U_S + 100 * l, 0.02),
+              fill_bf16((H, I), synth.W_D_S + 100 * l, 0.02))
         Wr = torch.empty((E, H), dtype=torch.float32, device=dev)
-        synth.fill_f32_dev(Wr.data_ptr(), Wr.numel(), 0, synth.W_R, 0, 0.01)
+        synth.fill_f32_dev(Wr.data_ptr(), Wr.numel(), 0, synth.W_R + 100 * l, 0, 0.01)
         return Wg, Wu, Wd, Ws, Wr
 
     ones = torch.ones(H, dtype=torch.bfloat16, device=dev)
     layers = []
-    moe = moe_weights()
+    moe = moe_weights(0)
     for c in range(copies):
-        if c > 0 and SHARD > 1:
-            moe = moe_weights()  # sharded steps are small: nothing may stay in L2 from step to step
+        l = c if distinct else 0
+        if c > 0 and (SHARD > 1 or distinct):
+            # sharded steps are small: nothing may stay in L2 from step to step; distinct layers: their own values
+            moe = moe_weights(l)
         Wg, Wu, Wd, Ws, Wr = moe
-        W_in = fill_bf16((N_IN, H), synth.W_IN, 0.02)
-        W_o = fill_bf16((H, K_OUT), synth.W_O, 0.02)
+        W_in = fill_bf16((N_IN, H), synth.W_IN + 100 * l, 0.02)
+        W_o = fill_bf16((H, K_OUT), synth.W_O + 100 * l, 0.02)
         layers.append(ML.LayerWeights(gamma1=ones, W_in=W_in, W_o=W_o, gamma2=ones, W_r=Wr, Wg=Wg, Wu=Wu, Wd=Wd,
                                       Wg_s=Ws[0], Wu_s=Ws[1], Wd_s=Ws[2], k=TOPK, k_out=K_OUT))
     torch.cuda.synchronize()
     return layers
 
 
-def run_ours(args, rank, local, world):
+def _graph_replays(step_fn, K: int, reps: int, dev, reset=None):
+    """Capture step_fn(i, stream) for i < K once as a CUDA graph on a side
+    stream and replay it `reps` times, each bracketed by CUDA events on the
+    launching stream (reset() runs before every replay, untimed). Returns the
+    microseconds per step of each replay."""
+    import torch
+    stream = torch.cuda.current_stream()
+    gs = torch.cuda.Stream(device=dev)
+    gs.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        for i in range(K):
+            step_fn(i, gs)
+    if reset:
+        reset()
+    graph.replay()  # (untimed: first replay)
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
+        if reset:
+            reset()
+        torch.cuda.synchronize()
+        barrier(dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dev)
+        out.append(g0.elapsed_time(g1) * 1000.0 / K)
+    del graph
+    return out
+
+
+def _spread(vals):
+    return {"median": round(statistics.median(vals), 2), "min": round(min(vals), 2), "max": round(max(vals), 2),
+            "n": len(vals)}
+
+
+def _kernel_table(prof: dict, K: int, bytes_of, peak: float) -> dict:
+    """Per-kernel event-timed averages of a profiled pass: launches per step,
+    µs per launch, algorithmic GB/s and fraction of the measured copy peak."""
+    kern = {}
+    for tag, (n, ms) in prof.items():
+        avg_us = ms * 1000.0 / max(n, 1)
+        kb = bytes_of(tag)
+        gbs = kb / (avg_us * 1e3) if kb and avg_us > 0 else None
+        kern[tag] = {"launches_per_step": n / K, "avg_us": round(avg_us, 2),
+                     "bytes": int(kb) if kb else None,
+                     "GBps": round(gbs, 1) if gbs else None, "frac": round(gbs / peak, 4) if gbs else None}
+    return kern
+
+
+def run_layer_sweep(args, h, layers, cws, dev, peaks):
+    """The decode layer (the headline workload) at every batch of the sweep."""
     import numpy as np
     import torch
     import moe_layers_gb300 as ML
     import synth
 
-    dev = f"cuda:{local}"
-    torch.cuda.set_device(local)
-    ML.build()
-    h = ML.Handle(local)
-    h.set_shared_sms(args.shared_sms)
-    h.set_prefetch_shared(args.prefetch_shared)
-    if args.l2_ahead is not None:
-        h.set_l2_ahead(args.l2_ahead)
-    h.set_one_token_shared(args.shared_in_routing)
-    h.set_force_variant({"auto": ML.VARIANT_AUTO, "small_m": ML.VARIANT_SMALL_M,
-                         "split_k": ML.VARIANT_SPLIT_K}[args.family])
-    layers = build_weights(dev, layer_copies())
-    if args.prefetch_next:
-        # Cross-layer prefetch: while layer l routes, the next layer's input
-        # projection is pulled into L2 (up to the given bytes).
-        for li, L in enumerate(layers):
-            nxt = layers[(li + 1) % len(layers)].W_in
-            L.prefetch_next = nxt
-            L.prefetch_bytes = min(int(args.prefetch_next), nxt.numel() * 2) // 16 * 16
-    cws = [L.c_struct() for L in layers]
     stream = torch.cuda.current_stream()
-    peaks = measured_peaks()
     sweep = sorted(set([int(m) for m in args.sweep.split(",") if m] + [args.batch]))
     results = {}
-    clocks = ClockSampler(local)
-    clock_started = False
-
     for M in sweep:
-        ws = h.workspace(("bench", M), ML.decode_layer_workspace_size(h, layers[0], M),
-                         ("layer", M))
+        ws = h.workspace(("bench", M), ML.decode_layer_workspace_size(h, layers[0], M), ("layer", M))
         if args.verify > 1:
             # speculative-verify batch: groups of `verify` related rows (one request's drafts)
             x0 = synth.correlated_rows(synth.X_BASE + 100, range(M), args.verify, H, 0, args.verify_noise)
@@ -324,21 +365,18 @@ def run_ours(args, rank, local, world):
         K = args.steps
         idx_all = torch.empty((K, M, TOPK), dtype=torch.int32, device=dev)
 
-        def step(i, trace=None):
-            ML.decode_layer(h, layers[i % len(layers)], hidden, trace=trace, ws=ws, _cw=cws[i % len(layers)])
+        def step(i, trace=None, stream=None):
+            ML.decode_layer(h, layers[i % len(layers)], hidden, trace=trace, ws=ws, _cw=cws[i % len(layers)],
+                            stream=stream)
 
         for i in range(args.warmup):
             step(i)
         torch.cuda.synchronize()
-        # Every timed pass (eager, graph, profiled) starts from the same input
-        # rows, so all of them route the same K steps (the routing, hence the
-        # distinct experts U and the bytes, drift as the hidden state evolves).
+        # Every timed pass (eager, graph, profiled, e2e) starts from the same
+        # input rows, so all of them route the same K steps (the routing, hence
+        # the distinct experts U and the bytes, drift as the hidden state evolves).
         hidden.copy_(host_in)
-        # ---- timed: inputs resident, K steps
-        if not clock_started:
-            clocks.start()
-            clock_started = True
-            time.sleep(0.3)
+        # ---- timed: inputs resident, K steps launched from the host
         barrier(dev)
         torch.cuda.synchronize()
         launches0 = h.launch_count
@@ -351,37 +389,15 @@ def run_ours(args, rank, local, world):
         barrier(dev)
         us_eager = ev0.elapsed_time(ev1) * 1000.0 / K
         launches = h.launch_count - launches0
+        reps = [us_eager]
+        if args.graph:
+            # The same K steps captured once as a CUDA graph (no host work per
+            # step) and replayed `repeats` times: the GPU-bound time.
+            reps = _graph_replays(lambda i, s: step(i, trace={"idx": idx_all[i]}, stream=s), K, args.repeats, dev,
+                                  reset=lambda: hidden.copy_(host_in))
         idx_host = idx_all.cpu().numpy()
         U = float(np.mean([len(np.unique(idx_host[i])) for i in range(K)]))
-        us = us_eager
-        if args.graph:
-            # The same K steps captured once as a CUDA graph (one launch per step
-            # sequence, no host work per step) and replayed: the GPU-bound time.
-            gs = torch.cuda.Stream(device=dev)
-            gs.wait_stream(stream)
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=gs):
-                for i in range(K):
-                    ML.decode_layer(h, layers[i % len(layers)], hidden, trace={"idx": idx_all[i]}, ws=ws,
-                                    _cw=cws[i % len(layers)],
-                                    stream=gs)
-            hidden.copy_(host_in)
-            graph.replay()
-            torch.cuda.synchronize()
-            hidden.copy_(host_in)
-            torch.cuda.synchronize()
-            barrier(dev)
-            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            g0.record(stream)
-            graph.replay()
-            g1.record(stream)
-            torch.cuda.synchronize()
-            barrier(dev)
-            us = g0.elapsed_time(g1) * 1000.0 / K
-            idx_host = idx_all.cpu().numpy()
-            U = float(np.mean([len(np.unique(idx_host[i])) for i in range(K)]))
-            del graph
-        us_max = reduce_max(us, dev)
+        us_max = reduce_max(statistics.median(reps), dev)
         us_eager = reduce_max(us_eager, dev)
         # ---- profiled pass: per-kernel event times (separate; events break PDL overlap)
         hidden.copy_(host_in)
@@ -397,10 +413,9 @@ def run_ours(args, rank, local, world):
         # device buffers alternate and the copies run on a copy stream, so step
         # i+1's upload and step i's download overlap the neighbouring steps'
         # layers (as a serving loop would run them); the timed region covers
-        # every copy.
-        # The inputs of the K steps (the evolving hidden state the device-timed
-        # passes saw, recorded by an untimed pass), so that e2e routes the
-        # same steps as value does.
+        # every copy. The inputs of the K steps are the evolving hidden state
+        # the device-timed passes saw (recorded by an untimed pass), so that
+        # e2e routes the same steps as value does.
         inputs_dev = torch.empty((K, M, H), dtype=torch.bfloat16, device=dev)
         hidden.copy_(host_in)
         for i in range(K):
@@ -437,20 +452,175 @@ def run_ours(args, rank, local, world):
         torch.cuda.synchronize()
         us_e2e = reduce_max(e0.elapsed_time(e1) * 1000.0 / K, dev)
         b = step_bytes(M, U)
-        kern = {}
         # batch 1: the shared expert runs inside the routing (or gate/up) and down launches
         shared_in = (None if "shared_gate_up" in prof else "front" if "moe_front" in prof else
                      "router" if args.shared_in_routing else "gate_up")
-        for tag, (n, ms) in prof.items():
-            avg_us = ms * 1000.0 / max(n, 1)
-            kb = kernel_bytes(tag, M, U_prof, shared_in)
-            kern[tag] = {"launches_per_step": n / K, "avg_us": round(avg_us, 2),
-                         "GBps": round(kb / (avg_us * 1e3), 1) if kb and avg_us > 0 else None}
-        results[M] = dict(M=M, us_per_step=round(us_max, 2), us_per_step_stream=round(us_eager, 2),
-                          e2e_us=round(us_e2e, 2), U=round(U, 2),
+        kern = _kernel_table(prof, K, lambda tag: kernel_bytes(tag, M, U_prof, shared_in), peaks["hbm_gbs"])
+        results[M] = dict(M=M, us_per_step=round(us_max, 2), us_per_step_replays=_spread(reps),
+                          us_per_step_stream=round(us_eager, 2), e2e_us=round(us_e2e, 2), U=round(U, 2),
                           step_bytes=int(b), weight_stream_GBps=round(b / (us_max * 1e3), 1),
                           hbm_frac=round(b / (us_max * 1e3) / peaks["hbm_gbs"], 4),
                           kernels_per_step=launches / K, gpu_launches=launches, kernels=kern)
+    return sweep, results
+
+
+def run_dense_config(args, h, dev, peaks, name, N, Kd, Ms, copies, residual, weights=None):
+    """One projection alone (dec_linear or, with residual, dec_linear_residual),
+    the workload's shape and N(0, 0.02) weights, at every batch in Ms. The
+    weights rotate over `copies` tensors so that every call streams its matrix
+    from HBM (copies x bytes >= 4 x L2). µs per call from CUDA-graph replays of
+    K calls; per-kernel event times from a profiled pass."""
+    import torch
+    import moe_layers_gb300 as ML
+    import synth
+    Ws = list(weights or [])
+    tid0 = synth.W_LINEAR + (40 if residual else 0)
+    while len(Ws) < copies:
+        t = torch.empty((N, Kd), dtype=torch.bfloat16, device=dev)
+        synth.fill_bf16_dev(t.data_ptr(), t.numel(), 0, tid0 + len(Ws), 0, 0.02)
+        Ws.append(t)
+    K = args.steps
+    out = {}
+    for M in Ms:
+        x = torch.empty((M, Kd), dtype=torch.bfloat16, device=dev)
+        synth.fill_bf16_dev(x.data_ptr(), x.numel(), 0, synth.X_BASE + 300, 0, 1.0)
+        r = None
+        if residual:
+            r = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            synth.fill_bf16_dev(r.data_ptr(), r.numel(), 0, synth.R_BASE + 300, 0, 1.0)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        nb = ML._load()
+        import ctypes
+        sz = ctypes.c_size_t()
+        ML._check(nb.dec_linear_workspace_size(h.ptr, M, N, Kd, ctypes.byref(sz)), "dec_linear_workspace_size")
+        ws = h.workspace(("bench_dense", name, M), sz.value, ("linear", name, M))
+
+        def call(i, s=None):
+            W = Ws[i % len(Ws)]
+            if residual:
+                ML.dec_linear_residual(h, x, W, r, out=y, stream=s, ws=ws)
+            else:
+                ML.dec_linear(h, x, W, y, stream=s, ws=ws)
+
+        for i in range(args.warmup):
+            call(i)
+        torch.cuda.synchronize()
+        l0 = h.launch_count
+        reps = _graph_replays(call, K, args.repeats, dev)
+        launches = (h.launch_count - l0) / K
+        h.set_profiling(True)
+        for i in range(K):
+            call(i)
+        prof = h.profile_read()
+        h.set_profiling(False)
+        variant = {ML.VARIANT_SMALL_M: "small_m", ML.VARIANT_SPLIT_K: "split_k"}.get(h.last_variant)
+        nbytes = N * Kd * 2 + M * Kd * 2 + M * N * 2 + (M * N * 2 if residual else 0)
+        us = statistics.median(reps)
+        gbs = nbytes / (us * 1e3)
+        out[M] = {"M": M, "us_per_call": _spread(reps), "bytes": nbytes, "GBps": round(gbs, 1),
+                  "frac": round(gbs / peaks["hbm_gbs"], 4), "family": variant, "launches_per_call": launches,
+                  "kernels": _kernel_table(prof, K, lambda tag: nbytes, peaks["hbm_gbs"])}
+    return {"shape": {"N": N, "K": Kd}, "weight_copies": len(Ws), "batches": out}
+
+
+def run_moe_config(args, h, dev, peaks, layer, Ms):
+    """The MoE layer alone (moe_layer: router, top-8, 384 routed + 1 shared
+    experts, combine; no RMSNorm, no residual) on fresh N(0, 1) rows every
+    step, so the routing and the experts read change from step to step."""
+    import numpy as np
+    import torch
+    import moe_layers_gb300 as ML
+    import synth
+    wts = ML.MoeWeights(W_r=layer.W_r, Wg=layer.Wg, Wu=layer.Wu, Wd=layer.Wd, Wg_s=layer.Wg_s, Wu_s=layer.Wu_s,
+                        Wd_s=layer.Wd_s, k=TOPK)
+    cw = wts.c_struct()
+    K = args.steps
+    res = {}
+    for M in Ms:
+        xs = torch.empty((K + args.warmup, M, H), dtype=torch.bfloat16, device=dev)
+        synth.fill_bf16_dev(xs.data_ptr(), xs.numel(), 0, synth.X_BASE + 400 + M, 0, 1.0)
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        idx_all = torch.empty((K, M, TOPK), dtype=torch.int32, device=dev)
+        ws = h.workspace(("bench_moe", M), ML.moe_layer_workspace_size(h, wts, M), ("moe_layer", M))
+
+        def call(i, s=None, warm=False):
+            x = xs[K + i] if warm else xs[i]
+            ML.moe_layer(h, wts, x, out=out, trace=None if warm else {"idx": idx_all[i]}, stream=s, ws=ws, _cw=cw)
+
+        for i in range(args.warmup):
+            call(i, warm=True)
+        torch.cuda.synchronize()
+        l0 = h.launch_count
+        reps = _graph_replays(call, K, args.repeats, dev)
+        launches = (h.launch_count - l0) / K
+        idx_host = idx_all.cpu().numpy()
+        U = float(np.mean([len(np.unique(idx_host[i])) for i in range(K)]))
+        h.set_profiling(True)
+        for i in range(K):
+            call(i)
+        prof = h.profile_read()
+        h.set_profiling(False)
+        nbytes = E * H * 4 + (U + 1) * EXPERT_BYTES + 2 * M * H * 2
+        us = statistics.median(reps)
+        gbs = nbytes / (us * 1e3)
+        shared_in = None if "shared_gate_up" in prof else "front" if "moe_front" in prof else "gate_up"
+        res[M] = {"M": M, "us_per_call": _spread(reps), "U": round(U, 2), "bytes": int(nbytes), "GBps": round(gbs, 1),
+                  "frac": round(gbs / peaks["hbm_gbs"], 4), "launches_per_call": launches,
+                  "kernels": _kernel_table(prof, K, lambda tag: kernel_bytes(tag, M, U, shared_in),
+                                           peaks["hbm_gbs"])}
+    return {"batches": res}
+
+
+def run_ours(args, rank, local, world):
+    import torch
+    import moe_layers_gb300 as ML
+
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    ML.build()
+    h = ML.Handle(local)
+    h.set_shared_sms(args.shared_sms)
+    h.set_prefetch_shared(args.prefetch_shared)
+    if args.l2_ahead is not None:
+        h.set_l2_ahead(args.l2_ahead)
+    h.set_one_token_shared(args.shared_in_routing)
+    h.set_force_variant({"auto": ML.VARIANT_AUTO, "small_m": ML.VARIANT_SMALL_M,
+                         "split_k": ML.VARIANT_SPLIT_K}[args.family])
+    layers = build_weights(dev, args.layers if args.layers > 0 else layer_copies(), distinct=args.layers > 0)
+    if args.prefetch_next:
+        # Cross-layer prefetch: while layer l routes, the next layer's input
+        # projection is pulled into L2 (up to the given bytes).
+        for li, L in enumerate(layers):
+            nxt = layers[(li + 1) % len(layers)].W_in
+            L.prefetch_next = nxt
+            L.prefetch_bytes = min(int(args.prefetch_next), nxt.numel() * 2) // 16 * 16
+    cws = [L.c_struct() for L in layers]
+    peaks = measured_peaks()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    sweep, results = run_layer_sweep(args, h, layers, cws, dev, peaks)
+    # The workload's other configurations, each alone through its entry point.
+    workloads = {}
+    cfgs = [c for c in args.configs.split(",") if c] if SHARD == 1 and E == 384 else []
+    for c in cfgs:
+        if c == "proj4096":
+            workloads[c] = run_dense_config(args, h, dev, peaks, c, 4096, 4096, [1], 16, False)
+            workloads[c]["workload"] = "single decode projection: x[1,4096] W[4096,4096] bf16, y = x W^T"
+        elif c == "in_proj":
+            workloads[c] = run_dense_config(args, h, dev, peaks, c, N_IN, H, [1, 2, 4, 8, 16, 32, 64], 3, False,
+                                            weights=[L.W_in for L in layers])
+            workloads[c]["workload"] = "batch-swept input projection: K=7168, N=12288 bf16"
+        elif c == "out_proj":
+            workloads[c] = run_dense_config(args, h, dev, peaks, c, H, K_OUT, [1, 4, 16, 64], 4, True,
+                                            weights=[L.W_o for L in layers])
+            workloads[c]["workload"] = "out-projection fused with residual: K=8192, N=7168 bf16, out = r + x W^T"
+        elif c == "moe":
+            workloads[c] = run_moe_config(args, h, dev, peaks, layers[0], [1, 8, 64])
+            workloads[c]["workload"] = ("MoE layer: router W_r[384,7168] fp32 sigmoid top-8 renormalised; 384 "
+                                        "routed + 1 shared SwiGLU experts 7168->2048->7168 bf16")
+        else:
+            raise SystemExit(f"unknown config {c}")
     clk = clocks.stop()
     if h.check_device_error() != ML.DEC_OK:
         raise RuntimeError("device error word set during the benchmark")
@@ -463,29 +633,35 @@ def run_ours(args, rank, local, world):
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
                 "traffic": captured_traffic(dom, args.batch),
-                "peak_source": peaks["source"], "avg_us": dk["avg_us"]}
+                "peak_source": peaks["source"], "avg_us": dk["avg_us"], "bytes_per_launch": dk["bytes"]}
     out = {"metric": METRIC, "value": hl["us_per_step"], "unit": "us/step", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(hl["us_per_step"] / 1000.0, 5), "higher_is_better": False,
            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
            "data": "synthetic: seeded random-init weights of the workload's shapes, seeded N(0,1) activations",
            "config": {"workload": WORKLOAD if E == 384 else WORKLOAD + f" (profiling variant: {E} routed experts)",
                       "weight_copies": len(layers),
+                      "layers": (f"{len(layers)} distinct layers applied in sequence, each step one layer"
+                                 if args.layers > 0 else "one layer's weights in rotating copies"),
+                      "prefetch_next_bytes": int(args.prefetch_next),
                       "token_rows": ("independent" if args.verify <= 1 else
                                      f"speculative verify: groups of {args.verify} related rows, noise {args.verify_noise}"),
                       "batch": args.batch, "parallelism": "replicas" if world > 1 else "1 GPU",
+                      "timing": f"CUDA-graph replays of the K steps, median of {args.repeats} (spread in the sweep)",
                       "l2": "inputs larger than L2: each step reads >= 1.1 GB (L2 129 MB); dense weights alternate "
                             "between 2 copies; routing changes every step",
                       "weight_stream_GBps": hl["weight_stream_GBps"], "hbm_frac": hl["hbm_frac"],
                       "distinct_experts_U": hl["U"], "shared_expert_sms": {0: "auto", -1: "overlap"}.get(args.shared_sms, args.shared_sms),
-                      "sweep": [{k: v for k, v in results[m].items() if k != "kernels"} for m in sweep],
+                      "sweep": [results[m] for m in sweep],
                       "kernels_at_batch": hl["kernels"]},
            "weight_stream_GBps": hl["weight_stream_GBps"], "hbm_frac": hl["hbm_frac"],
            "roofline": roofline,
            "e2e": {"value": hl["e2e_us"], "unit": "us/step", "h2d_bytes_per_step": args.batch * H * 2,
                    "d2h_bytes_per_step": args.batch * H * 2},
            "gpu_launches": hl["gpu_launches"], "clocks": clk}
+    if workloads:
+        out["workloads"] = workloads
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.batch, steps=1)
+        out["cpu_baseline"] = cpu_baseline(args.batch, steps=3)
     if rank == 0:
         print(json.dumps(out), flush=True)
     h.close()
@@ -612,6 +788,11 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=1, help="headline batch M (1..64)")
     ap.add_argument("--sweep", default="1,2,4,8,16,32,64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--repeats", type=int, default=3, help="CUDA-graph replays per timed point (median reported)")
+    ap.add_argument("--configs", default="proj4096,in_proj,out_proj,moe",
+                    help="the workload's other configurations, each timed alone (comma list; empty for none): "
+                         "proj4096 (4096x4096 projection, M=1), in_proj (7168->12288, M=1..64), out_proj "
+                         "(8192->7168 + residual, M=1,4,16,64), moe (the MoE layer, M=1,8,64)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time the K steps as stream launches only (default: also capture them in a CUDA graph "
                          "and report the replay time as the value)")
@@ -628,6 +809,9 @@ def main(argv=None):
                     help="at batch 1, pull the shared expert into L2 during the router phase (off: measured slower)")
     ap.add_argument("--prefetch-next", type=int, default=0,
                     help="bytes of the next layer's input projection to pull into L2 during the routing (0: none)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="L distinct layers (their own seeded weights, routers and expert banks, ~34.5 GB each) "
+                         "applied in sequence, one per step (0: one layer's weights in rotating copies)")
     ap.add_argument("--verify", type=int, default=1,
                     help="speculative-verify batch: groups of this many related token rows (1: independent rows)")
     ap.add_argument("--verify-noise", type=float, default=0.5,
@@ -643,6 +827,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.steps < 2:
         ap.error("--steps must be at least 2")
+    if not 0 <= args.layers <= 6:
+        ap.error("--layers must be 0..6 (each full-size layer holds about 34.5 GB)")
     rank, local, world = dist_env()
     if args.impl == "reference":
         if world > 1 and args.steps > 3:

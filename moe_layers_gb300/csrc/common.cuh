@@ -156,11 +156,13 @@ __device__ __forceinline__ uint4 norm8(const uint4& a, const uint4& g, float r) 
 
 // This thread's partial sum of squares over the vectors it holds of a row:
 // v[i] is vector t + T i (those below H8), taken in ascending i.
+// (tid: the thread's index among the T threads that hold the row.)
 template <int NV, int T>
-__device__ __forceinline__ float thread_sumsq(const uint4 (&v)[NV], int H8, float ss = 0.f) {
+__device__ __forceinline__ float thread_sumsq(const uint4 (&v)[NV], int H8, float ss = 0.f,
+                                              int tid = (int)threadIdx.x) {
 #pragma unroll
   for (int i = 0; i < NV; ++i)
-    if ((int)threadIdx.x + T * i < H8) ss = sumsq8(v[i], ss);
+    if (tid + T * i < H8) ss = sumsq8(v[i], ss);
   return ss;
 }
 
@@ -170,13 +172,19 @@ __device__ __forceinline__ float thread_sumsq(const uint4 (&v)[NV], int H8, floa
 // NW warps' sums in warp order. A row normalised by any of them therefore has
 // the same bits. red: NW floats of shared memory that no other thread is
 // still reading; one barrier.
+// bar: 0 for the whole block (__syncthreads), else the named barrier of the
+// NW warps that hold the row; warp: the calling warp's index among them.
 template <int NW>
-__device__ __forceinline__ float block_rms_scale(float ss, int H, float eps, float* red) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __forceinline__ float block_rms_scale(float ss, int H, float eps, float* red, int bar = 0,
+                                                 int warp = (int)(threadIdx.x >> 5)) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (lane == 0) red[warp] = ss;
-  __syncthreads();
+  if (bar == 0)
+    __syncthreads();
+  else
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(NW * 32) : "memory");
   float tot = 0.f;
 #pragma unroll
   for (int q = 0; q < NW; ++q) tot += red[q];
@@ -273,6 +281,19 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, co
   }
 }
 
+// Bounded wait that ignores the abort flag (used when draining in-flight work).
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err, uint64_t limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) == 0 && globaltimer() - t0 > limit) {
+      atomicOr(err, DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tmap_prefetch(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -287,6 +308,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(pol)
+      : "memory");
+}
+
+// 1-D bulk copy of `bytes` (a multiple of 16) from global `src` to shared
+// `dst` (both 16-byte aligned), completing on `bar` (complete_tx), with an L2
+// cache policy.
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                             uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 

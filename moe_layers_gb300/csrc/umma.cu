@@ -110,19 +110,6 @@ __device__ __forceinline__ long long total_kblocks(const EngineParams& P) {
   return nprob * P.tiles * P.KB;
 }
 
-// Bounded wait that ignores the abort flag (used when draining in-flight work).
-static __device__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err, uint64_t limit) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 15u) == 0 && globaltimer() - t0 > limit) {
-      atomicOr(err, DEV_ERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
 template <int EPI, int BROWS>
 __global__ void __launch_bounds__(kEngineThreads, 1)
     engine_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,

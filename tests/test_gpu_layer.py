@@ -432,3 +432,90 @@ def test_layer_tp_shapes(h, tp_layer, M):
     s_all = L.scores(hbits)
     i_all, _ = oracle.topk(s_all, L.k)
     assert np.array_equal(tr["idx"].cpu().numpy(), i_all)
+
+
+# ---------------------------------------------------------------------------- several distinct layers in sequence
+def _chain_gap_rows(layers, M, H, k, base, gap=1e-3, max_attempts=200):
+    """Token rows whose routing has the 1e-3 top-(k+1) score gap in every
+    layer of the chain, as the oracle computes it (layer l's input is layer
+    l-1's output stored as bf16)."""
+    from _util import gap_ok
+    bits = np.empty((M, H), dtype=np.uint16)
+    for r in range(M):
+        for attempt in range(max_attempts + 1):
+            row = synth.bf16_rows(base, [r], H, SEED, 1.0, [attempt])
+            x, ok = row, True
+            for L, ex, sh in layers:
+                s = L.scores(x)
+                if not gap_ok(s[0], L.k, gap):
+                    ok = False
+                    break
+                o = L.oracle(x, ex, sh)
+                x = _bits(oracle.round_bf16(o["out"]))
+            if ok:
+                bits[r] = row[0]
+                break
+        else:
+            raise RuntimeError("gap rule: too many redraws")
+    return bits
+
+
+@pytest.mark.parametrize("M", [1, 2, 8])
+def test_layers_in_sequence_with_cross_layer_prefetch(h, M):
+    """Three distinct layers (their own seeded weights, routers and expert
+    banks) applied in sequence, layer l's output (bf16) being layer l+1's
+    input, each layer's prefetch_next region set to the next layer's input
+    projection (the last to the first) and, in a second run, to nothing:
+    - the outputs of the two runs are bit-identical (the prefetch moves data
+      into L2 only);
+    - every layer's top-k indices are bit-exact against the oracle's chain;
+    - every layer's output passes the layer rule against the oracle applied
+      to that layer's GPU input;
+    - the chain's final output is within 3 x 1e-2 rms of the oracle's chain
+      (each of the three layers may contribute up to the one-layer budget)."""
+    import torch
+    import moe_layers_gb300 as ML
+    H, N_in, K_out, E, I, k = 1152, 1040, 1024, 40, 256, 8
+    layers = []
+    for l in range(3):
+        L = Layer(H, N_in, K_out, E, I, k, base=9200 + 20 * l)
+        n = E * I * H
+        g = synth.bf16(n, SEED, 9210 + 20 * l, 0, 0.05).reshape(E, I, H)
+        u = synth.bf16(n, SEED, 9211 + 20 * l, 0, 0.05).reshape(E, I, H)
+        d = synth.bf16(n, SEED, 9212 + 20 * l, 0, 0.05).reshape(E, H, I)
+        sh = (synth.bf16(I * H, SEED, 9213 + 20 * l, 0, 0.05).reshape(I, H),
+              synth.bf16(I * H, SEED, 9214 + 20 * l, 0, 0.05).reshape(I, H),
+              synth.bf16(H * I, SEED, 9215 + 20 * l, 0, 0.05).reshape(H, I))
+        ex = (lambda g, u, d: (lambda e: (g[e], u[e], d[e])))(g, u, d)
+        dev_w = L.device(dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
+                         tuple(dev_bf16(a, a.shape) for a in sh))
+        layers.append((L, ex, sh, dev_w))
+    hbits = _chain_gap_rows([(L, ex, sh) for L, ex, sh, _ in layers], M, H, k, base=9300 + M)
+    outs = {}
+    for pf in (True, False):
+        for l, (_, _, _, dev_w) in enumerate(layers):
+            nxt = layers[(l + 1) % 3][3].W_in
+            dev_w.prefetch_next = nxt if pf else None
+            dev_w.prefetch_bytes = nxt.numel() * 2 if pf else 0
+        hid = dev_bf16(hbits, hbits.shape)
+        ins, trs = [], []
+        for l, (_, _, _, dev_w) in enumerate(layers):
+            ins.append(host_bits(hid))
+            trs.append(ML.decode_layer(h, dev_w, hid, trace=True))
+        torch.cuda.synchronize()
+        outs[pf] = (host_bits(hid), ins, [{k_: v.clone() for k_, v in t.items()} for t in trs])
+    assert h.check_device_error() == ML.DEC_OK
+    assert np.array_equal(outs[True][0], outs[False][0]), "cross-layer prefetch changed the result"
+    final, ins, trs = outs[True]
+    x, last = hbits, None
+    for l, (L, ex, sh, _) in enumerate(layers):
+        # this layer on the GPU's own input to it
+        ref = L.oracle(ins[l], ex, sh)
+        got = ins[l + 1] if l + 1 < 3 else final
+        hid_l = dev_bf16(got, got.shape)
+        _check_layer(trs[l], hid_l, ref, slice(None), f"chain M={M} layer {l}", L, ex, sh)
+        # the oracle's own chain
+        oc = L.oracle(x, ex, sh)
+        assert np.array_equal(trs[l]["idx"].cpu().numpy(), oc["idx"]), f"chain M={M} layer {l}: top-k"
+        x, last = _bits(oracle.round_bf16(oc["out"])), oc["out"]
+    assert_bf16_close(final, last, f"chain M={M}: final output against the oracle's chain", tol=3e-2)
