@@ -452,9 +452,8 @@ def run_layer_sweep(args, h, layers, cws, dev, peaks):
         torch.cuda.synchronize()
         us_e2e = reduce_max(e0.elapsed_time(e1) * 1000.0 / K, dev)
         b = step_bytes(M, U)
-        # batch 1: the shared expert runs inside the routing (or gate/up) and down launches
-        shared_in = (None if "shared_gate_up" in prof else "front" if "moe_front" in prof else
-                     "router" if args.shared_in_routing else "gate_up")
+        # one and two tokens: the shared expert runs inside the MoE front (or gate/up) and down launches
+        shared_in = None if "shared_gate_up" in prof else "front" if "moe_front" in prof else "gate_up"
         kern = _kernel_table(prof, K, lambda tag: kernel_bytes(tag, M, U_prof, shared_in), peaks["hbm_gbs"])
         results[M] = dict(M=M, us_per_step=round(us_max, 2), us_per_step_replays=_spread(reps),
                           us_per_step_stream=round(us_eager, 2), e2e_us=round(us_e2e, 2), U=round(U, 2),
@@ -580,10 +579,8 @@ def run_ours(args, rank, local, world):
     ML.build()
     h = ML.Handle(local)
     h.set_shared_sms(args.shared_sms)
-    h.set_prefetch_shared(args.prefetch_shared)
     if args.l2_ahead is not None:
         h.set_l2_ahead(args.l2_ahead)
-    h.set_one_token_shared(args.shared_in_routing)
     h.set_force_variant({"auto": ML.VARIANT_AUTO, "small_m": ML.VARIANT_SMALL_M,
                          "split_k": ML.VARIANT_SPLIT_K}[args.family])
     layers = build_weights(dev, args.layers if args.layers > 0 else layer_copies(), distinct=args.layers > 0)
@@ -800,13 +797,8 @@ def main(argv=None):
                     help="SMs for the shared expert: 0 automatic share (default), -1 every SM overlapped, n fixed")
     ap.add_argument("--family", choices=("auto", "small_m", "split_k"), default="auto",
                     help="kernel family (auto: by batch and size; small_m covers batch <= 4)")
-    ap.add_argument("--shared-in-routing", type=int, choices=(0, 1, 2), default=2,
-                    help="batch 1: one launch of the routing and both gate/ups (2, default), the shared "
-                         "expert's gate/up inside the routing launch (1) or the gate/up launch (0)")
     ap.add_argument("--l2-ahead", type=int, default=None,
                     help="bytes per CTA the small-matrix kernels keep requested into L2 ahead (default: library's)")
-    ap.add_argument("--prefetch-shared", action="store_true",
-                    help="at batch 1, pull the shared expert into L2 during the router phase (off: measured slower)")
     ap.add_argument("--prefetch-next", type=int, default=0,
                     help="bytes of the next layer's input projection to pull into L2 during the routing (0: none)")
     ap.add_argument("--layers", type=int, default=0,

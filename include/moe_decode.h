@@ -109,27 +109,6 @@ dec_status dec_set_pdl(dec_handle* h, int enable);
  *  n > 0: it keeps n SMs. */
 dec_status dec_set_shared_sms(dec_handle* h, int sms);
 
-/* At batch 1 decode_layer runs the shared expert inside the routed experts'
- * launches and, while the router / top-k phase leaves the memory idle, pulls
- * its weights into L2 on a side stream [K3 P1§4]. 1 enables that prefetch,
- * 0 (default) disables it: measured on GB300 it slows the step, because 88 MB
- * of evict-last lines crowd the weight stream out of the 129 MB L2. */
-dec_status dec_set_prefetch_shared(dec_handle* h, int enable);
-
-/* Where decode_layer runs the shared expert's gate/up at batch 1
- * [K3 P1§3, §4]: 1 inside the routing launch, whose CTAs stream it while the
- * router / top-k chain runs; 0 as problem 0 of the routed gate/up launch;
- * 2 (default) inside one MoE front launch that also streams the routed
- * experts' gate/up once its top-k CTA has published the routing (its CTAs wait
- * for that with the handle's wait limit, raising DEC_ERR_TIMEOUT in the device
- * error word past it), leaving four launches per layer. At two to four tokens
- * on the small-matrix family the routing launch always streams the shared
- * gate/up, and 2 also folds the entries' gate/up into it (at most 32 (token,
- * expert) entries). All compute the same layer (fp32 sums of the routed rows
- * may run in another order); the switch exists to measure and test the
- * schedules. in_routing in {0, 1, 2}, else DEC_ERR_INVALID_ARG. */
-dec_status dec_set_one_token_shared(dec_handle* h, int in_routing);
-
 /* The small-matrix kernels (batch 1) keep about `bytes` of each CTA's
  * upcoming weight rows requested into L2 (bulk L2 prefetches, issued from
  * before the dependency wait on), beyond the rows their registers hold, so
@@ -395,6 +374,16 @@ dec_status dec_test_wait_timeout(dec_handle* h, cudaStream_t stream);
  * `stream`. Used to test that the routing wait surfaces as DEC_ERR_TIMEOUT
  * with the context still usable. tokens outside {1, 2}: DEC_ERR_INVALID_ARG. */
 dec_status dec_test_routing_wait_timeout(dec_handle* h, int tokens, cudaStream_t stream);
+
+/* 1 (default): decode_layer and moe_layer use the MoE front launches at one
+ * and two tokens when there is a shared expert (routing, the shared expert's
+ * gate/up and the selected experts' gate/up in one launch). 0: they use the
+ * launches taken where a front does not apply (no shared expert, or shapes
+ * outside its limits): the routing launch, then the grouped gate/up with the
+ * shared expert as one more problem, then the down projection. Both compute
+ * the same layer; the hook lets tests run the second path with a shared
+ * expert. */
+dec_status dec_test_set_moe_front(dec_handle* h, int enable);
 
 /* Hold `ctas` SMs (1 <= ctas <= the device's SM count) for hold_ns
  * nanoseconds (at most 2 s) with a kernel on `stream`: one CTA per SM that

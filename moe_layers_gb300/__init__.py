@@ -73,9 +73,8 @@ def _load():
         "dec_set_pdl": [P, I],
         "dec_set_force_variant": [P, I],
         "dec_set_shared_sms": [P, I],
-        "dec_set_prefetch_shared": [P, I],
         "dec_set_l2_ahead": [P, I],
-        "dec_set_one_token_shared": [P, I],
+        "dec_test_set_moe_front": [P, I],
         "dec_check_device_error": [P],
         "dec_linear_workspace_size": [P, I, I, I, ctypes.POINTER(Z)],
         "dec_linear": [P, P, I, P, P, I, I, I, P, Z, P],
@@ -202,14 +201,9 @@ class Handle:
         """0: automatic SM share by expected bytes; -1: every SM, overlapped; n > 0: a fixed n-SM partition."""
         _check(_load().dec_set_shared_sms(self._h, int(n)), "dec_set_shared_sms")
 
-    def set_prefetch_shared(self, enable: bool) -> None:
-        _check(_load().dec_set_prefetch_shared(self._h, 1 if enable else 0), "dec_set_prefetch_shared")
-
-    def set_one_token_shared(self, in_routing) -> None:
-        """False / True: the shared gate/up in the routed launch / the routing
-        launch; 2: one MoE front launch (routing, shared and routed gate/up)."""
-        v = int(in_routing) if not isinstance(in_routing, bool) else (1 if in_routing else 0)
-        _check(_load().dec_set_one_token_shared(self._h, v), "dec_set_one_token_shared")
+    def test_set_moe_front(self, enable: bool) -> None:
+        """Test hook: False runs the path taken where an MoE front does not apply."""
+        _check(_load().dec_test_set_moe_front(self._h, 1 if enable else 0), "dec_test_set_moe_front")
 
     def set_l2_ahead(self, nbytes: int) -> None:
         _check(_load().dec_set_l2_ahead(self._h, int(nbytes)), "dec_set_l2_ahead")

@@ -272,12 +272,11 @@ dec_status moe_shared_fork(dec_handle* h, const uint16_t* x, int M, int k, int E
 // launch per matrix over every SM (the shared expert is problem 0), the down
 // projection fused with the combine and the residual where supported. The
 // routing table in ws.table is complete; slot j's activation row is at
-// x + j * ldx (ldx 0: one row for all slots). shared_gate_up_done: the
-// routing launch already wrote the shared expert's SwiGLU output to ws.hs.
+// x + j * ldx (ldx 0: one row for all slots).
 dec_status moe_small(dec_handle* h, const uint16_t* x, long long ldx, const float* w, int k, const uint16_t* Wg,
                      const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I, const uint16_t* Wg_s,
                      const uint16_t* Wu_s, const uint16_t* Wd_s, const uint16_t* residual, uint16_t* out,
-                     const MoeWs& ws, cudaStream_t s, bool shared_gate_up_done = false) {
+                     const MoeWs& ws, cudaStream_t s) {
   const bool has_shared = Wg_s != nullptr;
   h->last_expert_variant = DEC_VARIANT_SMALL_M;
   // the shared expert's activation: slot 0's row (every slot holds the token's row)
@@ -290,8 +289,7 @@ dec_status moe_small(dec_handle* h, const uint16_t* x, long long ldx, const floa
     // next routing launch from starting before this one's predecessor (the
     // routing launch, whose row queue it reuses) has completed.
     DEC_CUDA(launch_gemv_moe(h, true, Wg, Wu, I, I, H, x, ldx, ws.table, E, k, ws.hbuf, I, h->sms, s,
-                             (has_shared && !shared_gate_up_done) ? &sgu : nullptr, k,
-                             fused_down || shared_gate_up_done));
+                             has_shared ? &sgu : nullptr, k, fused_down));
   }
   if (fused_down) {
     // down projection + weighted combine + residual in one kernel; the routing
@@ -535,13 +533,11 @@ dec_status moe_layer_impl(dec_handle* h, const MoeLayerArgs& A, const MoeLayerWs
   // The MoE front launches (one token; two to four on the small-matrix
   // family) pull the next-operator region themselves, from the CTAs that wait
   // for the routing, so the side stream then carries only the shared expert.
-  const bool front1 = one_token && A.Wg_s != nullptr && h->fuse_shared_routing == 2 &&
-                      route_shared_supported(h, 1, H, A.E, A.k) && gemv_down_combine_supported(A.k, A.I);
-  const bool front_few = few_tokens && A.Wg_s != nullptr && h->fuse_shared_routing == 2 && M * A.k <= 32;
+  const bool front1 = one_token && A.Wg_s != nullptr && h->moe_front && route_shared_supported(h, 1, H, A.E, A.k) &&
+                      gemv_down_combine_supported(A.k, A.I);
+  const bool front_few = few_tokens && A.Wg_s != nullptr && h->moe_front && M * A.k <= 32;
   const bool next_in_front = (front1 || front_few) && A.pf != nullptr && A.pf_bytes > 0;
-  const bool pf_shared = A.Wg_s != nullptr && one_token && h->prefetch_shared;
-  const bool pf_next_side = A.pf != nullptr && A.pf_bytes > 0 && !next_in_front;
-  const bool pf = pf_next_side || pf_shared;
+  const bool pf = A.pf != nullptr && A.pf_bytes > 0 && !next_in_front;
   const void* pf_front = next_in_front ? A.pf : nullptr;
   const size_t pf_front_bytes = next_in_front ? A.pf_bytes : 0;
   if (pf) {
@@ -549,13 +545,7 @@ dec_status moe_layer_impl(dec_handle* h, const MoeLayerArgs& A, const MoeLayerWs
     DEC_CUDA(cudaStreamWaitEvent(h->pf, h->ev_pf_fork, 0));
     {
       LaunchScope scope(h, "prefetch", h->pf);
-      if (pf_shared) {
-        const size_t mat = (size_t)A.I * H * sizeof(uint16_t);
-        DEC_CUDA(launch_prefetch(h, A.Wg_s, mat, 16, h->pf));
-        DEC_CUDA(launch_prefetch(h, A.Wu_s, mat, 16, h->pf));
-        DEC_CUDA(launch_prefetch(h, A.Wd_s, mat, 16, h->pf));
-      }
-      if (pf_next_side) DEC_CUDA(launch_prefetch(h, A.pf, A.pf_bytes, 16, h->pf));
+      DEC_CUDA(launch_prefetch(h, A.pf, A.pf_bytes, 16, h->pf));
     }
     DEC_CUDA(cudaEventRecord(h->ev_pf_join, h->pf));
   }
@@ -563,8 +553,6 @@ dec_status moe_layer_impl(dec_handle* h, const MoeLayerArgs& A, const MoeLayerWs
   // The router / top-k phase is latency-bound; the shared expert and the
   // prefetch stream use the idle bandwidth meanwhile.
   if (one_token) {
-    // With a shared expert the routing launch also streams its gate/up.
-    const bool fuse_shared = A.Wg_s != nullptr && h->fuse_shared_routing && route_shared_supported(h, 1, H, A.E, A.k);
     if (front1) {
       // One MoE front launch (routing, shared gate/up, routed gate/up), then
       // the down projection with the combine and the residual.
@@ -583,17 +571,16 @@ dec_status moe_layer_impl(dec_handle* h, const MoeLayerArgs& A, const MoeLayerWs
       if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
       return DEC_OK;
     }
+    // Without the front (no shared expert, or shapes outside its limits): the
+    // routing launch, then the grouped kernels with the shared expert as
+    // problem 0 of the gate/up launch and one more matrix of the down launch.
     {
       LaunchScope scope(h, "router", s);
-      if (fuse_shared)
-        DEC_CUDA(launch_route_shared(h, 1, A.x, A.gamma, A.eps, A.Wr, H, A.E, A.k, w.b, w.parts, w.sel_counter, A.idx,
-                                     A.w, A.scores, w.moe.table, A.Wg_s, A.Wu_s, A.I, w.moe.hs, s));
-      else
-        DEC_CUDA(launch_router_select(h, A.x, A.gamma, A.eps, A.Wr, H, A.E, A.k, w.b, w.parts, w.sel_counter, A.idx,
-                                      A.w, A.scores, w.moe.table, s));
+      DEC_CUDA(launch_router_select(h, A.x, A.gamma, A.eps, A.Wr, H, A.E, A.k, w.b, w.parts, w.sel_counter, A.idx,
+                                    A.w, A.scores, w.moe.table, s));
     }
     st = moe_small(h, b, 0, A.w, A.k, A.Wg, A.Wu, A.Wd, A.E, H, A.I, A.Wg_s, A.Wu_s, A.Wd_s, A.residual, A.out, w.moe,
-                   s, fuse_shared);
+                   s);
     if (st != DEC_OK) return st;
     if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
     return DEC_OK;
@@ -729,15 +716,9 @@ dec_status dec_set_pdl(dec_handle* h, int enable) {
   return DEC_OK;
 }
 
-dec_status dec_set_prefetch_shared(dec_handle* h, int enable) {
+dec_status dec_test_set_moe_front(dec_handle* h, int enable) {
   if (h == nullptr) return DEC_ERR_INVALID_ARG;
-  h->prefetch_shared = enable ? 1 : 0;
-  return DEC_OK;
-}
-
-dec_status dec_set_one_token_shared(dec_handle* h, int in_routing) {
-  if (h == nullptr || in_routing < 0 || in_routing > 2) return DEC_ERR_INVALID_ARG;
-  h->fuse_shared_routing = in_routing;
+  h->moe_front = enable ? 1 : 0;
   return DEC_OK;
 }
 

@@ -24,9 +24,8 @@ struct dec_handle {
   int last_variant = 0;
   int last_expert_variant = 0;      // kernel family of the most recent expert launches
   int shared_ctas = 0;              // CTAs for the shared expert's kernels (0 = default)
-  int fuse_shared_routing = 2;      // batch 1: 1 the routing launch also streams the shared gate/up, 2 and the routed
+  int moe_front = 1;                // one to a few tokens: the MoE front launches (0: test hook, the fallback path)
   int l2_ahead = 49152;             // small-matrix kernels: weight bytes per CTA requested into L2 ahead
-  int prefetch_shared = 0;          // batch 1: pull the shared expert into L2 during the router phase
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   // measurement
   uint64_t launches = 0;

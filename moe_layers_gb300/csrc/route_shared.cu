@@ -1,41 +1,40 @@
-// One token: routing and the shared expert's gate/up in one launch.
+// The MoE fronts: routing and expert gate/up in one launch at one to a few
+// tokens, and the few-token routing launch.
 //
 // Kimi K3 article, Part 1 §3 "Mejorar la programación de MoE" (the shared
 // expert runs beside the routing, on its own stream) and §4 (while the
 // latency-bound router / top-k phase leaves the memory idle, weights that
 // come next are streamed). At one token the routing chain (RMSNorm, router
 // logits, hand-off, top-k, routing table) is a few microseconds of pure
-// latency; here the same CTAs stream the shared expert's 2 x I x H gate/up
-// weights meanwhile, so the memory stays busy and the routed gate/up launch
-// that follows streams only the selected experts.
+// latency; the same CTAs stream the shared expert's 2 x I x H gate/up
+// weights meanwhile, so the memory stays busy, and then the selected
+// experts' gate/up rows once the routing is published.
 //
-// Grid: two 256-thread CTAs per SM. Every CTA
-//  1. loads its router unit's fp32 W_r rows (a unit: 8 router rows x 1024
-//     columns, one row per warp; unit c, and unit c + G after the norm where
-//     it exists) and its RMSNorm gains before the dependency wait;
-//  2. normalises the token's row (the RMSNorm kernel's order, so the bits are
-//     the same) into registers and shared memory; CTA 0 also writes it out
-//     for the routed experts;
-//  3. stores its units' logit pieces and arrives on the hand-off counter
-//     (barrier, then thread 0's acq_rel add); the last CTA to arrive takes the
-//     top-k and writes idx, w, scores and the one-token routing table;
+// Grid: two 256-thread CTAs per SM. Every CTA of a front
+//  1. takes a router unit (8 router rows x 1024 columns of fp32 W_r, one row
+//     per warp) from a ticket counter and loads its rows, and its RMSNorm
+//     gains, before the dependency wait;
+//  2. normalises the token rows (the RMSNorm kernel's order, so the bits are
+//     the same) into shared memory;
+//  3. computes its units' logit pieces (taking further units while any
+//     remain) and arrives on the hand-off once per unit; the arrival that
+//     completes the last unit takes the top-k, writes idx, w, scores and the
+//     routing table, and publishes the routing with a release flag;
 //  4. streams shared-expert row pairs (row r of W_g and of W_u ->
 //     h_s[r] = bf16(silu(g) * u)) taken from a row queue (an atomic counter),
-//     so the CTA that ran the top-k simply takes fewer rows. The queue and a
-//     "done" counter are reset by the last CTA to finish.
-//
-// The MoE front kernel (the default at one token) goes on: once the top-k CTA
-// has published the routing (a release flag), every CTA streams the k routed
-// experts' gate/up rows as well, so the routing, the shared expert and the
-// routed experts take one launch and the down projection follows directly.
-// Because its CTAs wait for that flag, the front does not own router units by
-// block index as in step 1: a CTA takes units from a ticket counter
+//     so the CTA that ran the top-k simply takes fewer rows;
+//  5. waits for the routing flag (bounded), then streams its static share of
+//     the selected experts' gate/up rows and then rows from a tail queue.
+// The queues, the flag and a "done" counter are reset by the last CTA to
+// finish. Because the CTAs wait for a flag that one of them sets, the router
+// units are not owned by block index: a CTA takes them from a ticket counter
 // (take_unit) and the hand-off counts units, so the routing never waits for a
 // CTA that the SMs cannot hold yet.
-// Two to four tokens: route_shared_multi_kernel (the routing launch for M
-// rows; the last CTA scores every token and each warp selects one token's
-// experts) and moe_front_multi_kernel (that launch plus the (token, expert)
-// entries' gate/up, the default).
+//
+// Two to four tokens: moe_front_multi_kernel (the same for the (token,
+// expert) entries), and route_shared_multi_kernel (the routing launch alone,
+// with the shared expert's gate/up when there is one, for the shapes outside
+// the front's limits).
 #include <algorithm>
 
 #include "common.cuh"
@@ -146,177 +145,6 @@ __device__ __forceinline__ void norm_rows(const uint16_t* rows, int M, bool has_
         }
       }
     }
-  }
-}
-
-template <int J, int VPT>
-__global__ void __launch_bounds__(kThreads, 2) route_shared_kernel(const RouteSharedParams P) {
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int G = gridDim.x, c = blockIdx.x;
-  const int H = P.H, H8 = H >> 3;
-  const int ngrp = (P.E + 7) / 8;
-  extern __shared__ __align__(16) uint16_t sx[];  // the normalised row [H]
-  __shared__ float s_norm[kThreads / 32];
-  __shared__ float red[2][kThreads / 32][2];
-  __shared__ int s_row[2];
-  __shared__ int s_next[2];
-  __shared__ int s_last;
-  const uint64_t pol = policy_evict_first();
-  pdl_trigger();
-
-  // 1. static weights before the wait: router unit c, RMSNorm gains. (Unit
-  // c + G, which CTAs c < nunits - G also own, is loaded after the norm: held
-  // across it, its registers would spill.)
-  float4 wv[kUnitCols / 128];
-  auto load_unit = [&](int u) {
-    const int e = (u % ngrp) * 8 + warp, k0 = (u / ngrp) * kUnitCols;
-    const int kn = min(kUnitCols, H - k0);
-#pragma unroll
-    for (int i = 0; i < kUnitCols / 128; ++i) {
-      const int kk = 4 * (lane + 32 * i);
-      wv[i] = (u < P.nunits && e < P.E && kk < kn)
-                  ? __ldg(reinterpret_cast<const float4*>(P.Wr + (size_t)e * H + k0 + kk))
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  };
-  load_unit(c);
-  // The first three queue rows are taken now and requested into L2: the
-  // shared weights are static, so the memory streams them while the previous
-  // launch drains and the routing chain runs. (The queue was reset by the
-  // previous launch of this kernel, which completed before the launch before
-  // this one started.)
-  int base = 0;
-  if (t == 0) {
-    base = atomicAdd(&P.ctr[1], 3);
-    for (int q = 0; q < 3; ++q)
-      if (base + q < P.I) {
-        request_l2(P.Wg + (size_t)(base + q) * H, (size_t)H * 2);
-        request_l2(P.Wu + (size_t)(base + q) * H, (size_t)H * 2);
-      }
-  }
-  uint4 xr[VPT];
-#pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int v = t + kThreads * i;
-    xr[i] = (P.gamma != nullptr && v < H8) ? *reinterpret_cast<const uint4*>(P.gamma + (size_t)v * 8)
-                                           : make_uint4(0, 0, 0, 0);
-  }
-  pdl_wait();
-
-  // 2. RMSNorm of the row (xr holds the gains until normalised)
-  norm_row<VPT>(P.h1, P.gamma != nullptr, P.eps, H, xr, sx, s_norm, c == 0 ? P.xn : nullptr);
-  int pending = base + 2;  // (thread 0) the third row; the first two are published at the hand-off
-  __syncthreads();
-
-  // 3. router logit pieces of this CTA's units, then the hand-off
-#pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    const int u = c + m * G;
-    if (m == 1 && u < P.nunits) load_unit(u);
-    if (u < P.nunits) {
-      const int e = (u % ngrp) * 8 + warp, ks = u / ngrp, k0 = ks * kUnitCols;
-      const int kn = min(kUnitCols, H - k0);
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < kUnitCols / 128; ++i) {
-        const int kk = 4 * (lane + 32 * i);
-        if (kk < kn) {
-          const uint2 xv = *reinterpret_cast<const uint2*>(&sx[k0 + kk]);
-          acc = fmaf(wv[i].x, bf_lo(xv.x), acc);
-          acc = fmaf(wv[i].y, bf_hi(xv.x), acc);
-          acc = fmaf(wv[i].z, bf_lo(xv.y), acc);
-          acc = fmaf(wv[i].w, bf_hi(xv.y), acc);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0 && e < P.E) P.parts[(size_t)ks * P.E + e] = acc;
-    }
-  }
-  if (t == 0) {
-    s_row[0] = base;
-    s_row[1] = base + 1;
-  }
-  // The barrier orders this CTA's stores before thread 0's acquire-release
-  // add; in the last CTA the barrier after it orders every read after it.
-  __syncthreads();
-  if (t == 0) s_last = atom_add_acq_rel_gpu(&P.ctr[0], 1) == G - 1;
-  __syncthreads();
-  if (s_last) {
-    int se = 0;
-    float sw = 0.f;
-    block_topk<J, true>(P.parts, (H + kUnitCols - 1) / kUnitCols, 1, 0, P.E, P.k, P.idx, P.w, P.scores, &se, &sw);
-    if (warp == 0) write_one_token_table(P.table, P.E, P.k, se);
-    if (t == 0) P.ctr[0] = 0;  // leave the workspace reusable
-  }
-
-  // 4. shared-expert gate/up rows from the queue. At step i the registers
-  // hold row cur's weights, every thread knows the next row, and thread 0
-  // holds the queue's answer for the row after it (`pending`).
-  uint4 wa[2][VPT], wb[2][VPT];
-  auto load = [&](uint4(&wr)[2][VPT], int row) {
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int v = t + kThreads * i;
-        wr[a][i] = v < H8 ? ld_stream((a == 0 ? P.Wg : P.Wu) + (size_t)row * H + (size_t)v * 8, pol)
-                          : make_uint4(0, 0, 0, 0);
-      }
-  };
-  int cur = s_row[0], nxt = s_row[1];
-  if (cur < P.I) load(wa, cur);
-  int buf = 0;
-  while (cur < P.I) {
-    if (nxt < P.I) load(wb, nxt);
-    float g = 0.f, up = 0.f;
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      g = dot8(wa[0][i], xr[i], g);
-      up = dot8(wa[1][i], xr[i], up);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      g += __shfl_xor_sync(0xffffffffu, g, o);
-      up += __shfl_xor_sync(0xffffffffu, up, o);
-    }
-    if (lane == 0) {
-      red[buf][warp][0] = g;
-      red[buf][warp][1] = up;
-    }
-    if (t == 0) {
-      s_next[buf] = pending;
-      if (pending < P.I) {
-        // the row after next into L2 now, its register loads come a step later
-        request_l2(P.Wg + (size_t)pending * H, (size_t)H * 2);
-        request_l2(P.Wu + (size_t)pending * H, (size_t)H * 2);
-        pending = atomicAdd(&P.ctr[1], 1);
-      }
-    }
-    __syncthreads();
-    if (t == 0) {
-      float gs = 0.f, us = 0.f;
-#pragma unroll
-      for (int q = 0; q < kThreads / 32; ++q) {
-        gs += red[buf][q][0];
-        us += red[buf][q][1];
-      }
-      P.hs[cur] = swiglu_bf16(gs, us);
-    }
-    const int nn = s_next[buf];
-    cur = nxt;
-    nxt = nn;
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) wa[a][i] = wb[a][i];
-    buf ^= 1;
-  }
-  // Done with the queue (this CTA's last add on it precedes the release
-  // below); the last CTA to finish resets both counters for the next call.
-  if (t == 0 && atom_add_acq_rel_gpu(&P.ctr[2], 1) == G - 1) {
-    P.ctr[1] = 0;
-    P.ctr[2] = 0;
   }
 }
 
@@ -1227,15 +1055,6 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_multi_kernel(const Rout
 }
 
 template <int J>
-cudaError_t launch_j(dec_handle* h, const RouteSharedParams& P, int vpt, cudaStream_t s) {
-  const dim3 g(2 * h->sms), b(kThreads);
-  const size_t smem = (size_t)P.H * sizeof(uint16_t);
-  if (vpt == 1) return launch_k(h, route_shared_kernel<J, 1>, g, b, smem, s, P);
-  if (vpt == 2) return launch_k(h, route_shared_kernel<J, 2>, g, b, smem, s, P);
-  return launch_k(h, route_shared_kernel<J, 4>, g, b, smem, s, P);
-}
-
-template <int J>
 cudaError_t launch_front_j(dec_handle* h, const RouteSharedParams& P, int vpt, cudaStream_t s) {
   const dim3 g(2 * h->sms), b(kThreads);
   const size_t smem = (size_t)P.H * sizeof(uint16_t);
@@ -1291,8 +1110,7 @@ cudaError_t launch_route_shared(dec_handle* h, int M, const uint16_t* h1, const 
                                 const float* Wr, int H, int E, int k, uint16_t* xn, float* parts, int* ctr,
                                 int32_t* idx, float* w, float* scores, int* table, const uint16_t* Wg_s,
                                 const uint16_t* Wu_s, int I, uint16_t* hs, cudaStream_t s) {
-  if (!route_shared_supported(h, M, H, E, k)) return cudaErrorInvalidValue;
-  if (M == 1 && Wg_s == nullptr) return cudaErrorInvalidValue;  // (one token without a shared expert: router_select)
+  if (M < 2 || !route_shared_supported(h, M, H, E, k)) return cudaErrorInvalidValue;  // (one token: router_select)
   RouteSharedParams P;
   P.M = M;
   P.h1 = h1;
@@ -1316,11 +1134,6 @@ cudaError_t launch_route_shared(dec_handle* h, int M, const uint16_t* h1, const 
   P.hs = hs;
   const int H8 = H / 8, vpt = H8 <= kThreads ? 1 : (H8 <= 2 * kThreads ? 2 : 4);
   const int Ew = (E + 7) / 8;
-  if (M == 1) {
-    if (Ew <= 32) return launch_j<1>(h, P, vpt, s);
-    if (Ew <= 64) return launch_j<2>(h, P, vpt, s);
-    return launch_j<4>(h, P, vpt, s);
-  }
   if (M == 2) {
     if (Ew <= 32) return launch_multi<1, 2>(h, P, vpt, s);
     if (Ew <= 64) return launch_multi<2, 2>(h, P, vpt, s);

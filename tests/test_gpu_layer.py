@@ -94,16 +94,17 @@ def test_layer_small(h, M, shared):
     _check_layer(tr, hid, ref, slice(None), f"layer M={M}", L, ex, sh)
 
 
-@pytest.mark.parametrize("in_routing", [True, False, 2])
+@pytest.mark.parametrize("front", [True, False])
 @pytest.mark.parametrize("H,E,k,shared", [(1152, 37, 5, True), (1152, 37, 5, False), (256, 9, 8, True),
                                           (2048, 300, 8, True)])
-def test_layer_one_token_shapes(h, H, E, k, shared, in_routing):
+def test_layer_one_token_shapes(h, H, E, k, shared, front):
     """One token: the fused RMSNorm / router / top-k / routing-table launch on
     a router row split into a full and a ragged chunk (H = 1152), with a
     number of experts that leaves a partial row group, k = 8 (the fused down
-    projection + combine) over only 9 experts, and 300 experts; the shared
-    expert's gate/up in the routing launch, in the routed gate/up launch, and
-    the MoE front launch (routing, shared and routed gate/up)."""
+    projection + combine) over only 9 experts, and 300 experts; the MoE front
+    launch (routing, shared and routed gate/up), and with the front switched
+    off the routing launch followed by the grouped gate/up with the shared
+    expert as problem 0."""
     N_in, K_out, I = 264, 256, 128
     L = Layer(H, N_in, K_out, E, I, k, base=6500 + E)
     n = E * I * H
@@ -116,13 +117,13 @@ def test_layer_one_token_shapes(h, H, E, k, shared, in_routing):
               synth.bf16(H * I, SEED, 6515, 0, 0.05).reshape(H, I))
     dev_w = L.device(dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
                      None if sh is None else tuple(dev_bf16(a, a.shape) for a in sh))
-    h.set_one_token_shared(in_routing)
+    h.test_set_moe_front(front)
     for rep in range(3):  # the hand-off and queue counters must be left at zero by every call
         hbits, _ = gap_rows(L.scores, 1, H, k, base=6600 + 10 * E + rep)
         try:
             hid, tr = _run(h, L, dev_w, hbits)
         finally:
-            h.set_one_token_shared(2)
+            h.test_set_moe_front(True)
         ex = lambda e: (g[e], u[e], d[e])
         ref = L.oracle(hbits, ex, sh)
         _check_layer(tr, hid, ref, slice(None), f"layer one token H={H} E={E} rep={rep}", L, ex, sh)
@@ -234,18 +235,18 @@ def test_layer_speculative_verify_batch(h, M, group):
         assert U < 0.8 * E * (1 - (1 - k / E) ** M), U
 
 
-@pytest.mark.parametrize("sched", [2, 1])
+@pytest.mark.parametrize("front", [True, False])
 @pytest.mark.parametrize("M", [2, 3, 4])
 @pytest.mark.parametrize("I,shared", [(128, True), (256, False), (256, True), (384, True), (512, False)])
-def test_layer_few_tokens(h, M, I, shared, sched):
+def test_layer_few_tokens(h, M, I, shared, front):
     """Two to four tokens on the small-matrix family (forced): one routing
     launch (second RMSNorm, router, per-token top-k, a routing table with one
     problem per (token, expert) entry, and the shared expert's gate/up), the
-    entries' gate/up (sched 2, with a shared expert: inside that launch, the
-    MoE front; sched 1: a launch of its own), down over the shared expert's M
-    rows plus the entries, then the combine. At two tokens with I > 256 the
-    down, the combine and the residual are one kernel (I = 384: a ragged
-    thread count; I = 512 without a shared expert)."""
+    entries' gate/up (with a shared expert and the front on: inside that
+    launch, the MoE front; otherwise a launch of its own), down over the
+    shared expert's M rows plus the entries, then the combine. At two tokens
+    with I > 256 the down, the combine and the residual are one kernel
+    (I = 384: a ragged thread count; I = 512 without a shared expert)."""
     import moe_layers_gb300 as ML
     H, N_in, K_out, E, k = 1152, 264, 256, 40, 8
     L = Layer(H, N_in, K_out, E, I, k, base=6800 + I + M)
@@ -260,7 +261,7 @@ def test_layer_few_tokens(h, M, I, shared, sched):
     dev_w = L.device(dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
                      None if sh is None else tuple(dev_bf16(a, a.shape) for a in sh))
     h.set_force_variant(ML.VARIANT_SMALL_M)
-    h.set_one_token_shared(sched)
+    h.test_set_moe_front(front)
     try:
         for rep in range(2):  # the counters must be back at zero after every call
             hbits, _ = gap_rows(L.scores, M, H, k, base=6900 + 10 * M + I + rep)
@@ -268,10 +269,10 @@ def test_layer_few_tokens(h, M, I, shared, sched):
             assert h.last_expert_variant == ML.VARIANT_SMALL_M
             ex = lambda e: (g[e], u[e], d[e])
             ref = L.oracle(hbits, ex, sh)
-            _check_layer(tr, hid, ref, slice(None), f"layer few tokens M={M} I={I} sched={sched} rep={rep}", L, ex, sh)
+            _check_layer(tr, hid, ref, slice(None), f"layer few tokens M={M} I={I} front={front} rep={rep}", L, ex, sh)
     finally:
         h.set_force_variant(ML.VARIANT_AUTO)
-        h.set_one_token_shared(2)
+        h.test_set_moe_front(True)
 
 
 @pytest.mark.parametrize("M", [1, 2])
@@ -366,20 +367,21 @@ def full_layer():
                  gamma_noise=False)
 
 
-@pytest.mark.parametrize("M,sched", [(1, 2), (1, 1), (1, 0), (2, 2), (2, 1), (4, 2), (8, 2), (16, 2), (32, 2), (64, 2)])
-def test_layer_full_size(h, full_bank, full_layer, M, sched):
-    """The full-size layer; at one and two tokens also the other schedules of
-    the shared expert (sched: set_one_token_shared). Output rows are compared
+@pytest.mark.parametrize("M,front", [(1, True), (1, False), (2, True), (2, False), (4, True), (8, True), (16, True),
+                                     (32, True), (64, True)])
+def test_layer_full_size(h, full_bank, full_layer, M, front):
+    """The full-size layer; at one and two tokens also with the MoE front
+    switched off (the routing launch, then the grouped kernels). Output rows are compared
     with the oracle on every row up to 16 tokens and on 16 rows spread over
     the batch above; the top-k indices on every row."""
     Wg, Wu, Wd, sh = full_bank
     L = full_layer
     hbits, _ = gap_rows(L.scores, M, H_FULL, K_FULL, base=synth.X_BASE + 30)
-    h.set_one_token_shared(sched)
+    h.test_set_moe_front(front)
     try:
         hid, tr = _run(h, L, L.device(Wg, Wu, Wd, sh), hbits)
     finally:
-        h.set_one_token_shared(2)
+        h.test_set_moe_front(True)
     bank = HostBank(E_FULL, H_FULL, I_FULL, cache=160)
     shared = tuple(oracle.bf16_to_f64(synth.bf16(I_FULL * H_FULL, SEED, tid, 0, 0.02)).reshape(shape)
                    for tid, shape in ((synth.W_G_S, (I_FULL, H_FULL)), (synth.W_U_S, (I_FULL, H_FULL)),

@@ -42,8 +42,7 @@ def _defaults(h):
     h.set_shared_sms(0)
     h.set_pdl(True)
     h.set_l2_ahead(49152)
-    h.set_one_token_shared(2)
-    h.set_prefetch_shared(False)
+    h.test_set_moe_front(True)
 
 
 SETTINGS = {
@@ -51,11 +50,9 @@ SETTINGS = {
     "no_pdl": {"pdl": False},
     "no_l2_ahead": {"l2_ahead": 0},
     "big_l2_ahead": {"l2_ahead": 1 << 20},
-    "shared_in_gate_up": {"one_token_shared": False},
-    "shared_in_routing": {"one_token_shared": True},
+    "no_moe_front": {"moe_front": False},
     "shared_overlap": {"shared_sms": -1},
     "shared_fixed_4": {"shared_sms": 4},
-    "prefetch_shared": {"prefetch_shared": True},
     "prefetch_next": {"prefetch_next": True},
     "split_k_family": {"force": "split_k"},
     "small_m_family": {"force": "small_m"},
@@ -78,12 +75,10 @@ def test_layer_settings_change_schedule_not_result(h, small_layer, M, name):
             h.set_pdl(cfg["pdl"])
         if "l2_ahead" in cfg:
             h.set_l2_ahead(cfg["l2_ahead"])
-        if "one_token_shared" in cfg:
-            h.set_one_token_shared(cfg["one_token_shared"])
+        if "moe_front" in cfg:
+            h.test_set_moe_front(cfg["moe_front"])
         if "shared_sms" in cfg:
             h.set_shared_sms(cfg["shared_sms"])
-        if "prefetch_shared" in cfg:
-            h.set_prefetch_shared(cfg["prefetch_shared"])
         if cfg.get("force") == "split_k":
             h.set_force_variant(ML.VARIANT_SPLIT_K)
         if cfg.get("force") == "small_m":
