@@ -437,17 +437,20 @@ def test_layer_tp_shapes(h, tp_layer, M):
 
 
 # ---------------------------------------------------------------------------- several distinct layers in sequence
-def _chain_gap_rows(layers, M, H, k, base, gap=1e-3, max_attempts=200):
-    """Token rows whose routing has the 1e-3 top-(k+1) score gap in every
-    layer of the chain, as the oracle computes it (layer l's input is layer
-    l-1's output stored as bf16)."""
+def _chain_gap_rows(layers, M, H, k, base, gaps=(1e-3, 3e-3, 3e-3), max_attempts=400):
+    """Token rows whose routing has a top-(k+1) score gap in every layer of
+    the chain, as the oracle computes it (layer l's input is layer l-1's
+    output stored as bf16): 1e-3 in the first layer, whose input is drawn,
+    and 3e-3 in the later ones, whose inputs on the GPU carry the earlier
+    layers' roundings (measured: after two layers they can move a score by
+    more than half of 1e-3)."""
     from _util import gap_ok
     bits = np.empty((M, H), dtype=np.uint16)
     for r in range(M):
         for attempt in range(max_attempts + 1):
             row = synth.bf16_rows(base, [r], H, SEED, 1.0, [attempt])
             x, ok = row, True
-            for L, ex, sh in layers:
+            for (L, ex, sh), gap in zip(layers, gaps):
                 s = L.scores(x)
                 if not gap_ok(s[0], L.k, gap):
                     ok = False
@@ -470,9 +473,11 @@ def test_layers_in_sequence_with_cross_layer_prefetch(h, M):
     projection (the last to the first) and, in a second run, to nothing:
     - the outputs of the two runs are bit-identical (the prefetch moves data
       into L2 only);
-    - every layer's top-k indices are bit-exact against the oracle's chain;
-    - every layer's output passes the layer rule against the oracle applied
-      to that layer's GPU input;
+    - every layer's output and top-k indices pass the layer rule against the
+      oracle applied to that layer's GPU input;
+    - every layer's top-k indices are bit-exact against the oracle's own
+      chain (its rows drawn with a wider score gap in the later layers, see
+      _chain_gap_rows);
     - the chain's final output is within 3 x 1e-2 rms of the oracle's chain
       (each of the three layers may contribute up to the one-layer budget)."""
     import torch
@@ -480,7 +485,7 @@ def test_layers_in_sequence_with_cross_layer_prefetch(h, M):
     H, N_in, K_out, E, I, k = 1152, 1040, 1024, 40, 256, 8
     layers = []
     for l in range(3):
-        L = Layer(H, N_in, K_out, E, I, k, base=9200 + 20 * l)
+        L = Layer(H, N_in, K_out, E, I, k, base=9200 + 20 * l, sr=0.03)
         n = E * I * H
         g = synth.bf16(n, SEED, 9210 + 20 * l, 0, 0.05).reshape(E, I, H)
         u = synth.bf16(n, SEED, 9211 + 20 * l, 0, 0.05).reshape(E, I, H)
