@@ -437,13 +437,13 @@ def test_layer_tp_shapes(h, tp_layer, M):
 
 
 # ---------------------------------------------------------------------------- several distinct layers in sequence
-def _chain_gap_rows(layers, M, H, k, base, gaps=(1e-3, 3e-3, 3e-3), max_attempts=400):
+def _chain_gap_rows(layers, M, H, k, base, gaps=(1e-3, 2.5e-3, 2.5e-3), max_attempts=4000):
     """Token rows whose routing has a top-(k+1) score gap in every layer of
     the chain, as the oracle computes it (layer l's input is layer l-1's
     output stored as bf16): 1e-3 in the first layer, whose input is drawn,
-    and 3e-3 in the later ones, whose inputs on the GPU carry the earlier
+    and 2.5e-3 in the later ones, whose inputs on the GPU carry the earlier
     layers' roundings (measured: after two layers they can move a score by
-    more than half of 1e-3)."""
+    more than half of 1e-3). About 2% of rows pass all three."""
     from _util import gap_ok
     bits = np.empty((M, H), dtype=np.uint16)
     for r in range(M):
@@ -477,7 +477,9 @@ def test_layers_in_sequence_with_cross_layer_prefetch(h, M):
       oracle applied to that layer's GPU input;
     - every layer's top-k indices are bit-exact against the oracle's own
       chain (its rows drawn with a wider score gap in the later layers, see
-      _chain_gap_rows);
+      _chain_gap_rows; the router is the workload's N(0, 0.01), at which one
+      last-bit difference of a normalised row stays within the 1e-4 score
+      tolerance);
     - the chain's final output is within 3 x 1e-2 rms of the oracle's chain
       (each of the three layers may contribute up to the one-layer budget)."""
     import torch
@@ -485,7 +487,7 @@ def test_layers_in_sequence_with_cross_layer_prefetch(h, M):
     H, N_in, K_out, E, I, k = 1152, 1040, 1024, 40, 256, 8
     layers = []
     for l in range(3):
-        L = Layer(H, N_in, K_out, E, I, k, base=9200 + 20 * l, sr=0.03)
+        L = Layer(H, N_in, K_out, E, I, k, base=9200 + 20 * l)
         n = E * I * H
         g = synth.bf16(n, SEED, 9210 + 20 * l, 0, 0.05).reshape(E, I, H)
         u = synth.bf16(n, SEED, 9211 + 20 * l, 0, 0.05).reshape(E, I, H)
