@@ -78,17 +78,15 @@ int choose_variant(const dec_handle* h, int M, int N, int K) {
 
 // gamma (small-matrix kernel): the input rows are RMS-normalised inside the
 // projection kernel.
-// gemv_ctr: the small-matrix kernel's chunk-ticket counter (one int, zero
-// between launches).
 dec_status linear_impl(dec_handle* h, const uint16_t* x, int ldx, const uint16_t* W, const uint16_t* r, uint16_t* y,
-                       int M, int N, int K, EngineRegion eng, int* gemv_ctr, cudaStream_t s,
-                       const char* tag = "linear", const uint16_t* gamma = nullptr, float eps = 0.f) {
+                       int M, int N, int K, EngineRegion eng, cudaStream_t s, const char* tag = "linear",
+                       const uint16_t* gamma = nullptr, float eps = 0.f) {
   const int v = choose_variant(h, M, N, K);
   cudaError_t e;
   LaunchScope scope(h, tag, s);
   if (v == DEC_VARIANT_SMALL_M) {
     if (!gemv_supported(M, K)) return DEC_ERR_UNSUPPORTED;
-    e = launch_gemv(h, x, ldx, W, r, N, y, N, M, N, K, s, gemv_ctr, gamma, eps);
+    e = launch_gemv(h, x, ldx, W, r, N, y, N, M, N, K, s, gamma, eps);
   } else {
     EngineLaunch L;
     L.epi = EPI_LINEAR;
@@ -451,7 +449,6 @@ struct MoeLayerWs {
 };
 
 struct LayerWs {
-  int* gemv_ctr = nullptr;  // the small-matrix projections' ticket counters [2]
   uint16_t* a = nullptr;
   uint16_t* yin = nullptr;
   uint16_t* h1 = nullptr;
@@ -485,7 +482,6 @@ void carve_layer(Carver& c, const dec_handle* h, const dec_layer_weights* L, int
   const int H = L->H;
   const long long dense_tiles = std::max<long long>((L->N_in + kTileN - 1) / kTileN, H / kTileN);
   carve_moe_layer_head(c, L->E, H, L->I, dense_tiles, &w->ml);
-  w->gemv_ctr = c.take<int>(2);
   w->a = c.take<uint16_t>((size_t)M * H);
   w->yin = c.take<uint16_t>((size_t)M * L->N_in);
   w->h1 = c.take<uint16_t>((size_t)M * H);
@@ -755,19 +751,10 @@ dec_status dec_check_device_error(dec_handle* h) {
 }
 
 // ---------------------------------------------------------------- projections
-// Layout of a projection's workspace: the small-matrix kernel's ticket
-// counter, then the split-K engine's tile counters and partial sums.
-void carve_linear(Carver& c, const dec_handle* h, int N, int** gemv_ctr, EngineRegion* eng) {
-  *gemv_ctr = c.take<int>(1);
-  *eng = carve_engine(c, engine_grid(h), 1, (N + kTileN - 1) / kTileN);
-}
-
 dec_status dec_linear_workspace_size(const dec_handle* h, int M, int N, int K, size_t* bytes) {
   if (h == nullptr || bytes == nullptr || !linear_shape_ok(M, N, K, K)) return DEC_ERR_INVALID_ARG;
   Carver c(nullptr);
-  int* ctr;
-  EngineRegion eng;
-  carve_linear(c, h, N, &ctr, &eng);
+  carve_engine(c, engine_grid(h), 1, (N + kTileN - 1) / kTileN);
   *bytes = c.used;
   return DEC_OK;
 }
@@ -777,14 +764,15 @@ static dec_status linear_entry(dec_handle* h, const dec_bf16* x, int ldx, const 
   if (h == nullptr || x == nullptr || W == nullptr || out == nullptr) return DEC_ERR_INVALID_ARG;
   if (!al16(x) || !al16(W) || !al16(out) || (r != nullptr && !al16(r))) return DEC_ERR_INVALID_ARG;
   if (!linear_shape_ok(M, N, K, ldx)) return DEC_ERR_INVALID_ARG;
-  size_t need = 0;
-  dec_linear_workspace_size(h, M, N, K, &need);
-  if (ws == nullptr || !al16(ws) || ws_bytes < need) return DEC_ERR_INVALID_ARG;
-  Carver c(ws);
-  int* ctr;
   EngineRegion eng;
-  carve_linear(c, h, N, &ctr, &eng);
-  return linear_impl(h, x, ldx, W, r, out, M, N, K, eng, ctr, s, r ? "linear_residual" : "linear");
+  if (choose_variant(h, M, N, K) == DEC_VARIANT_SPLIT_K) {
+    size_t need = 0;
+    dec_linear_workspace_size(h, M, N, K, &need);
+    if (ws == nullptr || !al16(ws) || ws_bytes < need) return DEC_ERR_INVALID_ARG;
+    Carver c(ws);
+    eng = carve_engine(c, engine_grid(h), 1, (N + kTileN - 1) / kTileN);
+  }
+  return linear_impl(h, x, ldx, W, r, out, M, N, K, eng, s, r ? "linear_residual" : "linear");
 }
 
 dec_status dec_linear(dec_handle* h, const dec_bf16* x, int ldx, const dec_bf16* W, dec_bf16* y, int M, int N,
@@ -928,12 +916,11 @@ dec_status decode_layer(dec_handle* h, const dec_layer_weights* Wt, dec_bf16* hi
     if (launch_rmsnorm(h, hidden, L.gamma1, w.a, M, H, L.eps, s) != cudaSuccess) return DEC_ERR_CUDA;
   }
   EngineRegion dense = w.ml.moe.r0;
-  dec_status st = fuse_norm1 ? linear_impl(h, hidden, H, L.W_in, nullptr, w.yin, M, L.N_in, H, dense, w.gemv_ctr, s,
-                                           "in_proj", L.gamma1, L.eps)
-                             : linear_impl(h, w.a, H, L.W_in, nullptr, w.yin, M, L.N_in, H, dense, w.gemv_ctr, s,
-                                           "in_proj");
+  dec_status st = fuse_norm1 ? linear_impl(h, hidden, H, L.W_in, nullptr, w.yin, M, L.N_in, H, dense, s, "in_proj",
+                                           L.gamma1, L.eps)
+                             : linear_impl(h, w.a, H, L.W_in, nullptr, w.yin, M, L.N_in, H, dense, s, "in_proj");
   if (st != DEC_OK) return st;
-  st = linear_impl(h, w.yin, L.N_in, L.W_o, hidden, h1, M, H, L.K_out, dense, w.gemv_ctr + 1, s, "out_proj");
+  st = linear_impl(h, w.yin, L.N_in, L.W_o, hidden, h1, M, H, L.K_out, dense, s, "out_proj");
   if (st != DEC_OK) return st;
   // The MoE block, pre-norm with its own residual: hidden = h1 + MoE(RMSNorm(h1)).
   MoeLayerArgs A;

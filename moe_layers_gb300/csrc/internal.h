@@ -89,11 +89,9 @@ struct EngineLaunch {
 
 cudaError_t launch_engine(dec_handle* h, const EngineLaunch& L, cudaStream_t s);
 
-// gamma: normalise the input rows first (RMSNorm with eps), fused. ctr: the
-// ring kernel's chunk-ticket counter (one int, zero between launches; null:
-// static chunks only).
+// gamma: normalise the input rows first (RMSNorm with eps), fused.
 cudaError_t launch_gemv(dec_handle* h, const uint16_t* x, long long ldx, const uint16_t* W, const uint16_t* res,
-                        long long ldr, uint16_t* y, long long ldy, int M, int N, int K, cudaStream_t s, int* ctr,
+                        long long ldr, uint16_t* y, long long ldy, int M, int N, int K, cudaStream_t s,
                         const uint16_t* gamma = nullptr, float eps = 0.f);
 bool gemv_supported(int M, int K);
 
