@@ -67,6 +67,12 @@ constexpr int kMaxPieces = 256;
 #ifndef DEC_ENGINE_KSUB_PAIR
 #define DEC_ENGINE_KSUB_PAIR 1
 #endif
+// Weight k-blocks requested into L2 (TMA tile prefetches) ahead of the ring's
+// loads: the L2 requests hold no shared memory, so more of the weight stream
+// is in flight than the ring holds (0 disables them).
+#ifndef DEC_ENGINE_L2_AHEAD
+#define DEC_ENGINE_L2_AHEAD 8
+#endif
 
 template <int NA, int BROWS>
 struct EngineSmem {
@@ -186,10 +192,20 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
           for (int b = 0; b < nb; ++b) tma_load_2d(st + S::b_off(u) + b * 2048, &tmB, &full[s], k0, row0 + 16 * b, pol_x);
         }
       };
+      // k-block j's weight tiles (row a_row of the bank) requested into L2
+      auto prefetch_A = [&](int kb, long long a_row) {
+#pragma unroll
+        for (int u = 0; u < S::kKSub; ++u) {
+          const int k0 = (kb * S::kKSub + u) * kBlockK;
+          tma_prefetch_l2_2d(&tmA, k0, (int)a_row, pol_w);
+          if (NA == 2) tma_prefetch_l2_2d(&tmA2, k0, (int)a_row, pol_w);
+        }
+      };
       if (P.table == nullptr) {
         // Dense: the k-block range is known before the dependency wait, so the
         // first ring's worth of static weights streams in while the previous
-        // kernel drains. Activations are loaded only after pdl_wait().
+        // kernel drains, and the next DEC_ENGINE_L2_AHEAD k-blocks are
+        // requested into L2. Activations are loaded only after pdl_wait().
         const long long W = (long long)tiles * KB;
         const long long j0 = range_start(c, W, G), j1 = range_start(c + 1, W, G);
         const int nb = (P.count + 15) >> 4;
@@ -200,6 +216,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
           mbar_arrive_expect_tx(&full[i], bytes);
           load_A((int)i, (int)(j / KB), (int)(j % KB), (j / KB) * kTileN);
         }
+        for (long long j = j0 + npre; j < min(j1, j0 + npre + DEC_ENGINE_L2_AHEAD); ++j)
+          prefetch_A((int)(j % KB), (j / KB) * kTileN);
         pdl_wait();
         for (long long i = 0; i < j1 - j0; ++i) {
           const long long j = j0 + i;
@@ -210,6 +228,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
             if (!mbar_wait(&empty[s], ph ^ 1u, wc)) break;
             mbar_arrive_expect_tx(&full[s], bytes);
             load_A(s, (int)(j / KB), kb, (j / KB) * kTileN);
+            const long long jp = j + DEC_ENGINE_L2_AHEAD;
+            if (DEC_ENGINE_L2_AHEAD > 0 && jp < j1) prefetch_A((int)(jp % KB), (jp / KB) * kTileN);
           }
           load_B(s, kb, 0, nb);
           issued = i + 1;
@@ -218,17 +238,35 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
         pdl_wait();
         const long long W = total_kblocks(P);
         const long long j0 = range_start(c, W, G), j1 = range_start(c + 1, W, G);
+        // The L2 requests run DEC_ENGINE_L2_AHEAD k-blocks ahead of the loads;
+        // each stream keeps its current problem's table entry.
+        int p_ld = -1, p_pf = -1;
+        Prob pr_ld{0, 0, 0}, pr_pf{0, 0, 0};
+        auto prefetch_kb = [&](long long jp) {
+          const int tau = (int)(jp / KB), p = tau / tiles;
+          if (p != p_pf) {
+            pr_pf = prob_info(P, p);
+            p_pf = p;
+          }
+          prefetch_A((int)(jp % KB), (long long)pr_pf.e * P.a_rows_per_prob + (long long)(tau % tiles) * kTileN);
+        };
+        for (long long j = j0; j < min(j1, j0 + DEC_ENGINE_L2_AHEAD); ++j) prefetch_kb(j);
         for (long long i = 0; i < j1 - j0; ++i) {
           const long long j = j0 + i;
           const int s = (int)(i % S::kStages);
           const uint32_t ph = (uint32_t)((i / S::kStages) & 1);
           const int tau = (int)(j / KB), kb = (int)(j % KB);
-          const Prob pr = prob_info(P, tau / tiles);
-          const int nb = (pr.cnt + 15) >> 4;
+          if (tau / tiles != p_ld) {
+            p_ld = tau / tiles;
+            pr_ld = prob_info(P, p_ld);
+          }
+          const int nb = (pr_ld.cnt + 15) >> 4;
           if (!mbar_wait(&empty[s], ph ^ 1u, wc)) break;
           mbar_arrive_expect_tx(&full[s], S::kABytes + S::kKSub * nb * 2048);
-          load_A(s, tau, kb, (long long)pr.e * P.a_rows_per_prob + (long long)(tau % tiles) * kTileN);
-          load_B(s, kb, pr.off, nb);
+          load_A(s, tau, kb, (long long)pr_ld.e * P.a_rows_per_prob + (long long)(tau % tiles) * kTileN);
+          load_B(s, kb, pr_ld.off, nb);
+          const long long jp = j + DEC_ENGINE_L2_AHEAD;
+          if (DEC_ENGINE_L2_AHEAD > 0 && jp < j1) prefetch_kb(jp);
           issued = i + 1;
         }
       }
@@ -391,17 +429,36 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
       if (*s_last) {
         __threadfence();
         const int np = min(*s_np, kMaxPieces);
+        // The pieces' partials are read RB pieces at a time, every load of a
+        // batch issued before any is added (one L2 round trip per batch, not
+        // per piece), and added in k order (the same sums as one by one).
+        constexpr int RB = (NA == 2) ? 2 : 4;
         for (int ch = 0; ch < nch; ++ch) {
           float a0[16], a1[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) a0[i] = a1[i] = 0.f;
-          for (int p = 0; p < np; ++p) {
-            const float* ps = P.partials + (size_t)s_piece[p] * P.slot_floats + (size_t)ch * 16 * kTileN + row;
+          for (int p0 = 0; p0 < np; p0 += RB) {
+            float t0[RB][16], t1[RB][16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (ch * 16 + i < pr.cnt) {
-                a0[i] += __ldcg(ps + (size_t)i * kTileN);
-                if (NA == 2) a1[i] += __ldcg(ps + (size_t)P.cols * kTileN + (size_t)i * kTileN);
+            for (int q = 0; q < RB; ++q) {
+              const int p = p0 + q < np ? p0 + q : p0;
+              const float* ps = P.partials + (size_t)s_piece[p] * P.slot_floats + (size_t)ch * 16 * kTileN + row;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const bool ok = p0 + q < np && ch * 16 + i < pr.cnt;
+                t0[q][i] = ok ? __ldcg(ps + (size_t)i * kTileN) : 0.f;
+                if (NA == 2) t1[q][i] = ok ? __ldcg(ps + (size_t)P.cols * kTileN + (size_t)i * kTileN) : 0.f;
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < RB; ++q)
+              if (p0 + q < np) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  if (ch * 16 + i < pr.cnt) {
+                    a0[i] += t0[q][i];
+                    if (NA == 2) a1[i] += t1[q][i];
+                  }
               }
           }
           if (valid_row) emit_chunk(pr, n, ch, a0, a1);
