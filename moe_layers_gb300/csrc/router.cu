@@ -228,76 +228,12 @@ __global__ void __launch_bounds__(256) route_table_kernel(const int32_t* idx, in
   int* eidx = run + E;
   int* stok = eidx + n;
   int* eslot = stok + n;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const TableLayout L(E, n);
+  const int tid = threadIdx.x;
   pdl_trigger();
   pdl_wait();
-  for (int e = tid; e < E; e += blockDim.x) {
-    cnt[e] = 0;
-    run[e] = 0;
-  }
   for (int i = tid; i < n; i += blockDim.x) eidx[i] = ld_act_s32(idx + i);
   __syncthreads();
-  for (int i = tid; i < n; i += blockDim.x) atomicAdd(&cnt[eidx[i]], 1);
-  __syncthreads();
-  if (warp == 0) {
-    const int per = (E + 31) / 32;
-    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-    int s_sum = 0, a_sum = 0;
-    for (int e = e0; e < e1; ++e) {
-      s_sum += cnt[e];
-      a_sum += cnt[e] > 0 ? 1 : 0;
-    }
-    int s_inc = s_sum, a_inc = a_sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int vs = __shfl_up_sync(0xffffffffu, s_inc, o);
-      const int va = __shfl_up_sync(0xffffffffu, a_inc, o);
-      if (lane >= o) {
-        s_inc += vs;
-        a_inc += va;
-      }
-    }
-    int s_run = s_inc - s_sum, a_run = a_inc - a_sum;
-    for (int e = e0; e < e1; ++e) {
-      off[e] = s_run;
-      if (cnt[e] > 0) {
-        if (blockIdx.x == 0) {
-          table[L.expert() + a_run] = e;
-          table[L.offset() + a_run] = s_run;
-          table[L.count() + a_run] = cnt[e];
-        }
-        ++a_run;
-      }
-      s_run += cnt[e];
-    }
-    if (lane == 31 && blockIdx.x == 0) table[L.U()] = a_inc;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    for (int base = 0; base < n; base += 32) {
-      const int i = base + lane;
-      const bool valid = i < n;
-      const int e = valid ? eidx[i] : -1 - lane;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      if (valid) {
-        const int slot = off[e] + run[e] + rank;
-        eslot[i] = slot;
-        stok[slot] = i / k;
-      }
-      __syncwarp();
-      if (valid && rank == 0) run[e] += __popc(peers);
-      __syncwarp();
-    }
-  }
-  __syncthreads();
-  if (blockIdx.x == 0) {
-    for (int i = tid; i < n; i += blockDim.x) {
-      table[L.slot_token() + i] = stok[i];
-      table[L.entry_slot() + i] = eslot[i];
-    }
-  }
+  block_route_table(eidx, n, k, E, cnt, off, run, stok, eslot, table, blockIdx.x == 0);
   const int H8 = H >> 3;
   const long long total = (long long)n * H8;
   for (long long q = (long long)blockIdx.x * blockDim.x + tid; q < total; q += (long long)gridDim.x * blockDim.x) {

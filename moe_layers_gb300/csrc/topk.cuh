@@ -44,6 +44,83 @@ __device__ __forceinline__ void write_entry_table(int* table, int E, int M, int 
   if (t == 0 && lane == 0) table[L.U()] = M * k;
 }
 
+// Grouped routing table from the n = M k entries eidx[i] (entry i = token
+// i / k, choice i % k) held in shared memory, by a 256-thread block: per
+// active expert (ascending id) its first slot and token count; slots ordered
+// by (expert, token, choice). Shared scratch: cnt, off, run [E] and stok,
+// eslot [n] ints. write: this block writes the table out. On return
+// stok[slot] is the slot's token for every thread of the block.
+__device__ __forceinline__ void block_route_table(const int* eidx, int n, int k, int E, int* cnt, int* off, int* run,
+                                                  int* stok, int* eslot, int* table, bool write) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const TableLayout L(E, n);
+  for (int e = tid; e < E; e += blockDim.x) {
+    cnt[e] = 0;
+    run[e] = 0;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) atomicAdd(&cnt[eidx[i]], 1);
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int s_sum = 0, a_sum = 0;
+    for (int e = e0; e < e1; ++e) {
+      s_sum += cnt[e];
+      a_sum += cnt[e] > 0 ? 1 : 0;
+    }
+    int s_inc = s_sum, a_inc = a_sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int vs = __shfl_up_sync(0xffffffffu, s_inc, o);
+      const int va = __shfl_up_sync(0xffffffffu, a_inc, o);
+      if (lane >= o) {
+        s_inc += vs;
+        a_inc += va;
+      }
+    }
+    int s_run = s_inc - s_sum, a_run = a_inc - a_sum;
+    for (int e = e0; e < e1; ++e) {
+      off[e] = s_run;
+      if (cnt[e] > 0) {
+        if (write) {
+          table[L.expert() + a_run] = e;
+          table[L.offset() + a_run] = s_run;
+          table[L.count() + a_run] = cnt[e];
+        }
+        ++a_run;
+      }
+      s_run += cnt[e];
+    }
+    if (lane == 31 && write) table[L.U()] = a_inc;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      const bool valid = i < n;
+      const int e = valid ? eidx[i] : -1 - lane;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      if (valid) {
+        const int slot = off[e] + run[e] + rank;
+        eslot[i] = slot;
+        stok[slot] = i / k;
+      }
+      __syncwarp();
+      if (valid && rank == 0) run[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  if (write) {
+    for (int i = tid; i < n; i += blockDim.x) {
+      table[L.slot_token() + i] = stok[i];
+      table[L.entry_slot() + i] = eslot[i];
+    }
+  }
+}
+
 // k rounds of arg-max over E scores in shared memory (score descending,
 // expert id ascending), by one warp: lane l holds experts l, l + 32, ... (JW
 // per lane, E <= 32 JW). Each round takes the lane's best (a strict > over
