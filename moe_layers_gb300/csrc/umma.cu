@@ -67,11 +67,15 @@ constexpr int kMaxPieces = 256;
 #ifndef DEC_ENGINE_KSUB_PAIR
 #define DEC_ENGINE_KSUB_PAIR 1
 #endif
-// Weight k-blocks requested into L2 (TMA tile prefetches) ahead of the ring's
-// loads: the L2 requests hold no shared memory, so more of the weight stream
-// is in flight than the ring holds (0 disables them).
-#ifndef DEC_ENGINE_L2_AHEAD
-#define DEC_ENGINE_L2_AHEAD 8
+// Shared memory for the ring and CTAs per SM (build-time tunables): the ring
+// takes as many stages as the budget allows; with two CTAs per SM a launch's
+// CTAs can start beside the previous launch's and stream their first weights
+// while it drains.
+#ifndef DEC_ENGINE_SMEM_BUDGET
+#define DEC_ENGINE_SMEM_BUDGET (232448 - 1024 - 512 - 4 * kMaxPieces)
+#endif
+#ifndef DEC_ENGINE_CTAS_PER_SM
+#define DEC_ENGINE_CTAS_PER_SM 1
 #endif
 
 template <int NA, int BROWS>
@@ -82,7 +86,7 @@ struct EngineSmem {
   static constexpr int kBBox = BROWS * kBlockK * 2;        // activation box of one sub-block
   static constexpr int kABytes = NA * kKSub * kABox;
   static constexpr int kStageBytes = kABytes + kKSub * kBBox;
-  static constexpr int kBudget = 232448 - 1024 - 512 - 4 * kMaxPieces;  // opt-in maximum minus slack, barriers, pieces
+  static constexpr int kBudget = DEC_ENGINE_SMEM_BUDGET;  // ring bytes (the opt-in maximum minus slack, barriers, pieces)
   static constexpr int kStages = (kBudget / kStageBytes) < 12 ? (kBudget / kStageBytes) : 12;
   static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kNumBars = 2 * kStages + 5;
@@ -117,7 +121,7 @@ __device__ __forceinline__ long long total_kblocks(const EngineParams& P) {
 }
 
 template <int EPI, int BROWS>
-__global__ void __launch_bounds__(kEngineThreads, 1)
+__global__ void __launch_bounds__(kEngineThreads, DEC_ENGINE_CTAS_PER_SM)
     engine_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                   const __grid_constant__ CUtensorMap tmB, const EngineParams P) {
   constexpr int NA = (EPI == EPI_SWIGLU) ? 2 : 1;
@@ -192,20 +196,10 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
           for (int b = 0; b < nb; ++b) tma_load_2d(st + S::b_off(u) + b * 2048, &tmB, &full[s], k0, row0 + 16 * b, pol_x);
         }
       };
-      // k-block j's weight tiles (row a_row of the bank) requested into L2
-      auto prefetch_A = [&](int kb, long long a_row) {
-#pragma unroll
-        for (int u = 0; u < S::kKSub; ++u) {
-          const int k0 = (kb * S::kKSub + u) * kBlockK;
-          tma_prefetch_l2_2d(&tmA, k0, (int)a_row, pol_w);
-          if (NA == 2) tma_prefetch_l2_2d(&tmA2, k0, (int)a_row, pol_w);
-        }
-      };
       if (P.table == nullptr) {
         // Dense: the k-block range is known before the dependency wait, so the
         // first ring's worth of static weights streams in while the previous
-        // kernel drains, and the next DEC_ENGINE_L2_AHEAD k-blocks are
-        // requested into L2. Activations are loaded only after pdl_wait().
+        // kernel drains. Activations are loaded only after pdl_wait().
         const long long W = (long long)tiles * KB;
         const long long j0 = range_start(c, W, G), j1 = range_start(c + 1, W, G);
         const int nb = (P.count + 15) >> 4;
@@ -216,8 +210,6 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
           mbar_arrive_expect_tx(&full[i], bytes);
           load_A((int)i, (int)(j / KB), (int)(j % KB), (j / KB) * kTileN);
         }
-        for (long long j = j0 + npre; j < min(j1, j0 + npre + DEC_ENGINE_L2_AHEAD); ++j)
-          prefetch_A((int)(j % KB), (j / KB) * kTileN);
         pdl_wait();
         for (long long i = 0; i < j1 - j0; ++i) {
           const long long j = j0 + i;
@@ -228,8 +220,6 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
             if (!mbar_wait(&empty[s], ph ^ 1u, wc)) break;
             mbar_arrive_expect_tx(&full[s], bytes);
             load_A(s, (int)(j / KB), kb, (j / KB) * kTileN);
-            const long long jp = j + DEC_ENGINE_L2_AHEAD;
-            if (DEC_ENGINE_L2_AHEAD > 0 && jp < j1) prefetch_A((int)(jp % KB), (jp / KB) * kTileN);
           }
           load_B(s, kb, 0, nb);
           issued = i + 1;
@@ -238,19 +228,8 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
         pdl_wait();
         const long long W = total_kblocks(P);
         const long long j0 = range_start(c, W, G), j1 = range_start(c + 1, W, G);
-        // The L2 requests run DEC_ENGINE_L2_AHEAD k-blocks ahead of the loads;
-        // each stream keeps its current problem's table entry.
-        int p_ld = -1, p_pf = -1;
-        Prob pr_ld{0, 0, 0}, pr_pf{0, 0, 0};
-        auto prefetch_kb = [&](long long jp) {
-          const int tau = (int)(jp / KB), p = tau / tiles;
-          if (p != p_pf) {
-            pr_pf = prob_info(P, p);
-            p_pf = p;
-          }
-          prefetch_A((int)(jp % KB), (long long)pr_pf.e * P.a_rows_per_prob + (long long)(tau % tiles) * kTileN);
-        };
-        for (long long j = j0; j < min(j1, j0 + DEC_ENGINE_L2_AHEAD); ++j) prefetch_kb(j);
+        int p_ld = -1;  // the current problem and its table entry
+        Prob pr_ld{0, 0, 0};
         for (long long i = 0; i < j1 - j0; ++i) {
           const long long j = j0 + i;
           const int s = (int)(i % S::kStages);
@@ -265,8 +244,6 @@ __global__ void __launch_bounds__(kEngineThreads, 1)
           mbar_arrive_expect_tx(&full[s], S::kABytes + S::kKSub * nb * 2048);
           load_A(s, tau, kb, (long long)pr_ld.e * P.a_rows_per_prob + (long long)(tau % tiles) * kTileN);
           load_B(s, kb, pr_ld.off, nb);
-          const long long jp = j + DEC_ENGINE_L2_AHEAD;
-          if (DEC_ENGINE_L2_AHEAD > 0 && jp < j1) prefetch_kb(jp);
           issued = i + 1;
         }
       }
