@@ -354,12 +354,10 @@ dec_status moe_few(dec_handle* h, int M, const uint16_t* x, const float* w, int 
   return DEC_OK;
 }
 
-// table_done: the routing launch already wrote the grouped table and gathered
-// the slot rows into ws.xs.
 dec_status moe_routed(dec_handle* h, const uint16_t* x, const int32_t* idx, const float* w, int M, int k,
                       const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int E, int H, int I,
                       const uint16_t* Wg_s, const uint16_t* Wu_s, const uint16_t* Wd_s, const uint16_t* residual,
-                      uint16_t* out, const MoeWs& ws, cudaStream_t s, bool table_done = false) {
+                      uint16_t* out, const MoeWs& ws, cudaStream_t s) {
   const bool has_shared = Wg_s != nullptr;
   const int n = M * k;
   const int g0 = routed_grid(h, M, k, E, H, I, has_shared);
@@ -370,7 +368,7 @@ dec_status moe_routed(dec_handle* h, const uint16_t* x, const int32_t* idx, cons
     }
     return moe_small(h, x, 0, w, k, Wg, Wu, Wd, E, H, I, Wg_s, Wu_s, Wd_s, residual, out, ws, s);
   }
-  if (!table_done) {
+  {
     LaunchScope scope(h, "route_table", s);
     DEC_CUDA(launch_route_table(h, idx, M, k, E, x, H, ws.table, ws.xs, s));
   }
@@ -612,27 +610,17 @@ dec_status moe_layer_impl(dec_handle* h, const MoeLayerArgs& A, const MoeLayerWs
   }
   st = moe_shared_fork(h, b, M, A.k, A.E, H, A.I, A.Wg_s, A.Wu_s, A.Wd_s, w.moe, s);
   if (st != DEC_OK) return st;
-  // Three to eight tokens: router, top-k, routing table and the gather in one
-  // launch (the shared expert, forked above, overlaps it). Above: the router,
-  // top-k and table launches.
-  const bool group = route_group_supported(M, H, A.E, A.k);
-  if (group) {
-    LaunchScope scope(h, "routing", s);
-    DEC_CUDA(launch_route_group(h, M, b, A.Wr, H, A.E, A.k, w.parts, w.sel_counter, A.idx, A.w, A.scores,
-                                w.moe.table, w.moe.xs, s));
-  } else {
-    {
-      LaunchScope scope(h, "router", s);
-      if (launch_router(h, b, A.Wr, M, H, A.E, w.parts, s) != cudaSuccess) return DEC_ERR_CUDA;
-    }
-    {
-      LaunchScope scope(h, "topk", s);
-      if (launch_topk(h, w.parts, router_ksplit(H), M, A.E, A.k, A.idx, A.w, A.scores, s) != cudaSuccess)
-        return DEC_ERR_CUDA;
-    }
+  {
+    LaunchScope scope(h, "router", s);
+    if (launch_router(h, b, A.Wr, M, H, A.E, w.parts, s) != cudaSuccess) return DEC_ERR_CUDA;
+  }
+  {
+    LaunchScope scope(h, "topk", s);
+    if (launch_topk(h, w.parts, router_ksplit(H), M, A.E, A.k, A.idx, A.w, A.scores, s) != cudaSuccess)
+      return DEC_ERR_CUDA;
   }
   st = moe_routed(h, b, A.idx, A.w, M, A.k, A.Wg, A.Wu, A.Wd, A.E, H, A.I, A.Wg_s, A.Wu_s, A.Wd_s, A.residual, A.out,
-                  w.moe, s, group);
+                  w.moe, s);
   if (st != DEC_OK) return st;
   if (pf) DEC_CUDA(cudaStreamWaitEvent(s, h->ev_pf_join, 0));
   return DEC_OK;

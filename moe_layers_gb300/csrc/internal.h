@@ -169,13 +169,6 @@ cudaError_t launch_route_shared(dec_handle* h, int M, const uint16_t* h1, const 
                                 const float* Wr, int H, int E, int k, uint16_t* xn, float* parts, int* ctr,
                                 int32_t* idx, float* w, float* scores, int* table, const uint16_t* Wg_s,
                                 const uint16_t* Wu_s, int I, uint16_t* hs, cudaStream_t s);
-// Three to eight tokens: router logits, top-k, the grouped routing table and
-// the gather of the slot rows xs from the normalised rows x, in one launch;
-// counters ctr [0], [2], [3], [6] zero between launches.
-bool route_group_supported(int M, int H, int E, int k);
-cudaError_t launch_route_group(dec_handle* h, int M, const uint16_t* x, const float* Wr, int H, int E, int k,
-                               float* parts, int* ctr, int32_t* idx, float* w, float* scores, int* table,
-                               uint16_t* xs, cudaStream_t s);
 cudaError_t launch_one_token_table(dec_handle* h, const int32_t* idx, int E, int k, int* table, cudaStream_t s);
 cudaError_t launch_route_table(dec_handle* h, const int32_t* idx, int M, int k, int E, const uint16_t* x, int H,
                                int* table, uint16_t* xs, cudaStream_t s);

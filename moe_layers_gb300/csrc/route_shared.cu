@@ -1054,173 +1054,6 @@ __global__ void __launch_bounds__(kThreads, 2) moe_front_multi_kernel(const Rout
   }
 }
 
-// Three to eight tokens on the split-K family: the router logits, the top-k of
-// every token, the grouped routing table (per expert its tokens' slots) and
-// the gather of each slot's token row into the slot-ordered rows xs that the
-// experts' TMA loads read, in one launch instead of three. The rows x are the
-// layer's normalised rows (the RMSNorm launch before this one writes them, so
-// the shared expert, forked after it, overlaps this launch).
-// Router units come from the ticket counter and the hand-off counts units, as
-// in the fronts; the arrival that completes the last unit scores the tokens
-// (four at a time), warp t selects token t's experts, builds the table and
-// publishes it with the routing flag. Every CTA then waits for the flag
-// (bounded) and copies its even share of the slot rows. The "done" counter's
-// last CTA resets the flag before it triggers the next launch.
-constexpr int kGroupTok = 8;
-
-struct RouteGroupParams {
-  const uint16_t* x;  // normalised rows [M][H]
-  const float* Wr;
-  int H, E, k, M, nunits;
-  float* parts;       // [ksplit][M][E]
-  int* ctr;           // [0] hand-off, [2] done, [3] routing flag, [6] unit tickets
-  int32_t* idx;
-  float* w;
-  float* scores;      // or null
-  int* table;
-  uint16_t* xs;       // slot rows [M k][H]
-  int* err;
-  unsigned long long wait_ns;
-};
-
-template <int J>
-__global__ void __launch_bounds__(kThreads, 2) route_group_kernel(const RouteGroupParams P) {
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int G = gridDim.x, c = blockIdx.x;
-  const int H = P.H, M = P.M, n = P.M * P.k;
-  const int ngrp = (P.E + 7) / 8, ksplit = (H + kUnitCols - 1) / kUnitCols;
-  extern __shared__ __align__(16) uint8_t smg[];
-  uint16_t(*sxc)[kUnitCols] = reinterpret_cast<uint16_t(*)[kUnitCols]>(smg);  // [kGroupTok][1024]: a unit's columns
-  float(*s_sc)[256 * J] = reinterpret_cast<float(*)[256 * J]>(smg + kGroupTok * kUnitCols * 2);  // [kGroupTok][E]
-  int* tab = reinterpret_cast<int*>(smg + kGroupTok * kUnitCols * 2 + kGroupTok * 256 * J * 4);
-  int *cnt = tab, *off = cnt + P.E, *run = off + P.E, *eidx = run + P.E, *stok = eidx + n, *eslot = stok + n;
-  __shared__ int s_unit, s_last, s_ok;
-
-  float4 wv[kUnitCols / 128];
-  auto load_unit = [&](int u) {
-    const int e = (u % ngrp) * 8 + warp, k0 = (u / ngrp) * kUnitCols;
-    const int kn = min(kUnitCols, H - k0);
-#pragma unroll
-    for (int i = 0; i < kUnitCols / 128; ++i) {
-      const int kk = 4 * (lane + 32 * i);
-      wv[i] = (u < P.nunits && e < P.E && kk < kn)
-                  ? __ldg(reinterpret_cast<const float4*>(P.Wr + (size_t)e * H + k0 + kk))
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  };
-  if (t == 0) s_unit = take_unit(P.ctr, P.nunits, G);
-  __syncthreads();
-  int u = s_unit;
-  load_unit(u);
-  pdl_wait();
-  for (;;) {
-    if (u < P.nunits) {
-      const int e = (u % ngrp) * 8 + warp, ks = u / ngrp, k0 = ks * kUnitCols;
-      const int kn = min(kUnitCols, H - k0), kv = kn >> 3;
-      for (int q = t; q < M * kv; q += kThreads) {
-        const int tt = q / kv, v = q - tt * kv;
-        *reinterpret_cast<uint4*>(&sxc[tt][v * 8]) = ld_act16(P.x + (size_t)tt * H + k0 + (size_t)v * 8);
-      }
-      __syncthreads();
-      float acc[kGroupTok];
-#pragma unroll
-      for (int q = 0; q < kGroupTok; ++q) acc[q] = 0.f;
-#pragma unroll
-      for (int i = 0; i < kUnitCols / 128; ++i) {
-        const int kk = 4 * (lane + 32 * i);
-        if (kk < kn) {
-#pragma unroll
-          for (int q = 0; q < kGroupTok; ++q) {
-            if (q < M) {
-              const uint2 xv = *reinterpret_cast<const uint2*>(&sxc[q][kk]);
-              float a = acc[q];
-              a = fmaf(wv[i].x, bf_lo(xv.x), a);
-              a = fmaf(wv[i].y, bf_hi(xv.x), a);
-              a = fmaf(wv[i].z, bf_lo(xv.y), a);
-              a = fmaf(wv[i].w, bf_hi(xv.y), a);
-              acc[q] = a;
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kGroupTok; ++q) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
-        if (lane == 0 && e < P.E && q < M) P.parts[((size_t)ks * M + q) * P.E + e] = acc[q];
-      }
-    }
-    __syncthreads();  // the unit's stores before thread 0's acquire-release add (and sxc free for the next unit)
-    if (t == 0) {
-      s_last = u < P.nunits && atom_add_acq_rel_gpu(&P.ctr[0], 1) == P.nunits - 1;
-      s_unit = u < P.nunits ? take_unit(P.ctr, P.nunits, G) : P.nunits;
-    }
-    __syncthreads();
-    if (s_last) {
-      // scores of every token (four at a time), warp t selects token t's experts
-      block_scores<J, 4, true>(P.parts, ksplit, M, 0, min(M, 4), P.E, P.scores, s_sc);
-      if (M > 4) block_scores<J, 4, true>(P.parts, ksplit, M, 4, M - 4, P.E, P.scores, s_sc + 4);
-      __syncthreads();
-      if (warp < M) {
-        float fv, wt;
-        int fi;
-        warp_select<8 * J>(s_sc[warp], P.E, P.k, fv, fi, wt);
-        if (lane < P.k) {
-          P.idx[(size_t)warp * P.k + lane] = fi;
-          P.w[(size_t)warp * P.k + lane] = wt;
-          eidx[warp * P.k + lane] = fi;
-        }
-      }
-      __syncthreads();
-      block_route_table(eidx, n, P.k, P.E, cnt, off, run, stok, eslot, P.table, true);
-      __syncthreads();  // every thread's table entries are written before the release
-      if (t == 0) {
-        P.ctr[0] = 0;
-        st_release_gpu(&P.ctr[3], 1);  // the routing is written
-      }
-    }
-    u = s_unit;
-    if (u >= P.nunits) break;  // (the last arrival's next ticket is always past the units)
-    load_unit(u);
-  }
-
-  // the routing, then this CTA's share of the slot rows
-  if (t == 0) {
-    const unsigned long long t0 = globaltimer();
-    int ok = 1;
-    while (ld_acquire_gpu(&P.ctr[3]) == 0) {
-      if (globaltimer() - t0 > P.wait_ns) {
-        atomicOr(P.err, DEV_ERR_TIMEOUT);
-        ok = 0;
-        break;
-      }
-      __nanosleep(64);
-    }
-    s_ok = ok;
-  }
-  __syncthreads();
-  if (s_ok) {
-    const TableLayout L(P.E, n);
-    for (int i = t; i < n; i += kThreads) stok[i] = ld_cg_s32(P.table + L.slot_token() + i);
-    __syncthreads();
-    const int H8 = H >> 3;
-    const long long total = (long long)n * H8;
-    const long long q0 = (long long)c * total / G, q1 = (long long)(c + 1) * total / G;
-    for (long long q = q0 + t; q < q1; q += kThreads) {
-      const int sl = (int)(q / H8), v = (int)(q - (long long)sl * H8);
-      *reinterpret_cast<uint4*>(P.xs + (size_t)sl * H + (size_t)v * 8) =
-          ld_act16(P.x + (size_t)stok[sl] * H + (size_t)v * 8);
-    }
-  }
-  __syncthreads();
-  if (t == 0 && atom_add_acq_rel_gpu(&P.ctr[2], 1) == G - 1) {
-    P.ctr[2] = 0;
-    P.ctr[3] = 0;
-  }
-  __syncthreads();
-  pdl_trigger();  // (after the reset: the next launch on these counters finds them clear)
-}
-
 template <int J>
 cudaError_t launch_front_j(dec_handle* h, const RouteSharedParams& P, int vpt, cudaStream_t s) {
   const dim3 g(2 * h->sms), b(kThreads);
@@ -1260,16 +1093,6 @@ cudaError_t launch_multi(dec_handle* h, const RouteSharedParams& P, int vpt, cud
   if (vpt == 1) return go(route_shared_multi_kernel<J, 1, MT>);
   if (vpt == 2) return go(route_shared_multi_kernel<J, 2, MT>);
   return go(route_shared_multi_kernel<J, 4, MT>);
-}
-
-template <int J>
-cudaError_t launch_group_j(dec_handle* h, const RouteGroupParams& P, cudaStream_t s) {
-  const size_t smem = (size_t)kGroupTok * kUnitCols * 2 + (size_t)kGroupTok * 256 * J * 4 +
-                      (size_t)(3 * P.E + 3 * P.M * P.k) * sizeof(int);
-  const cudaError_t e =
-      cudaFuncSetAttribute(route_group_kernel<J>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  return launch_k(h, route_group_kernel<J>, dim3(2 * h->sms), dim3(kThreads), smem, s, P);
 }
 
 }  // namespace
@@ -1409,37 +1232,6 @@ cudaError_t launch_moe_front_multi(dec_handle* h, int M, const uint16_t* h1, con
   if (Ew <= 32) return launch_front_multi<1, 4>(h, P, vpt, s);
   if (Ew <= 64) return launch_front_multi<2, 4>(h, P, vpt, s);
   return launch_front_multi<4, 4>(h, P, vpt, s);
-}
-
-bool route_group_supported(int M, int H, int E, int k) {
-  return M >= 1 && M <= kGroupTok && H >= 8 && H % 8 == 0 && E >= k && E <= 1024 && k >= 1 && k <= 16;
-}
-
-cudaError_t launch_route_group(dec_handle* h, int M, const uint16_t* x, const float* Wr, int H, int E, int k,
-                               float* parts, int* ctr, int32_t* idx, float* w, float* scores, int* table,
-                               uint16_t* xs, cudaStream_t s) {
-  if (!route_group_supported(M, H, E, k)) return cudaErrorInvalidValue;
-  RouteGroupParams P;
-  P.x = x;
-  P.Wr = Wr;
-  P.H = H;
-  P.E = E;
-  P.k = k;
-  P.M = M;
-  P.nunits = ((E + 7) / 8) * ((H + kUnitCols - 1) / kUnitCols);
-  P.parts = parts;
-  P.ctr = ctr;
-  P.idx = idx;
-  P.w = w;
-  P.scores = scores;
-  P.table = table;
-  P.xs = xs;
-  P.err = h->d_err;
-  P.wait_ns = h->wait_ns;
-  const int Ew = (E + 7) / 8;
-  if (Ew <= 32) return launch_group_j<1>(h, P, s);
-  if (Ew <= 64) return launch_group_j<2>(h, P, s);
-  return launch_group_j<4>(h, P, s);
 }
 
 }  // namespace dec
