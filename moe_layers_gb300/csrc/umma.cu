@@ -59,6 +59,9 @@ struct EngineParams {
 // Upper bound on the pieces one tile is split into: at most one per CTA, and
 // the grid never exceeds this (checked on the host).
 constexpr int kMaxPieces = 256;
+// How long the CTA that finishes a split tile waits for the other pieces
+// before it publishes its own and leaves the tile to the last publisher.
+constexpr uint64_t kFinishWaitNs = 5000;
 
 // 64-wide k sub-blocks per stage (build-time tunables; the defaults are the measured best).
 #ifndef DEC_ENGINE_KSUB_SINGLE
@@ -72,7 +75,7 @@ constexpr int kMaxPieces = 256;
 // CTAs can start beside the previous launch's and stream their first weights
 // while it drains.
 #ifndef DEC_ENGINE_SMEM_BUDGET
-#define DEC_ENGINE_SMEM_BUDGET (232448 - 1024 - 512 - 4 * kMaxPieces)
+#define DEC_ENGINE_SMEM_BUDGET (232448 - 1024 - 512 - 8 * kMaxPieces)
 #endif
 #ifndef DEC_ENGINE_CTAS_PER_SM
 #define DEC_ENGINE_CTAS_PER_SM 1
@@ -91,7 +94,7 @@ struct EngineSmem {
   static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kNumBars = 2 * kStages + 5;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kTotal = kMiscOff + 16 + 4 * kMaxPieces + 1024;  // + piece list + alignment slack
+  static constexpr int kTotal = kMiscOff + 32 + 8 * kMaxPieces + 1024;  // + two piece lists + alignment slack
   static constexpr uint32_t kTmemCols = NA * kMaxCols * 2; // two accumulator buffers
   static_assert(kStages >= 2, "engine ring too shallow");
   static_assert(kTotal <= 232448, "engine shared memory above the opt-in maximum");
@@ -136,8 +139,11 @@ __global__ void __launch_bounds__(kEngineThreads, DEC_ENGINE_CTAS_PER_SM)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kMiscOff + 4);
   volatile int* s_last = reinterpret_cast<volatile int*>(smem + S::kMiscOff + 8);
-  volatile int* s_np = reinterpret_cast<volatile int*>(smem + S::kMiscOff + 12);
-  int* s_piece = reinterpret_cast<int*>(smem + S::kMiscOff + 16);  // kMaxPieces ints
+  // Piece lists of split tiles, two by segment parity: the next segment's list
+  // is written while threads may still read the previous one.
+  volatile int* s_np = reinterpret_cast<volatile int*>(smem + S::kMiscOff + 12);    // [2]
+  volatile int* s_mine = reinterpret_cast<volatile int*>(smem + S::kMiscOff + 20);  // [2]
+  int* s_piece = reinterpret_cast<int*>(smem + S::kMiscOff + 32);                   // [2][kMaxPieces]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long G = gridDim.x, c = blockIdx.x;
@@ -345,35 +351,250 @@ __global__ void __launch_bounds__(kEngineThreads, DEC_ENGINE_CTAS_PER_SM)
       }
     };
 
-    for (long long j = j0; j < j1;) {
+    // The residual rows of a tile can be staged in shared memory with 16-byte copies.
+    const bool res_stageable = EPI == EPI_LINEAR && P.res != nullptr &&
+                               (reinterpret_cast<uintptr_t>(P.res) & 15) == 0 && (P.ldr & 7) == 0 && (P.N & 7) == 0;
+    const bool partials_aligned = (reinterpret_cast<uintptr_t>(P.partials) & 15) == 0;
+    constexpr int kOutBytes = (EPI == EPI_F32) ? 4 : 2;
+    // Output rows can take 16-byte stores.
+    const bool out_vec = (reinterpret_cast<uintptr_t>(P.out) & 15) == 0 && (P.ldo * kOutBytes) % 16 == 0;
+
+    // Copies this thread's row of the accumulator (all tokens, every
+    // accumulator) into shared memory laid out like a published partial:
+    // [NA][cnt][128] floats from `dst` (consecutive rows: no bank conflicts).
+    auto acc_to_smem = [&](float* dst, int cnt, uint32_t taddr) {
+      for (int ch = 0; ch < (cnt + 15) >> 4; ++ch) {
+        float v0[16], v1[16];
+        tmem_ld16(taddr + ch * 16, v0);
+        if (NA == 2) tmem_ld16(taddr + kMaxCols + ch * 16, v1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (ch * 16 + i < cnt) {
+            dst[(ch * 16 + i) * kTileN + row] = v0[i];
+            if (NA == 2) dst[(cnt + ch * 16 + i) * kTileN + row] = v1[i];
+          }
+      }
+    };
+
+    // Writes eight consecutive outputs (token t of the problem, columns
+    // [c, c + 8) with c < N) from their fp32 sums; `rs` holds the tile's staged
+    // residual rows ([cnt][128] bf16, column c - n0) or is null.
+    auto emit8 = [&](const Prob& pr, int t, int n0, int c, const float (&a0)[8], const float (&a1)[8],
+                     const uint16_t* rs) {
+      const long long orow = ((long long)pr.off + t) * P.ldo;
+      const bool vec = out_vec && c + 8 <= P.N;
+      if (EPI == EPI_F32) {
+        float* o = reinterpret_cast<float*>(P.out) + orow + c;
+        if (vec) {
+          reinterpret_cast<float4*>(o)[0] = make_float4(a0[0], a0[1], a0[2], a0[3]);
+          reinterpret_cast<float4*>(o)[1] = make_float4(a0[4], a0[5], a0[6], a0[7]);
+        } else {
+          for (int e = 0; e < 8 && c + e < P.N; ++e) o[e] = a0[e];
+        }
+        return;
+      }
+      uint16_t b[8];
+      if (EPI == EPI_SWIGLU) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) b[e] = swiglu_bf16(a0[e], a1[e]);
+      } else {
+        float r[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r[e] = 0.f;
+        if (rs != nullptr) {
+          const uint4 rv = *reinterpret_cast<const uint4*>(rs + t * kTileN + (c - n0));
+          const uint32_t w[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) r[e] = bf2f((uint16_t)(w[e >> 1] >> ((e & 1) * 16)));
+        } else if (P.res != nullptr) {
+          const uint16_t* rp = P.res + ((long long)pr.off + t) * P.ldr + c;
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (c + e < P.N) r[e] = bf2f(ld_act_u16(rp + e));
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) b[e] = f2bf(a0[e] + r[e]);
+      }
+      uint16_t* o = reinterpret_cast<uint16_t*>(P.out) + orow + c;
+      if (vec) {
+        *reinterpret_cast<uint4*>(o) = make_uint4(b[0] | ((uint32_t)b[1] << 16), b[2] | ((uint32_t)b[3] << 16),
+                                                  b[4] | ((uint32_t)b[5] << 16), b[6] | ((uint32_t)b[7] << 16));
+      } else {
+        for (int e = 0; e < 8 && c + e < P.N; ++e) o[e] = b[e];
+      }
+    };
+
+    // Finishes a split tile from its pieces staged in the ring's shared
+    // memory, which is idle once every MMA of the CTA has completed. The
+    // partials of every piece but `own` are copied in (16-byte copies through
+    // L2) with the tile's residual rows when they can be staged; piece `own`
+    // (`own` < 0: none) comes from this CTA's accumulator. Each thread then
+    // adds the pieces in k order (the sums of a reduction from the published
+    // partials) for eight consecutive columns of one token at a time, and
+    // stores them with one 16-byte store.
+    auto finish_staged = [&](const Prob& pr, int n0, uint32_t taddr, const int* pieces, int np, int own) {
+      const int cnt = pr.cnt;
+      const int acc_floats = cnt * kTileN;
+      const int piece_floats = NA * acc_floats;
+      float* sp = reinterpret_cast<float*>(smem);                                       // [np][NA][cnt][128]
+      uint16_t* sr = reinterpret_cast<uint16_t*>(smem + (size_t)np * piece_floats * 4);  // [cnt][128]
+      __threadfence();
+      for (int p = 0; p < np; ++p) {
+        if (p == own) continue;
+        const float* src = P.partials + (size_t)pieces[p] * P.slot_floats;
+        float* dst = sp + (size_t)p * piece_floats;
+#pragma unroll
+        for (int a = 0; a < NA; ++a)
+          for (int g = et; g < acc_floats / 4; g += 128)
+            cp_async16(dst + (size_t)a * acc_floats + g * 4, src + (size_t)a * P.cols * kTileN + g * 4);
+      }
+      if (res_stageable)
+        for (int g = et; g < cnt * (kTileN / 8); g += 128) {  // 8 columns per granule
+          const int t = g / (kTileN / 8), c8 = (g % (kTileN / 8)) * 8;
+          if (n0 + c8 < P.N) cp_async16(sr + t * kTileN + c8, P.res + ((long long)pr.off + t) * P.ldr + n0 + c8);
+        }
+      if (own >= 0) acc_to_smem(sp + (size_t)own * piece_floats, cnt, taddr);
+      cp_async_wait_all();
+      named_bar_sync(1, 128);
+      for (int g = et; g < cnt * (kTileN / 8); g += 128) {
+        const int t = g / (kTileN / 8), c8 = (g % (kTileN / 8)) * 8;
+        if (n0 + c8 >= P.N) continue;
+        float a0[8], a1[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a0[e] = a1[e] = 0.f;
+        const float* base = sp + t * kTileN + c8;
+        // Pieces four at a time: every load of a batch before any add.
+        for (int p0 = 0; p0 < np; p0 += 4) {
+          float4 x[4][2], y[4][2];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const float4* s4 = reinterpret_cast<const float4*>(base + (size_t)min(p0 + qq, np - 1) * piece_floats);
+            x[qq][0] = s4[0];
+            x[qq][1] = s4[1];
+            if (NA == 2) {
+              y[qq][0] = s4[acc_floats / 4];
+              y[qq][1] = s4[acc_floats / 4 + 1];
+            }
+          }
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+            if (p0 + qq < np) {
+              const float v[8] = {x[qq][0].x, x[qq][0].y, x[qq][0].z, x[qq][0].w,
+                                  x[qq][1].x, x[qq][1].y, x[qq][1].z, x[qq][1].w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) a0[e] += v[e];
+              if (NA == 2) {
+                const float u[8] = {y[qq][0].x, y[qq][0].y, y[qq][0].z, y[qq][0].w,
+                                    y[qq][1].x, y[qq][1].y, y[qq][1].z, y[qq][1].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a1[e] += u[e];
+              }
+            }
+        }
+        emit8(pr, t, n0, n0 + c8, a0, a1, res_stageable ? sr : nullptr);
+      }
+    };
+
+    // Publishes this thread's share of a piece's partial from the accumulator
+    // staged in shared memory (the ring is idle): 16-byte stores.
+    auto publish_staged = [&](float* slot, int cnt, uint32_t taddr) {
+      float* sp = reinterpret_cast<float*>(smem);
+      acc_to_smem(sp, cnt, taddr);
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int a = 0; a < NA; ++a)
+        for (int g = et; g < cnt * kTileN / 4; g += 128)
+          reinterpret_cast<float4*>(slot + (size_t)a * P.cols * kTileN)[g] =
+              reinterpret_cast<const float4*>(sp + (size_t)a * cnt * kTileN)[g];
+    };
+
+    int seg = 0;  // segments so far (parity selects the piece list)
+    for (long long j = j0; j < j1; ++seg) {
       const int tau = (int)(j / KB), kb0 = (int)(j % KB);
       const int kb1 = (int)min((long long)KB, kb0 + (j1 - j));
       const bool first_seg = (j == j0);
       j += kb1 - kb0;
+      const bool last_seg = (j == j1);
+      const bool whole = (kb0 == 0 && kb1 == KB);
+      const int lp = seg & 1;
+      int* pieces = s_piece + lp * kMaxPieces;
+      if (!whole && et == 0) {
+        // The non-empty CTAs that hold pieces of this tile, in k order, their
+        // partial slots and this CTA's place among them (computed while the
+        // MMAs run: it takes 64-bit divisions).
+        const long long kfirst = (long long)tau * KB;
+        const long long c_first = cta_of(kfirst, W, G), c_last = cta_of(kfirst + KB - 1, W, G);
+        int np = 0, mine = 0;
+        for (long long cc = c_first; cc <= c_last; ++cc) {
+          const long long st = range_start(cc, W, G);
+          if (range_start(cc + 1, W, G) <= st) continue;
+          if (cc == c) mine = np;
+          if (np < kMaxPieces) pieces[np] = (int)(cc * 2 + ((st >= kfirst) ? 0 : 1));
+          ++np;
+        }
+        s_np[lp] = np;
+        s_mine[lp] = mine;
+      }
       const bool got = mbar_wait(&tfull[buf], tphase[buf], wc);
       if (!named_bar_and(1, 128, got)) break;  // leave together if any thread gave up
       tc_fence_after();
       const Prob pr = prob_info(P, tau / tiles);
-      const int n = (tau % tiles) * kTileN + row;
+      const int n0 = (tau % tiles) * kTileN;
+      const int n = n0 + row;
       const bool valid_row = n < P.N;
       const int nch = (pr.cnt + 15) >> 4;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NA * kMaxCols);
-      const bool whole = (kb0 == 0 && kb1 == KB);
+      const size_t piece_bytes = (size_t)NA * pr.cnt * kTileN * 4;
+      const size_t res_bytes = res_stageable ? (size_t)pr.cnt * kTileN * 2 : 0;
+      if (!whole) {
+        if (et == 0) {
+          // The CTA that holds the tile's first piece (the end of its range, so
+          // its ring is idle by now) finishes the tile: it waits a bounded time
+          // for the other pieces, then adds them to its own accumulator without
+          // publishing it. Past the bound it publishes like the others, and
+          // whichever CTA publishes last finishes the tile.
+          const int np = s_np[lp];
+          int mode = 0;
+          if (s_mine[lp] == 0 && last_seg && partials_aligned && np <= kMaxPieces &&
+              (size_t)np * piece_bytes + res_bytes <= (size_t)S::kBarOff) {
+            const uint64_t t0 = globaltimer();
+            int arrived;
+            while ((arrived = ld_acquire_gpu(&P.counters[tau])) < np - 1 && globaltimer() - t0 < kFinishWaitNs) {
+            }
+            if (arrived == np - 1) mode = 2;
+          }
+          *s_last = mode;
+        }
+        named_bar_sync(1, 128);
+        if (*s_last == 2) {
+          finish_staged(pr, n0, taddr, pieces, s_np[lp], s_mine[lp]);
+          tc_fence_before();
+          mbar_arrive(&tempty[buf]);
+          tphase[buf] ^= 1u;
+          buf ^= 1;
+          if (et == 0) P.counters[tau] = 0;  // leave the workspace reusable
+          continue;
+        }
+      }
       float* slot = nullptr;
       if (!whole) slot = P.partials + (size_t)(c * 2 + (first_seg ? 0 : 1)) * P.slot_floats;
-      for (int ch = 0; ch < nch; ++ch) {
-        float v0[16], v1[16];
-        tmem_ld16(taddr + ch * 16, v0);
-        if (NA == 2) tmem_ld16(taddr + kMaxCols + ch * 16, v1);
-        if (whole) {
-          if (valid_row) emit_chunk(pr, n, ch, v0, v1);
-        } else {
+      if (!whole && last_seg && partials_aligned && piece_bytes <= (size_t)S::kBarOff) {
+        publish_staged(slot, pr.cnt, taddr);
+      } else {
+        for (int ch = 0; ch < nch; ++ch) {
+          float v0[16], v1[16];
+          tmem_ld16(taddr + ch * 16, v0);
+          if (NA == 2) tmem_ld16(taddr + kMaxCols + ch * 16, v1);
+          if (whole) {
+            if (valid_row) emit_chunk(pr, n, ch, v0, v1);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int jc = ch * 16 + i;
-            if (jc < pr.cnt) {
-              slot[(size_t)jc * kTileN + row] = v0[i];
-              if (NA == 2) slot[(size_t)P.cols * kTileN + (size_t)jc * kTileN + row] = v1[i];
+            for (int i = 0; i < 16; ++i) {
+              const int jc = ch * 16 + i;
+              if (jc < pr.cnt) {
+                slot[(size_t)jc * kTileN + row] = v0[i];
+                if (NA == 2) slot[(size_t)P.cols * kTileN + (size_t)jc * kTileN + row] = v1[i];
+              }
             }
           }
         }
@@ -384,28 +605,21 @@ __global__ void __launch_bounds__(kEngineThreads, DEC_ENGINE_CTAS_PER_SM)
       buf ^= 1;
       if (whole) continue;
 
-      // Split tile: the last of its CTAs to finish adds all pieces in k order.
+      // Published piece: the CTA whose arrival completes the count finishes the
+      // tile (the first piece's CTA counts only when it gave up waiting).
       __threadfence();
       named_bar_sync(1, 128);
-      const long long kfirst = (long long)tau * KB;
-      const long long c_first = cta_of(kfirst, W, G), c_last = cta_of(kfirst + KB - 1, W, G);
       if (et == 0) {
-        // The non-empty CTAs that hold pieces of this tile, in k order, and their partial slots.
-        int np = 0;
-        for (long long cc = c_first; cc <= c_last; ++cc) {
-          const long long st = range_start(cc, W, G);
-          if (range_start(cc + 1, W, G) <= st) continue;
-          if (np < kMaxPieces) s_piece[np] = (int)(cc * 2 + ((st >= kfirst) ? 0 : 1));
-          ++np;
-        }
         const int old = atomicAdd(&P.counters[tau], 1);
-        *s_last = (old == np - 1) ? 1 : 0;
-        *s_np = np;
+        *s_last = (old == s_np[lp] - 1) ? 1 : 0;
       }
       named_bar_sync(1, 128);
-      if (*s_last) {
+      if (!*s_last) continue;
+      const int np = min(s_np[lp], kMaxPieces);
+      if (last_seg && partials_aligned && (size_t)np * piece_bytes + res_bytes <= (size_t)S::kBarOff) {
+        finish_staged(pr, n0, taddr, pieces, np, -1);
+      } else {
         __threadfence();
-        const int np = min(*s_np, kMaxPieces);
         // The pieces' partials are read RB pieces at a time, every load of a
         // batch issued before any is added (one L2 round trip per batch, not
         // per piece), and added in k order (the same sums as one by one).
@@ -419,7 +633,7 @@ __global__ void __launch_bounds__(kEngineThreads, DEC_ENGINE_CTAS_PER_SM)
 #pragma unroll
             for (int q = 0; q < RB; ++q) {
               const int p = p0 + q < np ? p0 + q : p0;
-              const float* ps = P.partials + (size_t)s_piece[p] * P.slot_floats + (size_t)ch * 16 * kTileN + row;
+              const float* ps = P.partials + (size_t)pieces[p] * P.slot_floats + (size_t)ch * 16 * kTileN + row;
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 const bool ok = p0 + q < np && ch * 16 + i < pr.cnt;
@@ -440,8 +654,8 @@ __global__ void __launch_bounds__(kEngineThreads, DEC_ENGINE_CTAS_PER_SM)
           }
           if (valid_row) emit_chunk(pr, n, ch, a0, a1);
         }
-        if (et == 0) P.counters[tau] = 0;  // leave the workspace reusable
       }
+      if (et == 0) P.counters[tau] = 0;  // leave the workspace reusable
     }
   }
 

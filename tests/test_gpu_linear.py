@@ -77,10 +77,14 @@ def test_linear_integer_exact_bit_for_bit(h, M):
 
 
 @pytest.mark.parametrize("M", [1, 2, 4, 64])
-def test_linear_residual_and_alias(h, M):
+@pytest.mark.parametrize("N,K", [(520, 704), (1001, 4096), (1000, 8192)])
+def test_linear_residual_and_alias(h, M, N, K):
+    """Residual add, also in place. On the split-K kernel (M > 2) the shapes
+    split every 128-row tile into pieces over several CTAs, so the tile is
+    finished by the reduction of its pieces, with the residual rows staged in
+    shared memory (N a multiple of 8) or read from global memory (N = 1001)."""
     import moe_layers_gb300 as ML
-    N, K = 520, 704
-    x, W = _mats(M, N, K, 700 + M)
+    x, W = _mats(M, N, K, 700 + M + N)
     r = synth.bf16(M * N, SEED, synth.R_BASE + M, 0, 1.0).reshape(M, N)
     ref = oracle.linear_residual(x, W, r)
     out = ML.dec_linear_residual(h, dev_bf16(x, (M, K)), dev_bf16(W, (N, K)), dev_bf16(r, (M, N)))
