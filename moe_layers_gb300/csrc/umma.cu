@@ -51,9 +51,9 @@ struct EngineParams {
 
 // Shared-memory plan of one engine instantiation. A stage holds KSUB 64-wide
 // k sub-blocks of NA weight tiles (128 rows x 64 bf16 = 16 KB each, 128-byte
-// swizzle) and of the activation tile (BROWS rows). Single-matrix kernels
-// take two sub-blocks per stage; the SwiGLU kernel already loads two weight
-// tiles (gate and up). The activation slice is sized to the batch, and the
+// swizzle) and of the activation tile (BROWS rows); the SwiGLU kernel loads
+// two weight tiles (gate and up) per sub-block. The activation slice is sized
+// to the batch, and the
 // ring takes as many stages as the 227 KB of shared memory allow: the weight
 // bytes in flight per SM are what sets the streaming rate.
 // Upper bound on the pieces one tile is split into: at most one per CTA, and
@@ -63,9 +63,22 @@ constexpr int kMaxPieces = 256;
 // before it publishes its own and leaves the tile to the last publisher.
 constexpr uint64_t kFinishWaitNs = 5000;
 
-// 64-wide k sub-blocks per stage (build-time tunables; the defaults are the measured best).
-#ifndef DEC_ENGINE_KSUB_SINGLE
-#define DEC_ENGINE_KSUB_SINGLE 2
+// 64-wide k sub-blocks per stage, by the stage's activation rows (16 / 32 /
+// 64) for single-matrix kernels, and for the SwiGLU pair (build-time
+// tunables; the defaults are the measured best). Wider stages read more
+// contiguous bytes of each weight row per stage: with 64 activation rows, 4
+// sub-blocks (2 stages of 96 KB) stream faster than 2 (4 stages of 48 KB)
+// with the same weight bytes in flight; with 16 rows, 3 sub-blocks (4 stages
+// of 54 KB) beat 2 and 4. The last k-block of a row may reach past K: those
+// columns load as zeros.
+#ifndef DEC_ENGINE_KSUB_R16
+#define DEC_ENGINE_KSUB_R16 3
+#endif
+#ifndef DEC_ENGINE_KSUB_R32
+#define DEC_ENGINE_KSUB_R32 4
+#endif
+#ifndef DEC_ENGINE_KSUB_R64
+#define DEC_ENGINE_KSUB_R64 4
 #endif
 #ifndef DEC_ENGINE_KSUB_PAIR
 #define DEC_ENGINE_KSUB_PAIR 1
@@ -83,7 +96,10 @@ constexpr uint64_t kFinishWaitNs = 5000;
 
 template <int NA, int BROWS>
 struct EngineSmem {
-  static constexpr int kKSub = (NA == 1) ? DEC_ENGINE_KSUB_SINGLE : DEC_ENGINE_KSUB_PAIR;
+  static constexpr int kKSub = (NA == 2)        ? DEC_ENGINE_KSUB_PAIR
+                               : (BROWS == 16) ? DEC_ENGINE_KSUB_R16
+                               : (BROWS == 32) ? DEC_ENGINE_KSUB_R32
+                                               : DEC_ENGINE_KSUB_R64;
   static constexpr int kBK = kBlockK * kKSub;              // reduction elements per k-block (stage)
   static constexpr int kABox = kTileN * kBlockK * 2;       // 16 KB weight box
   static constexpr int kBBox = BROWS * kBlockK * 2;        // activation box of one sub-block
