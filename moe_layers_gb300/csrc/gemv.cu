@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
       for (int m = 0; m < M; ++m) {
         float a = 0.f;
 #pragma unroll
-        for (int i = 0; i < VPT; ++i) a = dot8(wa[r][i], xr[m][i], a);
+        for (int i = 0; i < VPT; ++i) a = M == 1 ? dot8_widened(wa[r][i], xr[m][i], a) : dot8(wa[r][i], xr[m][i], a);
         acc[r][m] = a;
       }
 #pragma unroll
