@@ -20,13 +20,25 @@ namespace dec {
 constexpr int kRouterChunk = 1024;  // reduction elements per split (one CTA column)
 constexpr int kRouterRows = 8;      // router rows per CTA, one per warp
 constexpr int kRouterTok = 4;       // tokens staged in shared memory per pass (8 KB: co-resides with the engine)
+// Tokens per CTA (grid z; build-time tunable). Measured (layer step, one box):
+// groups of 16 tokens make the router launch faster at 64 tokens (34.0 against
+// 40.9 us event-timed) but the step slower at 32 (2418.3 against 2405.4 us):
+// the extra CTAs compete for SMs with the shared expert on the side stream.
+#ifndef DEC_ROUTER_GROUP
+#define DEC_ROUTER_GROUP 64
+#endif
+constexpr int kRouterGroup = DEC_ROUTER_GROUP;
 
 int router_ksplit(int H) { return (H + kRouterChunk - 1) / kRouterChunk; }
 
 // parts[ks][t][e] = sum over the ks-th chunk of H of x[t][h] * Wr[e][h] (fp32).
-// Grid: (ceil(E / 8), ksplit). Each warp owns one router row and keeps its
-// chunk of fp32 weights in registers (loaded before the dependency wait); the
-// tokens' bf16 activations pass through shared memory four at a time.
+// Grid: (ceil(E / 8), ksplit, ceil(M / kRouterGroup)). Each warp owns one
+// router row and keeps its chunk of fp32 weights in registers (loaded before
+// the dependency wait); the CTA's group of tokens passes through shared
+// memory four at a time, the next four tokens' activations loaded into
+// registers while the current four are multiplied. Every partial sum is the
+// same whatever the grid: the token groups only spread the work over more
+// CTAs (the router matrix, 11 MB at the workload's size, is re-read from L2).
 __global__ void __launch_bounds__(256) router_kernel(const uint16_t* x, const float* __restrict__ Wr, int M, int H,
                                                      int E, float* parts) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -34,6 +46,7 @@ __global__ void __launch_bounds__(256) router_kernel(const uint16_t* x, const fl
   const int ks = blockIdx.y;
   const int k0 = ks * kRouterChunk;
   const int kn = min(kRouterChunk, H - k0);
+  const int tg0 = blockIdx.z * kRouterGroup, tg1 = min(M, tg0 + kRouterGroup);
   __shared__ __align__(16) uint16_t xs[kRouterTok][kRouterChunk];
   pdl_trigger();
   float4 wv[kRouterChunk / 128];
@@ -45,14 +58,29 @@ __global__ void __launch_bounds__(256) router_kernel(const uint16_t* x, const fl
   }
   pdl_wait();
   const int kv = kn >> 3;
-  for (int t0 = 0; t0 < M; t0 += kRouterTok) {
-    const int nt = min(kRouterTok, M - t0);
-    __syncthreads();
-    for (int q = threadIdx.x; q < nt * kv; q += blockDim.x) {
-      const int tt = q / kv, v = q - tt * kv;
-      *reinterpret_cast<uint4*>(&xs[tt][v * 8]) = ld_act16(x + (size_t)(t0 + tt) * H + k0 + v * 8);
+  // This thread's share of a pass's activation vectors: q = threadIdx.x + 256 j.
+  constexpr int kQ = kRouterTok * (kRouterChunk / 8) / 256;
+  uint4 xr[kQ];
+  auto load_pass = [&](int t0) {
+    const int nt = min(kRouterTok, tg1 - t0);
+#pragma unroll
+    for (int j = 0; j < kQ; ++j) {
+      const int q = threadIdx.x + 256 * j;
+      const int tt = q / (kRouterChunk / 8), v = q % (kRouterChunk / 8);
+      xr[j] = (tt < nt && v < kv) ? ld_act16(x + (size_t)(t0 + tt) * H + k0 + v * 8) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  if (tg0 < tg1) load_pass(tg0);
+  for (int t0 = tg0; t0 < tg1; t0 += kRouterTok) {
+    const int nt = min(kRouterTok, tg1 - t0);
+    __syncthreads();  // the previous pass's readers are done
+#pragma unroll
+    for (int j = 0; j < kQ; ++j) {
+      const int q = threadIdx.x + 256 * j;
+      *reinterpret_cast<uint4*>(&xs[q / (kRouterChunk / 8)][(q % (kRouterChunk / 8)) * 8]) = xr[j];
     }
     __syncthreads();
+    if (t0 + kRouterTok < tg1) load_pass(t0 + kRouterTok);
     float acc[kRouterTok];
 #pragma unroll
     for (int tt = 0; tt < kRouterTok; ++tt) acc[tt] = 0.f;
@@ -234,11 +262,30 @@ __global__ void __launch_bounds__(256) route_table_kernel(const int32_t* idx, in
   for (int i = tid; i < n; i += blockDim.x) eidx[i] = ld_act_s32(idx + i);
   __syncthreads();
   block_route_table(eidx, n, k, E, cnt, off, run, stok, eslot, table, blockIdx.x == 0);
+  // The gather: four 16-byte vectors per thread in flight (all loads of a
+  // group issued before its stores), then the remainder one at a time.
   const int H8 = H >> 3;
   const long long total = (long long)n * H8;
-  for (long long q = (long long)blockIdx.x * blockDim.x + tid; q < total; q += (long long)gridDim.x * blockDim.x) {
-    const int s = (int)(q / H8), v = (int)(q - (long long)s * H8);
-    *reinterpret_cast<uint4*>(xs + (size_t)s * H + (size_t)v * 8) = ld_act16(x + (size_t)stok[s] * H + (size_t)v * 8);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  long long q = (long long)blockIdx.x * blockDim.x + tid;
+  for (; q + 3 * stride < total; q += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const long long qu = q + u * stride;
+      const int s = (int)(qu / H8), c = (int)(qu - (long long)s * H8);
+      v[u] = ld_act16(x + (size_t)stok[s] * H + (size_t)c * 8);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const long long qu = q + u * stride;
+      const int s = (int)(qu / H8), c = (int)(qu - (long long)s * H8);
+      *reinterpret_cast<uint4*>(xs + (size_t)s * H + (size_t)c * 8) = v[u];
+    }
+  }
+  for (; q < total; q += stride) {
+    const int s = (int)(q / H8), c = (int)(q - (long long)s * H8);
+    *reinterpret_cast<uint4*>(xs + (size_t)s * H + (size_t)c * 8) = ld_act16(x + (size_t)stok[s] * H + (size_t)c * 8);
   }
 }
 
@@ -285,7 +332,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* y, const int*
 // ---------------------------------------------------------------------------- launchers
 cudaError_t launch_router(dec_handle* h, const uint16_t* x, const float* Wr, int M, int H, int E, float* parts,
                           cudaStream_t s) {
-  const dim3 grid((E + kRouterRows - 1) / kRouterRows, router_ksplit(H));
+  const dim3 grid((E + kRouterRows - 1) / kRouterRows, router_ksplit(H), (M + kRouterGroup - 1) / kRouterGroup);
   return launch_k(h, router_kernel, grid, dim3(256), 0, s, x, Wr, M, H, E, parts);
 }
 
