@@ -101,14 +101,14 @@ def step_bytes(M: int, U: float) -> float:
 # sha256 of the listed files at capture time); null otherwise.
 NCU_TRAFFIC = {
     # one-token MoE front launch: dram__bytes_read.sum + dram__bytes_write.sum of two launches of one
-    # ncu capture on the 32-expert bank (read 529,541,376 / 529,542,912 B, write 2,996,992 /
-    # 64,768 B), scaled to the 384-expert workload: at one token a launch reads what it reads
+    # ncu capture on the 32-expert bank (read 529,536,512 / 529,547,776 B, write 3,065,344 /
+    # 241,152 B), scaled to the 384-expert workload: at one token a launch reads what it reads
     # with 384 experts except the router, 352 x 7168 x 4 B more.
-    ("moe_front", 1): {"bytes": (529541376 + 529542912) // 2 + (384 - 32) * 7168 * 4 + (2996992 + 64768) // 2,
+    ("moe_front", 1): {"bytes": (529536512 + 529547776) // 2 + (384 - 32) * 7168 * 4 + (3065344 + 241152) // 2,
                        "sources": ("moe_layers_gb300/csrc/route_shared.cu", "moe_layers_gb300/csrc/topk.cuh",
                                    "moe_layers_gb300/csrc/common.cuh", "moe_layers_gb300/csrc/internal.h",
                                    "moe_layers_gb300/csrc/api.cu"),
-                       "sha256": "acbd9cbedccda1d6368e18d4d8929391b46167985df9e7f4ab57f8937436e1ce"},
+                       "sha256": "a4bf807d2488fc1f89b9f4821ea1978bd0ee1bb9a478bd9d1f1784aa9bf080f5"},
 }
 
 

@@ -132,6 +132,33 @@ def test_input_projection_batch_sweep(h, w_in, M):
     assert_bf16_close(host_bits(y), oracle.linear(x, w_in), f"in-proj M={M}")
 
 
+@pytest.mark.parametrize("N,K", [(3001, 7168), (4096, 4096), (1000, 1024)])
+def test_mixed_precision_fma_matches_widened(h, N, K):
+    """The two-token small-matrix kernel multiplies bf16 operands with fp32
+    fused multiply-adds (fma.rn.f32.bf16); the one-token kernel widens them to
+    fp32 first. The product of two bf16 values is exact in fp32 and the
+    per-row reduction order is the same, so two copies of a token must give
+    the one-token output bit for bit. The narrow kernel (K <= 1024) takes the
+    mixed form at every batch, so there the two calls are compared with the
+    oracle only."""
+    import moe_layers_gb300 as ML
+    x1, W = _mats(1, N, K, 820 + K % 97)
+    x2 = np.concatenate([x1, x1], axis=0)
+    Wd = dev_bf16(W, (N, K))
+    h.set_force_variant(ML.VARIANT_SMALL_M)
+    try:
+        y1 = host_bits(ML.dec_linear(h, dev_bf16(x1, (1, K)), Wd))
+        y2 = host_bits(ML.dec_linear(h, dev_bf16(x2, (2, K)), Wd))
+    finally:
+        h.set_force_variant(ML.VARIANT_AUTO)
+    ref = oracle.linear(x1, W)
+    assert_bf16_close(y1, ref, f"M=1 N={N} K={K}")
+    assert_bf16_close(y2[1:], ref, f"M=2 N={N} K={K}")
+    assert np.array_equal(y2[0], y2[1]), "the two copies of the token differ"
+    if K > 1024:
+        assert np.array_equal(y1[0], y2[0]), "mixed-precision FMA differs from the widened form"
+
+
 def test_automatic_choice_by_size(h):
     """Up to four tokens a matrix of at most 48 MB stays on the small-matrix
     kernel (the split-K kernel's per-launch cost outweighs its rate there)."""
