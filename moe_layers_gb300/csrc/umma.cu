@@ -4,12 +4,13 @@
 // Kimi K3 article, Part 1 §1 "Ajustar las formas": at batch sizes above two
 // the projection is a split-K kernel that shares the matrix product among
 // more GPU workers. Here a "worker" is an SM: the weight matrix is cut into
-// tiles of 128 rows, each tile into k-blocks of 64 columns, and the sequence
-// of all (tile, k-block) pairs is divided into one contiguous, equal-length
-// range per CTA (one persistent CTA per SM). Every SM therefore streams the
-// same number of weight bytes; a tile that straddles two ranges is finished by
-// whichever of its CTAs arrives last, which adds the fp32 partials of all
-// pieces in k order (deterministic, no float atomics).
+// tiles of 128 rows, each tile into k-blocks of 64 x KSUB columns (one ring
+// stage each), and the sequence of all (tile, k-block) pairs is divided into
+// one contiguous, equal-length range per CTA (one persistent CTA per SM).
+// Every SM therefore streams the same number of weight bytes. A tile that
+// straddles several ranges is finished by the CTA that holds its first piece
+// (the end of that CTA's range): it adds the fp32 partials of all pieces in k
+// order (deterministic, no float atomics), its own from its accumulator.
 //
 // Per CTA: warp 0 issues TMA loads of weight tiles (128 x 64 bf16, 128-byte
 // swizzle, evict-first) and activation tiles (16-row boxes) into an smem ring;
