@@ -787,7 +787,7 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=1, help="headline batch M (1..64)")
     ap.add_argument("--sweep", default="1,2,4,8,16,32,64")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--repeats", type=int, default=3, help="CUDA-graph replays per timed point (median reported)")
+    ap.add_argument("--repeats", type=int, default=5, help="CUDA-graph replays per timed point (median reported)")
     ap.add_argument("--configs", default="proj4096,in_proj,out_proj,moe",
                     help="the workload's other configurations, each timed alone (comma list; empty for none): "
                          "proj4096 (4096x4096 projection, M=1), in_proj (7168->12288, M=1..64), out_proj "
