@@ -385,6 +385,19 @@ dec_status dec_test_routing_wait_timeout(dec_handle* h, int tokens, cudaStream_t
  * expert. */
 dec_status dec_test_set_moe_front(dec_handle* h, int enable);
 
+/* How the split-K kernel finishes a tile split between CTAs (a tile's partial
+ * sums from several CTAs' ranges of k). 0 (default): the CTA holding the
+ * first piece waits a bounded time for the others, then adds all pieces in k
+ * order from shared memory; past the bound it publishes its piece, and the
+ * CTA that completes the count finishes the tile. 1: every CTA publishes its
+ * piece at once, so the tile is always finished by the CTA that completes the
+ * count (from shared memory when that CTA is at the end of its range). 2: as
+ * 1, and the finishing CTA always reads the pieces with batched loads from
+ * L2. All three add the same fp32 partials in the same k order, so they give
+ * the same bits; the hook lets tests check that. Other values:
+ * DEC_ERR_INVALID_ARG. */
+dec_status dec_test_set_engine_finish(dec_handle* h, int mode);
+
 /* Hold `ctas` SMs (1 <= ctas <= the device's SM count) for hold_ns
  * nanoseconds (at most 2 s) with a kernel on `stream`: one CTA per SM that
  * takes the whole per-block shared memory, so nothing else fits beside it,

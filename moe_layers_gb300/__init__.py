@@ -75,6 +75,7 @@ def _load():
         "dec_set_shared_sms": [P, I],
         "dec_set_l2_ahead": [P, I],
         "dec_test_set_moe_front": [P, I],
+        "dec_test_set_engine_finish": [P, I],
         "dec_check_device_error": [P],
         "dec_linear_workspace_size": [P, I, I, I, ctypes.POINTER(Z)],
         "dec_linear": [P, P, I, P, P, I, I, I, P, Z, P],
@@ -204,6 +205,10 @@ class Handle:
     def test_set_moe_front(self, enable: bool) -> None:
         """Test hook: False runs the path taken where an MoE front does not apply."""
         _check(_load().dec_test_set_moe_front(self._h, 1 if enable else 0), "dec_test_set_moe_front")
+
+    def test_set_engine_finish(self, mode: int) -> None:
+        """Test hook: how the split-K kernel finishes split tiles (0 default; 1, 2 the fallback paths)."""
+        _check(_load().dec_test_set_engine_finish(self._h, int(mode)), "dec_test_set_engine_finish")
 
     def set_l2_ahead(self, nbytes: int) -> None:
         _check(_load().dec_set_l2_ahead(self._h, int(nbytes)), "dec_set_l2_ahead")

@@ -718,6 +718,12 @@ dec_status dec_test_set_moe_front(dec_handle* h, int enable) {
   return DEC_OK;
 }
 
+dec_status dec_test_set_engine_finish(dec_handle* h, int mode) {
+  if (h == nullptr || mode < 0 || mode > 2) return DEC_ERR_INVALID_ARG;
+  h->engine_finish = mode;
+  return DEC_OK;
+}
+
 dec_status dec_set_l2_ahead(dec_handle* h, int bytes) {
   if (h == nullptr || bytes < 0 || bytes > (16 << 20)) return DEC_ERR_INVALID_ARG;
   h->l2_ahead = bytes;

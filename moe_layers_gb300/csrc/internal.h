@@ -25,6 +25,7 @@ struct dec_handle {
   int last_expert_variant = 0;      // kernel family of the most recent expert launches
   int shared_ctas = 0;              // CTAs for the shared expert's kernels (0 = default)
   int moe_front = 1;                // one to a few tokens: the MoE front launches (0: test hook, the fallback path)
+  int engine_finish = 0;            // split-K split-tile finish (test hook: 1, 2 force the fallback paths)
   int l2_ahead = 49152;             // small-matrix kernels: weight bytes per CTA requested into L2 ahead
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   // measurement

@@ -48,6 +48,7 @@ struct EngineParams {
   int* counters;
   int* err;
   unsigned long long wait_ns;
+  int finish;  // split-tile finish: 0 first piece's CTA; 1 the last to publish; 2 as 1, from L2 (test hook)
 };
 
 // Shared-memory plan of one engine instantiation. A stage holds KSUB 64-wide
@@ -572,7 +573,7 @@ __global__ void __launch_bounds__(kEngineThreads, DEC_ENGINE_CTAS_PER_SM)
           // whichever CTA publishes last finishes the tile.
           const int np = s_np[lp];
           int mode = 0;
-          if (s_mine[lp] == 0 && last_seg && partials_aligned && np <= kMaxPieces &&
+          if (P.finish == 0 && s_mine[lp] == 0 && last_seg && partials_aligned && np <= kMaxPieces &&
               (size_t)np * piece_bytes + res_bytes <= (size_t)S::kBarOff) {
             const uint64_t t0 = globaltimer();
             int arrived;
@@ -633,7 +634,8 @@ __global__ void __launch_bounds__(kEngineThreads, DEC_ENGINE_CTAS_PER_SM)
       named_bar_sync(1, 128);
       if (!*s_last) continue;
       const int np = min(s_np[lp], kMaxPieces);
-      if (last_seg && partials_aligned && (size_t)np * piece_bytes + res_bytes <= (size_t)S::kBarOff) {
+      if (P.finish <= 1 && last_seg && partials_aligned &&
+          (size_t)np * piece_bytes + res_bytes <= (size_t)S::kBarOff) {
         finish_staged(pr, n0, taddr, pieces, np, -1);
       } else {
         __threadfence();
@@ -775,6 +777,7 @@ cudaError_t launch_engine(dec_handle* h, const EngineLaunch& L, cudaStream_t s) 
   P.counters = L.counters;
   P.err = h->d_err;
   P.wait_ns = h->wait_ns;
+  P.finish = h->engine_finish;
   const int grid = L.grid > 0 ? L.grid : engine_grid(h);
   if (grid > kMaxPieces) return cudaErrorInvalidConfiguration;
   const int max_cols = L.count;  // dense: the tokens; grouped: the batch, a bound on any expert's tokens

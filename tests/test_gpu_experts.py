@@ -78,6 +78,37 @@ def test_experts_small(h, M, E, H, I, k, shared, resid, skew, family):
     assert h.check_device_error() == ML.DEC_OK
 
 
+@pytest.mark.parametrize("M,E,H,I,k", [(8, 16, 1024, 512, 4), (64, 24, 768, 256, 8)])
+def test_split_tile_finish_paths_give_the_same_bits(h, M, E, H, I, k):
+    """The split-K kernel's three ways of finishing a tile split between CTAs
+    (the first piece's CTA from shared memory; the CTA that completes the count;
+    the same with the pieces read from L2) add the same fp32 partials in the
+    same k order: the grouped experts' outputs agree bit for bit."""
+    import torch
+    import moe_layers_gb300 as ML
+    rng = np.random.default_rng(M * 7 + E)
+    g, u, d = _small_bank(E, H, I, 4600 + E)
+    x = synth.bf16(M * H, SEED, 4700 + M, 0, 1.0).reshape(M, H)
+    idx, w = _routing(M, E, k, rng, False)
+    sh = tuple(synth.bf16(n, SEED, 4800 + i, 0, 0.05).reshape(shape)
+               for i, (n, shape) in enumerate([(I * H, (I, H)), (I * H, (I, H)), (H * I, (H, I))]))
+    r = synth.bf16(M * H, SEED, 4900 + M, 0, 1.0).reshape(M, H)
+    outs = []
+    try:
+        for mode in (0, 1, 2):
+            h.test_set_engine_finish(mode)
+            out = ML.moe_experts(h, dev_bf16(x, (M, H)), torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(),
+                                 dev_bf16(g, g.shape), dev_bf16(u, u.shape), dev_bf16(d, d.shape),
+                                 shared=tuple(dev_bf16(a, a.shape) for a in sh), residual=dev_bf16(r, (M, H)))
+            assert h.last_expert_variant == ML.VARIANT_SPLIT_K
+            outs.append(host_bits(out))
+    finally:
+        h.test_set_engine_finish(0)
+    assert_bf16_close(outs[0], oracle.moe(x, idx, w, lambda e: (g[e], u[e], d[e]), sh, r), f"moe M={M}")
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2]), "finish paths differ"
+    assert h.check_device_error() == ML.DEC_OK
+
+
 # ---------------------------------------------------------------------------- workload size
 from conftest import E_FULL, H_FULL, I_FULL, K_FULL
 

@@ -159,6 +159,38 @@ def test_mixed_precision_fma_matches_widened(h, N, K):
         assert np.array_equal(y1[0], y2[0]), "mixed-precision FMA differs from the widened form"
 
 
+@pytest.mark.parametrize("M,N,K,resid", [(16, 1000, 8192, True), (64, 520, 4096, False), (4, 1001, 4096, True),
+                                          (3, 128, 8192, True)])
+def test_split_tile_finish_paths_give_the_same_bits(h, M, N, K, resid):
+    """The split-K kernel's three ways of finishing a tile split between CTAs
+    add the same fp32 partials in the same k order, so the outputs agree bit
+    for bit: the first piece's CTA from shared memory (default), the CTA that
+    completes the count (mode 1), and the same with the pieces read from L2
+    (mode 2). The shapes split tiles over two to many CTAs, with the residual
+    staged in shared memory (N a multiple of 8) or read from global memory."""
+    import moe_layers_gb300 as ML
+    x, W = _mats(M, N, K, 960 + M + N)
+    r = synth.bf16(M * N, SEED, 970 + M, 0, 1.0).reshape(M, N) if resid else None
+    with pytest.raises(ML.DecodeError):
+        h.test_set_engine_finish(3)
+    outs = []
+    h.set_force_variant(ML.VARIANT_SPLIT_K)
+    try:
+        for mode in (0, 1, 2):
+            h.test_set_engine_finish(mode)
+            if resid:
+                y = ML.dec_linear_residual(h, dev_bf16(x, (M, K)), dev_bf16(W, (N, K)), dev_bf16(r, (M, N)))
+            else:
+                y = ML.dec_linear(h, dev_bf16(x, (M, K)), dev_bf16(W, (N, K)))
+            outs.append(host_bits(y))
+    finally:
+        h.test_set_engine_finish(0)
+        h.set_force_variant(ML.VARIANT_AUTO)
+    ref = oracle.linear_residual(x, W, r) if resid else oracle.linear(x, W)
+    assert_bf16_close(outs[0], ref, f"split-K M={M} N={N} K={K}")
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2]), "finish paths differ"
+
+
 def test_automatic_choice_by_size(h):
     """Up to four tokens a matrix of at most 48 MB stays on the small-matrix
     kernel (the split-K kernel's per-launch cost outweighs its rate there)."""
