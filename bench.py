@@ -101,14 +101,14 @@ def step_bytes(M: int, U: float) -> float:
 # sha256 of the listed files at capture time); null otherwise.
 NCU_TRAFFIC = {
     # one-token MoE front launch: dram__bytes_read.sum + dram__bytes_write.sum of two launches of one
-    # ncu capture on the 32-expert bank (read 529,536,512 / 529,547,776 B, write 3,065,344 /
-    # 241,152 B), scaled to the 384-expert workload: at one token a launch reads what it reads
+    # ncu capture on the 32-expert bank (read 529,535,488 / 529,539,328 B, write 2,992,384 /
+    # 42,240 B), scaled to the 384-expert workload: at one token a launch reads what it reads
     # with 384 experts except the router, 352 x 7168 x 4 B more.
-    ("moe_front", 1): {"bytes": (529536512 + 529547776) // 2 + (384 - 32) * 7168 * 4 + (3065344 + 241152) // 2,
+    ("moe_front", 1): {"bytes": (529535488 + 529539328) // 2 + (384 - 32) * 7168 * 4 + (2992384 + 42240) // 2,
                        "sources": ("moe_layers_gb300/csrc/route_shared.cu", "moe_layers_gb300/csrc/topk.cuh",
                                    "moe_layers_gb300/csrc/common.cuh", "moe_layers_gb300/csrc/internal.h",
                                    "moe_layers_gb300/csrc/api.cu"),
-                       "sha256": "a4bf807d2488fc1f89b9f4821ea1978bd0ee1bb9a478bd9d1f1784aa9bf080f5"},
+                       "sha256": "cedfd26c79fdaaafe0e327ce0c8345ecc0dc74ab4725773f053a438cca476b66"},
 }
 
 
