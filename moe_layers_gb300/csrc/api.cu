@@ -160,16 +160,24 @@ bool experts_small(const dec_handle* h, int M, int H, int I) {
 // A few tokens: the small-matrix kernels over one problem per (token, expert)
 // entry (an expert chosen by several tokens is read once per entry), unless
 // the split-K family is forced. Measured on GB300 (layer step, graph replay,
-// this path against the split-K experts): at two tokens 297 against 312 us
-// (full shapes), 74 against 77 (TP8 shard shapes), 54 against 67 (TP16); at
-// three and four tokens mixed or slower (up to 6% more expert bytes, the
-// shared down projection read once per token). So: two tokens; with the
-// small-matrix family forced, two to four.
+// this path against the split-K experts, one box):
+//  - two tokens: 297 against 312 us (full shapes), 74 against 77 (TP8 shard
+//    shapes), 54 against 67 (TP16);
+//  - three tokens: slower at full shapes (409.7 against 402.6 us), faster at
+//    TP8 (86.7 against 89.8) and TP16 (60.5 against 68.3): for small experts
+//    the split-K chain's seven launches outweigh the extra reads (repeated
+//    experts, the shared down projection once per token);
+//  - four tokens: slower at full shapes (511.0 against 492.7) and TP8 (110.2
+//    against 105.8), faster at TP16 (71.3 against 76.7).
+// So: two tokens; three when one expert's gate/up is at most 8 MB; four when
+// it is at most 4 MB; with the small-matrix family forced, two to four.
 bool experts_few(const dec_handle* h, int M, int k, int E, int H, int I) {
   if (M < 2 || M > 4 || !gemv_moe_supported(H) || !gemv_moe_supported(I) || !route_shared_supported(h, M, H, E, k))
     return false;
   if (h->force_variant == DEC_VARIANT_SMALL_M) return true;
-  return h->force_variant == DEC_VARIANT_AUTO && M == 2;
+  if (h->force_variant != DEC_VARIANT_AUTO) return false;
+  const double gate_up_bytes = 2.0 * I * H * 2;  // one expert's gate and up matrices, bf16
+  return M == 2 || (M == 3 && gate_up_bytes <= 8e6) || (M == 4 && gate_up_bytes <= 4e6);
 }
 
 // SM shares of the shared and the routed experts ("the schedule controls how

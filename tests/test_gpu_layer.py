@@ -275,8 +275,8 @@ def test_layer_few_tokens(h, M, I, shared, front):
         h.test_set_moe_front(True)
 
 
-@pytest.mark.parametrize("M", [1, 2, 4])
-def test_layer_front_with_sms_held_by_another_stream(h, M):
+@pytest.mark.parametrize("M,family", [(1, "auto"), (2, "auto"), (4, "auto"), (4, "split_k")])
+def test_layer_front_with_sms_held_by_another_stream(h, M, family):
     """The MoE front's CTAs wait for the routing that one of them publishes.
     Here a kernel on another stream holds half the SMs for 150 ms, so only
     half of the front's CTAs can be resident at once, and the routing wait is
@@ -284,7 +284,11 @@ def test_layer_front_with_sms_held_by_another_stream(h, M):
     running (router units go to whichever CTAs take them), so the layer
     returns DEC_OK with the oracle's result instead of a timeout. (A front
     whose router units belonged to fixed CTAs would wait for CTAs that cannot
-    start until the other kernel ends, and time out.)"""
+    start until the other kernel ends, and time out.) At four tokens these small
+    experts take the few-token front; with the split-K family forced, the
+    engine's launches run with half the SMs held: the CTA that finishes a
+    split tile waits a bounded time for the other pieces, then leaves the tile
+    to the last piece's CTA, so it completes as well."""
     import time
     import torch
     import moe_layers_gb300 as ML
@@ -306,17 +310,21 @@ def test_layer_front_with_sms_held_by_another_stream(h, M):
     torch.cuda.synchronize()
     side, main = torch.cuda.Stream(), torch.cuda.Stream()
     h.set_wait_limit_ns(30_000_000)
+    if family == "split_k":
+        h.set_force_variant(ML.VARIANT_SPLIT_K)
     try:
         ML.test_occupy_sms(h, sms // 2, 150_000_000, stream=side)
         time.sleep(0.002)  # the holding kernel is resident before the layer is launched
         launches0 = h.launch_count
         with torch.cuda.stream(main):
             tr = ML.decode_layer(h, dev_w, hid, trace=True, stream=main)
-        # the MoE front schedule at one and two tokens; at four the split-K family, whose kernels wait on nothing
-        assert h.launch_count - launches0 == (4 if M <= 2 else 11)
+        # the MoE front schedule: four launches at one and two tokens, five at four (down and combine
+        # apart); the split-K family: twelve (the first RMSNorm is a launch of its own there)
+        assert h.launch_count - launches0 == (12 if family == "split_k" else 4 if M <= 2 else 5)
         torch.cuda.synchronize()
     finally:
         h.set_wait_limit_ns(500_000_000)
+        h.set_force_variant(ML.VARIANT_AUTO)
     assert h.check_device_error() == ML.DEC_OK
     _check_layer(tr, hid, ref, slice(None), f"layer M={M} beside a kernel holding {sms // 2} SMs", L, ex, sh)
 
