@@ -101,14 +101,14 @@ def step_bytes(M: int, U: float) -> float:
 # sha256 of the listed files at capture time); null otherwise.
 NCU_TRAFFIC = {
     # one-token MoE front launch: dram__bytes_read.sum + dram__bytes_write.sum of two launches of one
-    # ncu capture on the 32-expert bank (read 529,535,488 / 529,539,328 B, write 2,992,384 /
-    # 42,240 B), scaled to the 384-expert workload: at one token a launch reads what it reads
+    # ncu capture on the 32-expert bank (read 529,558,528 / 529,543,168 B, write 3,401,216 /
+    # 242,432 B), scaled to the 384-expert workload: at one token a launch reads what it reads
     # with 384 experts except the router, 352 x 7168 x 4 B more.
-    ("moe_front", 1): {"bytes": (529535488 + 529539328) // 2 + (384 - 32) * 7168 * 4 + (2992384 + 42240) // 2,
+    ("moe_front", 1): {"bytes": (529558528 + 529543168) // 2 + (384 - 32) * 7168 * 4 + (3401216 + 242432) // 2,
                        "sources": ("moe_layers_gb300/csrc/route_shared.cu", "moe_layers_gb300/csrc/topk.cuh",
                                    "moe_layers_gb300/csrc/common.cuh", "moe_layers_gb300/csrc/internal.h",
                                    "moe_layers_gb300/csrc/api.cu"),
-                       "sha256": "cedfd26c79fdaaafe0e327ce0c8345ecc0dc74ab4725773f053a438cca476b66"},
+                       "sha256": "be162b5a3613baf933db184505311049afaa36e83adfa3a0f0da48ce9996eea6"},
 }
 
 
